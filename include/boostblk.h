@@ -1,0 +1,144 @@
+/*
+ * boostblk.h -- C ABI of the GB300 low-rank bottleneck block library.
+ *
+ * One CoLA-style decoder block, forward and backward, on one GPU (sm_103a).
+ * Every linear layer of the block is a bottleneck  out = B . sigma(A . x)
+ * with A [r, d_in] (down-projection) and B [d_out, r] (up-projection);
+ * "BOOST: BOttleneck-Optimized Scalable Training Framework for Low-Rank Large
+ * Language Models", project page, section "Move the chunk boundary to the
+ * bottleneck" (first paragraph and the decoder-block figure).
+ *
+ * The block (full kind), with sigma = SiLU or identity:
+ *   z_qkv = OnlineRMSNorm_S(x; w_norm1) . A_qkv^T         [T, 3r]  grouped Q/K/V down
+ *   Q, K, V = sigma(z_q) B_q^T, sigma(z_k) B_k^T, sigma(z_v) B_v^T   [T, d] each
+ *   x1 = x + sigma(V A_o^T) B_o^T                          (attention core excluded)
+ *   z_gu = OnlineRMSNorm_S(x1; w_norm2) . A_gu^T           [T, 2r]  grouped gate/up down
+ *   G, U = sigma(z_g) B_g^T, sigma(z_u) B_u^T              [T, d_ff]
+ *   m = SiLU(G) * U ;  y = x1 + sigma(m A_d^T) B_d^T
+ * The MLP kind is the second half alone with x1 = x.
+ *
+ * Online RMSNorm: the hidden dimension is split into S equal column shards;
+ * each shard's slice of the down-projection is normalised by the shard's own
+ * RMS and the per-row correction alpha = RMS_local / RMS_global is applied in
+ * the GEMM epilogue, which gives plain RMSNorm exactly (project page, "Three
+ * supporting changes" -> Online RMSNorm; BOOST-MLSys26 summary page, core
+ * method -> Online RMSNorm). RMS = sqrt(mean of squares + eps), eps inside
+ * both the local and the global square root.
+ * Grouping (project page, "Three supporting changes" -> Linear layer
+ * grouping): the Q/K/V down-projections are one GEMM over
+ * A_qkv = [A_q; A_k; A_v], the gate/up ones one GEMM over A_gu = [A_g; A_u];
+ * the up-projections of a group run in one launch.
+ * Checkpointing (same section -> Checkpointing without communication): with
+ * desc.checkpoint = 1 the forward saves only the r-wide pre-activations
+ * z_qkv, z_o, z_gu, z_d and the backward recomputes everything else.
+ *
+ * Conventions (all entry points):
+ *  - Row-major everywhere. Weights are [out, in]. Token rows are T.
+ *  - All pointers are device pointers owned by the caller; the library
+ *    allocates no device memory and keeps no state except cached device
+ *    properties. Every pointer must be 16-byte aligned.
+ *  - The element type of every tensor is desc.dtype (fp32 or bf16). bf16 runs
+ *    multiply on the tensor cores and accumulate in fp32; fp32 runs use plain
+ *    fp32 FFMA.
+ *  - Argument errors return synchronously, before anything is launched.
+ *    Launches are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream). A kernel whose internal wait exceeds its time limit
+ *    records a timeout in the status word at the start of `scratch`, which
+ *    bn_get_device_status() reads.
+ *  - Gradients are overwritten, never accumulated.
+ *  - d_ff-wide tensors (A_d, its gradient, and internal G, U, m) use the
+ *    leading dimension desc.ld_ff >= d_ff; columns d_ff .. ld_ff-1 are neither
+ *    read nor written.
+ */
+#ifndef BOOSTBLK_H
+#define BOOSTBLK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* bn_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+  BN_OK = 0,
+  BN_ERR_INVALID_ARG = 1, /* a size, enum or pointer is out of range */
+  BN_ERR_ALIGNMENT = 2,   /* a pointer or leading dimension breaks the 16-byte rule */
+  BN_ERR_UNSUPPORTED = 3, /* valid, but outside what this build implements */
+  BN_ERR_CUDA = 4,        /* a CUDA runtime call failed (see bn_last_cuda_error) */
+  BN_ERR_TIMEOUT = 5      /* a kernel gave up on an internal wait (device status) */
+} bn_status;
+
+typedef enum { BN_F32 = 0, BN_BF16 = 1 } bn_dtype;
+typedef enum { BN_SIGMA_IDENTITY = 0, BN_SIGMA_SILU = 1 } bn_sigma;
+typedef enum { BN_BLOCK_FULL = 0, BN_BLOCK_MLP = 1 } bn_kind;
+
+/* Shapes and options of one block. */
+typedef struct {
+  int64_t T;      /* tokens (micro-batch x sequence), >= 1 */
+  int64_t d;      /* hidden width; d % S == 0; bf16 also needs (d / S) % 64 == 0 */
+  int64_t r;      /* bottleneck rank; a multiple of 8 */
+  int64_t d_ff;   /* MLP width, >= 1 */
+  int64_t ld_ff;  /* leading dimension of d_ff-wide tensors: >= d_ff, a multiple of 8 */
+  int32_t S;      /* emulated column shards of Online RMSNorm, 1 .. 16 */
+  int32_t sigma;  /* bn_sigma: the bottleneck nonlinearity */
+  int32_t dtype;  /* bn_dtype */
+  int32_t kind;   /* bn_kind */
+  int32_t dense;  /* 1 = full-rank baseline block: A_* hold the dense W, B_* are NULL */
+  int32_t checkpoint; /* 1 = save only the r-wide pre-activations (factorised block only) */
+  float eps;      /* RMSNorm epsilon, e.g. 1e-5 */
+} bn_block_desc;
+
+/* Parameters (forward) or their gradients (backward). Shapes, low-rank block:
+ *   w_norm1 [d], A_qkv [3r, d], B_q/B_k/B_v [d, r], A_o [r, d], B_o [d, r],
+ *   w_norm2 [d], A_gu [2r, d], B_g/B_u [d_ff, r], A_d [r, ld_ff], B_d [d, r].
+ * Dense block: A_qkv [3d, d], A_o [d, d], A_gu [2 d_ff, d], A_d [d, ld_ff], B_* NULL.
+ * MLP kind: w_norm1, A_qkv, B_q, B_k, B_v, A_o, B_o are NULL. */
+typedef struct {
+  void* w_norm1; void* A_qkv; void* B_q; void* B_k; void* B_v; void* A_o; void* B_o;
+  void* w_norm2; void* A_gu; void* B_g; void* B_u; void* A_d; void* B_d;
+} bn_block_params;
+
+/* Bytes the caller must provide: `saved` (activations kept from forward to
+ * backward) and `scratch` (temporaries of either pass; its first 256 bytes hold
+ * the device status word). Both depend on desc only. */
+bn_status bn_block_workspace_size(const bn_block_desc* desc, size_t* saved_bytes,
+                                  size_t* scratch_bytes);
+
+/* Forward pass. x [T, d] in; y [T, d] out; q_out, k_out [T, d] out for the
+ * full kind (NULL for the MLP kind). `saved` receives what the backward reads. */
+bn_status bn_block_forward(const bn_block_desc* desc, const bn_block_params* W,
+                           const void* x, void* y, void* q_out, void* k_out,
+                           void* saved, void* scratch, bn_stream_t stream);
+
+/* Backward pass for upstream gradients dy [T, d] and dq, dk [T, d] (full kind;
+ * either may be NULL, meaning zero). `saved` must come from bn_block_forward
+ * with the same desc, W and x. Writes dx [T, d] and every gradient in dW
+ * (same shapes as W). Outputs may not alias inputs. */
+bn_status bn_block_backward(const bn_block_desc* desc, const bn_block_params* W,
+                            const void* x, const void* saved, const void* dy,
+                            const void* dq, const void* dk, void* dx,
+                            const bn_block_params* dW, void* scratch, bn_stream_t stream);
+
+/* Synchronises `stream`, reads and clears the device status word at the start
+ * of `scratch`, and returns BN_OK or BN_ERR_TIMEOUT (BN_ERR_CUDA if the
+ * synchronisation itself failed). */
+bn_status bn_get_device_status(void* scratch, bn_stream_t stream);
+
+/* Number of kernels the last bn_block_forward / bn_block_backward call made by
+ * this thread launched. */
+int bn_last_launch_count(void);
+
+/* Name of a status code (static storage). */
+const char* bn_status_string(bn_status s);
+
+/* Text of the last CUDA error this library saw on this thread (static storage). */
+const char* bn_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BOOSTBLK_H */
