@@ -1,0 +1,914 @@
+// Block scheduler and C ABI: validates a bn_block_desc, lays out the caller's
+// `saved` / `scratch` buffers, and issues the forward / backward kernel
+// sequence of one low-rank (or dense) decoder block on the caller's stream.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/boostblk.h"
+#include "common.cuh"
+#include "gemm.h"
+#include "rowops.h"
+
+namespace bn {
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+thread_local int g_last_launches = 0;
+thread_local char g_cuda_err[256] = "no error";
+
+struct Shape {
+  int64_t T, d, r, d_ff, ld_ff;
+  int S, sigma, dtype, kind, dense, ckpt;
+  float eps;
+  int64_t E;  // bytes per element
+  bool full() const { return kind == BN_BLOCK_FULL; }
+};
+
+// activations written by the forward and read by the backward
+struct Acts {
+  float *ss1 = nullptr, *rstd1 = nullptr, *ss2 = nullptr, *rstd2 = nullptr;
+  void *z_qkv = nullptr, *h_qkv = nullptr, *V = nullptr, *z_o = nullptr, *h_o = nullptr;
+  void *x1 = nullptr, *z_gu = nullptr, *h_gu = nullptr, *G = nullptr, *U = nullptr, *m = nullptr;
+  void *z_d = nullptr, *h_d = nullptr;
+};
+// temporaries in `scratch`
+struct Tmp {
+  int* status = nullptr;
+  void *A1f = nullptr, *A2f = nullptr;  // down-projections with the norm weight folded in
+  void *dz_d = nullptr, *dG = nullptr, *dU = nullptr, *dz_gu = nullptr, *dn = nullptr;
+  void *dx1 = nullptr, *dz_o = nullptr, *dV = nullptr, *dz_qkv = nullptr, *dqkv = nullptr;
+  float* dw_part = nullptr;
+  float* partial = nullptr;
+  size_t partial_bytes = 0;
+  int nblk = 0;
+};
+
+struct Bump {
+  char* base;
+  size_t off = 0;
+  explicit Bump(void* b) : base(static_cast<char*>(b)) {}
+  void* take(size_t bytes) {
+    off = (off + 255) & ~static_cast<size_t>(255);
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+int device_sms() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// Largest M x ldp(N) summed over the problems of one weight-gradient launch.
+int64_t max_wgrad_elems(const Shape& s) {
+  auto ldp = [](int64_t n) { return (n + 7) / 8 * 8; };
+  int64_t best = 0;
+  auto cand = [&](int64_t v) { best = std::max(best, v); };
+  if (s.dense) {
+    cand(s.d * ldp(s.d_ff));
+    cand(2 * s.d_ff * ldp(s.d));
+    if (s.full()) {
+      cand(s.d * ldp(s.d));
+      cand(3 * s.d * ldp(s.d));
+    }
+  } else {
+    cand(s.d * ldp(s.r));
+    cand(s.r * ldp(s.d_ff));
+    cand(2 * s.d_ff * ldp(s.r));
+    cand(2 * s.r * ldp(s.d));
+    if (s.full()) {
+      cand(s.r * ldp(s.d));
+      cand(3 * s.d * ldp(s.r));
+      cand(3 * s.r * ldp(s.d));
+    }
+  }
+  return best;
+}
+
+void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
+          size_t* saved_bytes, size_t* scratch_bytes) {
+  Bump sv(saved_base), sc(scratch_base);
+  const int64_t T = s.T, E = s.E;
+  B.status = static_cast<int*>(sc.take(256));
+  // in checkpoint mode only the pre-activations go to `saved`
+  Bump& keep = sv;
+  Bump& rest = s.ckpt ? sc : sv;
+  if (s.full()) {
+    A.ss1 = static_cast<float*>(rest.take(T * s.S * 4));
+    A.rstd1 = static_cast<float*>(rest.take(T * 4));
+    if (!s.dense) {
+      A.z_qkv = keep.take(T * 3 * s.r * E);
+      A.h_qkv = rest.take(T * 3 * s.r * E);
+      A.z_o = keep.take(T * s.r * E);
+      A.h_o = rest.take(T * s.r * E);
+    }
+    A.V = rest.take(T * s.d * E);
+    A.x1 = rest.take(T * s.d * E);
+  }
+  A.ss2 = static_cast<float*>(rest.take(T * s.S * 4));
+  A.rstd2 = static_cast<float*>(rest.take(T * 4));
+  if (!s.dense) {
+    A.z_gu = keep.take(T * 2 * s.r * E);
+    A.h_gu = rest.take(T * 2 * s.r * E);
+    A.z_d = keep.take(T * s.r * E);
+    A.h_d = rest.take(T * s.r * E);
+  }
+  A.G = rest.take(T * s.ld_ff * E);
+  A.U = rest.take(T * s.ld_ff * E);
+  A.m = rest.take(T * s.ld_ff * E);
+
+  const int64_t n1 = s.dense ? 3 * s.d : 3 * s.r, n2 = s.dense ? 2 * s.d_ff : 2 * s.r;
+  if (s.full()) B.A1f = sc.take(n1 * s.d * E);
+  B.A2f = sc.take(n2 * s.d * E);
+  if (!s.dense) {
+    B.dz_d = sc.take(T * s.r * E);
+    B.dz_gu = sc.take(T * 2 * s.r * E);
+  }
+  B.dG = sc.take(T * s.ld_ff * E);
+  B.dU = sc.take(T * s.ld_ff * E);
+  B.dn = sc.take(T * s.d * E);
+  if (s.full()) {
+    B.dx1 = sc.take(T * s.d * E);
+    if (s.dense) {
+      B.dqkv = sc.take(T * 3 * s.d * E);
+    } else {
+      B.dz_o = sc.take(T * s.r * E);
+      B.dV = sc.take(T * s.d * E);
+      B.dz_qkv = sc.take(T * 3 * s.r * E);
+    }
+  }
+  B.nblk = norm_bwd_blocks(device_sms());
+  B.dw_part = static_cast<float*>(sc.take(static_cast<size_t>(B.nblk) * s.d * 4));
+  if (s.dtype == BN_BF16) {
+    B.partial_bytes = std::min<size_t>(static_cast<size_t>(8) * max_wgrad_elems(s) * 4,
+                                       static_cast<size_t>(1) << 30);
+    B.partial = static_cast<float*>(sc.take(B.partial_bytes));
+  }
+  if (saved_bytes) *saved_bytes = sv.off;
+  if (scratch_bytes) *scratch_bytes = sc.off;
+}
+
+bn_status check_desc(const bn_block_desc* D, Shape& s) {
+  if (D == nullptr) return BN_ERR_INVALID_ARG;
+  s.T = D->T;
+  s.d = D->d;
+  s.r = D->r;
+  s.d_ff = D->d_ff;
+  s.ld_ff = D->ld_ff;
+  s.S = D->S;
+  s.sigma = D->sigma;
+  s.dtype = D->dtype;
+  s.kind = D->kind;
+  s.dense = D->dense;
+  s.ckpt = D->checkpoint;
+  s.eps = D->eps;
+  if (s.dtype != BN_F32 && s.dtype != BN_BF16) return BN_ERR_INVALID_ARG;
+  if (s.sigma != BN_SIGMA_IDENTITY && s.sigma != BN_SIGMA_SILU) return BN_ERR_INVALID_ARG;
+  if (s.kind != BN_BLOCK_FULL && s.kind != BN_BLOCK_MLP) return BN_ERR_INVALID_ARG;
+  if ((s.dense != 0 && s.dense != 1) || (s.ckpt != 0 && s.ckpt != 1)) return BN_ERR_INVALID_ARG;
+  if (s.T < 1 || s.d < 1 || s.d_ff < 1 || s.ld_ff < s.d_ff || s.S < 1 || s.S > 16)
+    return BN_ERR_INVALID_ARG;
+  if (!(s.eps >= 0.f) || s.eps > 1.f) return BN_ERR_INVALID_ARG;
+  if (!s.dense && s.r < 1) return BN_ERR_INVALID_ARG;
+  // the RMSNorm backward keeps 4 x d fp32 column sums in shared memory
+  if (s.T > (int64_t(1) << 31) - 256 || s.d > 12288 || s.ld_ff > (int64_t(1) << 22) ||
+      s.r > (int64_t(1) << 20))
+    return BN_ERR_UNSUPPORTED;
+  if (s.d % s.S != 0 || (s.d / s.S) % 8 != 0) return BN_ERR_INVALID_ARG;
+  if (s.ld_ff % 8 != 0 || (!s.dense && s.r % 8 != 0)) return BN_ERR_ALIGNMENT;
+  if (s.dense && s.ckpt) return BN_ERR_UNSUPPORTED;
+  if (s.dtype == BN_BF16 && (s.d / s.S) % 64 != 0) return BN_ERR_UNSUPPORTED;
+  s.E = (s.dtype == BN_BF16) ? 2 : 4;
+  return BN_OK;
+}
+
+bool aligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Every pointer that must be present is non-null and aligned; every pointer
+// that must be absent is null.
+bn_status check_params(const Shape& s, const bn_block_params* W) {
+  if (W == nullptr) return BN_ERR_INVALID_ARG;
+  const bool f = s.full(), lr = !s.dense;
+  const void* need[] = {W->w_norm2, W->A_gu, W->A_d};
+  for (const void* p : need)
+    if (p == nullptr) return BN_ERR_INVALID_ARG;
+  struct Item { const void* p; bool required; };
+  const Item items[] = {{W->w_norm1, f},        {W->A_qkv, f},        {W->B_q, f && lr},
+                        {W->B_k, f && lr},      {W->B_v, f && lr},    {W->A_o, f},
+                        {W->B_o, f && lr},      {W->w_norm2, true},   {W->A_gu, true},
+                        {W->B_g, lr},           {W->B_u, lr},         {W->A_d, true},
+                        {W->B_d, lr}};
+  for (const Item& it : items) {
+    if (it.required && it.p == nullptr) return BN_ERR_INVALID_ARG;
+    if (!it.required && it.p != nullptr) return BN_ERR_INVALID_ARG;
+    if (it.p != nullptr && !aligned(it.p)) return BN_ERR_ALIGNMENT;
+  }
+  return BN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// launch helpers
+// ---------------------------------------------------------------------------
+Operand op(const void* p, int64_t ld, bool mn_major) {
+  Operand o;
+  o.ptr = p;
+  o.ld = ld;
+  o.mn_major = mn_major;
+  return o;
+}
+constexpr bool KM = false, MN = true;
+
+const void* at(const void* p, int64_t elems, const Shape& s) {
+  return p ? static_cast<const char*>(p) + elems * s.E : nullptr;
+}
+void* at(void* p, int64_t elems, const Shape& s) {
+  return p ? static_cast<char*>(p) + elems * s.E : nullptr;
+}
+
+void gemm(Ctx& c, const Shape& s, const GemmLaunch& g) {
+  if (s.dtype == BN_BF16)
+    gemm_tc(c, g);
+  else
+    gemm_simt(c, g);
+}
+
+GemmLaunch launch(Epi e, const Shape& s) {
+  GemmLaunch g;
+  g.epi = e;
+  g.sigma = s.sigma;
+  g.S = s.S;
+  g.eps = s.eps;
+  return g;
+}
+
+// weight gradient: out[M, N] = colv[j] * sum_t Aop[t, i] Bop[t, j]
+GemmProblem wgrad(int64_t M, int64_t N, int64_t T, const void* a, int64_t lda, const void* b,
+                  int64_t ldb, void* out, int64_t ldo, const void* colv = nullptr) {
+  GemmProblem p;
+  p.M = M;
+  p.N = N;
+  p.K = T;
+  p.a[0] = op(a, lda, MN);
+  p.b[0] = op(b, ldb, MN);
+  p.out[0] = out;
+  p.ldo[0] = ldo;
+  p.colv = colv;
+  return p;
+}
+
+#define DT_CALL(s, FN, ...)                                          \
+  do {                                                               \
+    if ((s).dtype == BN_BF16)                                        \
+      FN<bf16>(__VA_ARGS__);                                         \
+    else                                                             \
+      FN<float>(__VA_ARGS__);                                        \
+  } while (0)
+
+template <typename T>
+void stats(Ctx& c, const void* x, const Shape& s, float* ss, float* rstd) {
+  launch_stats<T>(c, static_cast<const T*>(x), s.T, s.d, s.S, s.eps, ss, rstd);
+}
+template <typename T>
+void fold(Ctx& c, const void* A, const void* w, int64_t rows, int64_t cols, void* out) {
+  launch_fold_cols<T>(c, static_cast<const T*>(A), static_cast<const T*>(w), rows, cols,
+                      static_cast<T*>(out));
+}
+template <typename T>
+void normbwd(Ctx& c, const Shape& s, const Tmp& B, const void* dn, const void* x, const void* w,
+             const float* rstd, const void* dres, void* dx, void* dw) {
+  launch_norm_bwd<T>(c, static_cast<const T*>(dn), static_cast<const T*>(x),
+                     static_cast<const T*>(w), rstd, static_cast<const T*>(dres), s.T, s.d,
+                     static_cast<T*>(dx), B.dw_part, B.nblk, static_cast<T*>(dw));
+}
+template <typename T>
+void sigma_ew(Ctx& c, const Shape& s, const void* z, int64_t cols, int64_t ld, void* h) {
+  launch_sigma<T>(c, static_cast<const T*>(z), s.T, cols, ld, static_cast<T*>(h), ld, s.sigma);
+}
+template <typename T>
+void swiglu_ew(Ctx& c, const Shape& s, const void* G, const void* U, void* m) {
+  launch_swiglu<T>(c, static_cast<const T*>(G), static_cast<const T*>(U), s.T, s.d_ff, s.ld_ff,
+                   static_cast<T*>(m), s.ld_ff);
+}
+template <typename T>
+void rowscale(Ctx& c, const Shape& s, const void* in, int64_t ldi, const float* rowv, int64_t cols,
+              void* out, int64_t ldo) {
+  launch_rowscale<T>(c, static_cast<const T*>(in), ldi, rowv, s.T, cols, static_cast<T*>(out), ldo);
+}
+
+void zero2d(Ctx& c, void* p, int64_t ld_bytes, int64_t width_bytes, int64_t rows) {
+  cudaError_t e = cudaMemset2DAsync(p, ld_bytes, 0, width_bytes, rows, c.stream);
+  if (e != cudaSuccess && c.err == cudaSuccess) c.err = e;
+}
+
+bn_status finish(Ctx& c) {
+  g_last_launches = c.launches;
+  if (c.bad) return BN_ERR_UNSUPPORTED;
+  if (c.err != cudaSuccess) {
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "%s", cudaGetErrorString(c.err));
+    return BN_ERR_CUDA;
+  }
+  return BN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// forward pieces (shared by the forward and the checkpoint recompute)
+// ---------------------------------------------------------------------------
+
+// V (and Q, K when wanted) = sigma(z) B^T for the grouped Q/K/V bottlenecks.
+void qkv_up(Ctx& c, const Shape& s, const bn_block_params* W, const Acts& A, void* q, void* k) {
+  GemmLaunch g = launch(EPI_STORE, s);
+  const void* Bs[3] = {W->B_q, W->B_k, W->B_v};
+  void* outs[3] = {q, k, A.V};
+  for (int i = 0; i < 3; ++i) {
+    if (outs[i] == nullptr) continue;
+    GemmProblem& p = g.p[g.nprob++];
+    p.M = s.T;
+    p.N = s.d;
+    p.K = s.r;
+    p.a[0] = op(at(A.h_qkv, i * s.r, s), 3 * s.r, KM);
+    p.b[0] = op(Bs[i], s.r, KM);
+    p.out[0] = outs[i];
+    p.ldo[0] = s.d;
+  }
+  gemm(c, s, g);
+}
+
+// x1 = x + sigma(z_o) B_o^T
+void o_up(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, const Acts& A) {
+  GemmLaunch g = launch(EPI_RESID, s);
+  g.nprob = 1;
+  GemmProblem& p = g.p[0];
+  p.M = s.T;
+  p.N = s.d;
+  p.K = s.r;
+  p.a[0] = op(A.h_o, s.r, KM);
+  p.b[0] = op(W->B_o, s.r, KM);
+  p.in[0] = x;
+  p.ldi[0] = s.d;
+  p.out[0] = A.x1;
+  p.ldo[0] = s.d;
+  gemm(c, s, g);
+}
+
+// G, U = sigma(z_g) B_g^T, sigma(z_u) B_u^T; m = SiLU(G) U
+void gu_up(Ctx& c, const Shape& s, const bn_block_params* W, const Acts& A, bool keep_gu) {
+  GemmLaunch g = launch(EPI_SWIGLU, s);
+  g.nprob = 1;
+  GemmProblem& p = g.p[0];
+  p.M = s.T;
+  p.N = s.d_ff;
+  p.K = s.r;
+  p.a[0] = op(A.h_gu, 2 * s.r, KM);
+  p.b[0] = op(W->B_g, s.r, KM);
+  p.a[1] = op(at(A.h_gu, s.r, s), 2 * s.r, KM);
+  p.b[1] = op(W->B_u, s.r, KM);
+  p.out[0] = keep_gu ? A.G : nullptr;
+  p.out[1] = keep_gu ? A.U : nullptr;
+  p.out[2] = A.m;
+  p.ldo[0] = p.ldo[1] = p.ldo[2] = s.ld_ff;
+  gemm(c, s, g);
+}
+
+// y = x1 + sigma(z_d) B_d^T
+void down_up(Ctx& c, const Shape& s, const bn_block_params* W, const Acts& A, const void* x1,
+             void* y) {
+  GemmLaunch g = launch(EPI_RESID, s);
+  g.nprob = 1;
+  GemmProblem& p = g.p[0];
+  p.M = s.T;
+  p.N = s.d;
+  p.K = s.r;
+  p.a[0] = op(A.h_d, s.r, KM);
+  p.b[0] = op(W->B_d, s.r, KM);
+  p.in[0] = x1;
+  p.ldi[0] = s.d;
+  p.out[0] = y;
+  p.ldo[0] = s.d;
+  gemm(c, s, g);
+}
+
+// z = OnlineRMSNorm_S(x) Af^T (Af has the norm weight folded in), h = sigma(z)
+void norm_down(Ctx& c, const Shape& s, const void* x, const float* ss, const void* Af, int64_t n,
+               void* z, void* h) {
+  GemmLaunch g = launch(EPI_NORM, s);
+  g.nprob = 1;
+  GemmProblem& p = g.p[0];
+  p.M = s.T;
+  p.N = n;
+  p.K = s.d;
+  p.a[0] = op(x, s.d, KM);
+  p.b[0] = op(Af, s.d, KM);
+  p.rowv = ss;
+  p.out[0] = z;
+  p.ldo[0] = n;
+  p.out[1] = h;
+  p.ldo[1] = n;
+  gemm(c, s, g);
+}
+
+// z = X A^T, h = sigma(z)   (X [T, K] with leading dimension ldx)
+void plain_down(Ctx& c, const Shape& s, const void* X, int64_t K, int64_t ldx, const void* Adown,
+                int64_t lda, void* z, void* h) {
+  GemmLaunch g = launch(EPI_SIGMA, s);
+  g.nprob = 1;
+  GemmProblem& p = g.p[0];
+  p.M = s.T;
+  p.N = s.r;
+  p.K = K;
+  p.a[0] = op(X, ldx, KM);
+  p.b[0] = op(Adown, lda, KM);
+  p.out[0] = z;
+  p.ldo[0] = s.r;
+  p.out[1] = h;
+  p.ldo[1] = s.r;
+  gemm(c, s, g);
+}
+
+// ---------------------------------------------------------------------------
+// forward
+// ---------------------------------------------------------------------------
+void forward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, void* y,
+                     void* q, void* k, const Acts& A, const Tmp& B) {
+  const void* x1 = x;
+  if (s.full()) {
+    DT_CALL(s, stats, c, x, s, A.ss1, A.rstd1);
+    DT_CALL(s, fold, c, W->A_qkv, W->w_norm1, 3 * s.r, s.d, B.A1f);
+    norm_down(c, s, x, A.ss1, B.A1f, 3 * s.r, A.z_qkv, A.h_qkv);
+    qkv_up(c, s, W, A, q, k);
+    plain_down(c, s, A.V, s.d, s.d, W->A_o, s.d, A.z_o, A.h_o);
+    o_up(c, s, W, x, A);
+    x1 = A.x1;
+  }
+  DT_CALL(s, stats, c, x1, s, A.ss2, A.rstd2);
+  DT_CALL(s, fold, c, W->A_gu, W->w_norm2, 2 * s.r, s.d, B.A2f);
+  norm_down(c, s, x1, A.ss2, B.A2f, 2 * s.r, A.z_gu, A.h_gu);
+  gu_up(c, s, W, A, !s.ckpt);
+  plain_down(c, s, A.m, s.d_ff, s.ld_ff, W->A_d, s.ld_ff, A.z_d, A.h_d);
+  down_up(c, s, W, A, x1, y);
+}
+
+void forward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, void* y,
+                   void* q, void* k, const Acts& A, const Tmp& B) {
+  const void* x1 = x;
+  if (s.full()) {
+    DT_CALL(s, stats, c, x, s, A.ss1, A.rstd1);
+    DT_CALL(s, fold, c, W->A_qkv, W->w_norm1, 3 * s.d, s.d, B.A1f);
+    GemmLaunch g = launch(EPI_NORM, s);
+    void* outs[3] = {q, k, A.V};
+    for (int i = 0; i < 3; ++i) {
+      GemmProblem& p = g.p[g.nprob++];
+      p.M = s.T;
+      p.N = s.d;
+      p.K = s.d;
+      p.a[0] = op(x, s.d, KM);
+      p.b[0] = op(at(B.A1f, i * s.d * s.d, s), s.d, KM);
+      p.rowv = A.ss1;
+      p.out[0] = outs[i];
+      p.ldo[0] = s.d;
+    }
+    gemm(c, s, g);
+    GemmLaunch o = launch(EPI_RESID, s);
+    o.nprob = 1;
+    GemmProblem& p = o.p[0];
+    p.M = s.T;
+    p.N = s.d;
+    p.K = s.d;
+    p.a[0] = op(A.V, s.d, KM);
+    p.b[0] = op(W->A_o, s.d, KM);
+    p.in[0] = x;
+    p.ldi[0] = s.d;
+    p.out[0] = A.x1;
+    p.ldo[0] = s.d;
+    gemm(c, s, o);
+    x1 = A.x1;
+  }
+  DT_CALL(s, stats, c, x1, s, A.ss2, A.rstd2);
+  DT_CALL(s, fold, c, W->A_gu, W->w_norm2, 2 * s.d_ff, s.d, B.A2f);
+  GemmLaunch g = launch(EPI_NORM, s);
+  void* outs[2] = {A.G, A.U};
+  for (int i = 0; i < 2; ++i) {
+    GemmProblem& p = g.p[g.nprob++];
+    p.M = s.T;
+    p.N = s.d_ff;
+    p.K = s.d;
+    p.a[0] = op(x1, s.d, KM);
+    p.b[0] = op(at(B.A2f, i * s.d_ff * s.d, s), s.d, KM);
+    p.rowv = A.ss2;
+    p.out[0] = outs[i];
+    p.ldo[0] = s.ld_ff;
+  }
+  gemm(c, s, g);
+  DT_CALL(s, swiglu_ew, c, s, A.G, A.U, A.m);
+  GemmLaunch d = launch(EPI_RESID, s);
+  d.nprob = 1;
+  GemmProblem& p = d.p[0];
+  p.M = s.T;
+  p.N = s.d;
+  p.K = s.d_ff;
+  p.a[0] = op(A.m, s.ld_ff, KM);
+  p.b[0] = op(W->A_d, s.ld_ff, KM);
+  p.in[0] = x1;
+  p.ldi[0] = s.d;
+  p.out[0] = y;
+  p.ldo[0] = s.d;
+  gemm(c, s, d);
+}
+
+// Checkpoint mode: rebuild every activation the backward reads from the saved
+// pre-activations, with the same kernels (bit-identical to the forward).
+void recompute(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, const Acts& A) {
+  const void* x1 = x;
+  if (s.full()) {
+    DT_CALL(s, stats, c, x, s, A.ss1, A.rstd1);
+    DT_CALL(s, sigma_ew, c, s, A.z_qkv, 3 * s.r, 3 * s.r, A.h_qkv);
+    qkv_up(c, s, W, A, nullptr, nullptr);
+    DT_CALL(s, sigma_ew, c, s, A.z_o, s.r, s.r, A.h_o);
+    o_up(c, s, W, x, A);
+    x1 = A.x1;
+  }
+  DT_CALL(s, stats, c, x1, s, A.ss2, A.rstd2);
+  DT_CALL(s, sigma_ew, c, s, A.z_gu, 2 * s.r, 2 * s.r, A.h_gu);
+  gu_up(c, s, W, A, true);
+  DT_CALL(s, sigma_ew, c, s, A.z_d, s.r, s.r, A.h_d);
+}
+
+// ---------------------------------------------------------------------------
+// backward
+// ---------------------------------------------------------------------------
+// dz = (dY Bup) * sigma'(z) * rowv: one problem of a grouped DSIGMA launch
+GemmProblem dsigma(const Shape& s, const void* dY, int64_t ldy, int64_t K, const void* Bup,
+                   const void* z, int64_t ldz, void* dz, const float* rowv) {
+  GemmProblem p;
+  p.M = s.T;
+  p.N = s.r;
+  p.K = K;
+  p.a[0] = op(dY, ldy, KM);
+  p.b[0] = op(Bup, s.r, MN);
+  p.in[0] = z;
+  p.ldi[0] = ldz;
+  p.out[0] = dz;
+  p.ldo[0] = ldz;
+  p.rowv = rowv;
+  return p;
+}
+
+// dX = dz A  (dz [T, K] K-major, A [K, N] row-major)
+void dx_gemm(Ctx& c, const Shape& s, const void* dz, int64_t K, const void* A, int64_t lda,
+             int64_t N, void* out, int64_t ldo, const float* rowv = nullptr) {
+  GemmLaunch g = launch(EPI_STORE, s);
+  g.nprob = 1;
+  GemmProblem& p = g.p[0];
+  p.M = s.T;
+  p.N = N;
+  p.K = K;
+  p.a[0] = op(dz, K, KM);
+  p.b[0] = op(A, lda, MN);
+  p.out[0] = out;
+  p.ldo[0] = ldo;
+  p.rowv = rowv;
+  gemm(c, s, g);
+}
+
+void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const void* x,
+                      const void* dy, const void* dq, const void* dk, void* dx,
+                      const bn_block_params* dW, const Acts& A, const Tmp& B) {
+  const int64_t T = s.T, d = s.d, r = s.r;
+  const void* x1 = s.full() ? A.x1 : x;
+  // ---- down bottleneck: y = x1 + B_d sigma(A_d m)
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    g.nprob = 1;
+    g.p[0] = wgrad(d, r, T, dy, d, A.h_d, r, dW->B_d, r);
+    gemm(c, s, g);
+  }
+  {
+    GemmLaunch g = launch(EPI_DSIGMA, s);
+    g.nprob = 1;
+    g.p[0] = dsigma(s, dy, d, d, W->B_d, A.z_d, r, B.dz_d, nullptr);
+    gemm(c, s, g);
+  }
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    g.nprob = 1;
+    g.p[0] = wgrad(r, s.d_ff, T, B.dz_d, r, A.m, s.ld_ff, dW->A_d, s.ld_ff);
+    gemm(c, s, g);
+  }
+  {
+    // dm = dz_d A_d, then the SwiGLU backward in the epilogue
+    GemmLaunch g = launch(EPI_DSWIGLU, s);
+    g.nprob = 1;
+    GemmProblem& p = g.p[0];
+    p.M = T;
+    p.N = s.d_ff;
+    p.K = r;
+    p.a[0] = op(B.dz_d, r, KM);
+    p.b[0] = op(W->A_d, s.ld_ff, MN);
+    p.in[0] = A.G;
+    p.in[1] = A.U;
+    p.ldi[0] = p.ldi[1] = s.ld_ff;
+    p.out[0] = B.dG;
+    p.out[1] = B.dU;
+    p.ldo[0] = p.ldo[1] = s.ld_ff;
+    gemm(c, s, g);
+  }
+  // ---- gate / up bottlenecks
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    g.nprob = 2;
+    g.p[0] = wgrad(s.d_ff, r, T, B.dG, s.ld_ff, A.h_gu, 2 * r, dW->B_g, r);
+    g.p[1] = wgrad(s.d_ff, r, T, B.dU, s.ld_ff, at(A.h_gu, r, s), 2 * r, dW->B_u, r);
+    gemm(c, s, g);
+  }
+  {
+    GemmLaunch g = launch(EPI_DSIGMA, s);
+    g.nprob = 2;
+    g.p[0] = dsigma(s, B.dG, s.ld_ff, s.d_ff, W->B_g, A.z_gu, 2 * r, B.dz_gu, A.rstd2);
+    g.p[1] = dsigma(s, B.dU, s.ld_ff, s.d_ff, W->B_u, at(A.z_gu, r, s), 2 * r,
+                    at(B.dz_gu, r, s), A.rstd2);
+    gemm(c, s, g);
+  }
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    g.nprob = 1;
+    g.p[0] = wgrad(2 * r, d, T, B.dz_gu, 2 * r, x1, d, dW->A_gu, d, W->w_norm2);
+    gemm(c, s, g);
+  }
+  dx_gemm(c, s, B.dz_gu, 2 * r, W->A_gu, d, d, B.dn, d);
+  void* dx1 = s.full() ? B.dx1 : dx;
+  DT_CALL(s, normbwd, c, s, B, B.dn, x1, W->w_norm2, A.rstd2, dy, dx1, dW->w_norm2);
+  if (!s.full()) return;
+
+  // ---- O bottleneck: x1 = x + B_o sigma(A_o V)
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    g.nprob = 1;
+    g.p[0] = wgrad(d, r, T, dx1, d, A.h_o, r, dW->B_o, r);
+    gemm(c, s, g);
+  }
+  {
+    GemmLaunch g = launch(EPI_DSIGMA, s);
+    g.nprob = 1;
+    g.p[0] = dsigma(s, dx1, d, d, W->B_o, A.z_o, r, B.dz_o, nullptr);
+    gemm(c, s, g);
+  }
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    g.nprob = 1;
+    g.p[0] = wgrad(r, d, T, B.dz_o, r, A.V, d, dW->A_o, d);
+    gemm(c, s, g);
+  }
+  dx_gemm(c, s, B.dz_o, r, W->A_o, d, d, B.dV, d);
+
+  // ---- Q / K / V bottlenecks
+  const void* dQKV[3] = {dq, dk, B.dV};
+  const void* Bup[3] = {W->B_q, W->B_k, W->B_v};
+  void* dB[3] = {dW->B_q, dW->B_k, dW->B_v};
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    for (int i = 0; i < 3; ++i) {
+      if (dQKV[i] == nullptr) {
+        zero2d(c, dB[i], r * s.E, r * s.E, d);
+        continue;
+      }
+      g.p[g.nprob++] = wgrad(d, r, T, dQKV[i], d, at(A.h_qkv, i * r, s), 3 * r, dB[i], r);
+    }
+    gemm(c, s, g);
+  }
+  {
+    GemmLaunch g = launch(EPI_DSIGMA, s);
+    for (int i = 0; i < 3; ++i) {
+      if (dQKV[i] == nullptr) {
+        zero2d(c, at(B.dz_qkv, i * r, s), 3 * r * s.E, r * s.E, T);
+        continue;
+      }
+      g.p[g.nprob++] = dsigma(s, dQKV[i], d, d, Bup[i], at(A.z_qkv, i * r, s), 3 * r,
+                              at(B.dz_qkv, i * r, s), A.rstd1);
+    }
+    gemm(c, s, g);
+  }
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    g.nprob = 1;
+    g.p[0] = wgrad(3 * r, d, T, B.dz_qkv, 3 * r, x, d, dW->A_qkv, d, W->w_norm1);
+    gemm(c, s, g);
+  }
+  dx_gemm(c, s, B.dz_qkv, 3 * r, W->A_qkv, d, d, B.dn, d);
+  DT_CALL(s, normbwd, c, s, B, B.dn, x, W->w_norm1, A.rstd1, dx1, dx, dW->w_norm1);
+}
+
+void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void* x,
+                    const void* dy, const void* dq, const void* dk, void* dx,
+                    const bn_block_params* dW, const Acts& A, const Tmp& B) {
+  const int64_t T = s.T, d = s.d, dff = s.d_ff;
+  const void* x1 = s.full() ? A.x1 : x;
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    g.nprob = 1;
+    g.p[0] = wgrad(d, dff, T, dy, d, A.m, s.ld_ff, dW->A_d, s.ld_ff);
+    gemm(c, s, g);
+  }
+  {
+    // dm = dy W_d with the SwiGLU backward; rows scaled by rstd2 for the norm GEMMs
+    GemmLaunch g = launch(EPI_DSWIGLU, s);
+    g.nprob = 1;
+    GemmProblem& p = g.p[0];
+    p.M = T;
+    p.N = dff;
+    p.K = d;
+    p.a[0] = op(dy, d, KM);
+    p.b[0] = op(W->A_d, s.ld_ff, MN);
+    p.in[0] = A.G;
+    p.in[1] = A.U;
+    p.ldi[0] = p.ldi[1] = s.ld_ff;
+    p.out[0] = B.dG;
+    p.out[1] = B.dU;
+    p.ldo[0] = p.ldo[1] = s.ld_ff;
+    p.rowv = A.rstd2;
+    gemm(c, s, g);
+  }
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    g.nprob = 2;
+    g.p[0] = wgrad(dff, d, T, B.dG, s.ld_ff, x1, d, dW->A_gu, d, W->w_norm2);
+    g.p[1] = wgrad(dff, d, T, B.dU, s.ld_ff, x1, d, at(dW->A_gu, dff * d, s), d, W->w_norm2);
+    gemm(c, s, g);
+  }
+  {
+    GemmLaunch g = launch(EPI_STORE_CHAIN, s);
+    g.nprob = 1;
+    GemmProblem& p = g.p[0];
+    p.M = T;
+    p.N = d;
+    p.K = dff;
+    p.a[0] = op(B.dG, s.ld_ff, KM);
+    p.b[0] = op(W->A_gu, d, MN);
+    p.a[1] = op(B.dU, s.ld_ff, KM);
+    p.b[1] = op(at(W->A_gu, dff * d, s), d, MN);
+    p.out[0] = B.dn;
+    p.ldo[0] = d;
+    gemm(c, s, g);
+  }
+  void* dx1 = s.full() ? B.dx1 : dx;
+  DT_CALL(s, normbwd, c, s, B, B.dn, x1, W->w_norm2, A.rstd2, dy, dx1, dW->w_norm2);
+  if (!s.full()) return;
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    g.nprob = 1;
+    g.p[0] = wgrad(d, d, T, dx1, d, A.V, d, dW->A_o, d);
+    gemm(c, s, g);
+  }
+  DT_CALL(s, rowscale, c, s, dq, d, A.rstd1, d, B.dqkv, 3 * d);
+  DT_CALL(s, rowscale, c, s, dk, d, A.rstd1, d, at(B.dqkv, d, s), 3 * d);
+  dx_gemm(c, s, dx1, d, W->A_o, d, d, at(B.dqkv, 2 * d, s), 3 * d, A.rstd1);
+  {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    g.nprob = 1;
+    g.p[0] = wgrad(3 * d, d, T, B.dqkv, 3 * d, x, d, dW->A_qkv, d, W->w_norm1);
+    gemm(c, s, g);
+  }
+  dx_gemm(c, s, B.dqkv, 3 * d, W->A_qkv, d, d, B.dn, d);
+  DT_CALL(s, normbwd, c, s, B, B.dn, x, W->w_norm1, A.rstd1, dx1, dx, dW->w_norm1);
+}
+
+Ctx make_ctx(void* scratch, bn_stream_t stream, const Tmp& B) {
+  Ctx c;
+  c.stream = reinterpret_cast<cudaStream_t>(stream);
+  c.status = B.status;
+  c.num_sms = device_sms();
+  c.partial = B.partial;
+  c.partial_bytes = B.partial_bytes;
+  (void)scratch;
+  return c;
+}
+
+}  // namespace
+}  // namespace bn
+
+using namespace bn;
+
+extern "C" {
+
+bn_status bn_block_workspace_size(const bn_block_desc* desc, size_t* saved_bytes,
+                                  size_t* scratch_bytes) {
+  Shape s;
+  bn_status st = check_desc(desc, s);
+  if (st != BN_OK) return st;
+  if (saved_bytes == nullptr || scratch_bytes == nullptr) return BN_ERR_INVALID_ARG;
+  Acts A;
+  Tmp B;
+  plan(s, nullptr, nullptr, A, B, saved_bytes, scratch_bytes);
+  return BN_OK;
+}
+
+bn_status bn_block_forward(const bn_block_desc* desc, const bn_block_params* W, const void* x,
+                           void* y, void* q_out, void* k_out, void* saved, void* scratch,
+                           bn_stream_t stream) {
+  g_last_launches = 0;
+  Shape s;
+  bn_status st = check_desc(desc, s);
+  if (st != BN_OK) return st;
+  if ((st = check_params(s, W)) != BN_OK) return st;
+  if (!x || !y || !saved || !scratch) return BN_ERR_INVALID_ARG;
+  if (s.full() != (q_out != nullptr) || s.full() != (k_out != nullptr)) return BN_ERR_INVALID_ARG;
+  for (const void* p : {x, static_cast<const void*>(y), static_cast<const void*>(q_out),
+                        static_cast<const void*>(k_out), static_cast<const void*>(saved),
+                        static_cast<const void*>(scratch)})
+    if (p && !aligned(p)) return BN_ERR_ALIGNMENT;
+  Acts A;
+  Tmp B;
+  plan(s, saved, scratch, A, B, nullptr, nullptr);
+  Ctx c = make_ctx(scratch, stream, B);
+  if (s.dense)
+    forward_dense(c, s, W, x, y, q_out, k_out, A, B);
+  else
+    forward_lowrank(c, s, W, x, y, q_out, k_out, A, B);
+  return finish(c);
+}
+
+bn_status bn_block_backward(const bn_block_desc* desc, const bn_block_params* W, const void* x,
+                            const void* saved, const void* dy, const void* dq, const void* dk,
+                            void* dx, const bn_block_params* dW, void* scratch,
+                            bn_stream_t stream) {
+  g_last_launches = 0;
+  Shape s;
+  bn_status st = check_desc(desc, s);
+  if (st != BN_OK) return st;
+  if ((st = check_params(s, W)) != BN_OK) return st;
+  if ((st = check_params(s, dW)) != BN_OK) return st;
+  if (!x || !saved || !dy || !dx || !scratch) return BN_ERR_INVALID_ARG;
+  if (!s.full() && (dq || dk)) return BN_ERR_INVALID_ARG;
+  for (const void* p : {x, saved, dy, dq, dk, static_cast<const void*>(dx),
+                        static_cast<const void*>(scratch)})
+    if (p && !aligned(p)) return BN_ERR_ALIGNMENT;
+  Acts A;
+  Tmp B;
+  plan(s, const_cast<void*>(saved), scratch, A, B, nullptr, nullptr);
+  Ctx c = make_ctx(scratch, stream, B);
+  if (s.ckpt) recompute(c, s, W, x, A);
+  if (s.dense)
+    backward_dense(c, s, W, x, dy, dq, dk, dx, dW, A, B);
+  else
+    backward_lowrank(c, s, W, x, dy, dq, dk, dx, dW, A, B);
+  return finish(c);
+}
+
+bn_status bn_get_device_status(void* scratch, bn_stream_t stream) {
+  if (scratch == nullptr) return BN_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int word = 0;
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemcpy(&word, scratch, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(scratch, 0, sizeof(int));
+  if (e != cudaSuccess) {
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "%s", cudaGetErrorString(e));
+    return BN_ERR_CUDA;
+  }
+  return (word & kStatusTimeout) ? BN_ERR_TIMEOUT : BN_OK;
+}
+
+int bn_last_launch_count(void) { return g_last_launches; }
+
+const char* bn_status_string(bn_status s) {
+  switch (s) {
+    case BN_OK: return "BN_OK";
+    case BN_ERR_INVALID_ARG: return "BN_ERR_INVALID_ARG";
+    case BN_ERR_ALIGNMENT: return "BN_ERR_ALIGNMENT";
+    case BN_ERR_UNSUPPORTED: return "BN_ERR_UNSUPPORTED";
+    case BN_ERR_CUDA: return "BN_ERR_CUDA";
+    case BN_ERR_TIMEOUT: return "BN_ERR_TIMEOUT";
+  }
+  return "unknown bn_status";
+}
+
+const char* bn_last_cuda_error(void) { return g_cuda_err; }
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+// Device helpers shared by the block library's kernels: element conversion,
+// the bottleneck nonlinearities, the device status word and bounded waits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bn {
+
+// Device status word bits (first word of the caller's scratch buffer).
+constexpr int kStatusTimeout = 1;
+
+// Upper limit of any single wait inside a kernel. Legitimate waits last
+// microseconds; after this much wall time the kernel records a timeout,
+// unwinds and returns instead of spinning on.
+constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// element conversion
+// ---------------------------------------------------------------------------
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+// Round a float to the storage precision of T and back.
+template <typename T> __device__ __forceinline__ float round_to(float v) {
+  return to_f<T>(from_f<T>(v));
+}
+
+// ---------------------------------------------------------------------------
+// nonlinearities. Written with explicit round-to-nearest intrinsics so that
+// every kernel that evaluates them (GEMM epilogues, the recompute kernel of
+// checkpoint mode) produces bit-identical results: no FMA contraction can
+// differ between call sites.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float sigmoid_f(float z) {
+  return __frcp_rn(__fadd_rn(1.0f, expf(-z)));
+}
+__device__ __forceinline__ float silu_f(float z) { return __fmul_rn(z, sigmoid_f(z)); }
+// d/dz SiLU(z) = s (1 + z (1 - s)), s = sigmoid(z)
+__device__ __forceinline__ float silu_grad_f(float z) {
+  float s = sigmoid_f(z);
+  return __fmul_rn(s, __fadd_rn(1.0f, __fmul_rn(z, __fsub_rn(1.0f, s))));
+}
+// sigma: 0 = identity, 1 = SiLU (bn_sigma)
+__device__ __forceinline__ float act_f(float z, int sigma) { return sigma ? silu_f(z) : z; }
+__device__ __forceinline__ float act_grad_f(float z, int sigma) {
+  return sigma ? silu_grad_f(z) : 1.0f;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// 8-element vectors (16 bytes of bf16, 32 bytes of fp32)
+// ---------------------------------------------------------------------------
+template <typename T> struct Vec8;
+template <> struct Vec8<__nv_bfloat16> {
+  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float* f) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 t = __bfloat1622float2(h[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  __device__ __forceinline__ static void store(__nv_bfloat16* p, const float* f) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    *reinterpret_cast<uint4*>(p) = u;
+  }
+};
+template <> struct Vec8<float> {
+  __device__ __forceinline__ static void load(const float* p, float* f) {
+    float4 a = *reinterpret_cast<const float4*>(p);
+    float4 b = *reinterpret_cast<const float4*>(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+  __device__ __forceinline__ static void store(float* p, const float* f) {
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
+  }
+};
+
+}  // namespace bn

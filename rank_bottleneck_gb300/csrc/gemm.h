@@ -1,0 +1,93 @@
+// Internal interface between the block scheduler and the two GEMM engines
+// (tcgen05 tensor cores for bf16, FFMA for fp32). Not part of the public ABI.
+//
+// Every GEMM computes, per problem, acc[i, j] = sum_k Aop[i, k] * Bop[j, k]
+// for i < M, j < N, k < K, and hands acc to a fused epilogue.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bn {
+
+enum Epi : int {
+  // out0 = acc * rowv[i] * colv[j]  (rowv fp32, colv element type; each optional).
+  // The tensor-core engine may split K across CTAs for it when allow_split is set.
+  EPI_STORE = 0,
+  // out0 = z = acc; out1 = h = sigma(z), sigma evaluated on z as stored.
+  EPI_SIGMA = 1,
+  // Online RMSNorm over S emulated shards of K (see ONLINE NORM below), then as
+  // EPI_SIGMA; out1 may be null (no sigma: the dense block).
+  EPI_NORM = 2,
+  // out0 = in0 + acc (residual add).
+  EPI_RESID = 3,
+  // Two segments: G from (a[0], b[0]), U from (a[1], b[1]).
+  // out0 = G, out1 = U (each optional), out2 = m = SiLU(G) * U (G, U as stored).
+  EPI_SWIGLU = 4,
+  // out0 = acc * sigma'(in0) * rowv[i]  (rowv optional): the bottleneck gradient dz.
+  EPI_DSIGMA = 5,
+  // dm = acc; in0 = G, in1 = U: out0 = dm U SiLU'(G) * rowv[i], out1 = dm SiLU(G) * rowv[i].
+  EPI_DSWIGLU = 6,
+  // Two segments accumulated into one sum (K split over two operand pairs), then as EPI_STORE.
+  EPI_STORE_CHAIN = 7,
+};
+// ONLINE NORM. rowv = ss [M, S] fp32 holds each row's sum of squares over each
+// of S equal shards of K (the raw input, before the norm weight). For shard s:
+//   rms_s = sqrt(ss_s / (K/S) + eps),  rms_g = sqrt(sum_s ss_s / K + eps)
+//   L_s   = P_s / rms_s           (the shard's partial product, locally normalised)
+//   z    += (rms_s / rms_g) * L_s (the per-row correction alpha = rms_s / rms_g)
+// where P_s is the GEMM over shard s's K range. The norm weight is folded into
+// the B operand by the caller.
+
+struct Operand {
+  const void* ptr = nullptr;
+  int64_t ld = 0;         // elements between consecutive stored rows
+  bool mn_major = false;  // false: stored [MN, K] (K contiguous); true: stored [K, MN]
+};
+
+struct GemmProblem {
+  int64_t M = 0, N = 0, K = 0;
+  Operand a[2], b[2];
+  void* out[3] = {nullptr, nullptr, nullptr};
+  int64_t ldo[3] = {0, 0, 0};
+  const void* in[2] = {nullptr, nullptr};
+  int64_t ldi[2] = {0, 0};
+  const float* rowv = nullptr;
+  const void* colv = nullptr;
+};
+
+struct GemmLaunch {
+  Epi epi = EPI_STORE;
+  int sigma = 0;      // bn_sigma
+  int S = 1;          // shards of the online norm
+  float eps = 1e-5f;
+  bool allow_split = false;  // EPI_STORE only: K may be split (deterministic reduction)
+  int nprob = 0;
+  GemmProblem p[3];
+};
+
+struct Ctx {
+  cudaStream_t stream = nullptr;
+  int* status = nullptr;       // device status word
+  int num_sms = 148;
+  float* partial = nullptr;    // split-K workspace (fp32)
+  size_t partial_bytes = 0;
+  int launches = 0;
+  cudaError_t err = cudaSuccess;
+  int bad = 0;                 // a bn_status other than BN_OK raised inside a launcher
+};
+
+// Record the result of a kernel launch.
+inline void note_launch(Ctx& c) {
+  ++c.launches;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess && c.err == cudaSuccess) c.err = e;
+}
+
+void gemm_tc(Ctx& c, const GemmLaunch& g);    // bf16 operands, tcgen05
+void gemm_simt(Ctx& c, const GemmLaunch& g);  // fp32 operands, FFMA
+
+// Largest split-K workspace gemm_tc may use for a GEMM of this size.
+size_t gemm_tc_partial_bytes(int64_t M, int64_t N, int num_sms);
+
+}  // namespace bn

@@ -1,0 +1,215 @@
+// Host side of the tcgen05 GEMM engine: tensor-map encoding, tile-width and
+// split-K choice, launch, and the deterministic split-K reduction.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "gemm.h"
+#include "gemm_tc_launch.h"
+#include "rowops.h"
+
+namespace bn {
+namespace tc {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major matrix [outer, inner] with row stride ld.
+static bool encode(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
+                   uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand of logical shape [mn, K]: K-major tiles are one box of 64 (K) x box_mn
+// rows; MN-major tiles are boxes of 64 (MN) x 64 (K).
+static bool encode_operand(CUtensorMap* m, const Operand& op, int64_t mn, int64_t K, int box_mn) {
+  if (op.ptr == nullptr || (reinterpret_cast<uintptr_t>(op.ptr) & 15) || (op.ld * 2) % 16)
+    return false;
+  if (!op.mn_major) return encode(m, op.ptr, K, mn, op.ld, 64, static_cast<uint32_t>(box_mn));
+  return encode(m, op.ptr, mn, K, op.ld, 64, 64);
+}
+
+static int epi_kind(Epi e) {
+  switch (e) {
+    case EPI_STORE: return K_STORE;
+    case EPI_SIGMA: return K_SIGMA;
+    case EPI_NORM: return K_NORM;
+    case EPI_RESID: return K_RESID;
+    case EPI_SWIGLU: return K_SWIGLU;
+    case EPI_DSIGMA: return K_DSIGMA;
+    case EPI_DSWIGLU: return K_DSWIGLU;
+    case EPI_STORE_CHAIN: return K_CHAIN;
+  }
+  return -1;
+}
+
+static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+static int64_t ldp_of(int64_t N) { return cdiv(N, 8) * 8; }
+
+// Split count minimising rounds x (k-blocks per split) plus the reduction's
+// HBM traffic, all in units of one 128 x BN x 64 k-block on one SM.
+static int choose_splits(int64_t tiles, int64_t nkb, int64_t MN_total, int grid, int BN,
+                         size_t cap_bytes) {
+  const double t_kb_us = 2.0 * 128 * BN * 64 / (1.6e15 / grid) * 1e6;
+  double best = 1e300;
+  int best_s = 1;
+  for (int s = 1; s <= 16; ++s) {
+    const int64_t per = cdiv(nkb, s);
+    if (s > 1 && per < 4) break;
+    const int64_t eff = cdiv(nkb, per);
+    if (eff != s) continue;
+    if (s > 1 && static_cast<size_t>(s) * MN_total * 4 > cap_bytes) break;
+    const double rounds = static_cast<double>(cdiv(tiles * s, grid));
+    double t = rounds * per * t_kb_us;
+    if (s > 1) t += (8.0 * s + 2.0) * MN_total / 6.0e12 * 1e6;
+    if (t < best * 0.97) {
+      best = t;
+      best_s = s;
+    }
+  }
+  return best_s;
+}
+
+}  // namespace tc
+
+size_t gemm_tc_partial_bytes(int64_t M, int64_t N, int num_sms) {
+  (void)num_sms;
+  return static_cast<size_t>(16) * M * tc::ldp_of(N) * 4;
+}
+
+void gemm_tc(Ctx& c, const GemmLaunch& g) {
+  using namespace tc;
+  int ek = epi_kind(g.epi);
+  if (ek < 0 || g.nprob < 1 || g.nprob > 3) {
+    c.bad = 1;
+    return;
+  }
+  // tile width: Online RMSNorm and SwiGLU keep a 128-column accumulator per thread
+  // row in registers / pair two slots, everything else prefers 256 when N allows
+  int BN = 256;
+  for (int i = 0; i < g.nprob; ++i)
+    if (g.p[i].N < 256) BN = 128;
+  if (ek == K_NORM || ek == K_SWIGLU) BN = 128;
+
+  thread_local static Params P;  // large kernel parameter block, filled per call
+  std::memset(&P, 0, sizeof(P));
+  P.nprob = g.nprob;
+  P.S = g.S;
+  P.sigma = g.sigma;
+  P.eps = g.eps;
+  P.status = c.status;
+
+  const bool a_mn = g.p[0].a[0].mn_major, b_mn = g.p[0].b[0].mn_major;
+  int64_t tiles_total = 0, mn_total = 0, nkb_max = 0;
+  for (int i = 0; i < g.nprob; ++i) {
+    const GemmProblem& q = g.p[i];
+    if (q.M <= 0 || q.N <= 0 || q.K <= 0 || q.a[0].mn_major != a_mn || q.b[0].mn_major != b_mn) {
+      c.bad = 1;
+      return;
+    }
+    tiles_total += cdiv(q.M, BM) * cdiv(q.N, BN);
+    mn_total += q.M * ldp_of(q.N);
+    nkb_max = std::max(nkb_max, cdiv(q.K, BK));
+  }
+  int splits = 1;
+  if (ek == K_STORE && g.allow_split) {
+    bool plain = true;
+    for (int i = 0; i < g.nprob; ++i) plain = plain && g.p[i].rowv == nullptr;
+    if (plain)
+      splits = choose_splits(tiles_total, nkb_max, mn_total, c.num_sms, BN, c.partial_bytes);
+  }
+  const bool split = splits > 1;
+  if (split) ek = K_PART;
+
+  int units = 0;
+  size_t part_off = 0;
+  for (int i = 0; i < g.nprob; ++i) {
+    const GemmProblem& q = g.p[i];
+    Prob& p = P.p[i];
+    const int npair = (ek == K_SWIGLU || ek == K_CHAIN) ? 2 : 1;
+    for (int j = 0; j < npair; ++j) {
+      if (!encode_operand(&p.ma[j], q.a[j], q.M, q.K, BM) ||
+          !encode_operand(&p.mb[j], q.b[j], q.N, q.K, BN)) {
+        c.bad = 2;
+        return;
+      }
+      p.nkb[j] = static_cast<int>(cdiv(q.K, BK));
+    }
+    if (ek == K_NORM && (q.K % (BK * g.S) != 0)) {
+      c.bad = 3;
+      return;
+    }
+    p.M = q.M;
+    p.N = q.N;
+    p.K = q.K;
+    for (int j = 0; j < 3; ++j) {
+      p.out[j] = q.out[j];
+      p.ldo[j] = q.ldo[j];
+    }
+    for (int j = 0; j < 2; ++j) {
+      p.in[j] = q.in[j];
+      p.ldi[j] = q.ldi[j];
+    }
+    p.rowv = q.rowv;
+    p.colv = q.colv;
+    p.tiles_m = static_cast<int>(cdiv(q.M, BM));
+    p.tiles_n = static_cast<int>(cdiv(q.N, BN));
+    p.kb_per_split = static_cast<int>(cdiv(p.nkb[0], splits));
+    p.splits = static_cast<int>(cdiv(p.nkb[0], p.kb_per_split));
+    if (split) {
+      p.out[0] = reinterpret_cast<char*>(c.partial) + part_off;
+      p.ldo[0] = ldp_of(q.N);
+      part_off += static_cast<size_t>(p.splits) * q.M * p.ldo[0] * 4;
+    }
+    p.unit_begin = units;
+    units += p.tiles_m * p.tiles_n * (split ? p.splits : 1);
+  }
+  if (split && part_off > c.partial_bytes) {
+    c.bad = 4;
+    return;
+  }
+  P.total_units = units;
+  const int grid = std::min(units, c.num_sms);
+  const bool ok = (BN == 256) ? launch_bn256(ek, a_mn, b_mn, P, grid, c.stream)
+                              : launch_bn128(ek, a_mn, b_mn, P, grid, c.stream);
+  if (!ok) {
+    c.bad = 5;
+    return;
+  }
+  note_launch(c);
+  if (split) {
+    for (int i = 0; i < g.nprob; ++i) {
+      const Prob& p = P.p[i];
+      launch_splitk_reduce(c, static_cast<const float*>(p.out[0]), p.splits, p.M, p.N, p.ldo[0],
+                           static_cast<const __nv_bfloat16*>(g.p[i].colv),
+                           static_cast<__nv_bfloat16*>(g.p[i].out[0]), g.p[i].ldo[0]);
+    }
+  }
+}
+
+}  // namespace bn

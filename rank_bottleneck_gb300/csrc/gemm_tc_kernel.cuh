@@ -1,0 +1,643 @@
+// tcgen05 / TMA / TMEM GEMM engine for sm_103a with fused epilogues.
+//
+// One persistent CTA per SM (192 threads):
+//   warp 0        TMA producer: fills a ring of shared-memory stages, each one
+//                 128 x 64 tile of A and one BN x 64 tile of B (bf16, 128-byte
+//                 swizzle), completion tracked by an mbarrier per stage;
+//   warp 1        owns the TMEM allocation (all 512 columns) and, from one
+//                 thread, issues tcgen05.mma (M = 128, N = BN, K = 16, fp32
+//                 accumulate) into a ring of TMEM accumulator slots of BN
+//                 columns; tcgen05.commit frees a stage / publishes a slot;
+//   warps 2..5    epilogue: tcgen05.ld each slot (warp w reads TMEM lanes
+//                 32 (w % 4) .. +31, i.e. one tile row per thread), apply the
+//                 fused epilogue, store to global memory, free the slot.
+// A work unit is one 128 x BN output tile (or one K split of it). A unit is a
+// sequence of segments; each segment is a K range, possibly of another operand
+// pair, and lands in its own slot: this is how Online RMSNorm sees each
+// emulated shard's partial product and how SwiGLU sees G and U side by side.
+//
+// Every mbarrier wait is bounded by wall time (kWaitLimitNs). On expiry the
+// thread sets a CTA-wide abort flag and the device status word, all roles
+// unwind, outstanding TMA copies and MMAs are drained (bounded), TMEM is
+// freed and the kernel returns.
+#pragma once
+
+#include <cuda.h>
+#include "common.cuh"
+
+namespace bn {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
+constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 4;
+
+// epilogue kinds of the kernel template
+enum : int {
+  K_STORE = 0, K_PART = 1, K_SIGMA = 2, K_NORM = 3, K_RESID = 4, K_SWIGLU = 5,
+  K_DSIGMA = 6, K_DSWIGLU = 7, K_CHAIN = 8
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int NSLOT = 512 / BN;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+};
+
+struct Prob {
+  CUtensorMap ma[2];  // A operand of segment pair 0 / 1
+  CUtensorMap mb[2];  // B operand of segment pair 0 / 1
+  int64_t M, N, K;
+  void* out[3];
+  int64_t ldo[3];
+  const void* in[2];
+  int64_t ldi[2];
+  const float* rowv;
+  const void* colv;
+  int tiles_m, tiles_n, unit_begin;
+  int nkb[2];         // k-blocks of operand pair 0 / 1
+  int splits, kb_per_split;
+};
+
+struct Params {
+  Prob p[3];
+  int nprob, total_units, S, sigma;
+  float eps;
+  int* status;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `bar` with parity `parity` to complete.
+static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      int* status, unsigned long long limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, one 128 x N x 16 step, issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane, waited for in the same statement.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor (tcgen05 format) of a 128-byte-swizzled tile.
+//  K-major:  rows of 64 bf16 (128 B), 8-row swizzle atoms 1024 B apart (SBO);
+//  MN-major: rows of 64 MN-contiguous bf16 per k, 8-k atoms 1024 B apart (SBO),
+//            64-element MN atoms 8192 B apart (LBO) -- one TMA box of 64 x 64.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, bool mn_major) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(mn_major ? (8192u >> 4) : 1u) << 16;  // leading byte offset
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;                     // stride byte offset
+  d |= 1ull << 46;                                                   // descriptor version
+  d |= 2ull << 61;                                                   // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, dense.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// epilogue I/O of one 32-column chunk of one row
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void st_chunk(__nv_bfloat16* base, int64_t ld, int64_t row,
+                                         int64_t col0, int64_t M, int64_t N, const float* v) {
+  if (base == nullptr || row >= M) return;
+  __nv_bfloat16* p = base + row * ld + col0;
+  if (col0 + 32 <= N) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) Vec8<__nv_bfloat16>::store(p + 8 * i, v + 8 * i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < N) p[i] = __float2bfloat16_rn(v[i]);
+  }
+}
+__device__ __forceinline__ void st_chunk_f32(float* base, int64_t ld, int64_t row, int64_t col0,
+                                             int64_t M, int64_t N, const float* v) {
+  if (row >= M) return;
+  float* p = base + row * ld + col0;
+  if (col0 + 32 <= N) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) Vec8<float>::store(p + 8 * i, v + 8 * i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < N) p[i] = v[i];
+  }
+}
+__device__ __forceinline__ void ld_chunk(const __nv_bfloat16* base, int64_t ld, int64_t row,
+                                         int64_t col0, int64_t M, int64_t N, float* v) {
+  if (row >= M) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+    return;
+  }
+  const __nv_bfloat16* p = base + row * ld + col0;
+  if (col0 + 32 <= N) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) Vec8<__nv_bfloat16>::load(p + 8 * i, v + 8 * i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = (col0 + i < N) ? __bfloat162float(p[i]) : 0.f;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// work decomposition
+// ---------------------------------------------------------------------------
+struct Work {
+  int pi, split;
+  int64_t m0, n0;
+};
+
+__device__ __forceinline__ Work decode(const Params& P, int u) {
+  int pi = 0;
+  while (pi + 1 < P.nprob && u >= P.p[pi + 1].unit_begin) ++pi;
+  const Prob& pr = P.p[pi];
+  const int local = u - pr.unit_begin;
+  const int tiles = pr.tiles_m * pr.tiles_n;
+  Work w;
+  w.pi = pi;
+  w.split = local / tiles;
+  const int t = local - w.split * tiles;
+  w.m0 = static_cast<int64_t>(t / pr.tiles_n) * BM;
+  w.n0 = t % pr.tiles_n;  // n-block index; the kernel scales it by BN
+  return w;
+}
+
+template <int EK>
+__device__ __forceinline__ int num_segments(const Params& P) {
+  return EK == K_NORM ? P.S : (EK == K_SWIGLU || EK == K_CHAIN) ? 2 : 1;
+}
+// k-block range and operand pair of segment s of a unit
+template <int EK>
+__device__ __forceinline__ void segment(const Params& P, const Prob& pr, int split, int s,
+                                        int& kb0, int& nkb, int& pair) {
+  if (EK == K_NORM) {
+    const int per = pr.nkb[0] / P.S;
+    kb0 = s * per;
+    nkb = per;
+    pair = 0;
+  } else if (EK == K_SWIGLU || EK == K_CHAIN) {
+    kb0 = 0;
+    nkb = pr.nkb[s];
+    pair = s;
+  } else {
+    kb0 = split * pr.kb_per_split;
+    nkb = min(pr.kb_per_split, pr.nkb[0] - kb0);
+    pair = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int BN, int EK, bool AMN, bool BMN>
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Params P) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* accf = empty + C::STAGES;
+  uint64_t* acce = accf + C::NSLOT;
+  uint64_t* drain = acce + C::NSLOT;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    for (int i = 0; i < C::NSLOT; ++i) {
+      mbar_init(smem_u32(&accf[i]), 1);
+      mbar_init(smem_u32(&acce[i]), NUM_EPI_WARPS);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nseg = num_segments<EK>(P);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int i = 0; i < P.nprob; ++i) {
+        tma_prefetch_desc(&P.p[i].ma[0]);
+        tma_prefetch_desc(&P.p[i].mb[0]);
+      }
+      int stage = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x) {
+        const Work w = decode(P, u);
+        const Prob& pr = P.p[w.pi];
+        const int m0 = static_cast<int>(w.m0);
+        const int n0 = static_cast<int>(w.n0) * BN;
+        for (int s = 0; ok && s < nseg; ++s) {
+          int kb0, nkb, pair;
+          segment<EK>(P, pr, w.split, s, kb0, nkb, pair);
+          const CUtensorMap* ma = &pr.ma[pair];
+          const CUtensorMap* mb = &pr.mb[pair];
+          for (int kb = kb0; kb < kb0 + nkb; ++kb) {
+            if (!wait_bar(smem_u32(&empty[stage]), ph ^ 1u, abort_flag, P.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+            const uint32_t sb = sa + C::A_BYTES;
+            const uint32_t fb = smem_u32(&full[stage]);
+            mbar_expect_tx(fb, C::STAGE_BYTES);
+            const int k0 = kb * BK;
+            if (AMN) {
+              tma_load_2d(sa, ma, m0, k0, fb);
+              tma_load_2d(sa + 8192, ma, m0 + 64, k0, fb);
+            } else {
+              tma_load_2d(sa, ma, k0, m0, fb);
+            }
+            if (BMN) {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, mb, n0 + 64 * j, k0, fb);
+            } else {
+              tma_load_2d(sb, mb, k0, n0, fb);
+            }
+            ++issued;
+            if (++stage == C::STAGES) {
+              stage = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // drain: the last phase issued on each stage must land before the CTA exits
+        int st = stage;
+        uint32_t p = ph;
+        for (int i = 0; i < C::STAGES && i < issued; ++i) {
+          if (--st < 0) {
+            st = C::STAGES - 1;
+            p ^= 1u;
+          }
+          wait_bar(smem_u32(&full[st]), p, abort_flag, P.status, 50ull * 1000 * 1000);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = instr_desc(BM, BN, AMN, BMN);
+      int stage = 0;
+      uint32_t ph = 0;
+      int slot = 0;
+      uint32_t sph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x) {
+        const Work w = decode(P, u);
+        const Prob& pr = P.p[w.pi];
+        for (int s = 0; ok && s < nseg; ++s) {
+          int kb0, nkb, pair;
+          segment<EK>(P, pr, w.split, s, kb0, nkb, pair);
+          const bool fresh = !(EK == K_CHAIN && s == 1);
+          if (fresh) {
+            if (!wait_bar(smem_u32(&acce[slot]), sph ^ 1u, abort_flag, P.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          const uint32_t d_tmem = tmem + static_cast<uint32_t>(slot * BN);
+          for (int i = 0; i < nkb; ++i) {
+            if (!wait_bar(smem_u32(&full[stage]), ph, abort_flag, P.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+            const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t ad = smem_desc(sa + (AMN ? kk * 2048 : kk * 32), AMN);
+              const uint64_t bd = smem_desc(sb + (BMN ? kk * 2048 : kk * 32), BMN);
+              mma_bf16(d_tmem, ad, bd, IDESC, (fresh && i == 0 && kk == 0) ? 0u : 1u);
+            }
+            mma_commit(smem_u32(&empty[stage]));
+            if (++stage == C::STAGES) {
+              stage = 0;
+              ph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          if (!(EK == K_CHAIN && s == 0)) {
+            mma_commit(smem_u32(&accf[slot]));
+            if (++slot == C::NSLOT) {
+              slot = 0;
+              sph ^= 1u;
+            }
+          }
+        }
+      }
+      // every MMA issued must complete before TMEM is released
+      mma_commit(smem_u32(drain));
+      wait_bar(smem_u32(drain), 0, abort_flag, P.status, ok ? kWaitLimitNs : 50ull * 1000 * 1000);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    int slot = 0;
+    uint32_t sph = 0;
+    bool ok = true;
+    auto acquire = [&](int sl, uint32_t p) -> bool {
+      if (!wait_bar(smem_u32(&accf[sl]), p, abort_flag, P.status)) return false;
+      tc_fence_after();
+      return true;
+    };
+    auto release = [&](int sl) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acce[sl]));
+    };
+    auto advance = [&]() {
+      if (++slot == C::NSLOT) {
+        slot = 0;
+        sph ^= 1u;
+      }
+    };
+    for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x) {
+      const Work w = decode(P, u);
+      const Prob& pr = P.p[w.pi];
+      const int64_t row = w.m0 + q * 32 + lane;
+      const int64_t n0 = w.n0 * BN;
+      const int64_t M = pr.M, N = pr.N;
+      if constexpr (EK == K_NORM) {
+        // Online RMSNorm: fold each shard's partial product with its own factors
+        float R[BN];
+        const int S = P.S;
+        const float* ss = pr.rowv + (row < M ? row : 0) * S;
+        float tot = 0.f;
+        for (int s = 0; s < S; ++s) tot += (row < M) ? ss[s] : 0.f;
+        const float shard_w = static_cast<float>(pr.K / S);
+        const float rms_g = sqrtf(tot / static_cast<float>(pr.K) + P.eps);
+        for (int s = 0; s < S; ++s) {
+          if (!acquire(slot, sph)) {
+            ok = false;
+            break;
+          }
+          const float ss_s = (row < M) ? ss[s] : 0.f;
+          const float rms_s = sqrtf(ss_s / shard_w + P.eps);
+          const float inv_local = 1.0f / rms_s;    // local normalisation
+          const float alpha = rms_s / rms_g;       // per-row correction
+          const uint32_t t0 = tmem + lane_base + static_cast<uint32_t>(slot * BN);
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(t0 + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float local = v[i] * inv_local;
+              R[c * 32 + i] = (s == 0) ? alpha * local : fmaf(alpha, local, R[c * 32 + i]);
+            }
+          }
+          release(slot);
+          advance();
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          float z[32], h[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            z[i] = round_to<__nv_bfloat16>(R[c * 32 + i]);
+            h[i] = act_f(z[i], P.sigma);
+          }
+          st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, n0 + c * 32, M, N, z);
+          st_chunk(static_cast<__nv_bfloat16*>(pr.out[1]), pr.ldo[1], row, n0 + c * 32, M, N, h);
+        }
+      } else if constexpr (EK == K_SWIGLU) {
+        const int sg = slot;
+        const uint32_t pg = sph;
+        advance();
+        const int su = slot;
+        const uint32_t pu = sph;
+        advance();
+        if (!acquire(sg, pg) || !acquire(su, pu)) {
+          ok = false;
+          break;
+        }
+        const uint32_t tg = tmem + lane_base + static_cast<uint32_t>(sg * BN);
+        const uint32_t tu = tmem + lane_base + static_cast<uint32_t>(su * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float G[32], U[32], m[32];
+          tmem_ld32(tg + c * 32, G);
+          tmem_ld32(tu + c * 32, U);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            G[i] = round_to<__nv_bfloat16>(G[i]);
+            U[i] = round_to<__nv_bfloat16>(U[i]);
+            m[i] = __fmul_rn(silu_f(G[i]), U[i]);
+          }
+          const int64_t col = n0 + c * 32;
+          st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, G);
+          st_chunk(static_cast<__nv_bfloat16*>(pr.out[1]), pr.ldo[1], row, col, M, N, U);
+          st_chunk(static_cast<__nv_bfloat16*>(pr.out[2]), pr.ldo[2], row, col, M, N, m);
+        }
+        release(sg);
+        release(su);
+      } else {
+        if (!acquire(slot, sph)) {
+          ok = false;
+          break;
+        }
+        const uint32_t t0 = tmem + lane_base + static_cast<uint32_t>(slot * BN);
+        float rs = 1.f;
+        if ((EK == K_STORE || EK == K_CHAIN || EK == K_DSIGMA || EK == K_DSWIGLU) &&
+            pr.rowv != nullptr && row < M)
+          rs = pr.rowv[row];
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(t0 + c * 32, v);
+          const int64_t col = n0 + c * 32;
+          if constexpr (EK == K_PART) {
+            float* base = static_cast<float*>(pr.out[0]) + static_cast<int64_t>(w.split) * M * pr.ldo[0];
+            st_chunk_f32(base, pr.ldo[0], row, col, M, N, v);
+          } else if constexpr (EK == K_STORE || EK == K_CHAIN) {
+            if (pr.colv != nullptr) {
+              float cv[32];
+              ld_chunk(static_cast<const __nv_bfloat16*>(pr.colv), 0, 0, col, 1, N, cv);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= cv[i];
+            }
+            if (pr.rowv != nullptr) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= rs;
+            }
+            st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, v);
+          } else if constexpr (EK == K_SIGMA) {
+            float h[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              v[i] = round_to<__nv_bfloat16>(v[i]);
+              h[i] = act_f(v[i], P.sigma);
+            }
+            st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, v);
+            st_chunk(static_cast<__nv_bfloat16*>(pr.out[1]), pr.ldo[1], row, col, M, N, h);
+          } else if constexpr (EK == K_RESID) {
+            float r[32];
+            ld_chunk(static_cast<const __nv_bfloat16*>(pr.in[0]), pr.ldi[0], row, col, M, N, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += r[i];
+            st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, v);
+          } else if constexpr (EK == K_DSIGMA) {
+            float z[32];
+            ld_chunk(static_cast<const __nv_bfloat16*>(pr.in[0]), pr.ldi[0], row, col, M, N, z);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = (v[i] * act_grad_f(z[i], P.sigma)) * rs;
+            st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, v);
+          } else if constexpr (EK == K_DSWIGLU) {
+            float G[32], U[32], dU[32];
+            ld_chunk(static_cast<const __nv_bfloat16*>(pr.in[0]), pr.ldi[0], row, col, M, N, G);
+            ld_chunk(static_cast<const __nv_bfloat16*>(pr.in[1]), pr.ldi[1], row, col, M, N, U);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              dU[i] = (v[i] * silu_f(G[i])) * rs;
+              v[i] = ((v[i] * U[i]) * silu_grad_f(G[i])) * rs;
+            }
+            st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, v);
+            st_chunk(static_cast<__nv_bfloat16*>(pr.out[1]), pr.ldo[1], row, col, M, N, dU);
+          }
+        }
+        release(slot);
+        advance();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace tc
+}  // namespace bn

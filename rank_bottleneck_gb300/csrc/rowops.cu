@@ -1,0 +1,265 @@
+// Row-wise kernels of the block: shard statistics of Online RMSNorm, the
+// RMSNorm backward, the split-K reduction and small elementwise passes.
+// All are HBM-bound: 16-byte vector loads, one warp per row, warp-shuffle
+// reductions, and fixed reduction orders (results are bit-reproducible).
+#include <algorithm>
+
+#include "common.cuh"
+#include "rowops.h"
+
+namespace bn {
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------------------------
+// F0: per-row, per-shard sums of squares (one warp per row)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) stats_kernel(const T* __restrict__ x, int64_t rows, int d,
+                                                    int S, float eps, float* __restrict__ ss,
+                                                    float* __restrict__ rstd) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (row >= rows) return;
+  const T* xr = x + row * d;
+  const int w = d / S;
+  float tot = 0.f;
+  for (int s = 0; s < S; ++s) {
+    float acc = 0.f;
+    for (int c = s * w + lane * 8; c < (s + 1) * w; c += 256) {
+      float v[8];
+      Vec8<T>::load(xr + c, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc = fmaf(v[i], v[i], acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) ss[row * S + s] = acc;
+    tot += acc;
+  }
+  if (lane == 0) rstd[row] = 1.0f / sqrtf(tot / static_cast<float>(d) + eps);
+}
+
+template <typename T>
+void launch_stats(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float eps, float* ss,
+                  float* rstd) {
+  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  stats_kernel<T><<<grid, 256, 0, c.stream>>>(x, rows, static_cast<int>(d), S, eps, ss, rstd);
+  note_launch(c);
+}
+
+// ---------------------------------------------------------------------------
+// weight fold: out = A diag(w)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void fold_cols_kernel(const T* __restrict__ A, const T* __restrict__ w, int64_t rows,
+                                 int64_t cols, T* __restrict__ out) {
+  const int64_t nvec = cols / 8;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows * nvec;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / nvec, c = (i - r * nvec) * 8;
+    float a[8], ww[8];
+    Vec8<T>::load(A + r * cols + c, a);
+    Vec8<T>::load(w + c, ww);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] *= ww[k];
+    Vec8<T>::store(out + r * cols + c, a);
+  }
+}
+
+template <typename T>
+void launch_fold_cols(Ctx& c, const T* A, const T* w, int64_t rows, int64_t cols, T* out) {
+  const int64_t n = rows * (cols / 8);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 8));
+  fold_cols_kernel<T><<<grid, 256, 0, c.stream>>>(A, w, rows, cols, out);
+  note_launch(c);
+}
+
+// ---------------------------------------------------------------------------
+// B3: RMSNorm backward. One warp per row; each warp keeps its own column
+// accumulators for dw in shared memory (lane-exclusive columns, no atomics),
+// summed over the 4 warps and then over blocks in a fixed order.
+// ---------------------------------------------------------------------------
+constexpr int kNormBwdWarps = 4;
+
+template <typename T>
+__global__ void __launch_bounds__(kNormBwdWarps * 32)
+    norm_bwd_kernel(const T* __restrict__ dn, const T* __restrict__ x, const T* __restrict__ w,
+                    const float* __restrict__ rstd, const T* __restrict__ dres, int64_t rows,
+                    int d, T* __restrict__ dx, float* __restrict__ part) {
+  extern __shared__ float acc[];  // [kNormBwdWarps][d]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kNormBwdWarps * d; i += blockDim.x) acc[i] = 0.f;
+  __syncthreads();
+  float* my = acc + warp * d;
+  const float inv_d = 1.0f / static_cast<float>(d);
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kNormBwdWarps + warp; row < rows;
+       row += static_cast<int64_t>(gridDim.x) * kNormBwdWarps) {
+    const T* dnr = dn + row * d;
+    const T* xr = x + row * d;
+    float s = 0.f;
+    for (int c = lane * 8; c < d; c += 256) {
+      float a[8], b[8], ww[8];
+      Vec8<T>::load(dnr + c, a);
+      Vec8<T>::load(xr + c, b);
+      Vec8<T>::load(w + c, ww);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s = fmaf(a[i] * ww[i], b[i], s);
+    }
+    s = warp_sum(s);
+    const float r = rstd[row];
+    const float coef = r * r * s * inv_d;
+    const T* dr = dres + row * d;
+    T* o = dx + row * d;
+    for (int c = lane * 8; c < d; c += 256) {
+      float a[8], b[8], ww[8], g[8];
+      Vec8<T>::load(dnr + c, a);
+      Vec8<T>::load(xr + c, b);
+      Vec8<T>::load(w + c, ww);
+      Vec8<T>::load(dr + c, g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        g[i] = g[i] + (a[i] * ww[i] - b[i] * coef);
+        my[c + i] = fmaf(a[i], b[i], my[c + i]);
+      }
+      Vec8<T>::store(o + c, g);
+    }
+  }
+  __syncthreads();
+  for (int col = threadIdx.x; col < d; col += blockDim.x) {
+    float v = acc[col];
+    for (int k = 1; k < kNormBwdWarps; ++k) v += acc[k * d + col];
+    part[static_cast<int64_t>(blockIdx.x) * d + col] = v;
+  }
+}
+
+template <typename T>
+__global__ void colsum_kernel(const float* __restrict__ part, int nblk, int d, T* __restrict__ out) {
+  const int col = blockIdx.x * blockDim.x + threadIdx.x;
+  if (col >= d) return;
+  float v = 0.f;
+  for (int b = 0; b < nblk; ++b) v += part[static_cast<int64_t>(b) * d + col];
+  out[col] = from_f<T>(v);
+}
+
+int norm_bwd_blocks(int num_sms) { return 2 * num_sms; }
+
+template <typename T>
+void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rstd,
+                     const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw) {
+  const size_t smem = sizeof(float) * kNormBwdWarps * static_cast<size_t>(d);
+  static const bool attr = [] {
+    cudaFuncSetAttribute(norm_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         200 * 1024);
+    return true;
+  }();
+  (void)attr;
+  norm_bwd_kernel<T><<<nblk, kNormBwdWarps * 32, smem, c.stream>>>(dn, x, w, rstd, dres, rows,
+                                                                   static_cast<int>(d), dx, part);
+  note_launch(c);
+  colsum_kernel<T><<<static_cast<unsigned>((d + 255) / 256), 256, 0, c.stream>>>(
+      part, nblk, static_cast<int>(d), dw);
+  note_launch(c);
+}
+
+// ---------------------------------------------------------------------------
+// split-K reduction (fixed order over splits)
+// ---------------------------------------------------------------------------
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t M,
+                                     int64_t N, int64_t ldp, const bf16* __restrict__ colv,
+                                     bf16* __restrict__ out, int64_t ldo) {
+  const int64_t nvec = (N + 7) / 8;
+  const int64_t plane = M * ldp;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M * nvec;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / nvec, c0 = (i - r * nvec) * 8;
+    float a[8];
+    Vec8<float>::load(part + r * ldp + c0, a);
+    for (int s = 1; s < splits; ++s) {
+      float b[8];
+      Vec8<float>::load(part + s * plane + r * ldp + c0, b);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) a[k] += b[k];
+    }
+    if (colv != nullptr) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (c0 + k < N) a[k] *= __bfloat162float(colv[c0 + k]);
+    }
+    bf16* o = out + r * ldo + c0;
+    if (c0 + 8 <= N) {
+      Vec8<bf16>::store(o, a);
+    } else {
+      for (int k = 0; c0 + k < N; ++k) o[k] = __float2bfloat16_rn(a[k]);
+    }
+  }
+}
+
+void launch_splitk_reduce(Ctx& c, const float* part, int splits, int64_t M, int64_t N,
+                          int64_t ldp, const bf16* colv, bf16* out, int64_t ldo) {
+  const int64_t n = M * ((N + 7) / 8);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 8));
+  splitk_reduce_kernel<<<grid, 256, 0, c.stream>>>(part, splits, M, N, ldp, colv, out, ldo);
+  note_launch(c);
+}
+
+// ---------------------------------------------------------------------------
+// elementwise passes
+// ---------------------------------------------------------------------------
+template <typename T, int OP>  // OP 0: h = sigma(z); 1: m = SiLU(G) U; 2: out = in * rowv
+__global__ void ew_kernel(const T* __restrict__ a, int64_t lda, const T* __restrict__ b,
+                          int64_t rows, int64_t cols, const float* __restrict__ rowv, int sigma,
+                          T* __restrict__ out, int64_t ldo) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows * cols;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / cols, col = i - r * cols;
+    float v;
+    if (OP == 0) {
+      v = act_f(to_f<T>(a[r * lda + col]), sigma);
+    } else if (OP == 1) {
+      v = __fmul_rn(silu_f(to_f<T>(a[r * lda + col])), to_f<T>(b[r * lda + col]));
+    } else {
+      v = (a == nullptr) ? 0.f : to_f<T>(a[r * lda + col]) * rowv[r];
+    }
+    out[r * ldo + col] = from_f<T>(v);
+  }
+}
+
+template <typename T, int OP>
+static void launch_ew(Ctx& c, const T* a, int64_t lda, const T* b, int64_t rows, int64_t cols,
+                      const float* rowv, int sigma, T* out, int64_t ldo) {
+  const int64_t n = rows * cols;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 16));
+  ew_kernel<T, OP><<<grid, 256, 0, c.stream>>>(a, lda, b, rows, cols, rowv, sigma, out, ldo);
+  note_launch(c);
+}
+
+template <typename T>
+void launch_sigma(Ctx& c, const T* z, int64_t rows, int64_t cols, int64_t ldz, T* h, int64_t ldh,
+                  int sigma) {
+  launch_ew<T, 0>(c, z, ldz, nullptr, rows, cols, nullptr, sigma, h, ldh);
+}
+template <typename T>
+void launch_swiglu(Ctx& c, const T* G, const T* U, int64_t rows, int64_t cols, int64_t ld, T* m,
+                   int64_t ldm) {
+  launch_ew<T, 1>(c, G, ld, U, rows, cols, nullptr, 0, m, ldm);
+}
+template <typename T>
+void launch_rowscale(Ctx& c, const T* in, int64_t ldi, const float* rowv, int64_t rows,
+                     int64_t cols, T* out, int64_t ldo) {
+  launch_ew<T, 2>(c, in, ldi, nullptr, rows, cols, rowv, 0, out, ldo);
+}
+
+#define BN_INSTANTIATE(T)                                                                        \
+  template void launch_stats<T>(Ctx&, const T*, int64_t, int64_t, int, float, float*, float*);   \
+  template void launch_fold_cols<T>(Ctx&, const T*, const T*, int64_t, int64_t, T*);             \
+  template void launch_norm_bwd<T>(Ctx&, const T*, const T*, const T*, const float*, const T*,   \
+                                   int64_t, int64_t, T*, float*, int, T*);                       \
+  template void launch_sigma<T>(Ctx&, const T*, int64_t, int64_t, int64_t, T*, int64_t, int);    \
+  template void launch_swiglu<T>(Ctx&, const T*, const T*, int64_t, int64_t, int64_t, T*,        \
+                                 int64_t);                                                       \
+  template void launch_rowscale<T>(Ctx&, const T*, int64_t, const float*, int64_t, int64_t, T*,  \
+                                   int64_t);
+BN_INSTANTIATE(float)
+BN_INSTANTIATE(bf16)
+
+}  // namespace bn

@@ -1,0 +1,48 @@
+// Launchers of the row-wise (HBM-bound) kernels of the block.
+#pragma once
+
+#include <cuda_bf16.h>
+#include "gemm.h"
+
+namespace bn {
+
+// ss[t, s] = sum of x[t, j]^2 over shard s (S equal column shards of d);
+// rstd[t] = 1 / sqrt(sum_s ss[t, s] / d + eps). x is [rows, d], row stride d.
+template <typename T>
+void launch_stats(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float eps, float* ss,
+                  float* rstd);
+
+// out[j, k] = A[j, k] * w[k]: the RMSNorm weight folded into a down-projection.
+template <typename T>
+void launch_fold_cols(Ctx& c, const T* A, const T* w, int64_t rows, int64_t cols, T* out);
+
+// RMSNorm backward from dn' = rstd * dn (the gradient of the normalised input
+// times the row's 1/rms):
+//   dx[t, j] = dres[t, j] + dn'[t, j] w[j] - x[t, j] rstd[t]^2 sum_k(dn' w x)[t, k] / d
+//   dw[j]    = sum_t dn'[t, j] x[t, j]
+// dw is reduced deterministically through `part` (nblk x d fp32).
+template <typename T>
+void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rstd,
+                     const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw);
+int norm_bwd_blocks(int num_sms);
+
+// out[i, j] = colv[j] * sum_s part[s][i][j] (fixed order over s), bf16 output.
+void launch_splitk_reduce(Ctx& c, const float* part, int splits, int64_t M, int64_t N,
+                          int64_t ldp, const __nv_bfloat16* colv, __nv_bfloat16* out, int64_t ldo);
+
+// h = sigma(z) elementwise, rounded exactly like the GEMM epilogues round it.
+template <typename T>
+void launch_sigma(Ctx& c, const T* z, int64_t rows, int64_t cols, int64_t ldz, T* h, int64_t ldh,
+                  int sigma);
+
+// m = SiLU(G) * U elementwise.
+template <typename T>
+void launch_swiglu(Ctx& c, const T* G, const T* U, int64_t rows, int64_t cols, int64_t ld, T* m,
+                   int64_t ldm);
+
+// out[i, j] = in[i, j] * rowv[i]; in == nullptr writes zeros.
+template <typename T>
+void launch_rowscale(Ctx& c, const T* in, int64_t ldi, const float* rowv, int64_t rows,
+                     int64_t cols, T* out, int64_t ldo);
+
+}  // namespace bn

@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function the header declares, sizes workspaces, and rejects bad
+arguments synchronously, before anything touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "boostblk.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rank_bottleneck_gb300 import _build
+    _build.build()
+    from rank_bottleneck_gb300 import block as B
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert "bn_block_forward" in names and "bn_block_backward" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def cfg(**kw):
+    from rank_bottleneck_gb300.block import BlockConfig
+    base = dict(T=16384, d=2048, r=512, d_ff=5461, S=4)
+    base.update(kw)
+    return BlockConfig(**base)
+
+
+def test_workspace_sizes_and_checkpoint_saving():
+    from rank_bottleneck_gb300.block import workspace_size
+    saved, scratch = workspace_size(cfg())
+    saved_ck, scratch_ck = workspace_size(cfg(checkpoint=True))
+    T, d, r = 16384, 2048, 512
+    # checkpoint mode saves exactly the four pre-activation tensors, [T, 7r] bf16
+    assert abs(saved_ck - T * 7 * r * 2) <= 4 * 256
+    assert saved > 5 * saved_ck
+    assert scratch_ck > scratch  # the recomputed activations live in scratch instead
+
+
+@pytest.mark.parametrize("bad, code", [
+    (dict(dtype="f32", S=3), 1),          # d % S != 0
+    (dict(d_ff=100, ld_ff=50), 1),        # ld_ff < d_ff
+    (dict(ld_ff=5462), 2),                # 16-byte rows of d_ff-wide tensors
+    (dict(r=500), 2),                     # rank must be a multiple of 8
+    (dict(S=17), 1),
+    (dict(dense=True, checkpoint=True), 3),
+    (dict(S=64), 1),
+    (dict(d=512, S=16), 3),               # bf16 shards narrower than 64 columns
+])
+def test_bad_descriptors_are_rejected(lib, bad, code):
+    from rank_bottleneck_gb300.block import workspace_size
+    c = cfg(**bad)
+    with pytest.raises(RuntimeError) as e:
+        workspace_size(c)
+    assert ["BN_ERR_INVALID_ARG", "BN_ERR_ALIGNMENT", "BN_ERR_UNSUPPORTED"][code - 1] in str(e.value)
+
+
+def _params_struct(**ptrs):
+    from rank_bottleneck_gb300.block import PARAM_NAMES, _Params
+    p = _Params()
+    for n in PARAM_NAMES:
+        setattr(p, n, ptrs.get(n))
+    return p
+
+
+def test_pointer_checks_before_any_launch(lib):
+    from rank_bottleneck_gb300.block import PARAM_NAMES
+    c = cfg(T=256, d=256, r=64, d_ff=688, dtype="f32")
+    d = c.desc()
+    good = {n: 4096 * (i + 1) for i, n in enumerate(PARAM_NAMES)}
+    # a misaligned parameter pointer
+    bad = dict(good, B_q=good["B_q"] + 4)
+    st = lib.bn_block_forward(ctypes.byref(d), ctypes.byref(_params_struct(**bad)), 1 << 20,
+                              1 << 21, 1 << 22, 1 << 23, 1 << 24, 1 << 25, None)
+    assert lib.bn_status_string(st) == b"BN_ERR_ALIGNMENT"
+    # a missing parameter
+    miss = dict(good)
+    miss.pop("A_o")
+    st = lib.bn_block_forward(ctypes.byref(d), ctypes.byref(_params_struct(**miss)), 1 << 20,
+                              1 << 21, 1 << 22, 1 << 23, 1 << 24, 1 << 25, None)
+    assert lib.bn_status_string(st) == b"BN_ERR_INVALID_ARG"
+    # the MLP kind must not get attention-half tensors
+    m = cfg(T=256, d=256, r=64, d_ff=688, dtype="f32", kind="mlp").desc()
+    st = lib.bn_block_forward(ctypes.byref(m), ctypes.byref(_params_struct(**good)), 1 << 20,
+                              1 << 21, None, None, 1 << 24, 1 << 25, None)
+    assert lib.bn_status_string(st) == b"BN_ERR_INVALID_ARG"
+    # dense blocks take no up-projection factors
+    dn = cfg(T=256, d=256, r=64, d_ff=688, dtype="f32", dense=True).desc()
+    st = lib.bn_block_forward(ctypes.byref(dn), ctypes.byref(_params_struct(**good)), 1 << 20,
+                              1 << 21, 1 << 22, 1 << 23, 1 << 24, 1 << 25, None)
+    assert lib.bn_status_string(st) == b"BN_ERR_INVALID_ARG"
+    assert lib.bn_last_launch_count() == 0
+
+
+def test_status_strings(lib):
+    for code, name in enumerate([b"BN_OK", b"BN_ERR_INVALID_ARG", b"BN_ERR_ALIGNMENT",
+                                 b"BN_ERR_UNSUPPORTED", b"BN_ERR_CUDA", b"BN_ERR_TIMEOUT"]):
+        assert lib.bn_status_string(code) == name
