@@ -1,0 +1,63 @@
+/*
+ * boostblk_testing.h -- test hook into the GEMM engine of libboostblk.
+ *
+ * Not needed to run a block: it exposes one launch of the engine that
+ * bn_block_forward / bn_block_backward use internally, so each fused epilogue
+ * and each operand layout can be checked on its own. Every GEMM of the block
+ * ("BOOST: BOttleneck-Optimized Scalable Training Framework for Low-Rank
+ * Large Language Models", project page, "Move the chunk boundary to the
+ * bottleneck" and "Three supporting changes") is one such launch.
+ *
+ * Per problem: acc[i, j] = sum_k Aop[i, k] Bop[j, k], i < M, j < N, k < K.
+ * An operand is stored row-major either as [MN, K] (mn_major = 0, rows of K
+ * elements) or as [K, MN] (mn_major = 1); `ld` is its row stride in elements.
+ * Epilogues (bn_gemm_epi):
+ *   STORE      out0 = acc * rowv[i] * colv[j]   (rowv fp32, colv element type; optional)
+ *   SIGMA      out0 = z = acc, out1 = sigma(z)
+ *   NORM       Online RMSNorm over S equal shards of K: rowv = per-row, per-shard
+ *              sums of squares [M, S] fp32; z = sum_s (rms_s / rms_g)(P_s / rms_s),
+ *              rms_s = sqrt(ss_s/(K/S) + eps), rms_g = sqrt(sum_s ss_s / K + eps);
+ *              out0 = z, out1 = sigma(z) (out1 optional)
+ *   RESID      out0 = in0 + acc
+ *   SWIGLU     G from (a, b), U from (a2, b2): out0 = G, out1 = U (optional), out2 = SiLU(G) U
+ *   DSIGMA     out0 = acc * sigma'(in0) * rowv[i]
+ *   DSWIGLU    out0 = acc * in1 * SiLU'(in0) * rowv[i], out1 = acc * SiLU(in0) * rowv[i]
+ *   CHAIN      acc over (a, b) then (a2, b2) summed, then as STORE
+ * All outputs/inputs use leading dimension ldo / ldi.
+ */
+#ifndef BOOSTBLK_TESTING_H
+#define BOOSTBLK_TESTING_H
+
+#include "boostblk.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BN_GEMM_STORE = 0, BN_GEMM_SIGMA = 1, BN_GEMM_NORM = 2, BN_GEMM_RESID = 3,
+  BN_GEMM_SWIGLU = 4, BN_GEMM_DSIGMA = 5, BN_GEMM_DSWIGLU = 6, BN_GEMM_CHAIN = 7
+} bn_gemm_epi;
+
+typedef struct {
+  int64_t M, N, K;
+  const void* a; const void* a2; int64_t lda; int32_t a_mn_major;
+  const void* b; const void* b2; int64_t ldb; int32_t b_mn_major;
+  void* out0; void* out1; void* out2; int64_t ldo;
+  const void* in0; const void* in1; int64_t ldi;
+  const float* rowv; const void* colv;
+} bn_gemm_problem;
+
+/* Launch 1..3 problems of one epilogue in one engine launch. dtype: bn_dtype.
+ * allow_split lets the tensor-core engine split K for STORE (fp32 partials in
+ * `scratch` after its 256-byte status word, reduced in a fixed order).
+ * Pointers are device pointers, 16-byte aligned. Asynchronous on `stream`. */
+bn_status bn_testing_gemm(int32_t dtype, int32_t epi, int32_t sigma, int32_t S, float eps,
+                          int32_t allow_split, int32_t nprob, const bn_gemm_problem* probs,
+                          void* scratch, size_t scratch_bytes, bn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BOOSTBLK_TESTING_H */

@@ -33,7 +33,8 @@ def sources():
 
 def _newest_input() -> float:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(ROOT, "include", "boostblk.h"))
+    inc = os.path.join(ROOT, "include")
+    files += [os.path.join(inc, f) for f in os.listdir(inc)]
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 

@@ -1,0 +1,67 @@
+// bn_testing_gemm: one launch of the GEMM engine, for unit tests of each
+// epilogue and operand layout.
+#include <cstdio>
+
+#include "../../include/boostblk_testing.h"
+#include "gemm.h"
+
+using namespace bn;
+
+extern "C" bn_status bn_testing_gemm(int32_t dtype, int32_t epi, int32_t sigma, int32_t S,
+                                     float eps, int32_t allow_split, int32_t nprob,
+                                     const bn_gemm_problem* probs, void* scratch,
+                                     size_t scratch_bytes, bn_stream_t stream) {
+  if (probs == nullptr || nprob < 1 || nprob > 3 || epi < 0 || epi > 7 || S < 1 || S > 16 ||
+      (dtype != BN_F32 && dtype != BN_BF16) || scratch == nullptr || scratch_bytes < 256)
+    return BN_ERR_INVALID_ARG;
+  GemmLaunch g;
+  g.epi = static_cast<Epi>(epi);
+  g.sigma = sigma;
+  g.S = S;
+  g.eps = eps;
+  g.allow_split = allow_split != 0;
+  g.nprob = nprob;
+  for (int i = 0; i < nprob; ++i) {
+    const bn_gemm_problem& q = probs[i];
+    GemmProblem& p = g.p[i];
+    p.M = q.M;
+    p.N = q.N;
+    p.K = q.K;
+    p.a[0].ptr = q.a;
+    p.a[1].ptr = q.a2;
+    p.b[0].ptr = q.b;
+    p.b[1].ptr = q.b2;
+    for (int j = 0; j < 2; ++j) {
+      p.a[j].ld = q.lda;
+      p.a[j].mn_major = q.a_mn_major != 0;
+      p.b[j].ld = q.ldb;
+      p.b[j].mn_major = q.b_mn_major != 0;
+    }
+    p.out[0] = q.out0;
+    p.out[1] = q.out1;
+    p.out[2] = q.out2;
+    p.ldo[0] = p.ldo[1] = p.ldo[2] = q.ldo;
+    p.in[0] = q.in0;
+    p.in[1] = q.in1;
+    p.ldi[0] = p.ldi[1] = q.ldi;
+    p.rowv = q.rowv;
+    p.colv = q.colv;
+    if (q.M < 1 || q.N < 1 || q.K < 1) return BN_ERR_INVALID_ARG;
+  }
+  Ctx c;
+  c.stream = reinterpret_cast<cudaStream_t>(stream);
+  c.status = static_cast<int*>(scratch);
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+    c.num_sms = n;
+  c.partial = reinterpret_cast<float*>(static_cast<char*>(scratch) + 256);
+  c.partial_bytes = scratch_bytes - 256;
+  if (dtype == BN_BF16)
+    gemm_tc(c, g);
+  else
+    gemm_simt(c, g);
+  if (c.bad) return BN_ERR_UNSUPPORTED;
+  if (c.err != cudaSuccess) return BN_ERR_CUDA;
+  return BN_OK;
+}

@@ -1,0 +1,177 @@
+"""Parity of the block (forward + backward through the C ABI) with the fp64 oracle.
+
+Small cases compare every output and gradient element by element. Full-size
+cases (the benchmark shapes, same launch configuration) keep the upstream
+gradients dy / dq / dk only on a sample of token rows R and zero elsewhere: the
+block is row-independent, so y, q, k, dx on R and every weight gradient are
+then exactly what the oracle computes from the rows R alone.
+Bars (max |gpu - ref| / max |ref| per tensor): 1e-5 fp32, 2e-2 bf16.
+"""
+import numpy as np
+import pytest
+
+import _blockcase as C
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from rank_bottleneck_gb300 import _build
+    _build.build()
+
+
+def cfg_of(**kw):
+    from rank_bottleneck_gb300.block import BlockConfig
+    return BlockConfig(**kw)
+
+
+def case(kw, seed=0):
+    cfg = cfg_of(**kw)
+    inp = C.inputs(cfg.T, cfg.d, cfg.r, cfg.d_ff, kind=cfg.kind, dense=cfg.dense,
+                   dtype=cfg.dtype, seed=seed)
+    return cfg, inp
+
+
+SMALL = {
+    "mlp-f32-T256-d256-r64-dff688-S4": dict(T=256, d=256, r=64, d_ff=688, S=4, dtype="f32", kind="mlp"),
+    "full-f32-ragged": dict(T=77, d=128, r=32, d_ff=200, S=2, dtype="f32"),
+    "full-f32-identity": dict(T=64, d=128, r=16, d_ff=96, S=4, dtype="f32", sigma="identity"),
+    "full-f32-dense": dict(T=50, d=64, r=8, d_ff=72, S=2, dtype="f32", dense=True),
+    "full-f32-ckpt": dict(T=90, d=128, r=24, d_ff=100, S=4, dtype="f32", checkpoint=True),
+    "full-bf16-ragged": dict(T=300, d=256, r=64, d_ff=333, S=4),
+    "mlp-bf16": dict(T=200, d=256, r=64, d_ff=688, S=2, kind="mlp"),
+    "full-bf16-identity": dict(T=256, d=512, r=128, d_ff=1000, S=8, sigma="identity"),
+    "full-bf16-dense": dict(T=260, d=256, r=8, d_ff=344, S=4, dense=True),
+    "mlp-bf16-dense": dict(T=130, d=128, r=8, d_ff=200, S=2, dense=True, kind="mlp"),
+    "full-bf16-ckpt": dict(T=300, d=256, r=64, d_ff=333, S=4, checkpoint=True),
+    "full-bf16-T1": dict(T=1, d=128, r=8, d_ff=24, S=2),
+    "full-bf16-S16": dict(T=130, d=1024, r=64, d_ff=200, S=16),
+    "full-bf16-r8": dict(T=129, d=192, r=8, d_ff=40, S=3),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_block_matches_oracle(name):
+    cfg, inp = case(SMALL[name])
+    got = C.run_gpu(cfg, inp)
+    ref = C.run_oracle(cfg, inp)
+    C.compare(got, ref, C.TOL[cfg.dtype])
+
+
+def test_zero_rows_and_zero_shards():
+    cfg, inp = case(dict(T=200, d=256, r=64, d_ff=300, S=4))
+    inp["x"][5] = 0.0                 # an all-zero token row
+    inp["x"][9, :64] = 0.0            # a zero first shard
+    got = C.run_gpu(cfg, inp)
+    ref = C.run_oracle(cfg, inp)
+    C.compare(got, ref, C.TOL["bf16"])
+
+
+def test_absent_dq_dk_mean_zero():
+    cfg, inp = case(dict(T=160, d=256, r=64, d_ff=300, S=2))
+    got = C.run_gpu(cfg, inp, drop_dq=True, drop_dk=True)
+    inp0 = dict(inp, dq=np.zeros_like(inp["dq"]), dk=np.zeros_like(inp["dk"]))
+    ref = C.run_oracle(cfg, inp0)
+    assert np.all(got["dB_q"] == 0) and np.all(got["dB_k"] == 0)
+    C.compare(got, ref, C.TOL["bf16"])
+
+
+def test_fp32_online_norm_shards_match_single_shard():
+    """Online RMSNorm with S > 1 equals S = 1 (plain RMSNorm) to 1e-6 in fp32."""
+    base = dict(T=192, d=512, r=64, d_ff=400, dtype="f32")
+    res = {}
+    for S in (1, 2, 4, 8):
+        cfg, inp = case(dict(base, S=S))
+        res[S] = C.run_gpu(cfg, inp)
+    for S in (2, 4, 8):
+        for k in res[1]:
+            assert C.rel_err(res[S][k], res[1][k]) <= 1e-6, (S, k)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_checkpoint_is_bit_identical(dtype):
+    kw = dict(T=300, d=256, r=64, d_ff=333, S=4, dtype=dtype)
+    cfg_a, inp = case(kw)
+    cfg_b = cfg_of(**dict(kw, checkpoint=True))
+    a = C.run_gpu(cfg_a, inp)
+    b = C.run_gpu(cfg_b, inp)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_repeatable_bit_for_bit():
+    cfg, inp = case(dict(T=1000, d=512, r=128, d_ff=1400, S=4))
+    a = C.run_gpu(cfg, inp)
+    b = C.run_gpu(cfg, inp)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+# ---------------------------------------------------------------------------
+# full-size shapes, sampled rows
+# ---------------------------------------------------------------------------
+
+def sample_rows(T, n=48, seed=1):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, T // 2, T - 129, T - 2, T - 1]
+    rest = rng.choice(T, size=n - len(fixed), replace=False)
+    return np.unique(np.concatenate([fixed, rest]))
+
+
+def masked_case(kw, seed=0):
+    cfg, inp = case(kw, seed)
+    rows = sample_rows(cfg.T)
+    keep = np.zeros(cfg.T, dtype=bool)
+    keep[rows] = True
+    for k in ("dy", "dq", "dk"):
+        if k in inp:
+            inp[k][~keep] = 0.0
+    return cfg, inp, rows, keep
+
+
+def check_masked(cfg, inp, rows, keep, got=None):
+    got = C.run_gpu(cfg, inp) if got is None else got
+    ref = C.run_oracle(cfg, inp, rows=rows)
+    errs = C.compare(got, ref, C.TOL[cfg.dtype], rows=rows)
+    assert np.all(got["dx"][~keep][:64] == 0.0)
+    return got, errs
+
+
+FULL = {
+    "1B-T16384-d2048-r512-dff5461-S4": dict(T=16384, d=2048, r=512, d_ff=5461, S=4),
+    "7B-T16384-d4096-r1024-dff11008-S8": dict(T=16384, d=4096, r=1024, d_ff=11008, S=8),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_block(name):
+    cfg, inp, rows, keep = masked_case(FULL[name])
+    check_masked(cfg, inp, rows, keep)
+
+
+def test_13b_checkpoint_full_size():
+    kw = dict(T=16384, d=5120, r=1280, d_ff=13824, S=8)
+    cfg, inp, rows, keep = masked_case(kw)
+    got, _ = check_masked(cfg, inp, rows, keep)
+    cfg_ck = cfg_of(**dict(kw, checkpoint=True))
+    got_ck = C.run_gpu(cfg_ck, inp)
+    for k in got:
+        assert np.array_equal(got[k], got_ck[k]), k
+
+
+SWEEP = {
+    "svd-r256-T4096": dict(T=4096, d=4096, r=256, d_ff=11008, S=8, sigma="identity"),
+    "cola-r2048-T4096": dict(T=4096, d=4096, r=2048, d_ff=11008, S=8),
+    "cola-r512-T32768": dict(T=32768, d=4096, r=512, d_ff=11008, S=8),
+    "dense-T4096": dict(T=4096, d=4096, r=1024, d_ff=11008, S=8, dense=True),
+}
+
+
+@pytest.mark.parametrize("name", list(SWEEP))
+def test_sweep_points(name):
+    cfg, inp, rows, keep = masked_case(SWEEP[name])
+    check_masked(cfg, inp, rows, keep)
