@@ -1,7 +1,15 @@
-// fp32 GEMM engine on the FFMA pipes, for fp32 blocks (tf32 tensor cores would
+// fp32 GEMM engine on the FP32 pipes, for fp32 blocks (tf32 tensor cores would
 // not meet fp32 accuracy). Same problem/epilogue contract as the tcgen05 engine:
 // 64 x 64 output tiles, 16-deep K steps through shared memory, 4 x 4 outputs
 // per thread, segments folded exactly as the tensor-core epilogues fold them.
+//
+// Each dot product is accumulated with the compensated scheme "Dot2" of Ogita,
+// Rump and Oishi ("Accurate Sum and Dot Product", SIAM J. Sci. Comput. 2005):
+// the rounding error of every product (recovered exactly with an FMA) and of
+// every addition (recovered exactly with the TwoSum of Knuth) is summed into a
+// second accumulator. The result is as accurate as if computed in twice the
+// working precision and then rounded, so splitting K into the S shards of
+// Online RMSNorm changes it only by the final roundings of the fold.
 #include <algorithm>
 
 #include "common.cuh"
@@ -50,6 +58,17 @@ __device__ __forceinline__ void load_tile(float (*dst)[TM + 4], const Op& op, in
   }
 }
 
+// s + c += a * b, with the product's and the sum's rounding errors kept in c.
+__device__ __forceinline__ void dot2_step(float& s, float& c, float a, float b) {
+  const float p = __fmul_rn(a, b);
+  const float pe = __fmaf_rn(a, b, -p);        // a * b - p, exactly
+  const float t = __fadd_rn(s, p);
+  const float z = __fsub_rn(t, s);
+  const float se = __fadd_rn(__fsub_rn(s, __fsub_rn(t, z)), __fsub_rn(p, z));  // s + p - t, exactly
+  s = t;
+  c = __fadd_rn(c, __fadd_rn(se, pe));
+}
+
 template <int EK>
 __global__ void __launch_bounds__(THREADS) simt_kernel(const __grid_constant__ Params P) {
   const Prob& pr = P.p[blockIdx.z];
@@ -58,11 +77,11 @@ __global__ void __launch_bounds__(THREADS) simt_kernel(const __grid_constant__ P
   __shared__ float As[TK][TM + 4];
   __shared__ float Bs[TK][TN + 4];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float acc[4][4], R[4][4];
+  float acc[4][4], cmp[4][4], R[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = R[i][j] = 0.f;
+    for (int j = 0; j < 4; ++j) acc[i][j] = cmp[i][j] = R[i][j] = 0.f;
 
   const int nseg = (EK == EPI_NORM) ? P.S : (EK == EPI_SWIGLU || EK == EPI_STORE_CHAIN) ? 2 : 1;
   for (int s = 0; s < nseg; ++s) {
@@ -77,7 +96,7 @@ __global__ void __launch_bounds__(THREADS) simt_kernel(const __grid_constant__ P
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < 4; ++j) acc[i][j] = cmp[i][j] = 0.f;
     }
     for (int k0 = k_lo; k0 < k_hi; k0 += TK) {
       load_tile(As, pr.a[pair], m0, pr.M, k0, k_hi);
@@ -93,10 +112,17 @@ __global__ void __launch_bounds__(THREADS) simt_kernel(const __grid_constant__ P
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+          for (int j = 0; j < 4; ++j) dot2_step(acc[i][j], cmp[i][j], av[i], bv[j]);
       }
       __syncthreads();
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[i][j] = __fadd_rn(acc[i][j], cmp[i][j]);
+        cmp[i][j] = 0.f;
+      }
     if (EK == EPI_NORM) {
       // Online RMSNorm: local normalisation, then the per-row correction alpha
 #pragma unroll
