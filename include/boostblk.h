@@ -131,6 +131,26 @@ bn_status bn_get_device_status(void* scratch, bn_stream_t stream);
  * this thread launched. */
 int bn_last_launch_count(void);
 
+/* Launch timing (for benchmarks; off by default). After bn_profile_start(),
+ * every kernel the library launches from this thread is bracketed by two CUDA
+ * events on its stream and recorded with its kind (0 tcgen05 GEMM, 1 fp32 GEMM,
+ * 2 split-K reduction, 3 norm statistics, 4 weight fold, 5 RMSNorm backward,
+ * 6 dw column sum, 7 elementwise), its GEMM epilogue (or -1) and its
+ * algorithmic FLOPs and bytes (each input read once, each output written once).
+ * bn_profile_stop() ends recording, waits for the recorded events, copies up to
+ * max_records records (device time in ms) into `out` (host memory) and returns
+ * how many launches were recorded. */
+typedef struct {
+  int32_t kernel;
+  int32_t epi;
+  double flops;
+  double bytes;
+  float ms;
+} bn_launch_record;
+
+bn_status bn_profile_start(void);
+int bn_profile_stop(bn_launch_record* out, int max_records);
+
 /* Name of a status code (static storage). */
 const char* bn_status_string(bn_status s);
 

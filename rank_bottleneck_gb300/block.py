@@ -39,6 +39,14 @@ class _Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in PARAM_NAMES]
 
 
+class LaunchRecord(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("epi", ctypes.c_int32), ("flops", ctypes.c_double),
+                ("bytes", ctypes.c_double), ("ms", ctypes.c_float)]
+
+
+KERNEL_NAMES = ("gemm_tcgen05", "gemm_fp32", "splitk_reduce", "norm_stats", "norm_weight_fold",
+                "rmsnorm_backward", "dw_colsum", "elementwise")
+
 _lib = None
 
 
@@ -68,6 +76,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.bn_status_string.restype = ctypes.c_char_p
     lib.bn_last_cuda_error.argtypes = []
     lib.bn_last_cuda_error.restype = ctypes.c_char_p
+    lib.bn_profile_start.argtypes = []
+    lib.bn_profile_start.restype = st
+    lib.bn_profile_stop.argtypes = [ctypes.POINTER(LaunchRecord), ctypes.c_int]
+    lib.bn_profile_stop.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -215,3 +227,16 @@ def device_status(ws: Workspace, stream=None) -> int:
 
 def last_launch_count() -> int:
     return load().bn_last_launch_count()
+
+
+def profile_start():
+    """Record every kernel the library launches from this thread (CUDA events)."""
+    load().bn_profile_start()
+
+
+def profile_stop(max_records=1 << 16):
+    """Stop recording; returns [{"kernel", "epi", "flops", "bytes", "ms"}, ...]."""
+    buf = (LaunchRecord * max_records)()
+    n = load().bn_profile_stop(buf, max_records)
+    return [dict(kernel=KERNEL_NAMES[r.kernel], epi=r.epi, flops=r.flops, bytes=r.bytes, ms=r.ms)
+            for r in buf[:min(n, max_records)]]

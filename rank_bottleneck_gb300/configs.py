@@ -1,0 +1,48 @@
+"""Named workloads (synthetic LLaMA-2-shaped blocks) and the FLOP model used to
+report throughput. Shapes follow the project page's LLaMA-2 family with r = d/4
+("Move the chunk boundary to the bottleneck": the paper uses r = d/4)."""
+from __future__ import annotations
+
+WORKLOADS = {
+    # tiny fp32 MLP sub-block, correctness scale
+    "mlp-f32-T256-d256-r64-dff688": dict(T=256, d=256, r=64, d_ff=688, S=4, dtype="f32", kind="mlp"),
+    # 1B shape: micro-batch 4 x sequence 4096
+    "1b-T16384-d2048-r512-dff5461": dict(T=16384, d=2048, r=512, d_ff=5461, S=4),
+    "7b-T16384-d4096-r1024-dff11008": dict(T=16384, d=4096, r=1024, d_ff=11008, S=8),
+    "13b-ckpt-T16384-d5120-r1280-dff13824": dict(T=16384, d=5120, r=1280, d_ff=13824, S=8,
+                                                  checkpoint=True),
+    "13b-T16384-d5120-r1280-dff13824": dict(T=16384, d=5120, r=1280, d_ff=13824, S=8),
+}
+for _T in (4096, 16384, 32768):
+    for _r in (256, 512, 1024, 2048):
+        for _s in ("identity", "silu"):
+            WORKLOADS[f"sweep-{_s}-T{_T}-r{_r}"] = dict(T=_T, d=4096, r=_r, d_ff=11008, S=8, sigma=_s)
+    WORKLOADS[f"sweep-dense-T{_T}"] = dict(T=_T, d=4096, r=1024, d_ff=11008, S=8, dense=True)
+
+DEFAULT = "1b-T16384-d2048-r512-dff5461"
+
+
+def layers(cfg):
+    """(d_in, d_out) of every linear layer of the block."""
+    d, dff = cfg.d, cfg.d_ff
+    mlp = [(d, dff), (d, dff), (dff, d)]
+    attn = [(d, d)] * 4
+    return (attn + mlp) if cfg.kind == "full" else mlp
+
+
+def model_flops(cfg) -> float:
+    """Forward + backward FLOPs of the block's matrix multiplies: 6 T r (d_in + d_out)
+    per factorised layer, 6 T d_in d_out per dense layer."""
+    T, r = cfg.T, cfg.r
+    if cfg.dense:
+        return float(sum(6 * T * a * b for a, b in layers(cfg)))
+    return float(sum(6 * T * r * (a + b) for a, b in layers(cfg)))
+
+
+def recompute_flops(cfg) -> float:
+    """Checkpoint mode re-runs the V, O, gate and up up-projections: 2 T r d_out each."""
+    if not cfg.checkpoint:
+        return 0.0
+    T, r = cfg.T, cfg.r
+    outs = ([cfg.d, cfg.d] if cfg.kind == "full" else []) + [cfg.d_ff, cfg.d_ff]
+    return float(sum(2 * T * r * o for o in outs))

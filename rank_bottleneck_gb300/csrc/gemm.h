@@ -77,11 +77,44 @@ struct Ctx {
   int bad = 0;                 // a bn_status other than BN_OK raised inside a launcher
 };
 
-// Record the result of a kernel launch.
-inline void note_launch(Ctx& c) {
-  ++c.launches;
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess && c.err == cudaSuccess) c.err = e;
+// Kernel families, as reported by the launch-timing facility (bn_profile_*).
+enum KernelKind : int {
+  KK_GEMM_TC = 0,        // tcgen05 GEMM engine
+  KK_GEMM_FFMA = 1,      // fp32 GEMM engine
+  KK_SPLITK_REDUCE = 2,  // split-K reduction
+  KK_STATS = 3,          // Online RMSNorm shard statistics
+  KK_FOLD = 4,           // norm weight folded into a down-projection
+  KK_NORM_BWD = 5,       // RMSNorm backward
+  KK_COLSUM = 6,         // dw column reduction
+  KK_ELEMENTWISE = 7,    // sigma recompute / SwiGLU / row scaling
+};
+
+// Call right before a kernel launch: starts its timing record when the
+// launch-timing facility is on for this thread.
+void prof_start(Ctx& c);
+// Call right after a kernel launch: counts it, records a launch error, and
+// closes its timing record with the launch's algorithmic FLOPs and bytes.
+void note_launch(Ctx& c, int kind, int epi, double flops, double bytes);
+
+// Algorithmic work of one GEMM launch: 2 M N K FLOPs per operand pair, every
+// operand and epilogue input read once, every output written once.
+inline void gemm_work(const GemmLaunch& g, int esize, double& flops, double& bytes) {
+  flops = 0;
+  bytes = 0;
+  const int npair = (g.epi == EPI_SWIGLU || g.epi == EPI_STORE_CHAIN) ? 2 : 1;
+  for (int i = 0; i < g.nprob; ++i) {
+    const GemmProblem& p = g.p[i];
+    const double M = static_cast<double>(p.M), N = static_cast<double>(p.N),
+                 K = static_cast<double>(p.K);
+    flops += 2.0 * M * N * K * npair;
+    bytes += npair * (M + N) * K * esize;
+    for (int j = 0; j < 3; ++j)
+      if (p.out[j]) bytes += M * N * esize;
+    for (int j = 0; j < 2; ++j)
+      if (p.in[j]) bytes += M * N * esize;
+    if (p.rowv) bytes += M * 4.0 * (g.epi == EPI_NORM ? g.S : 1);
+    if (p.colv) bytes += N * esize;
+  }
 }
 
 void gemm_tc(Ctx& c, const GemmLaunch& g);    // bf16 operands, tcgen05

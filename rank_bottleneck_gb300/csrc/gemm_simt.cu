@@ -242,6 +242,9 @@ void gemm_simt(Ctx& c, const GemmLaunch& g) {
     gn = std::max(gn, (q.N + TN - 1) / TN);
   }
   dim3 grid(static_cast<unsigned>(gn), static_cast<unsigned>(gm), static_cast<unsigned>(g.nprob));
+  double flops, bytes;
+  gemm_work(g, 4, flops, bytes);
+  prof_start(c);
   switch (g.epi) {
     case EPI_STORE: go<EPI_STORE>(P, grid, c.stream); break;
     case EPI_SIGMA: go<EPI_SIGMA>(P, grid, c.stream); break;
@@ -252,7 +255,7 @@ void gemm_simt(Ctx& c, const GemmLaunch& g) {
     case EPI_DSWIGLU: go<EPI_DSWIGLU>(P, grid, c.stream); break;
     case EPI_STORE_CHAIN: go<EPI_STORE_CHAIN>(P, grid, c.stream); break;
   }
-  note_launch(c);
+  note_launch(c, KK_GEMM_FFMA, static_cast<int>(g.epi), flops, bytes);
 }
 
 }  // namespace bn

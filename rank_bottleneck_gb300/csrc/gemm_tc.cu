@@ -195,13 +195,16 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
   }
   P.total_units = units;
   const int grid = std::min(units, c.num_sms);
+  double flops, bytes;
+  gemm_work(g, 2, flops, bytes);
+  prof_start(c);
   const bool ok = (BN == 256) ? launch_bn256(ek, a_mn, b_mn, P, grid, c.stream)
                               : launch_bn128(ek, a_mn, b_mn, P, grid, c.stream);
   if (!ok) {
     c.bad = 5;
     return;
   }
-  note_launch(c);
+  note_launch(c, KK_GEMM_TC, static_cast<int>(g.epi), flops, bytes);
   if (split) {
     for (int i = 0; i < g.nprob; ++i) {
       const Prob& p = P.p[i];

@@ -43,8 +43,9 @@ template <typename T>
 void launch_stats(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float eps, float* ss,
                   float* rstd) {
   const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  prof_start(c);
   stats_kernel<T><<<grid, 256, 0, c.stream>>>(x, rows, static_cast<int>(d), S, eps, ss, rstd);
-  note_launch(c);
+  note_launch(c, KK_STATS, -1, 2.0 * rows * d, static_cast<double>(rows) * (d * sizeof(T) + 4 * S + 4));
 }
 
 // ---------------------------------------------------------------------------
@@ -70,8 +71,9 @@ template <typename T>
 void launch_fold_cols(Ctx& c, const T* A, const T* w, int64_t rows, int64_t cols, T* out) {
   const int64_t n = rows * (cols / 8);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 8));
+  prof_start(c);
   fold_cols_kernel<T><<<grid, 256, 0, c.stream>>>(A, w, rows, cols, out);
-  note_launch(c);
+  note_launch(c, KK_FOLD, -1, 1.0 * rows * cols, (2.0 * rows * cols + cols) * sizeof(T));
 }
 
 // ---------------------------------------------------------------------------
@@ -153,12 +155,15 @@ void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* r
     return true;
   }();
   (void)attr;
+  prof_start(c);
   norm_bwd_kernel<T><<<nblk, kNormBwdWarps * 32, smem, c.stream>>>(dn, x, w, rstd, dres, rows,
                                                                    static_cast<int>(d), dx, part);
-  note_launch(c);
+  note_launch(c, KK_NORM_BWD, -1, 8.0 * rows * d,
+              4.0 * rows * d * sizeof(T) + d * sizeof(T) + 4.0 * rows + 4.0 * nblk * d);
+  prof_start(c);
   colsum_kernel<T><<<static_cast<unsigned>((d + 255) / 256), 256, 0, c.stream>>>(
       part, nblk, static_cast<int>(d), dw);
-  note_launch(c);
+  note_launch(c, KK_COLSUM, -1, 1.0 * nblk * d, 4.0 * nblk * d + d * sizeof(T));
 }
 
 // ---------------------------------------------------------------------------
@@ -198,8 +203,9 @@ void launch_splitk_reduce(Ctx& c, const float* part, int splits, int64_t M, int6
                           int64_t ldp, const bf16* colv, bf16* out, int64_t ldo) {
   const int64_t n = M * ((N + 7) / 8);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 8));
+  prof_start(c);
   splitk_reduce_kernel<<<grid, 256, 0, c.stream>>>(part, splits, M, N, ldp, colv, out, ldo);
-  note_launch(c);
+  note_launch(c, KK_SPLITK_REDUCE, -1, 1.0 * splits * M * N, (4.0 * splits + 2.0) * M * N);
 }
 
 // ---------------------------------------------------------------------------
@@ -229,8 +235,9 @@ static void launch_ew(Ctx& c, const T* a, int64_t lda, const T* b, int64_t rows,
                       const float* rowv, int sigma, T* out, int64_t ldo) {
   const int64_t n = rows * cols;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 16));
+  prof_start(c);
   ew_kernel<T, OP><<<grid, 256, 0, c.stream>>>(a, lda, b, rows, cols, rowv, sigma, out, ldo);
-  note_launch(c);
+  note_launch(c, KK_ELEMENTWISE, OP, 4.0 * n, (OP == 1 ? 3.0 : 2.0) * n * sizeof(T));
 }
 
 template <typename T>
