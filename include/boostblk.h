@@ -151,6 +151,30 @@ typedef struct {
 bn_status bn_profile_start(void);
 int bn_profile_stop(bn_launch_record* out, int max_records);
 
+/* Weight gradient without any caller-provided scratch: for callers that cannot
+ * allocate GPU memory (their memory is reserved up front by their own pool, or
+ * a cudaMalloc is forbidden or would synchronise where they run). The paper has
+ * no counterpart; this is the split-K weight-gradient GEMM of bn_block_backward
+ * (dA = dz^T X, dB = dY^T h) offered on its own.
+ *   dW[i, j] = colscale[j] * sum_{t < T} A[t, i] * B[t, j],  i < M, j < N
+ * A [T, lda] and B [T, ldb] are row-major bf16 (token rows), dW [M, ldw] bf16;
+ * colscale (bf16, N values) may be NULL; fp32 accumulation on the tensor cores.
+ * Pointers 16-byte aligned, leading dimensions multiples of 8.
+ * Scratch: a 32 MiB array inside the library (held on every GPU that loads
+ * it until the process exits) holds the fp32 partial sums of the K split;
+ * sizes with M * round_up(N, 8) * 8 bytes > 32 MiB - 256 return
+ * BN_ERR_UNSUPPORTED. No device memory is allocated. The first call on each
+ * device looks the array's device address up (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture. All calls
+ * share the array, which keeps the last call's contents: calls whose kernels
+ * overlap on the GPU (other streams, other threads) race and must be ordered
+ * by the caller. Each call clears the array's status word first; a kernel
+ * time-out is recorded there but not reported by this entry point.
+ * Asynchronous on `stream`; argument errors return before any launch. */
+bn_status bn_weight_grad_noalloc(int64_t M, int64_t N, int64_t T, const void* A, int64_t lda,
+                                 const void* B, int64_t ldb, const void* colscale, void* dW,
+                                 int64_t ldw, bn_stream_t stream);
+
 /* Name of a status code (static storage). */
 const char* bn_status_string(bn_status s);
 
