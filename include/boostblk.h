@@ -102,8 +102,10 @@ typedef struct {
 } bn_block_params;
 
 /* Bytes the caller must provide: `saved` (activations kept from forward to
- * backward) and `scratch` (temporaries of either pass; its first 256 bytes hold
- * the device status word). Both depend on desc only. */
+ * backward) and `scratch` (temporaries of either pass). The first 256 bytes of
+ * `scratch` hold the device status word and the kernels' own counters: zero
+ * them once before the first call (the library keeps them consistent after
+ * that). Both sizes depend on desc only. */
 bn_status bn_block_workspace_size(const bn_block_desc* desc, size_t* saved_bytes,
                                   size_t* scratch_bytes);
 

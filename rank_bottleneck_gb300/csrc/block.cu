@@ -79,24 +79,25 @@ int device_sms() {
 // Largest M x ldp(N) summed over the problems of one weight-gradient launch.
 int64_t max_wgrad_elems(const Shape& s) {
   auto ldp = [](int64_t n) { return (n + 7) / 8 * 8; };
+  auto rows = [](int64_t m) { return (m + 127) / 128 * 128; };  // split planes hold whole tiles
   int64_t best = 0;
   auto cand = [&](int64_t v) { best = std::max(best, v); };
   if (s.dense) {
-    cand(s.d * ldp(s.d_ff));
-    cand(2 * s.d_ff * ldp(s.d));
+    cand(rows(s.d) * ldp(s.d_ff));
+    cand(2 * rows(s.d_ff) * ldp(s.d));
     if (s.full()) {
-      cand(s.d * ldp(s.d));
-      cand(3 * s.d * ldp(s.d));
+      cand(rows(s.d) * ldp(s.d));
+      cand(3 * rows(s.d) * ldp(s.d));
     }
   } else {
-    cand(s.d * ldp(s.r));
-    cand(s.r * ldp(s.d_ff));
-    cand(2 * s.d_ff * ldp(s.r));
-    cand(2 * s.r * ldp(s.d));
+    cand(rows(s.d) * ldp(s.r));
+    cand(rows(s.r) * ldp(s.d_ff));
+    cand(2 * rows(s.d_ff) * ldp(s.r));
+    cand(2 * rows(s.r) * ldp(s.d));
     if (s.full()) {
-      cand(s.r * ldp(s.d));
-      cand(3 * s.d * ldp(s.r));
-      cand(3 * s.r * ldp(s.d));
+      cand(rows(s.r) * ldp(s.d));
+      cand(3 * rows(s.d) * ldp(s.r));
+      cand(3 * rows(s.r) * ldp(s.d));
     }
   }
   return best;
@@ -187,8 +188,8 @@ bn_status check_desc(const bn_block_desc* D, Shape& s) {
     return BN_ERR_INVALID_ARG;
   if (!(s.eps >= 0.f) || s.eps > 1.f) return BN_ERR_INVALID_ARG;
   if (!s.dense && s.r < 1) return BN_ERR_INVALID_ARG;
-  // the RMSNorm backward keeps 4 x d fp32 column sums in shared memory
-  if (s.T > (int64_t(1) << 31) - 256 || s.d > 12288 || s.ld_ff > (int64_t(1) << 22) ||
+  // the RMSNorm backward keeps at least one row of d fp32 column sums in shared memory
+  if (s.T > (int64_t(1) << 31) - 256 || s.d > 43688 || s.ld_ff > (int64_t(1) << 22) ||
       s.r > (int64_t(1) << 20))
     return BN_ERR_UNSUPPORTED;
   if (s.d % s.S != 0 || (s.d / s.S) % 8 != 0) return BN_ERR_INVALID_ARG;

@@ -61,6 +61,43 @@ __device__ __forceinline__ float act_grad_f(float z, int sigma) {
   return sigma ? silu_grad_f(z) : 1.0f;
 }
 
+// Compact forms for bf16 data, whose results are rounded to 8 significant
+// bits: sigmoid(z) = 1 / (1 + 2^(-z log2 e)) from the hardware's approximate
+// base-2 exponential and reciprocal (relative error near 2^-22, far below
+// bf16's 2^-9). Every bf16 kernel uses these same instruction sequences, so
+// the forward epilogues and the checkpoint recompute stay bit-identical.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sigmoid_fast(float z) {
+  return rcp_approx(__fadd_rn(1.0f, ex2_approx(__fmul_rn(z, -1.4426950408889634f))));
+}
+__device__ __forceinline__ float silu_fast(float z) { return __fmul_rn(z, sigmoid_fast(z)); }
+__device__ __forceinline__ float silu_grad_fast(float z) {
+  const float s = sigmoid_fast(z);
+  return __fmul_rn(s, __fadd_rn(1.0f, __fmul_rn(z, __fsub_rn(1.0f, s))));
+}
+__device__ __forceinline__ float act_fast(float z, int sigma) { return sigma ? silu_fast(z) : z; }
+__device__ __forceinline__ float act_grad_fast(float z, int sigma) {
+  return sigma ? silu_grad_fast(z) : 1.0f;
+}
+// The nonlinearities for element type T: compact for bf16, accurate for fp32.
+template <typename T> __device__ __forceinline__ float act_t(float z, int sigma);
+template <> __device__ __forceinline__ float act_t<float>(float z, int sigma) { return act_f(z, sigma); }
+template <> __device__ __forceinline__ float act_t<__nv_bfloat16>(float z, int sigma) {
+  return act_fast(z, sigma);
+}
+template <typename T> __device__ __forceinline__ float silu_t(float z);
+template <> __device__ __forceinline__ float silu_t<float>(float z) { return silu_f(z); }
+template <> __device__ __forceinline__ float silu_t<__nv_bfloat16>(float z) { return silu_fast(z); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -31,17 +31,21 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major matrix [outer, inner] with row stride ld.
+// 2-D tensor map over a row-major matrix [outer, inner] with row stride ld
+// (elements of `esize` bytes: 2 = bf16, 4 = fp32).
 static bool encode(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld,
-                   uint32_t box_inner, uint32_t box_outer) {
+                   uint32_t box_inner, uint32_t box_outer,
+                   CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B, int esize = 2) {
   EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
+  if (fn == nullptr || ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) & 15) ||
+      (ld * esize) % 16)
+    return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(m, esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -99,7 +103,7 @@ static int choose_splits(int64_t tiles, int64_t nkb, int64_t MN_total, int grid,
 
 size_t gemm_tc_partial_bytes(int64_t M, int64_t N, int num_sms) {
   (void)num_sms;
-  return static_cast<size_t>(16) * M * tc::ldp_of(N) * 4;
+  return static_cast<size_t>(16) * tc::cdiv(M, tc::BM) * tc::BM * tc::ldp_of(N) * 4;
 }
 
 void gemm_tc(Ctx& c, const GemmLaunch& g) {
@@ -133,7 +137,7 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
       return;
     }
     tiles_total += cdiv(q.M, BM) * cdiv(q.N, BN);
-    mn_total += q.M * ldp_of(q.N);
+    mn_total += cdiv(q.M, BM) * BM * ldp_of(q.N);
     nkb_max = std::max(nkb_max, cdiv(q.K, BK));
   }
   int splits = 1;
@@ -148,6 +152,8 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
 
   int units = 0;
   size_t part_off = 0;
+  void* part_ptr[3] = {nullptr, nullptr, nullptr};
+  int64_t part_ld[3] = {0, 0, 0}, part_rows[3] = {0, 0, 0};
   for (int i = 0; i < g.nprob; ++i) {
     const GemmProblem& q = g.p[i];
     Prob& p = P.p[i];
@@ -167,13 +173,36 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     p.M = q.M;
     p.N = q.N;
     p.K = q.K;
+    // epilogue outputs: 32 x 32 boxes (bf16, 64-byte swizzle; fp32 partials, 128-byte)
+    const int nout = (ek == K_SWIGLU) ? 3 : (ek == K_SIGMA || ek == K_NORM || ek == K_DSWIGLU) ? 2 : 1;
+    const int nin = (ek == K_RESID || ek == K_DSIGMA) ? 1 : (ek == K_DSWIGLU) ? 2 : 0;
+    p.out_mask = 0;
+    p.N8 = q.N / 8 * 8;
     for (int j = 0; j < 3; ++j) {
       p.out[j] = q.out[j];
       p.ldo[j] = q.ldo[j];
     }
-    for (int j = 0; j < 2; ++j) {
-      p.in[j] = q.in[j];
-      p.ldi[j] = q.ldi[j];
+    for (int j = 0; j < nout; ++j) {
+      if (q.out[j] == nullptr) continue;
+      // TMA bounds the innermost dimension in 16-byte units: the map stops at N8
+      // and the epilogue writes columns [N8, N) itself
+      if (p.N8 > 0 &&
+          !encode(&p.mo[j], q.out[j], p.N8, q.M, q.ldo[j], 32, 32, CU_TENSOR_MAP_SWIZZLE_64B, 2)) {
+        c.bad = 2;
+        return;
+      }
+      p.out_mask |= 1 << j;
+    }
+    if (nout == 1 && !(p.out_mask & 1)) {
+      c.bad = 2;
+      return;
+    }
+    // epilogue inputs: 32-column x 128-row boxes
+    for (int j = 0; j < nin; ++j) {
+      if (!encode(&p.mi[j], q.in[j], q.N, q.M, q.ldi[j], 32, 128, CU_TENSOR_MAP_SWIZZLE_64B, 2)) {
+        c.bad = 2;
+        return;
+      }
     }
     p.rowv = q.rowv;
     p.colv = q.colv;
@@ -182,16 +211,22 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     p.kb_per_split = static_cast<int>(cdiv(p.nkb[0], splits));
     p.splits = static_cast<int>(cdiv(p.nkb[0], p.kb_per_split));
     if (split) {
-      p.out[0] = reinterpret_cast<char*>(c.partial) + part_off;
-      p.ldo[0] = ldp_of(q.N);
-      part_off += static_cast<size_t>(p.splits) * q.M * p.ldo[0] * 4;
+      // fp32 partials: split s of this problem is rows [s M, (s + 1) M) of one tensor
+      // split s of this problem owns rows [s * Mp, (s + 1) * Mp), Mp = M rounded up to 128
+      const int64_t Mp = static_cast<int64_t>(p.tiles_m) * BM;
+      part_ptr[i] = reinterpret_cast<char*>(c.partial) + part_off;
+      part_ld[i] = ldp_of(q.N);
+      part_rows[i] = Mp;
+      part_off += static_cast<size_t>(p.splits) * Mp * part_ld[i] * 4;
+      if (part_off > c.partial_bytes ||
+          !encode(&p.mo[0], part_ptr[i], q.N, Mp * p.splits, part_ld[i], 32, 32,
+                  CU_TENSOR_MAP_SWIZZLE_128B, 4)) {
+        c.bad = 4;
+        return;
+      }
     }
     p.unit_begin = units;
     units += p.tiles_m * p.tiles_n * (split ? p.splits : 1);
-  }
-  if (split && part_off > c.partial_bytes) {
-    c.bad = 4;
-    return;
   }
   P.total_units = units;
   const int grid = std::min(units, c.num_sms);
@@ -208,7 +243,8 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
   if (split) {
     for (int i = 0; i < g.nprob; ++i) {
       const Prob& p = P.p[i];
-      launch_splitk_reduce(c, static_cast<const float*>(p.out[0]), p.splits, p.M, p.N, p.ldo[0],
+      launch_splitk_reduce(c, static_cast<const float*>(part_ptr[i]), p.splits, p.M, part_rows[i],
+                           p.N, part_ld[i],
                            static_cast<const __nv_bfloat16*>(g.p[i].colv),
                            static_cast<__nv_bfloat16*>(g.p[i].out[0]), g.p[i].ldo[0]);
     }

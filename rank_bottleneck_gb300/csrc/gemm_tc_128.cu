@@ -8,11 +8,11 @@ template <int EK, bool AMN, bool BMN>
 static void go(const Params& P, int grid, cudaStream_t s) {
   auto k = gemm_kernel<128, EK, AMN, BMN>;
   static const bool attr_set = [&]() {
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<128>::SMEM_BYTES);
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<128, EK>::SMEM_BYTES);
     return true;
   }();
   (void)attr_set;
-  k<<<grid, NUM_THREADS, Cfg<128>::SMEM_BYTES, s>>>(P);
+  k<<<grid, NUM_THREADS, Cfg<128, EK>::SMEM_BYTES, s>>>(P);
 }
 
 bool launch_bn128(int ek, bool a_mn, bool b_mn, const Params& P, int grid, cudaStream_t s) {

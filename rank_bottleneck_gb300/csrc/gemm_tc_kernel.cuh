@@ -1,19 +1,28 @@
 // tcgen05 / TMA / TMEM GEMM engine for sm_103a with fused epilogues.
 //
-// One persistent CTA per SM (192 threads):
-//   warp 0        TMA producer: fills a ring of shared-memory stages, each one
-//                 128 x 64 tile of A and one BN x 64 tile of B (bf16, 128-byte
-//                 swizzle), completion tracked by an mbarrier per stage;
+// One persistent CTA per SM (352 threads):
+//   warp 0        operand producer: TMA loads into a ring of shared-memory
+//                 stages, each one 128 x 64 tile of A and one BN x 64 tile of
+//                 B (bf16, 128-byte swizzle), one mbarrier per stage;
 //   warp 1        owns the TMEM allocation (all 512 columns) and, from one
 //                 thread, issues tcgen05.mma (M = 128, N = BN, K = 16, fp32
 //                 accumulate) into a ring of TMEM accumulator slots of BN
 //                 columns; tcgen05.commit frees a stage / publishes a slot;
-//   warps 2..5    epilogue: tcgen05.ld each slot (warp w reads TMEM lanes
-//                 32 (w % 4) .. +31, i.e. one tile row per thread), apply the
-//                 fused epilogue, store to global memory, free the slot.
-// A work unit is one 128 x BN output tile (or one K split of it). A unit is a
-// sequence of segments; each segment is a K range, possibly of another operand
-// pair, and lands in its own slot: this is how Online RMSNorm sees each
+//   warps 2..9    epilogue, two groups of four: tcgen05.ld (warp w reads TMEM
+//                 lanes 32 (w % 4) .. +31: one tile row per thread; group g
+//                 takes the tile's 32-column subtiles c with c % 2 == g), fused
+//                 math, results written to a swizzled shared-memory subtile and
+//                 stored with TMA;
+//   warp 10       epilogue-input producer: TMA loads of the tensors an
+//                 epilogue reads (residual, z, G and U) into the same
+//                 subtile ring, ahead of the epilogue.
+// The epilogue works on 128 x 32 subtiles; warp w owns rows 32 (w % 4) .. +31
+// of each and stores them as one 32 x 32 TMA box, so every global access is a
+// bulk copy and the threads only touch conflict-free swizzled shared memory.
+//
+// A work unit is one 128 x BN output tile (or one K split of it), a sequence
+// of segments; each segment is a K range, possibly of another operand pair,
+// accumulated in its own TMEM slot: this is how Online RMSNorm sees each
 // emulated shard's partial product and how SwiGLU sees G and U side by side.
 //
 // Every mbarrier wait is bounded by wall time (kWaitLimitNs). On expiry the
@@ -30,8 +39,10 @@ namespace tc {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
-constexpr int NUM_THREADS = 192;
-constexpr int NUM_EPI_WARPS = 4;
+constexpr int NUM_EPI_WARPS = 8;                 // two groups of four
+constexpr int NUM_THREADS = 32 * (3 + NUM_EPI_WARPS);
+constexpr int EPI_GROUPS = NUM_EPI_WARPS / 4;
+constexpr int EPI_N = 32;  // columns per epilogue subtile
 
 // epilogue kinds of the kernel template
 enum : int {
@@ -39,30 +50,49 @@ enum : int {
   K_DSIGMA = 6, K_DSWIGLU = 7, K_CHAIN = 8
 };
 
-template <int BN>
+template <int EK>
+struct EpiShape {
+  static constexpr int NIN = (EK == K_RESID || EK == K_DSIGMA) ? 1 : (EK == K_DSWIGLU) ? 2 : 0;
+  static constexpr int NOUT =
+      (EK == K_SWIGLU) ? 3 : (EK == K_SIGMA || EK == K_NORM || EK == K_DSWIGLU) ? 2 : 1;
+  static constexpr int NT = NIN > NOUT ? NIN : NOUT;         // subtiles per ring entry
+  static constexpr int ELEM = (EK == K_PART) ? 4 : 2;        // output element bytes
+  static constexpr int SUB_BYTES = BM * EPI_N * ELEM;        // one 128 x 32 subtile
+  static constexpr int WARP_BYTES = 32 * EPI_N * ELEM;       // one warp's 32 rows of it
+  static constexpr int NE = (EK == K_PART) ? 2 : 4;          // ring entries
+  static constexpr int BYTES = NE * NT * SUB_BYTES;
+};
+
+template <int BN, int EK>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
   static constexpr int NSLOT = 512 / BN;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM_LIMIT = 232448;
+  static constexpr int EPI_BYTES = EpiShape<EK>::BYTES;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - 1024 - BAR_BYTES - EPI_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+  static_assert(STAGES >= 2, "shared memory too small for the pipeline");
 };
 
 struct Prob {
   CUtensorMap ma[2];  // A operand of segment pair 0 / 1
   CUtensorMap mb[2];  // B operand of segment pair 0 / 1
+  CUtensorMap mo[3];  // outputs: 32 x 32 boxes
+  CUtensorMap mi[2];  // epilogue inputs: 32-column x 128-row boxes
   int64_t M, N, K;
-  void* out[3];
+  int64_t N8;         // N rounded down to a multiple of 8: TMA stores cover [0, N8)
+  void* out[3];       // raw outputs, for the ragged columns [N8, N)
   int64_t ldo[3];
-  const void* in[2];
-  int64_t ldi[2];
   const float* rowv;
   const void* colv;
   int tiles_m, tiles_n, unit_begin;
   int nkb[2];         // k-blocks of operand pair 0 / 1
   int splits, kb_per_split;
+  int out_mask;       // bit k: output k is written
 };
 
 struct Params {
@@ -100,8 +130,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase of `bar` with parity `parity` to complete.
-static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                      int* status, unsigned long long limit_ns = kWaitLimitNs) {
+static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, int* status,
+                                             unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
@@ -124,6 +155,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// wait until at most N of this thread's bulk groups still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// make this thread's shared-memory writes visible to the TMA (async) proxy
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -201,48 +253,62 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool a_mn, bool 
 }
 
 // ---------------------------------------------------------------------------
-// epilogue I/O of one 32-column chunk of one row
+// one thread's row of a warp's 32 x 32 subtile block in shared memory
+//  bf16: 64-byte rows, 64-byte swizzle (16-byte chunk c of row t at c ^ ((t >> 1) & 3))
+//  fp32: 128-byte rows, 128-byte swizzle (chunk c of row t at c ^ (t & 7))
+// These are the layouts TMA reads and writes for boxes of 32 columns with
+// SWIZZLE_64B / SWIZZLE_128B, and a warp's 16-byte accesses are conflict free.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void st_chunk(__nv_bfloat16* base, int64_t ld, int64_t row,
-                                         int64_t col0, int64_t M, int64_t N, const float* v) {
-  if (base == nullptr || row >= M) return;
-  __nv_bfloat16* p = base + row * ld + col0;
-  if (col0 + 32 <= N) {
+__device__ __forceinline__ void smem_row_store_bf16(uint8_t* blk, int t, const float* v) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) Vec8<__nv_bfloat16>::store(p + 8 * i, v + 8 * i);
-  } else {
+  for (int c = 0; c < 4; ++c) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (col0 + i < N) p[i] = __float2bfloat16_rn(v[i]);
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * c + 2 * i], v[8 * c + 2 * i + 1]);
+    *reinterpret_cast<uint4*>(blk + t * 64 + ((c ^ ((t >> 1) & 3)) << 4)) = u;
   }
 }
-__device__ __forceinline__ void st_chunk_f32(float* base, int64_t ld, int64_t row, int64_t col0,
-                                             int64_t M, int64_t N, const float* v) {
-  if (row >= M) return;
-  float* p = base + row * ld + col0;
-  if (col0 + 32 <= N) {
+__device__ __forceinline__ void smem_row_load_bf16(const uint8_t* blk, int t, float* v) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) Vec8<float>::store(p + 8 * i, v + 8 * i);
-  } else {
+  for (int c = 0; c < 4; ++c) {
+    const uint4 u = *reinterpret_cast<const uint4*>(blk + t * 64 + ((c ^ ((t >> 1) & 3)) << 4));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (col0 + i < N) p[i] = v[i];
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[8 * c + 2 * i] = f.x;
+      v[8 * c + 2 * i + 1] = f.y;
+    }
   }
 }
-__device__ __forceinline__ void ld_chunk(const __nv_bfloat16* base, int64_t ld, int64_t row,
-                                         int64_t col0, int64_t M, int64_t N, float* v) {
-  if (row >= M) {
+__device__ __forceinline__ void smem_row_store_f32(uint8_t* blk, int t, const float* v) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0.f;
-    return;
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<float4*>(blk + t * 128 + ((c ^ (t & 7)) << 4)) =
+        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
+// Columns [max(col0, N8), min(col0 + 32, N)) of one row, written directly: TMA
+// bounds the innermost dimension in 16-byte units, so the maps stop at N8 and
+// this covers the last (N mod 8) columns.
+__device__ __forceinline__ void store_tail_bf16(void* base, int64_t ld, int64_t row, int64_t col0,
+                                                int64_t N8, int64_t N, const float* v) {
+  __nv_bfloat16* p = static_cast<__nv_bfloat16*>(base) + row * ld;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int64_t col = col0 + i;
+    if (col >= N8 && col < N) p[col] = __float2bfloat16_rn(v[i]);
   }
-  const __nv_bfloat16* p = base + row * ld + col0;
+}
+// 32 bf16 values starting at column col0 of a vector of length N (zero beyond N)
+__device__ __forceinline__ void ld_vec_bf16(const __nv_bfloat16* p, int64_t col0, int64_t N,
+                                            float* v) {
   if (col0 + 32 <= N) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) Vec8<__nv_bfloat16>::load(p + 8 * i, v + 8 * i);
+    for (int i = 0; i < 4; ++i) Vec8<__nv_bfloat16>::load(p + col0 + 8 * i, v + 8 * i);
   } else {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = (col0 + i < N) ? __bfloat162float(p[i]) : 0.f;
+    for (int i = 0; i < 32; ++i) v[i] = (col0 + i < N) ? __bfloat162float(p[col0 + i]) : 0.f;
   }
 }
 
@@ -251,7 +317,7 @@ __device__ __forceinline__ void ld_chunk(const __nv_bfloat16* base, int64_t ld, 
 // ---------------------------------------------------------------------------
 struct Work {
   int pi, split;
-  int64_t m0, n0;
+  int64_t m0, nb;
 };
 
 __device__ __forceinline__ Work decode(const Params& P, int u) {
@@ -265,7 +331,7 @@ __device__ __forceinline__ Work decode(const Params& P, int u) {
   w.split = local / tiles;
   const int t = local - w.split * tiles;
   w.m0 = static_cast<int64_t>(t / pr.tiles_n) * BM;
-  w.n0 = t % pr.tiles_n;  // n-block index; the kernel scales it by BN
+  w.nb = t % pr.tiles_n;  // n-block index; the kernel scales it by BN
   return w;
 }
 
@@ -298,16 +364,21 @@ __device__ __forceinline__ void segment(const Params& P, const Prob& pr, int spl
 // ---------------------------------------------------------------------------
 template <int BN, int EK, bool AMN, bool BMN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Params P) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EK>;
+  using E = EpiShape<EK>;
+  constexpr int NCH = BN / EPI_N;  // epilogue subtiles per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* epi = smem + C::STAGES * C::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::EPI_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = full + C::STAGES;
   uint64_t* accf = empty + C::STAGES;
   uint64_t* acce = accf + C::NSLOT;
-  uint64_t* drain = acce + C::NSLOT;
+  uint64_t* epi_full = acce + C::NSLOT;
+  uint64_t* epi_empty = epi_full + E::NE;
+  uint64_t* drain = epi_empty + E::NE;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -323,6 +394,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       mbar_init(smem_u32(&accf[i]), 1);
       mbar_init(smem_u32(&acce[i]), NUM_EPI_WARPS);
     }
+    for (int i = 0; i < E::NE; ++i) {
+      mbar_init(smem_u32(&epi_full[i]), 1);
+      mbar_init(smem_u32(&epi_empty[i]), 4);  // the four warps of the group that used it
+    }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -336,7 +411,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
   const int nseg = num_segments<EK>(P);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ operand producer
     if (lane == 0) {
       for (int i = 0; i < P.nprob; ++i) {
         tma_prefetch_desc(&P.p[i].ma[0]);
@@ -350,7 +425,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         const Work w = decode(P, u);
         const Prob& pr = P.p[w.pi];
         const int m0 = static_cast<int>(w.m0);
-        const int n0 = static_cast<int>(w.n0) * BN;
+        const int n0 = static_cast<int>(w.nb) * BN;
         for (int s = 0; ok && s < nseg; ++s) {
           int kb0, nkb, pair;
           segment<EK>(P, pr, w.split, s, kb0, nkb, pair);
@@ -457,12 +532,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       mma_commit(smem_u32(drain));
       wait_bar(smem_u32(drain), 0, abort_flag, P.status, ok ? kWaitLimitNs : 50ull * 1000 * 1000);
     }
+  } else if (warp == 2 + NUM_EPI_WARPS) {
+    // ------------------------------------------------------------ epilogue-input producer
+    if (E::NIN > 0 && lane == 0) {
+      int e = 0;
+      uint32_t eph = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x) {
+        const Work w = decode(P, u);
+        const Prob& pr = P.p[w.pi];
+        const int m0 = static_cast<int>(w.m0);
+        const int n0 = static_cast<int>(w.nb) * BN;
+        for (int c = 0; c < NCH; ++c) {
+          if (!wait_bar(smem_u32(&epi_empty[e]), eph ^ 1u, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&epi_full[e]);
+          mbar_expect_tx(fb, E::NIN * E::SUB_BYTES);
+#pragma unroll
+          for (int k = 0; k < E::NIN; ++k)
+            tma_load_2d(smem_u32(epi + (e * E::NT + k) * E::SUB_BYTES), &pr.mi[k], n0 + c * EPI_N,
+                        m0, fb);
+          ++issued;
+          if (++e == E::NE) {
+            e = 0;
+            eph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // drain the loads in flight before the CTA exits
+        int st = e;
+        uint32_t p = eph;
+        for (int i = 0; i < E::NE && i < issued; ++i) {
+          if (--st < 0) {
+            st = E::NE - 1;
+            p ^= 1u;
+          }
+          wait_bar(smem_u32(&epi_full[st]), p, abort_flag, P.status, 50ull * 1000 * 1000);
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;                 // TMEM lane quarter = tile rows 32q .. 32q + 31
+    const int grp = (warp - 2) >> 2;        // this warp's subtiles: c % EPI_GROUPS == grp
+    constexpr int MYCH = NCH / EPI_GROUPS;  // subtiles per warp per tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int slot = 0;
     uint32_t sph = 0;
+    int prev_e = 0, mine = 0;
+    int64_t tile_no = 0;                    // tiles this CTA has finished
     bool ok = true;
     auto acquire = [&](int sl, uint32_t p) -> bool {
       if (!wait_bar(smem_u32(&accf[sl]), p, abort_flag, P.status)) return false;
@@ -480,19 +602,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         sph ^= 1u;
       }
     };
-    for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x, ++tile_no) {
       const Work w = decode(P, u);
       const Prob& pr = P.p[w.pi];
       const int64_t row = w.m0 + q * 32 + lane;
-      const int64_t n0 = w.n0 * BN;
+      const int64_t n0 = w.nb * BN;
       const int64_t M = pr.M, N = pr.N;
+      const bool row_ok = row < M;
+      float R[EK == K_NORM ? MYCH * 32 : 1];
+      int sl0 = slot, sl1 = slot;  // TMEM slot(s) of this tile's accumulator(s)
       if constexpr (EK == K_NORM) {
         // Online RMSNorm: fold each shard's partial product with its own factors
-        float R[BN];
         const int S = P.S;
-        const float* ss = pr.rowv + (row < M ? row : 0) * S;
+        const float* ss = pr.rowv + (row_ok ? row : 0) * S;
         float tot = 0.f;
-        for (int s = 0; s < S; ++s) tot += (row < M) ? ss[s] : 0.f;
+        for (int s = 0; s < S; ++s) tot += row_ok ? ss[s] : 0.f;
         const float shard_w = static_cast<float>(pr.K / S);
         const float rms_g = sqrtf(tot / static_cast<float>(pr.K) + P.eps);
         for (int s = 0; s < S; ++s) {
@@ -500,135 +624,188 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             ok = false;
             break;
           }
-          const float ss_s = (row < M) ? ss[s] : 0.f;
+          const float ss_s = row_ok ? ss[s] : 0.f;
           const float rms_s = sqrtf(ss_s / shard_w + P.eps);
-          const float inv_local = 1.0f / rms_s;    // local normalisation
-          const float alpha = rms_s / rms_g;       // per-row correction
+          const float inv_local = 1.0f / rms_s;  // local normalisation
+          const float alpha = rms_s / rms_g;     // per-row correction
           const uint32_t t0 = tmem + lane_base + static_cast<uint32_t>(slot * BN);
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int k = 0; k < MYCH; ++k) {
             float v[32];
-            tmem_ld32(t0 + c * 32, v);
+            tmem_ld32(t0 + (k * EPI_GROUPS + grp) * 32, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float local = v[i] * inv_local;
-              R[c * 32 + i] = (s == 0) ? alpha * local : fmaf(alpha, local, R[c * 32 + i]);
+              R[k * 32 + i] = (s == 0) ? alpha * local : fmaf(alpha, local, R[k * 32 + i]);
             }
           }
           release(slot);
           advance();
         }
         if (!ok) break;
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          float z[32], h[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            z[i] = round_to<__nv_bfloat16>(R[c * 32 + i]);
-            h[i] = act_f(z[i], P.sigma);
-          }
-          st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, n0 + c * 32, M, N, z);
-          st_chunk(static_cast<__nv_bfloat16*>(pr.out[1]), pr.ldo[1], row, n0 + c * 32, M, N, h);
-        }
       } else if constexpr (EK == K_SWIGLU) {
-        const int sg = slot;
-        const uint32_t pg = sph;
+        sl0 = slot;
+        const uint32_t p0 = sph;
         advance();
-        const int su = slot;
-        const uint32_t pu = sph;
+        sl1 = slot;
+        const uint32_t p1 = sph;
         advance();
-        if (!acquire(sg, pg) || !acquire(su, pu)) {
+        if (!acquire(sl0, p0) || !acquire(sl1, p1)) {
           ok = false;
           break;
         }
-        const uint32_t tg = tmem + lane_base + static_cast<uint32_t>(sg * BN);
-        const uint32_t tu = tmem + lane_base + static_cast<uint32_t>(su * BN);
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float G[32], U[32], m[32];
-          tmem_ld32(tg + c * 32, G);
-          tmem_ld32(tu + c * 32, U);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            G[i] = round_to<__nv_bfloat16>(G[i]);
-            U[i] = round_to<__nv_bfloat16>(U[i]);
-            m[i] = __fmul_rn(silu_f(G[i]), U[i]);
-          }
-          const int64_t col = n0 + c * 32;
-          st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, G);
-          st_chunk(static_cast<__nv_bfloat16*>(pr.out[1]), pr.ldo[1], row, col, M, N, U);
-          st_chunk(static_cast<__nv_bfloat16*>(pr.out[2]), pr.ldo[2], row, col, M, N, m);
-        }
-        release(sg);
-        release(su);
       } else {
+        sl0 = slot;
         if (!acquire(slot, sph)) {
           ok = false;
           break;
         }
-        const uint32_t t0 = tmem + lane_base + static_cast<uint32_t>(slot * BN);
-        float rs = 1.f;
-        if ((EK == K_STORE || EK == K_CHAIN || EK == K_DSIGMA || EK == K_DSWIGLU) &&
-            pr.rowv != nullptr && row < M)
-          rs = pr.rowv[row];
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(t0 + c * 32, v);
-          const int64_t col = n0 + c * 32;
-          if constexpr (EK == K_PART) {
-            float* base = static_cast<float*>(pr.out[0]) + static_cast<int64_t>(w.split) * M * pr.ldo[0];
-            st_chunk_f32(base, pr.ldo[0], row, col, M, N, v);
-          } else if constexpr (EK == K_STORE || EK == K_CHAIN) {
-            if (pr.colv != nullptr) {
-              float cv[32];
-              ld_chunk(static_cast<const __nv_bfloat16*>(pr.colv), 0, 0, col, 1, N, cv);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= cv[i];
-            }
-            if (pr.rowv != nullptr) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= rs;
-            }
-            st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, v);
-          } else if constexpr (EK == K_SIGMA) {
-            float h[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              v[i] = round_to<__nv_bfloat16>(v[i]);
-              h[i] = act_f(v[i], P.sigma);
-            }
-            st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, v);
-            st_chunk(static_cast<__nv_bfloat16*>(pr.out[1]), pr.ldo[1], row, col, M, N, h);
-          } else if constexpr (EK == K_RESID) {
-            float r[32];
-            ld_chunk(static_cast<const __nv_bfloat16*>(pr.in[0]), pr.ldi[0], row, col, M, N, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] += r[i];
-            st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, v);
-          } else if constexpr (EK == K_DSIGMA) {
-            float z[32];
-            ld_chunk(static_cast<const __nv_bfloat16*>(pr.in[0]), pr.ldi[0], row, col, M, N, z);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = (v[i] * act_grad_f(z[i], P.sigma)) * rs;
-            st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, v);
-          } else if constexpr (EK == K_DSWIGLU) {
-            float G[32], U[32], dU[32];
-            ld_chunk(static_cast<const __nv_bfloat16*>(pr.in[0]), pr.ldi[0], row, col, M, N, G);
-            ld_chunk(static_cast<const __nv_bfloat16*>(pr.in[1]), pr.ldi[1], row, col, M, N, U);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              dU[i] = (v[i] * silu_f(G[i])) * rs;
-              v[i] = ((v[i] * U[i]) * silu_grad_f(G[i])) * rs;
-            }
-            st_chunk(static_cast<__nv_bfloat16*>(pr.out[0]), pr.ldo[0], row, col, M, N, v);
-            st_chunk(static_cast<__nv_bfloat16*>(pr.out[1]), pr.ldo[1], row, col, M, N, dU);
-          }
-        }
-        release(slot);
         advance();
       }
+      float rs = 1.f;
+      if ((EK == K_STORE || EK == K_CHAIN || EK == K_DSIGMA || EK == K_DSWIGLU) &&
+          pr.rowv != nullptr && row_ok)
+        rs = pr.rowv[row];
+
+      // the NORM fold keeps its accumulator in registers indexed by k: unrolled;
+      // the other epilogues stay rolled to keep the kernel small
+#pragma unroll(EK == K_NORM ? MYCH : 1)
+      for (int k = 0; k < MYCH; ++k) {
+        const int c = k * EPI_GROUPS + grp;            // subtile within the tile
+        const int64_t col0 = n0 + c * EPI_N;
+        const int64_t j = tile_no * NCH + c;           // subtile sequence number of this CTA
+        const int e = static_cast<int>(j % E::NE);
+        const uint32_t eph = static_cast<uint32_t>((j / E::NE) & 1);
+        if (E::NIN > 0) {
+          if (!wait_bar(smem_u32(&epi_full[e]), eph, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+        }
+        float v[32];
+        float v2[EK == K_SWIGLU ? 32 : 1];
+        if constexpr (EK == K_NORM) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = R[k * 32 + i];
+        } else {
+          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl0 * BN + c * 32), v);
+          if constexpr (EK == K_SWIGLU)
+            tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl1 * BN + c * 32), v2);
+          if (k == MYCH - 1) {
+            release(sl0);
+            if (EK == K_SWIGLU) release(sl1);
+          }
+        }
+        uint8_t* ent = epi + e * E::NT * E::SUB_BYTES + q * E::WARP_BYTES;
+        // this row holds some of the ragged columns [N8, N) (fp32 partials need none)
+        const bool tail = EK != K_PART && row_ok && col0 + EPI_N > pr.N8 && col0 < N;
+        if constexpr (EK == K_PART) {
+          smem_row_store_f32(ent, lane, v);
+        } else if constexpr (EK == K_STORE || EK == K_CHAIN) {
+          if (pr.colv != nullptr) {
+            float cv[32];
+            ld_vec_bf16(static_cast<const __nv_bfloat16*>(pr.colv), col0, N, cv);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= cv[i];
+          }
+          if (pr.rowv != nullptr) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= rs;
+          }
+          smem_row_store_bf16(ent, lane, v);
+          if (tail) store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, v);
+        } else if constexpr (EK == K_SIGMA || EK == K_NORM) {
+          float h[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v[i] = round_to<__nv_bfloat16>(v[i]);
+            h[i] = act_fast(v[i], P.sigma);
+          }
+          smem_row_store_bf16(ent, lane, v);
+          smem_row_store_bf16(ent + E::SUB_BYTES, lane, h);
+          if (tail) {
+            store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, v);
+            if (pr.out_mask & 2) store_tail_bf16(pr.out[1], pr.ldo[1], row, col0, pr.N8, N, h);
+          }
+        } else if constexpr (EK == K_SWIGLU) {
+          float m[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v[i] = round_to<__nv_bfloat16>(v[i]);
+            v2[i] = round_to<__nv_bfloat16>(v2[i]);
+            m[i] = __fmul_rn(silu_fast(v[i]), v2[i]);
+          }
+          smem_row_store_bf16(ent, lane, v);
+          smem_row_store_bf16(ent + E::SUB_BYTES, lane, v2);
+          smem_row_store_bf16(ent + 2 * E::SUB_BYTES, lane, m);
+          if (tail) {
+            if (pr.out_mask & 1) store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, v);
+            if (pr.out_mask & 2) store_tail_bf16(pr.out[1], pr.ldo[1], row, col0, pr.N8, N, v2);
+            store_tail_bf16(pr.out[2], pr.ldo[2], row, col0, pr.N8, N, m);
+          }
+        } else if constexpr (EK == K_RESID) {
+          float r[32];
+          smem_row_load_bf16(ent, lane, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] += r[i];
+          smem_row_store_bf16(ent, lane, v);
+          if (tail) store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, v);
+        } else if constexpr (EK == K_DSIGMA) {
+          float z[32];
+          smem_row_load_bf16(ent, lane, z);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = (v[i] * act_grad_fast(z[i], P.sigma)) * rs;
+          smem_row_store_bf16(ent, lane, v);
+          if (tail) store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, v);
+        } else if constexpr (EK == K_DSWIGLU) {
+          float G[32], U[32];
+          smem_row_load_bf16(ent, lane, G);
+          smem_row_load_bf16(ent + E::SUB_BYTES, lane, U);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float sg = sigmoid_fast(G[i]);
+            const float dsilu = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(G[i], __fsub_rn(1.0f, sg))));
+            U[i] = ((v[i] * U[i]) * dsilu) * rs;          // dG
+            G[i] = (v[i] * __fmul_rn(G[i], sg)) * rs;     // dU
+          }
+          smem_row_store_bf16(ent, lane, U);
+          smem_row_store_bf16(ent + E::SUB_BYTES, lane, G);
+          if (tail) {
+            store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, U);
+            store_tail_bf16(pr.out[1], pr.ldo[1], row, col0, pr.N8, N, G);
+          }
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t src = smem_u32(ent);
+          const int rt = static_cast<int>(w.m0) + q * 32;  // row within the problem
+          // split-K partials: split s owns rows [s * tiles_m * 128, (s + 1) * tiles_m * 128)
+          const int r0 = rt + (EK == K_PART ? w.split * pr.tiles_m * BM : 0);
+          const int64_t lim = (EK == K_PART) ? N : pr.N8;  // extent of the output maps
+          if (rt < M && col0 < lim) {  // boxes partly outside the tensor are clipped by TMA
+#pragma unroll
+            for (int o = 0; o < E::NOUT; ++o)
+              if (pr.out_mask & (1 << o))
+                tma_store_2d(&pr.mo[o], src + o * E::SUB_BYTES, static_cast<int>(col0), r0);
+          }
+          bulk_commit();
+          // a warp reuses a ring entry every NE / EPI_GROUPS of its own subtiles: the
+          // stores issued from that entry must have left shared memory by then
+          bulk_wait_read<E::NE / EPI_GROUPS - 1>();
+          if (E::NIN > 0 && mine > 0) mbar_arrive(smem_u32(&epi_empty[prev_e]));
+        }
+        __syncwarp();
+        prev_e = e;
+        ++mine;
+      }
     }
+    if (lane == 0) {
+      bulk_wait_read<0>();
+      if (E::NIN > 0 && mine > 0) mbar_arrive(smem_u32(&epi_empty[prev_e]));
+      bulk_wait_all();
+    }
+    __syncwarp();
   }
 
   tc_fence_before();

@@ -77,70 +77,117 @@ void launch_fold_cols(Ctx& c, const T* A, const T* w, int64_t rows, int64_t cols
 }
 
 // ---------------------------------------------------------------------------
-// B3: RMSNorm backward. One warp per row; each warp keeps its own column
-// accumulators for dw in shared memory (lane-exclusive columns, no atomics),
-// summed over the 4 warps and then over blocks in a fixed order.
+// B3: RMSNorm backward. One warp per row, 4 x 16 bytes of every tensor in
+// flight per lane; each warp keeps its own dw column sums in shared memory
+// (lane-exclusive columns, no atomics). Every block writes its column sums to
+// a row of `part`; colsum_kernel adds the rows in a fixed order, so dw is
+// bit-reproducible.
 // ---------------------------------------------------------------------------
-constexpr int kNormBwdWarps = 4;
+constexpr int kNormBwdMaxWarps = 8;
+constexpr int kNormBwdUnroll = 4;
+constexpr size_t kNormBwdSmemLimit = 200 * 1024;
 
 template <typename T>
-__global__ void __launch_bounds__(kNormBwdWarps * 32)
+__global__ void __launch_bounds__(kNormBwdMaxWarps * 32)
     norm_bwd_kernel(const T* __restrict__ dn, const T* __restrict__ x, const T* __restrict__ w,
                     const float* __restrict__ rstd, const T* __restrict__ dres, int64_t rows,
                     int d, T* __restrict__ dx, float* __restrict__ part) {
-  extern __shared__ float acc[];  // [kNormBwdWarps][d]
+  // [warps][d + d/8] column sums; column c lives at c + c/8, so the 8 columns a
+  // lane owns are 9 floats apart from the next lane's: no bank conflicts
+  extern __shared__ float acc[];
+  const int nw = blockDim.x >> 5;
+  const int dp = d + d / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < kNormBwdWarps * d; i += blockDim.x) acc[i] = 0.f;
+  for (int i = threadIdx.x; i < nw * dp; i += blockDim.x) acc[i] = 0.f;
   __syncthreads();
-  float* my = acc + warp * d;
+  float* my = acc + warp * dp;
   const float inv_d = 1.0f / static_cast<float>(d);
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kNormBwdWarps + warp; row < rows;
-       row += static_cast<int64_t>(gridDim.x) * kNormBwdWarps) {
+  constexpr int U = kNormBwdUnroll;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * nw + warp; row < rows;
+       row += static_cast<int64_t>(gridDim.x) * nw) {
     const T* dnr = dn + row * d;
     const T* xr = x + row * d;
     float s = 0.f;
-    for (int c = lane * 8; c < d; c += 256) {
-      float a[8], b[8], ww[8];
-      Vec8<T>::load(dnr + c, a);
-      Vec8<T>::load(xr + c, b);
-      Vec8<T>::load(w + c, ww);
+    for (int base = lane * 8; base < d; base += 256 * U) {
+      float a[U][8], b[U][8], ww[U][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s = fmaf(a[i] * ww[i], b[i], s);
+      for (int u = 0; u < U; ++u) {
+        const int c = base + u * 256;
+        if (c < d) {
+          Vec8<T>::load(dnr + c, a[u]);
+          Vec8<T>::load(xr + c, b[u]);
+          Vec8<T>::load(w + c, ww[u]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a[u][i] = b[u][i] = ww[u][i] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s = fmaf(a[u][i] * ww[u][i], b[u][i], s);
     }
     s = warp_sum(s);
     const float r = rstd[row];
     const float coef = r * r * s * inv_d;
     const T* dr = dres + row * d;
     T* o = dx + row * d;
-    for (int c = lane * 8; c < d; c += 256) {
-      float a[8], b[8], ww[8], g[8];
-      Vec8<T>::load(dnr + c, a);
-      Vec8<T>::load(xr + c, b);
-      Vec8<T>::load(w + c, ww);
-      Vec8<T>::load(dr + c, g);
+    for (int base = lane * 8; base < d; base += 256 * U) {
+      float a[U][8], b[U][8], ww[U][8], g[U][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        g[i] = g[i] + (a[i] * ww[i] - b[i] * coef);
-        my[c + i] = fmaf(a[i], b[i], my[c + i]);
+      for (int u = 0; u < U; ++u) {
+        const int c = base + u * 256;
+        if (c < d) {
+          Vec8<T>::load(dnr + c, a[u]);
+          Vec8<T>::load(xr + c, b[u]);
+          Vec8<T>::load(w + c, ww[u]);
+          Vec8<T>::load(dr + c, g[u]);
+        }
       }
-      Vec8<T>::store(o + c, g);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = base + u * 256;
+        if (c < d) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            g[u][i] = g[u][i] + (a[u][i] * ww[u][i] - b[u][i] * coef);
+            my[c + c / 8 + i] = fmaf(a[u][i], b[u][i], my[c + c / 8 + i]);
+          }
+          Vec8<T>::store(o + c, g[u]);
+        }
+      }
     }
   }
   __syncthreads();
   for (int col = threadIdx.x; col < d; col += blockDim.x) {
-    float v = acc[col];
-    for (int k = 1; k < kNormBwdWarps; ++k) v += acc[k * d + col];
+    float v = acc[col + col / 8];
+    for (int k = 1; k < nw; ++k) v += acc[k * dp + col + col / 8];
     part[static_cast<int64_t>(blockIdx.x) * d + col] = v;
   }
 }
 
+// dw[col] = sum over blocks b of part[b][col]: 32 columns per block, each of the
+// 8 warps sums a fixed contiguous range of b, the 8 sums are added in warp order.
 template <typename T>
-__global__ void colsum_kernel(const float* __restrict__ part, int nblk, int d, T* __restrict__ out) {
-  const int col = blockIdx.x * blockDim.x + threadIdx.x;
-  if (col >= d) return;
+__global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ part, int nblk, int d,
+                                                     T* __restrict__ out) {
+  __shared__ float red[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = blockIdx.x * 32 + lane;
+  const int per = (nblk + 7) / 8;
+  const int b0 = warp * per, b1 = min(nblk, b0 + per);
   float v = 0.f;
-  for (int b = 0; b < nblk; ++b) v += part[static_cast<int64_t>(b) * d + col];
-  out[col] = from_f<T>(v);
+  if (col < d) {
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) v += part[static_cast<int64_t>(b) * d + col];
+  }
+  red[warp][lane] = v;
+  __syncthreads();
+  if (warp == 0 && col < d) {
+    float t = red[0][lane];
+    for (int k = 1; k < 8; ++k) t += red[k][lane];
+    out[col] = from_f<T>(t);
+  }
 }
 
 int norm_bwd_blocks(int num_sms) { return 2 * num_sms; }
@@ -148,20 +195,24 @@ int norm_bwd_blocks(int num_sms) { return 2 * num_sms; }
 template <typename T>
 void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rstd,
                      const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw) {
-  const size_t smem = sizeof(float) * kNormBwdWarps * static_cast<size_t>(d);
+  // as many warps (<= 8) as their column sums fit in shared memory
+  const size_t row_bytes = sizeof(float) * static_cast<size_t>(d + d / 8);
+  const int nw = static_cast<int>(std::max<size_t>(
+      1, std::min<size_t>(kNormBwdMaxWarps, kNormBwdSmemLimit / row_bytes)));
+  const size_t smem = row_bytes * nw;
   static const bool attr = [] {
     cudaFuncSetAttribute(norm_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         200 * 1024);
+                         static_cast<int>(kNormBwdSmemLimit));
     return true;
   }();
   (void)attr;
   prof_start(c);
-  norm_bwd_kernel<T><<<nblk, kNormBwdWarps * 32, smem, c.stream>>>(dn, x, w, rstd, dres, rows,
-                                                                   static_cast<int>(d), dx, part);
+  norm_bwd_kernel<T><<<nblk, nw * 32, smem, c.stream>>>(
+      dn, x, w, rstd, dres, rows, static_cast<int>(d), dx, part);
   note_launch(c, KK_NORM_BWD, -1, 8.0 * rows * d,
               4.0 * rows * d * sizeof(T) + d * sizeof(T) + 4.0 * rows + 4.0 * nblk * d);
   prof_start(c);
-  colsum_kernel<T><<<static_cast<unsigned>((d + 255) / 256), 256, 0, c.stream>>>(
+  colsum_kernel<T><<<static_cast<unsigned>((d + 31) / 32), 256, 0, c.stream>>>(
       part, nblk, static_cast<int>(d), dw);
   note_launch(c, KK_COLSUM, -1, 1.0 * nblk * d, 4.0 * nblk * d + d * sizeof(T));
 }
@@ -170,10 +221,11 @@ void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* r
 // split-K reduction (fixed order over splits)
 // ---------------------------------------------------------------------------
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t M,
-                                     int64_t N, int64_t ldp, const bf16* __restrict__ colv,
-                                     bf16* __restrict__ out, int64_t ldo) {
+                                     int64_t plane_rows, int64_t N, int64_t ldp,
+                                     const bf16* __restrict__ colv, bf16* __restrict__ out,
+                                     int64_t ldo) {
   const int64_t nvec = (N + 7) / 8;
-  const int64_t plane = M * ldp;
+  const int64_t plane = plane_rows * ldp;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M * nvec;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = i / nvec, c0 = (i - r * nvec) * 8;
@@ -199,12 +251,13 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
   }
 }
 
-void launch_splitk_reduce(Ctx& c, const float* part, int splits, int64_t M, int64_t N,
-                          int64_t ldp, const bf16* colv, bf16* out, int64_t ldo) {
+void launch_splitk_reduce(Ctx& c, const float* part, int splits, int64_t M, int64_t plane_rows,
+                          int64_t N, int64_t ldp, const bf16* colv, bf16* out, int64_t ldo) {
   const int64_t n = M * ((N + 7) / 8);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 8));
   prof_start(c);
-  splitk_reduce_kernel<<<grid, 256, 0, c.stream>>>(part, splits, M, N, ldp, colv, out, ldo);
+  splitk_reduce_kernel<<<grid, 256, 0, c.stream>>>(part, splits, M, plane_rows, N, ldp, colv, out,
+                                                   ldo);
   note_launch(c, KK_SPLITK_REDUCE, -1, 1.0 * splits * M * N, (4.0 * splits + 2.0) * M * N);
 }
 
@@ -220,9 +273,9 @@ __global__ void ew_kernel(const T* __restrict__ a, int64_t lda, const T* __restr
     const int64_t r = i / cols, col = i - r * cols;
     float v;
     if (OP == 0) {
-      v = act_f(to_f<T>(a[r * lda + col]), sigma);
+      v = act_t<T>(to_f<T>(a[r * lda + col]), sigma);
     } else if (OP == 1) {
-      v = __fmul_rn(silu_f(to_f<T>(a[r * lda + col])), to_f<T>(b[r * lda + col]));
+      v = __fmul_rn(silu_t<T>(to_f<T>(a[r * lda + col])), to_f<T>(b[r * lda + col]));
     } else {
       v = (a == nullptr) ? 0.f : to_f<T>(a[r * lda + col]) * rowv[r];
     }

@@ -94,7 +94,8 @@ def problem(rng, M, N, K, a_mn, b_mn, dtype, two=False):
 
 
 LAYOUTS = [(False, False), (False, True), (True, True)]
-SHAPES = [(128, 256, 64), (300, 520, 200), (1000, 384, 1024), (77, 40, 24), (1, 8, 8)]
+SHAPES = [(128, 256, 64), (300, 520, 200), (1000, 384, 1024), (77, 40, 24), (1, 8, 8),
+          (130, 333, 205), (67, 5, 3)]  # ragged N and K (not multiples of 8)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -185,7 +186,7 @@ def test_resid_and_grouped(lib, dtype):
     from _gemmhook import run
     rng = np.random.default_rng(11)
     probs, refs = [], []
-    for N in (256, 128, 200):
+    for N in (256, 128, 203):
         q, r = problem(rng, 500, N, 128, False, False, dtype)
         R = rnd(rng, (500, N), dtype)
         q["out0"], q["ldo"] = out_buf(500, N, dtype)
@@ -219,7 +220,7 @@ def test_swiglu(lib, dtype):
 def test_dsigma_and_dswiglu(lib, dtype):
     from _gemmhook import run
     rng = np.random.default_rng(13)
-    M, N, K = 270, 136, 320
+    M, N, K = 270, 141, 317
     rowv = (rng.random(M) + 0.5).astype(np.float32)
     q, r = problem(rng, M, N, K, False, True, dtype)
     Z = rnd(rng, (M, N), dtype, 2.0)
@@ -250,7 +251,7 @@ def test_dsigma_and_dswiglu(lib, dtype):
 def test_chain(lib, dtype):
     from _gemmhook import run
     rng = np.random.default_rng(14)
-    M, N, K = 260, 264, 200
+    M, N, K = 260, 262, 203
     q, r = problem(rng, M, N, K, False, True, dtype, two=True)
     q["out0"], q["ldo"] = out_buf(M, N, dtype)
     run(lib, "chain", [q], dtype=dtype)
