@@ -79,7 +79,7 @@ int device_sms() {
 // Largest M x ldp(N) summed over the problems of one weight-gradient launch.
 int64_t max_wgrad_elems(const Shape& s) {
   auto ldp = [](int64_t n) { return (n + 7) / 8 * 8; };
-  auto rows = [](int64_t m) { return (m + 127) / 128 * 128; };  // split planes hold whole tiles
+  auto rows = [](int64_t m) { return (m + 255) / 256 * 256; };  // split planes hold whole tiles
   int64_t best = 0;
   auto cand = [&](int64_t v) { best = std::max(best, v); };
   if (s.dense) {

@@ -3,6 +3,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -103,8 +104,23 @@ static int choose_splits(int64_t tiles, int64_t nkb, int64_t MN_total, int grid,
 
 size_t gemm_tc_partial_bytes(int64_t M, int64_t N, int num_sms) {
   (void)num_sms;
-  return static_cast<size_t>(16) * tc::cdiv(M, tc::BM) * tc::BM * tc::ldp_of(N) * 4;
+  return static_cast<size_t>(16) * tc::cdiv(M, 2 * tc::BM) * 2 * tc::BM * tc::ldp_of(N) * 4;
 }
+
+namespace {
+// CTA pairs (2-SM MMA) unless the problems are at most one 128-row tile tall,
+// or BN_GEMM_CTA_PAIR=0 is set in the environment.
+int cta_group_for(const GemmLaunch& g) {
+  static const bool pairs_off = [] {
+    const char* v = std::getenv("BN_GEMM_CTA_PAIR");
+    return v != nullptr && v[0] == '0';
+  }();
+  if (pairs_off) return 1;
+  for (int i = 0; i < g.nprob; ++i)
+    if (g.p[i].M > tc::BM) return 2;
+  return 1;
+}
+}  // namespace
 
 void gemm_tc(Ctx& c, const GemmLaunch& g) {
   using namespace tc;
@@ -120,6 +136,8 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     if (g.p[i].N < 256) BN = 128;
   if (ek == K_NORM || ek == K_SWIGLU) BN = 128;
 
+  const int CG = cta_group_for(g);
+  const int BMP = BM * CG;  // rows per tile
   thread_local static Params P;  // large kernel parameter block, filled per call
   std::memset(&P, 0, sizeof(P));
   P.nprob = g.nprob;
@@ -136,8 +154,8 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
       c.bad = 1;
       return;
     }
-    tiles_total += cdiv(q.M, BM) * cdiv(q.N, BN);
-    mn_total += cdiv(q.M, BM) * BM * ldp_of(q.N);
+    tiles_total += cdiv(q.M, BMP) * cdiv(q.N, BN);
+    mn_total += cdiv(q.M, BMP) * BMP * ldp_of(q.N);
     nkb_max = std::max(nkb_max, cdiv(q.K, BK));
   }
   int splits = 1;
@@ -145,7 +163,8 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     bool plain = true;
     for (int i = 0; i < g.nprob; ++i) plain = plain && g.p[i].rowv == nullptr;
     if (plain)
-      splits = choose_splits(tiles_total, nkb_max, mn_total, c.num_sms, BN, c.partial_bytes);
+      splits = choose_splits(tiles_total, nkb_max, mn_total, c.num_sms / CG, BN * CG,
+                             c.partial_bytes);
   }
   const bool split = splits > 1;
   if (split) ek = K_PART;
@@ -159,8 +178,9 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     Prob& p = P.p[i];
     const int npair = (ek == K_SWIGLU || ek == K_CHAIN) ? 2 : 1;
     for (int j = 0; j < npair; ++j) {
+      // each CTA of a pair loads its own 128 rows of A and BN / CG rows of B
       if (!encode_operand(&p.ma[j], q.a[j], q.M, q.K, BM) ||
-          !encode_operand(&p.mb[j], q.b[j], q.N, q.K, BN)) {
+          !encode_operand(&p.mb[j], q.b[j], q.N, q.K, BN / CG)) {
         c.bad = 2;
         return;
       }
@@ -206,14 +226,14 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     }
     p.rowv = q.rowv;
     p.colv = q.colv;
-    p.tiles_m = static_cast<int>(cdiv(q.M, BM));
+    p.tiles_m = static_cast<int>(cdiv(q.M, BMP));
     p.tiles_n = static_cast<int>(cdiv(q.N, BN));
     p.kb_per_split = static_cast<int>(cdiv(p.nkb[0], splits));
     p.splits = static_cast<int>(cdiv(p.nkb[0], p.kb_per_split));
     if (split) {
       // fp32 partials: split s of this problem is rows [s M, (s + 1) M) of one tensor
       // split s of this problem owns rows [s * Mp, (s + 1) * Mp), Mp = M rounded up to 128
-      const int64_t Mp = static_cast<int64_t>(p.tiles_m) * BM;
+      const int64_t Mp = static_cast<int64_t>(p.tiles_m) * BMP;
       part_ptr[i] = reinterpret_cast<char*>(c.partial) + part_off;
       part_ld[i] = ldp_of(q.N);
       part_rows[i] = Mp;
@@ -229,12 +249,16 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     units += p.tiles_m * p.tiles_n * (split ? p.splits : 1);
   }
   P.total_units = units;
-  const int grid = std::min(units, c.num_sms);
   double flops, bytes;
   gemm_work(g, 2, flops, bytes);
   prof_start(c);
-  const bool ok = (BN == 256) ? launch_bn256(ek, a_mn, b_mn, P, grid, c.stream)
-                              : launch_bn128(ek, a_mn, b_mn, P, grid, c.stream);
+  bool ok;
+  if (CG == 2)
+    ok = (BN == 256) ? launch_bn256_cg2(ek, a_mn, b_mn, P, units, c.num_sms, c.stream)
+                     : launch_bn128_cg2(ek, a_mn, b_mn, P, units, c.num_sms, c.stream);
+  else
+    ok = (BN == 256) ? launch_bn256_cg1(ek, a_mn, b_mn, P, units, c.num_sms, c.stream)
+                     : launch_bn128_cg1(ek, a_mn, b_mn, P, units, c.num_sms, c.stream);
   if (!ok) {
     c.bad = 5;
     return;

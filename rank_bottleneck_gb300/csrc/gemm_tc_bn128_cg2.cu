@@ -1,0 +1,4 @@
+// tcgen05 GEMM instantiations: 128-column tiles, CTA group of 2.
+#define GEMM_BN 128
+#define GEMM_CG 2
+#include "gemm_tc_inst.cuh"

@@ -1,6 +1,10 @@
 // tcgen05 / TMA / TMEM GEMM engine for sm_103a with fused epilogues.
 //
-// One persistent CTA per SM (352 threads):
+// Persistent CTAs, one per SM (352 threads). With CG = 2 the CTAs run in
+// clusters of two and each pair computes one 256 x BN tile with the 2-SM MMA
+// (tcgen05.mma.cta_group::2): each CTA loads its own 128 rows of A and half of
+// B, the leader CTA (rank 0) issues the MMAs, the accumulator rows of each CTA
+// land in its own TMEM. Per CTA:
 //   warp 0        operand producer: TMA loads into a ring of shared-memory
 //                 stages, each one 128 x 64 tile of A and one BN x 64 tile of
 //                 B (bf16, 128-byte swizzle), one mbarrier per stage;
@@ -63,11 +67,12 @@ struct EpiShape {
   static constexpr int BYTES = NE * NT * SUB_BYTES;
 };
 
-template <int BN, int EK>
+template <int BN, int EK, int CG = 1>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = (BN / CG) * BK * 2;  // each CTA holds BN / CG rows of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TX_BYTES = CG * STAGE_BYTES;    // bytes one stage receives, whole pair
   static constexpr int NSLOT = 512 / BN;
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_LIMIT = 232448;
@@ -181,37 +186,117 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---- clusters of two CTAs (2-SM MMA)
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+// shared::cluster address of the variable at `addr` (own CTA) in CTA `rank`
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier that may live in the peer CTA of the pair
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0,
+                                                 int c1, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// TMEM allocation: cta_group::2 is executed by one warp in each CTA of the pair
+// and allocates the same columns in both.
+template <int CG>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (CG == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     dst_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
 }
+template <int CG>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, one 128 x N x 16 step, issued by one thread.
+// D[tmem] (+)= A[smem] * B[smem]^T, one (128 CG) x N x 16 step, issued by one thread
+// (with CG = 2 by the leader CTA, reading A and B halves from both CTAs).
+template <int CG>
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if constexpr (CG == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
-// Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has
+// completed; with CG = 2 on the barrier at the same offset in both CTAs.
+template <int CG>
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
+  if constexpr (CG == 1) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  } else {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+  }
+}
+// commit to this CTA's barrier only (the end-of-kernel drain)
+template <int CG>
+__device__ __forceinline__ void mma_commit_local(uint32_t bar) {
+  if constexpr (CG == 1)
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
 }
 // 32 consecutive fp32 columns of this thread's TMEM lane, waited for in the same statement.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
@@ -320,6 +405,8 @@ struct Work {
   int64_t m0, nb;
 };
 
+// Unit u -> problem, split, first row m0 of the (CG x 128)-row tile, n-block.
+template <int CG>
 __device__ __forceinline__ Work decode(const Params& P, int u) {
   int pi = 0;
   while (pi + 1 < P.nprob && u >= P.p[pi + 1].unit_begin) ++pi;
@@ -330,7 +417,7 @@ __device__ __forceinline__ Work decode(const Params& P, int u) {
   w.pi = pi;
   w.split = local / tiles;
   const int t = local - w.split * tiles;
-  w.m0 = static_cast<int64_t>(t / pr.tiles_n) * BM;
+  w.m0 = static_cast<int64_t>(t / pr.tiles_n) * BM * CG;
   w.nb = t % pr.tiles_n;  // n-block index; the kernel scales it by BN
   return w;
 }
@@ -362,9 +449,9 @@ __device__ __forceinline__ void segment(const Params& P, const Prob& pr, int spl
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int BN, int EK, bool AMN, bool BMN>
+template <int BN, int EK, bool AMN, bool BMN, int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Params P) {
-  using C = Cfg<BN, EK>;
+  using C = Cfg<BN, EK, CG>;
   using E = EpiShape<EK>;
   constexpr int NCH = BN / EPI_N;  // epilogue subtiles per tile
   extern __shared__ uint8_t smem_raw[];
@@ -384,6 +471,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA pairs: both CTAs of a pair walk the same units; rank 1 adds 128 rows
+  const uint32_t rank = (CG == 2) ? cluster_rank() : 0u;
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x) / CG;
+  const int npairs = static_cast<int>(gridDim.x) / CG;
+  const int row_off = BM * static_cast<int>(rank);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
@@ -392,7 +485,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     }
     for (int i = 0; i < C::NSLOT; ++i) {
       mbar_init(smem_u32(&accf[i]), 1);
-      mbar_init(smem_u32(&acce[i]), NUM_EPI_WARPS);
+      mbar_init(smem_u32(&acce[i]), NUM_EPI_WARPS * CG);  // the pair's epilogue warps
     }
     for (int i = 0; i < E::NE; ++i) {
       mbar_init(smem_u32(&epi_full[i]), 1);
@@ -403,7 +496,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers are initialised
+  if (warp == 1) tmem_alloc<CG>(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -421,16 +515,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       uint32_t ph = 0;
       int issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x) {
-        const Work w = decode(P, u);
+      for (int u = pair; ok && u < P.total_units; u += npairs) {
+        const Work w = decode<CG>(P, u);
         const Prob& pr = P.p[w.pi];
-        const int m0 = static_cast<int>(w.m0);
-        const int n0 = static_cast<int>(w.nb) * BN;
+        const int m0 = static_cast<int>(w.m0) + row_off;                  // this CTA's A rows
+        const int n0 = static_cast<int>(w.nb) * BN + static_cast<int>(rank) * (BN / CG);  // B rows
         for (int s = 0; ok && s < nseg; ++s) {
-          int kb0, nkb, pair;
-          segment<EK>(P, pr, w.split, s, kb0, nkb, pair);
-          const CUtensorMap* ma = &pr.ma[pair];
-          const CUtensorMap* mb = &pr.mb[pair];
+          int kb0, nkb, opair;
+          segment<EK>(P, pr, w.split, s, kb0, nkb, opair);
+          const CUtensorMap* ma = &pr.ma[opair];
+          const CUtensorMap* mb = &pr.mb[opair];
           for (int kb = kb0; kb < kb0 + nkb; ++kb) {
             if (!wait_bar(smem_u32(&empty[stage]), ph ^ 1u, abort_flag, P.status)) {
               ok = false;
@@ -438,20 +532,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             }
             const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
             const uint32_t sb = sa + C::A_BYTES;
+            // the stage's completion is counted on the leader's barrier, for the whole pair
             const uint32_t fb = smem_u32(&full[stage]);
-            mbar_expect_tx(fb, C::STAGE_BYTES);
+            const uint32_t fbc = (CG == 2) ? mapa(fb, 0) : fb;
+            if (leader) mbar_expect_tx(fb, C::TX_BYTES);
             const int k0 = kb * BK;
+            auto load = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1) {
+              if constexpr (CG == 2)
+                tma_load_2d_pair(dst, map, c0, c1, fbc);
+              else
+                tma_load_2d(dst, map, c0, c1, fb);
+            };
             if (AMN) {
-              tma_load_2d(sa, ma, m0, k0, fb);
-              tma_load_2d(sa + 8192, ma, m0 + 64, k0, fb);
+              load(sa, ma, m0, k0);
+              load(sa + 8192, ma, m0 + 64, k0);
             } else {
-              tma_load_2d(sa, ma, k0, m0, fb);
+              load(sa, ma, k0, m0);
             }
             if (BMN) {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, mb, n0 + 64 * j, k0, fb);
+              for (int j = 0; j < BN / CG / 64; ++j) load(sb + j * 8192, mb, n0 + 64 * j, k0);
             } else {
-              tma_load_2d(sb, mb, k0, n0, fb);
+              load(sb, mb, k0, n0);
             }
             ++issued;
             if (++stage == C::STAGES) {
@@ -461,7 +563,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           }
         }
       }
-      if (!ok) {
+      if (!ok && leader) {
         // drain: the last phase issued on each stage must land before the CTA exits
         int st = stage;
         uint32_t p = ph;
@@ -475,20 +577,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC = instr_desc(BM, BN, AMN, BMN);
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && leader) {
+      constexpr uint32_t IDESC = instr_desc(BM * CG, BN, AMN, BMN);
       int stage = 0;
       uint32_t ph = 0;
       int slot = 0;
       uint32_t sph = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x) {
-        const Work w = decode(P, u);
+      for (int u = pair; ok && u < P.total_units; u += npairs) {
+        const Work w = decode<CG>(P, u);
         const Prob& pr = P.p[w.pi];
         for (int s = 0; ok && s < nseg; ++s) {
-          int kb0, nkb, pair;
-          segment<EK>(P, pr, w.split, s, kb0, nkb, pair);
+          int kb0, nkb, opair;
+          segment<EK>(P, pr, w.split, s, kb0, nkb, opair);
           const bool fresh = !(EK == K_CHAIN && s == 1);
           if (fresh) {
             if (!wait_bar(smem_u32(&acce[slot]), sph ^ 1u, abort_flag, P.status)) {
@@ -510,9 +612,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             for (int kk = 0; kk < BK / 16; ++kk) {
               const uint64_t ad = smem_desc(sa + (AMN ? kk * 2048 : kk * 32), AMN);
               const uint64_t bd = smem_desc(sb + (BMN ? kk * 2048 : kk * 32), BMN);
-              mma_bf16(d_tmem, ad, bd, IDESC, (fresh && i == 0 && kk == 0) ? 0u : 1u);
+              mma_bf16<CG>(d_tmem, ad, bd, IDESC, (fresh && i == 0 && kk == 0) ? 0u : 1u);
             }
-            mma_commit(smem_u32(&empty[stage]));
+            mma_commit<CG>(smem_u32(&empty[stage]));
             if (++stage == C::STAGES) {
               stage = 0;
               ph ^= 1u;
@@ -520,7 +622,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           }
           if (!ok) break;
           if (!(EK == K_CHAIN && s == 0)) {
-            mma_commit(smem_u32(&accf[slot]));
+            mma_commit<CG>(smem_u32(&accf[slot]));
             if (++slot == C::NSLOT) {
               slot = 0;
               sph ^= 1u;
@@ -529,7 +631,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         }
       }
       // every MMA issued must complete before TMEM is released
-      mma_commit(smem_u32(drain));
+      mma_commit_local<CG>(smem_u32(drain));
       wait_bar(smem_u32(drain), 0, abort_flag, P.status, ok ? kWaitLimitNs : 50ull * 1000 * 1000);
     }
   } else if (warp == 2 + NUM_EPI_WARPS) {
@@ -539,10 +641,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       uint32_t eph = 0;
       int issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x) {
-        const Work w = decode(P, u);
+      for (int u = pair; ok && u < P.total_units; u += npairs) {
+        const Work w = decode<CG>(P, u);
         const Prob& pr = P.p[w.pi];
-        const int m0 = static_cast<int>(w.m0);
+        const int m0 = static_cast<int>(w.m0) + row_off;
         const int n0 = static_cast<int>(w.nb) * BN;
         for (int c = 0; c < NCH; ++c) {
           if (!wait_bar(smem_u32(&epi_empty[e]), eph ^ 1u, abort_flag, P.status)) {
@@ -591,10 +693,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       tc_fence_after();
       return true;
     };
-    auto release = [&](int sl) {
+    auto release = [&](int sl) {  // on the leader's barrier: its MMA warp refills the slot
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acce[sl]));
+      if (lane == 0) {
+        if (CG == 1 || leader)
+          mbar_arrive(smem_u32(&acce[sl]));
+        else
+          mbar_arrive_cluster(mapa(smem_u32(&acce[sl]), 0));
+      }
     };
     auto advance = [&]() {
       if (++slot == C::NSLOT) {
@@ -602,10 +709,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         sph ^= 1u;
       }
     };
-    for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x, ++tile_no) {
-      const Work w = decode(P, u);
+    for (int u = pair; ok && u < P.total_units; u += npairs, ++tile_no) {
+      const Work w = decode<CG>(P, u);
       const Prob& pr = P.p[w.pi];
-      const int64_t row = w.m0 + q * 32 + lane;
+      const int64_t row = w.m0 + row_off + q * 32 + lane;
       const int64_t n0 = w.nb * BN;
       const int64_t M = pr.M, N = pr.N;
       const bool row_ok = row < M;
@@ -779,9 +886,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         __syncwarp();
         if (lane == 0) {
           const uint32_t src = smem_u32(ent);
-          const int rt = static_cast<int>(w.m0) + q * 32;  // row within the problem
-          // split-K partials: split s owns rows [s * tiles_m * 128, (s + 1) * tiles_m * 128)
-          const int r0 = rt + (EK == K_PART ? w.split * pr.tiles_m * BM : 0);
+          const int rt = static_cast<int>(w.m0) + row_off + q * 32;  // row within the problem
+          // split-K partials: split s owns rows [s * Mp, (s + 1) * Mp), Mp = tiles_m * 128 CG
+          const int r0 = rt + (EK == K_PART ? w.split * pr.tiles_m * BM * CG : 0);
           const int64_t lim = (EK == K_PART) ? N : pr.N8;  // extent of the output maps
           if (rt < M && col0 < lim) {  // boxes partly outside the tensor are clipped by TMA
 #pragma unroll
@@ -810,9 +917,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the leader's MMAs and the peer's arrivals are done
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc<CG>(tmem, 512);
   }
 }
 
