@@ -129,12 +129,15 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     c.bad = 1;
     return;
   }
-  // tile width: Online RMSNorm and SwiGLU keep a 128-column accumulator per thread
-  // row in registers / pair two slots, everything else prefers 256 when N allows
+  // tile width: 256 columns (the MMA's most efficient shape) unless a problem is narrower
   int BN = 256;
   for (int i = 0; i < g.nprob; ++i)
     if (g.p[i].N < 256) BN = 128;
-  if (ek == K_NORM || ek == K_SWIGLU) BN = 128;
+  static const int forced_bn = [] {  // BN_GEMM_TILE_N=128 forces narrow tiles (tuning experiments)
+    const char* v = std::getenv("BN_GEMM_TILE_N");
+    return (v != nullptr && v[0] == '1') ? 128 : 0;
+  }();
+  if (forced_bn) BN = forced_bn;
 
   const int CG = cta_group_for(g);
   const int BMP = BM * CG;  // rows per tile

@@ -65,10 +65,8 @@ bool BN_CAT(launch_bn, GEMM_BN, BN_CAT(_cg, GEMM_CG, ))(int ek, bool a_mn, bool 
     case K_DSIGMA * 4 + 1: go<K_DSIGMA, false, true>(P, units, num_sms, s); return true;
     case K_DSWIGLU * 4 + 1: go<K_DSWIGLU, false, true>(P, units, num_sms, s); return true;
     case K_CHAIN * 4 + 1: go<K_CHAIN, false, true>(P, units, num_sms, s); return true;
-#if GEMM_BN == 128
     case K_NORM * 4 + 0: go<K_NORM, false, false>(P, units, num_sms, s); return true;
     case K_SWIGLU * 4 + 0: go<K_SWIGLU, false, false>(P, units, num_sms, s); return true;
-#endif
     default: return false;
   }
 }

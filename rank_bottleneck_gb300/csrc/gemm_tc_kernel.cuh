@@ -63,7 +63,7 @@ struct EpiShape {
   static constexpr int ELEM = (EK == K_PART) ? 4 : 2;        // output element bytes
   static constexpr int SUB_BYTES = BM * EPI_N * ELEM;        // one 128 x 32 subtile
   static constexpr int WARP_BYTES = 32 * EPI_N * ELEM;       // one warp's 32 rows of it
-  static constexpr int NE = (EK == K_PART) ? 2 : 4;          // ring entries
+  static constexpr int NE = (EK == K_PART) ? 2 : (NT == 1 ? 8 : 4);  // ring entries
   static constexpr int BYTES = NE * NT * SUB_BYTES;
 };
 
@@ -315,6 +315,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Store 32 fp32 columns into this thread's TMEM lane (and wait for the store).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
 }
 
 // Shared-memory matrix descriptor (tcgen05 format) of a 128-byte-swizzled tile.
@@ -584,14 +605,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       uint32_t ph = 0;
       int slot = 0;
       uint32_t sph = 0;
+      // Online RMSNorm keeps a tile's running sum in one slot (tile t: slot t % 2)
+      // while the shards' partial products land in the other
+      uint32_t norm_ph[2] = {0u, 0u};
+      int64_t tile_no = 0;
       bool ok = true;
-      for (int u = pair; ok && u < P.total_units; u += npairs) {
+      for (int u = pair; ok && u < P.total_units; u += npairs, ++tile_no) {
         const Work w = decode<CG>(P, u);
         const Prob& pr = P.p[w.pi];
         for (int s = 0; ok && s < nseg; ++s) {
           int kb0, nkb, opair;
           segment<EK>(P, pr, w.split, s, kb0, nkb, opair);
           const bool fresh = !(EK == K_CHAIN && s == 1);
+          if (EK == K_NORM) {
+            slot = static_cast<int>(tile_no & 1) ^ (s == 0 ? 0 : 1);
+            sph = norm_ph[slot];
+          }
           if (fresh) {
             if (!wait_bar(smem_u32(&acce[slot]), sph ^ 1u, abort_flag, P.status)) {
               ok = false;
@@ -623,7 +652,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           if (!ok) break;
           if (!(EK == K_CHAIN && s == 0)) {
             mma_commit<CG>(smem_u32(&accf[slot]));
-            if (++slot == C::NSLOT) {
+            if (EK == K_NORM) {
+              norm_ph[slot] ^= 1u;
+            } else if (++slot == C::NSLOT) {
               slot = 0;
               sph ^= 1u;
             }
@@ -685,6 +716,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int slot = 0;
     uint32_t sph = 0;
+    uint32_t norm_ph[2] = {0u, 0u};         // Online RMSNorm: per-slot phases (see the MMA warp)
     int prev_e = 0, mine = 0;
     int64_t tile_no = 0;                    // tiles this CTA has finished
     bool ok = true;
@@ -716,48 +748,80 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
       const int64_t n0 = w.nb * BN;
       const int64_t M = pr.M, N = pr.N;
       const bool row_ok = row < M;
-      float R[EK == K_NORM ? MYCH * 32 : 1];
+      uint32_t gpk[EK == K_SWIGLU ? MYCH : 1][16];  // SwiGLU: this warp's G, bf16 pairs
       int sl0 = slot, sl1 = slot;  // TMEM slot(s) of this tile's accumulator(s)
       if constexpr (EK == K_NORM) {
-        // Online RMSNorm: fold each shard's partial product with its own factors
+        // Online RMSNorm. The running sum R lives in TMEM slot sl0 = tile % 2; each
+        // shard's partial product P_s arrives in the other slot and is folded as
+        // R += alpha_s * (P_s / rms_s): local normalisation, then the per-row
+        // correction alpha_s = rms_s / rms_g.
+        sl0 = static_cast<int>(tile_no & 1);
+        const int slp = sl0 ^ 1;
         const int S = P.S;
         const float* ss = pr.rowv + (row_ok ? row : 0) * S;
         float tot = 0.f;
         for (int s = 0; s < S; ++s) tot += row_ok ? ss[s] : 0.f;
         const float shard_w = static_cast<float>(pr.K / S);
         const float rms_g = sqrtf(tot / static_cast<float>(pr.K) + P.eps);
+        const uint32_t tR = tmem + lane_base + static_cast<uint32_t>(sl0 * BN);
+        const uint32_t tP = tmem + lane_base + static_cast<uint32_t>(slp * BN);
         for (int s = 0; s < S; ++s) {
-          if (!acquire(slot, sph)) {
+          const int sl = (s == 0) ? sl0 : slp;
+          if (!acquire(sl, norm_ph[sl])) {
             ok = false;
             break;
           }
+          norm_ph[sl] ^= 1u;
           const float ss_s = row_ok ? ss[s] : 0.f;
           const float rms_s = sqrtf(ss_s / shard_w + P.eps);
           const float inv_local = 1.0f / rms_s;  // local normalisation
           const float alpha = rms_s / rms_g;     // per-row correction
-          const uint32_t t0 = tmem + lane_base + static_cast<uint32_t>(slot * BN);
-#pragma unroll
+#pragma unroll 1
           for (int k = 0; k < MYCH; ++k) {
+            const uint32_t col = static_cast<uint32_t>((k * EPI_GROUPS + grp) * 32);
             float v[32];
-            tmem_ld32(t0 + (k * EPI_GROUPS + grp) * 32, v);
+            if (s == 0) {
+              tmem_ld32(tR + col, v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float local = v[i] * inv_local;
-              R[k * 32 + i] = (s == 0) ? alpha * local : fmaf(alpha, local, R[k * 32 + i]);
+              for (int i = 0; i < 32; ++i) v[i] = alpha * (v[i] * inv_local);
+            } else {
+              float r[32];
+              tmem_ld32(tP + col, v);
+              tmem_ld32(tR + col, r);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = fmaf(alpha, v[i] * inv_local, r[i]);
             }
+            tmem_st32(tR + col, v);
           }
-          release(slot);
-          advance();
+          if (s > 0) release(slp);
         }
         if (!ok) break;
       } else if constexpr (EK == K_SWIGLU) {
+        // G first: keep this warp's columns of it as bf16 pairs and free its slot
+        // at once, so the MMAs of the next tile's G overlap this tile's epilogue
         sl0 = slot;
         const uint32_t p0 = sph;
         advance();
         sl1 = slot;
         const uint32_t p1 = sph;
         advance();
-        if (!acquire(sl0, p0) || !acquire(sl1, p1)) {
+        if (!acquire(sl0, p0)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int k = 0; k < MYCH; ++k) {
+          float g[32];
+          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl0 * BN + (k * EPI_GROUPS + grp) * 32),
+                    g);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(g[2 * i], g[2 * i + 1]);
+            gpk[k][i] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+        }
+        release(sl0);
+        if (!acquire(sl1, p1)) {
           ok = false;
           break;
         }
@@ -774,9 +838,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           pr.rowv != nullptr && row_ok)
         rs = pr.rowv[row];
 
-      // the NORM fold keeps its accumulator in registers indexed by k: unrolled;
-      // the other epilogues stay rolled to keep the kernel small
-#pragma unroll(EK == K_NORM ? MYCH : 1)
+      // SwiGLU indexes its register-held G by k: unrolled; the others stay rolled
+      // to keep the kernel small
+#pragma unroll(EK == K_SWIGLU ? MYCH : 1)
       for (int k = 0; k < MYCH; ++k) {
         const int c = k * EPI_GROUPS + grp;            // subtile within the tile
         const int64_t col0 = n0 + c * EPI_N;
@@ -791,17 +855,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         }
         float v[32];
         float v2[EK == K_SWIGLU ? 32 : 1];
-        if constexpr (EK == K_NORM) {
+        if constexpr (EK == K_SWIGLU) {
+          // v = G (already bf16), v2 = U
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = R[k * 32 + i];
+          for (int i = 0; i < 16; ++i) {
+            v[2 * i] = __uint_as_float(gpk[k][i] << 16);
+            v[2 * i + 1] = __uint_as_float(gpk[k][i] & 0xFFFF0000u);
+          }
+          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl1 * BN + c * 32), v2);
+          if (k == MYCH - 1) release(sl1);
         } else {
           tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl0 * BN + c * 32), v);
-          if constexpr (EK == K_SWIGLU)
-            tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl1 * BN + c * 32), v2);
-          if (k == MYCH - 1) {
-            release(sl0);
-            if (EK == K_SWIGLU) release(sl1);
-          }
+          if (k == MYCH - 1) release(sl0);
         }
         uint8_t* ent = epi + e * E::NT * E::SUB_BYTES + q * E::WARP_BYTES;
         // this row holds some of the ragged columns [N8, N) (fp32 partials need none)
@@ -838,7 +903,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           float m[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            v[i] = round_to<__nv_bfloat16>(v[i]);
             v2[i] = round_to<__nv_bfloat16>(v2[i]);
             m[i] = __fmul_rn(silu_fast(v[i]), v2[i]);
           }

@@ -87,8 +87,36 @@ constexpr int kNormBwdMaxWarps = 8;
 constexpr int kNormBwdUnroll = 4;
 constexpr size_t kNormBwdSmemLimit = 200 * 1024;
 
+// 8 elements of T kept packed in registers (16 bytes of bf16, 32 of fp32),
+// unpacked element by element where they are used.
+template <typename T> struct Pack8;
+template <> struct Pack8<__nv_bfloat16> {
+  uint4 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+    v = *reinterpret_cast<const uint4*>(p);
+  }
+  __device__ __forceinline__ void zero() { v = make_uint4(0, 0, 0, 0); }
+  __device__ __forceinline__ float operator[](int i) const {
+    const uint32_t w = (i < 2) ? v.x : (i < 4) ? v.y : (i < 6) ? v.z : v.w;
+    return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+};
+template <> struct Pack8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = *reinterpret_cast<const float4*>(p);
+    b = *reinterpret_cast<const float4*>(p + 4);
+  }
+  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ float operator[](int i) const {
+    const float4& q = (i < 4) ? a : b;
+    const int j = i & 3;
+    return j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
+  }
+};
+
 template <typename T>
-__global__ void __launch_bounds__(kNormBwdMaxWarps * 32)
+__global__ void __launch_bounds__(kNormBwdMaxWarps * 32, 2)
     norm_bwd_kernel(const T* __restrict__ dn, const T* __restrict__ x, const T* __restrict__ w,
                     const float* __restrict__ rstd, const T* __restrict__ dres, int64_t rows,
                     int d, T* __restrict__ dx, float* __restrict__ part) {
@@ -102,24 +130,25 @@ __global__ void __launch_bounds__(kNormBwdMaxWarps * 32)
   __syncthreads();
   float* my = acc + warp * dp;
   const float inv_d = 1.0f / static_cast<float>(d);
-  constexpr int U = kNormBwdUnroll;
+  constexpr int U = sizeof(T) == 2 ? kNormBwdUnroll : kNormBwdUnroll / 2;  // same bytes in flight
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * nw + warp; row < rows;
        row += static_cast<int64_t>(gridDim.x) * nw) {
     const T* dnr = dn + row * d;
     const T* xr = x + row * d;
     float s = 0.f;
     for (int base = lane * 8; base < d; base += 256 * U) {
-      float a[U][8], b[U][8], ww[U][8];
+      Pack8<T> a[U], b[U], ww[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int c = base + u * 256;
         if (c < d) {
-          Vec8<T>::load(dnr + c, a[u]);
-          Vec8<T>::load(xr + c, b[u]);
-          Vec8<T>::load(w + c, ww[u]);
+          a[u].load(dnr + c);
+          b[u].load(xr + c);
+          ww[u].load(w + c);
         } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) a[u][i] = b[u][i] = ww[u][i] = 0.f;
+          a[u].zero();
+          b[u].zero();
+          ww[u].zero();
         }
       }
 #pragma unroll
@@ -133,27 +162,28 @@ __global__ void __launch_bounds__(kNormBwdMaxWarps * 32)
     const T* dr = dres + row * d;
     T* o = dx + row * d;
     for (int base = lane * 8; base < d; base += 256 * U) {
-      float a[U][8], b[U][8], ww[U][8], g[U][8];
+      Pack8<T> a[U], b[U], ww[U], g[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int c = base + u * 256;
         if (c < d) {
-          Vec8<T>::load(dnr + c, a[u]);
-          Vec8<T>::load(xr + c, b[u]);
-          Vec8<T>::load(w + c, ww[u]);
-          Vec8<T>::load(dr + c, g[u]);
+          a[u].load(dnr + c);
+          b[u].load(xr + c);
+          ww[u].load(w + c);
+          g[u].load(dr + c);
         }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int c = base + u * 256;
         if (c < d) {
+          float out[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            g[u][i] = g[u][i] + (a[u][i] * ww[u][i] - b[u][i] * coef);
+            out[i] = g[u][i] + (a[u][i] * ww[u][i] - b[u][i] * coef);
             my[c + c / 8 + i] = fmaf(a[u][i], b[u][i], my[c + c / 8 + i]);
           }
-          Vec8<T>::store(o + c, g[u]);
+          Vec8<T>::store(o + c, out);
         }
       }
     }
