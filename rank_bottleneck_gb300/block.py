@@ -101,7 +101,7 @@ class BlockConfig:
 
     def __post_init__(self):
         if self.ld_ff is None:
-            self.ld_ff = (self.d_ff + 7) // 8 * 8
+            self.ld_ff = (self.d_ff + 63) // 64 * 64  # whole 128-byte rows
 
     @property
     def torch_dtype(self):

@@ -24,6 +24,7 @@ thread_local char g_cuda_err[256] = "no error";
 
 struct Shape {
   int64_t T, d, r, d_ff, ld_ff;
+  int64_t ld_act;  // row stride of the [T, d_ff] activations G, U, m, dG, dU: whole 128-byte lines
   int S, sigma, dtype, kind, dense, ckpt;
   float eps;
   int64_t E;  // bytes per element
@@ -131,9 +132,9 @@ void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
     A.z_d = keep.take(T * s.r * E);
     A.h_d = rest.take(T * s.r * E);
   }
-  A.G = rest.take(T * s.ld_ff * E);
-  A.U = rest.take(T * s.ld_ff * E);
-  A.m = rest.take(T * s.ld_ff * E);
+  A.G = rest.take(T * s.ld_act * E);
+  A.U = rest.take(T * s.ld_act * E);
+  A.m = rest.take(T * s.ld_act * E);
 
   const int64_t n1 = s.dense ? 3 * s.d : 3 * s.r, n2 = s.dense ? 2 * s.d_ff : 2 * s.r;
   if (s.full()) B.A1f = sc.take(n1 * s.d * E);
@@ -142,8 +143,8 @@ void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
     B.dz_d = sc.take(T * s.r * E);
     B.dz_gu = sc.take(T * 2 * s.r * E);
   }
-  B.dG = sc.take(T * s.ld_ff * E);
-  B.dU = sc.take(T * s.ld_ff * E);
+  B.dG = sc.take(T * s.ld_act * E);
+  B.dU = sc.take(T * s.ld_act * E);
   B.dn = sc.take(T * s.d * E);
   if (s.full()) {
     B.dx1 = sc.take(T * s.d * E);
@@ -173,6 +174,7 @@ bn_status check_desc(const bn_block_desc* D, Shape& s) {
   s.r = D->r;
   s.d_ff = D->d_ff;
   s.ld_ff = D->ld_ff;
+  s.ld_act = (s.d_ff + 63) / 64 * 64;
   s.S = D->S;
   s.sigma = D->sigma;
   s.dtype = D->dtype;
@@ -304,8 +306,8 @@ void sigma_ew(Ctx& c, const Shape& s, const void* z, int64_t cols, int64_t ld, v
 }
 template <typename T>
 void swiglu_ew(Ctx& c, const Shape& s, const void* G, const void* U, void* m) {
-  launch_swiglu<T>(c, static_cast<const T*>(G), static_cast<const T*>(U), s.T, s.d_ff, s.ld_ff,
-                   static_cast<T*>(m), s.ld_ff);
+  launch_swiglu<T>(c, static_cast<const T*>(G), static_cast<const T*>(U), s.T, s.d_ff, s.ld_act,
+                   static_cast<T*>(m), s.ld_act);
 }
 template <typename T>
 void rowscale(Ctx& c, const Shape& s, const void* in, int64_t ldi, const float* rowv, int64_t cols,
@@ -383,7 +385,7 @@ void gu_up(Ctx& c, const Shape& s, const bn_block_params* W, const Acts& A, bool
   p.out[0] = keep_gu ? A.G : nullptr;
   p.out[1] = keep_gu ? A.U : nullptr;
   p.out[2] = A.m;
-  p.ldo[0] = p.ldo[1] = p.ldo[2] = s.ld_ff;
+  p.ldo[0] = p.ldo[1] = p.ldo[2] = s.ld_act;
   gemm(c, s, g);
 }
 
@@ -461,7 +463,7 @@ void forward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const voi
   DT_CALL(s, fold, c, W->A_gu, W->w_norm2, 2 * s.r, s.d, B.A2f);
   norm_down(c, s, x1, A.ss2, B.A2f, 2 * s.r, A.z_gu, A.h_gu);
   gu_up(c, s, W, A, !s.ckpt);
-  plain_down(c, s, A.m, s.d_ff, s.ld_ff, W->A_d, s.ld_ff, A.z_d, A.h_d);
+  plain_down(c, s, A.m, s.d_ff, s.ld_act, W->A_d, s.ld_ff, A.z_d, A.h_d);
   down_up(c, s, W, A, x1, y);
 }
 
@@ -513,7 +515,7 @@ void forward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void*
     p.b[0] = op(at(B.A2f, i * s.d_ff * s.d, s), s.d, KM);
     p.rowv = A.ss2;
     p.out[0] = outs[i];
-    p.ldo[0] = s.ld_ff;
+    p.ldo[0] = s.ld_act;
   }
   gemm(c, s, g);
   DT_CALL(s, swiglu_ew, c, s, A.G, A.U, A.m);
@@ -523,7 +525,7 @@ void forward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void*
   p.M = s.T;
   p.N = s.d;
   p.K = s.d_ff;
-  p.a[0] = op(A.m, s.ld_ff, KM);
+  p.a[0] = op(A.m, s.ld_act, KM);
   p.b[0] = op(W->A_d, s.ld_ff, KM);
   p.in[0] = x1;
   p.ldi[0] = s.d;
@@ -610,7 +612,7 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
     GemmLaunch g = launch(EPI_STORE, s);
     g.allow_split = true;
     g.nprob = 1;
-    g.p[0] = wgrad(r, s.d_ff, T, B.dz_d, r, A.m, s.ld_ff, dW->A_d, s.ld_ff);
+    g.p[0] = wgrad(r, s.d_ff, T, B.dz_d, r, A.m, s.ld_act, dW->A_d, s.ld_ff);
     gemm(c, s, g);
   }
   {
@@ -625,10 +627,10 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
     p.b[0] = op(W->A_d, s.ld_ff, MN);
     p.in[0] = A.G;
     p.in[1] = A.U;
-    p.ldi[0] = p.ldi[1] = s.ld_ff;
+    p.ldi[0] = p.ldi[1] = s.ld_act;
     p.out[0] = B.dG;
     p.out[1] = B.dU;
-    p.ldo[0] = p.ldo[1] = s.ld_ff;
+    p.ldo[0] = p.ldo[1] = s.ld_act;
     gemm(c, s, g);
   }
   // ---- gate / up bottlenecks
@@ -636,15 +638,15 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
     GemmLaunch g = launch(EPI_STORE, s);
     g.allow_split = true;
     g.nprob = 2;
-    g.p[0] = wgrad(s.d_ff, r, T, B.dG, s.ld_ff, A.h_gu, 2 * r, dW->B_g, r);
-    g.p[1] = wgrad(s.d_ff, r, T, B.dU, s.ld_ff, at(A.h_gu, r, s), 2 * r, dW->B_u, r);
+    g.p[0] = wgrad(s.d_ff, r, T, B.dG, s.ld_act, A.h_gu, 2 * r, dW->B_g, r);
+    g.p[1] = wgrad(s.d_ff, r, T, B.dU, s.ld_act, at(A.h_gu, r, s), 2 * r, dW->B_u, r);
     gemm(c, s, g);
   }
   {
     GemmLaunch g = launch(EPI_DSIGMA, s);
     g.nprob = 2;
-    g.p[0] = dsigma(s, B.dG, s.ld_ff, s.d_ff, W->B_g, A.z_gu, 2 * r, B.dz_gu, A.rstd2);
-    g.p[1] = dsigma(s, B.dU, s.ld_ff, s.d_ff, W->B_u, at(A.z_gu, r, s), 2 * r,
+    g.p[0] = dsigma(s, B.dG, s.ld_act, s.d_ff, W->B_g, A.z_gu, 2 * r, B.dz_gu, A.rstd2);
+    g.p[1] = dsigma(s, B.dU, s.ld_act, s.d_ff, W->B_u, at(A.z_gu, r, s), 2 * r,
                     at(B.dz_gu, r, s), A.rstd2);
     gemm(c, s, g);
   }
@@ -731,7 +733,7 @@ void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void
     GemmLaunch g = launch(EPI_STORE, s);
     g.allow_split = true;
     g.nprob = 1;
-    g.p[0] = wgrad(d, dff, T, dy, d, A.m, s.ld_ff, dW->A_d, s.ld_ff);
+    g.p[0] = wgrad(d, dff, T, dy, d, A.m, s.ld_act, dW->A_d, s.ld_ff);
     gemm(c, s, g);
   }
   {
@@ -746,10 +748,10 @@ void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void
     p.b[0] = op(W->A_d, s.ld_ff, MN);
     p.in[0] = A.G;
     p.in[1] = A.U;
-    p.ldi[0] = p.ldi[1] = s.ld_ff;
+    p.ldi[0] = p.ldi[1] = s.ld_act;
     p.out[0] = B.dG;
     p.out[1] = B.dU;
-    p.ldo[0] = p.ldo[1] = s.ld_ff;
+    p.ldo[0] = p.ldo[1] = s.ld_act;
     p.rowv = A.rstd2;
     gemm(c, s, g);
   }
@@ -757,8 +759,8 @@ void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void
     GemmLaunch g = launch(EPI_STORE, s);
     g.allow_split = true;
     g.nprob = 2;
-    g.p[0] = wgrad(dff, d, T, B.dG, s.ld_ff, x1, d, dW->A_gu, d, W->w_norm2);
-    g.p[1] = wgrad(dff, d, T, B.dU, s.ld_ff, x1, d, at(dW->A_gu, dff * d, s), d, W->w_norm2);
+    g.p[0] = wgrad(dff, d, T, B.dG, s.ld_act, x1, d, dW->A_gu, d, W->w_norm2);
+    g.p[1] = wgrad(dff, d, T, B.dU, s.ld_act, x1, d, at(dW->A_gu, dff * d, s), d, W->w_norm2);
     gemm(c, s, g);
   }
   {
@@ -768,9 +770,9 @@ void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void
     p.M = T;
     p.N = d;
     p.K = dff;
-    p.a[0] = op(B.dG, s.ld_ff, KM);
+    p.a[0] = op(B.dG, s.ld_act, KM);
     p.b[0] = op(W->A_gu, d, MN);
-    p.a[1] = op(B.dU, s.ld_ff, KM);
+    p.a[1] = op(B.dU, s.ld_act, KM);
     p.b[1] = op(at(W->A_gu, dff * d, s), d, MN);
     p.out[0] = B.dn;
     p.ldo[0] = d;

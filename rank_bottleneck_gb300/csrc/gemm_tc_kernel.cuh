@@ -63,7 +63,8 @@ struct EpiShape {
   static constexpr int ELEM = (EK == K_PART) ? 4 : 2;        // output element bytes
   static constexpr int SUB_BYTES = BM * EPI_N * ELEM;        // one 128 x 32 subtile
   static constexpr int WARP_BYTES = 32 * EPI_N * ELEM;       // one warp's 32 rows of it
-  static constexpr int NE = (EK == K_PART) ? 2 : (NT == 1 ? 8 : 4);  // ring entries
+  // ring entries: kinds that read epilogue inputs keep several subtiles of them in flight
+  static constexpr int NE = (EK == K_PART) ? 2 : (NT == 1 || NIN > 0) ? 8 : 4;
   static constexpr int BYTES = NE * NT * SUB_BYTES;
 };
 
