@@ -15,7 +15,7 @@ void go(const Params& P, int units, int num_sms, cudaStream_t s) {
   constexpr int SMEM = Cfg<BN, EK, CG>::SMEM_BYTES;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.blockDim = dim3(kernel_threads<EK>(), 1, 1);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = s;
   if (CG == 2) {

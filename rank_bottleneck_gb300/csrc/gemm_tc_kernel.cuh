@@ -68,6 +68,13 @@ struct EpiShape {
   static constexpr int BYTES = NE * NT * SUB_BYTES;
 };
 
+// threads of a CTA: kinds without epilogue inputs leave out the input-producer
+// warp, which leaves the epilogue more registers
+template <int EK>
+constexpr int kernel_threads() {
+  return EpiShape<EK>::NIN > 0 ? NUM_THREADS : NUM_THREADS - 32;
+}
+
 template <int BN, int EK, int CG = 1>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
@@ -319,6 +326,57 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 }
 
 // Store 32 fp32 columns into this thread's TMEM lane (and wait for the store).
+// Split forms: several loads in flight before one wait. The wait names the
+// destination registers, so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tie32(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31]));
+}
+// wait for every tcgen05.ld this thread issued; a and b are their destinations
+__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tie32(a);
+  tie32(b);
+}
+__device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -375,6 +433,13 @@ __device__ __forceinline__ void smem_row_store_bf16(uint8_t* blk, int t, const f
     for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * c + 2 * i], v[8 * c + 2 * i + 1]);
     *reinterpret_cast<uint4*>(blk + t * 64 + ((c ^ ((t >> 1) & 3)) << 4)) = u;
   }
+}
+// the same row layout from 16 packed bf16 pairs
+__device__ __forceinline__ void smem_row_store_packed(uint8_t* blk, int t, const uint32_t* pk) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(blk + t * 64 + ((c ^ ((t >> 1) & 3)) << 4)) =
+        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
 }
 __device__ __forceinline__ void smem_row_load_bf16(const uint8_t* blk, int t, float* v) {
 #pragma unroll
@@ -472,7 +537,7 @@ __device__ __forceinline__ void segment(const Params& P, const Prob& pr, int spl
 // the kernel
 // ---------------------------------------------------------------------------
 template <int BN, int EK, bool AMN, bool BMN, int CG>
-__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __grid_constant__ Params P) {
   using C = Cfg<BN, EK, CG>;
   using E = EpiShape<EK>;
   constexpr int NCH = BN / EPI_N;  // epilogue subtiles per tile
@@ -786,14 +851,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = alpha * (v[i] * inv_local);
             } else {
-              float r[32];
-              tmem_ld32(tP + col, v);
-              tmem_ld32(tR + col, r);
+              // both loads in flight, one wait
+              uint32_t pv[32], rv[32];
+              tmem_ld32_nowait(tP + col, pv);
+              tmem_ld32_nowait(tR + col, rv);
+              tmem_wait_ld2(pv, rv);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = fmaf(alpha, v[i] * inv_local, r[i]);
+              for (int i = 0; i < 32; ++i)
+                v[i] = fmaf(alpha, __uint_as_float(pv[i]) * inv_local, __uint_as_float(rv[i]));
             }
-            tmem_st32(tR + col, v);
+            tmem_st32_nowait(tR + col, v);
           }
+          tmem_wait_st();  // R is complete before it is read again or P's slot is refilled
           if (s > 0) release(slp);
         }
         if (!ok) break;
@@ -822,10 +891,109 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           }
         }
         release(sl0);
+        // store G while the MMAs of U run: each chunk goes to subtile 0 of its ring
+        // entry, U and m follow in subtiles 1 and 2 once U has arrived
+        if (pr.out_mask & 1) {
+          const int rt = static_cast<int>(w.m0) + row_off + q * 32;
+#pragma unroll
+          for (int k = 0; k < MYCH; ++k) {
+            const int c = k * EPI_GROUPS + grp;
+            const int64_t col0 = n0 + c * EPI_N;
+            const int e = static_cast<int>((tile_no * NCH + c) % E::NE);
+            uint8_t* ent = epi + e * E::NT * E::SUB_BYTES + q * E::WARP_BYTES;
+            smem_row_store_packed(ent, lane, gpk[k]);
+            if (row_ok && col0 + EPI_N > pr.N8 && col0 < N) {
+              float g[32];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                g[2 * i] = __uint_as_float(gpk[k][i] << 16);
+                g[2 * i + 1] = __uint_as_float(gpk[k][i] & 0xFFFF0000u);
+              }
+              store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, g);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+              if (rt < M && col0 < pr.N8)
+                tma_store_2d(&pr.mo[0], smem_u32(ent), static_cast<int>(col0), rt);
+              bulk_commit();
+              bulk_wait_read<E::NE / EPI_GROUPS - 1>();
+            }
+            __syncwarp();
+          }
+        }
         if (!acquire(sl1, p1)) {
           ok = false;
           break;
         }
+        // U: all of this warp's columns into registers too, then its slot is free
+        // and the MMAs run a tile ahead while m = SiLU(G) * U is formed and stored
+        uint32_t upk[MYCH][16];
+#pragma unroll
+        for (int k = 0; k < MYCH; ++k) {
+          float u[32];
+          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl1 * BN + (k * EPI_GROUPS + grp) * 32),
+                    u);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(u[2 * i], u[2 * i + 1]);
+            upk[k][i] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+        }
+        release(sl1);
+        const int rt = static_cast<int>(w.m0) + row_off + q * 32;
+#pragma unroll
+        for (int k = 0; k < MYCH; ++k) {
+          const int c = k * EPI_GROUPS + grp;
+          const int64_t col0 = n0 + c * EPI_N;
+          const int e = static_cast<int>((tile_no * NCH + c) % E::NE);
+          uint8_t* ent = epi + e * E::NT * E::SUB_BYTES + q * E::WARP_BYTES;
+          uint32_t mpk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(gpk[k][i] << 16);
+            const float g1 = __uint_as_float(gpk[k][i] & 0xFFFF0000u);
+            const float u0 = __uint_as_float(upk[k][i] << 16);
+            const float u1 = __uint_as_float(upk[k][i] & 0xFFFF0000u);
+            const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(silu_fast(g0), u0),
+                                                           __fmul_rn(silu_fast(g1), u1));
+            mpk[i] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          smem_row_store_packed(ent + E::SUB_BYTES, lane, upk[k]);
+          smem_row_store_packed(ent + 2 * E::SUB_BYTES, lane, mpk);
+          if (row_ok && col0 + EPI_N > pr.N8 && col0 < N) {
+            float f[32];
+            if (pr.out_mask & 2) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                f[2 * i] = __uint_as_float(upk[k][i] << 16);
+                f[2 * i + 1] = __uint_as_float(upk[k][i] & 0xFFFF0000u);
+              }
+              store_tail_bf16(pr.out[1], pr.ldo[1], row, col0, pr.N8, N, f);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              f[2 * i] = __uint_as_float(mpk[i] << 16);
+              f[2 * i + 1] = __uint_as_float(mpk[i] & 0xFFFF0000u);
+            }
+            store_tail_bf16(pr.out[2], pr.ldo[2], row, col0, pr.N8, N, f);
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            if (rt < M && col0 < pr.N8) {
+              if (pr.out_mask & 2)
+                tma_store_2d(&pr.mo[1], smem_u32(ent + E::SUB_BYTES), static_cast<int>(col0), rt);
+              if (pr.out_mask & 4)
+                tma_store_2d(&pr.mo[2], smem_u32(ent + 2 * E::SUB_BYTES), static_cast<int>(col0),
+                             rt);
+            }
+            bulk_commit();
+            bulk_wait_read<E::NE / EPI_GROUPS - 1>();
+          }
+          __syncwarp();
+        }
+        continue;  // the tile is done
       } else {
         sl0 = slot;
         if (!acquire(slot, sph)) {
@@ -839,9 +1007,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           pr.rowv != nullptr && row_ok)
         rs = pr.rowv[row];
 
-      // SwiGLU indexes its register-held G by k: unrolled; the others stay rolled
-      // to keep the kernel small
-#pragma unroll(EK == K_SWIGLU ? MYCH : 1)
+#pragma unroll 1
       for (int k = 0; k < MYCH; ++k) {
         const int c = k * EPI_GROUPS + grp;            // subtile within the tile
         const int64_t col0 = n0 + c * EPI_N;
@@ -855,20 +1021,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           }
         }
         float v[32];
-        float v2[EK == K_SWIGLU ? 32 : 1];
-        if constexpr (EK == K_SWIGLU) {
-          // v = G (already bf16), v2 = U
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            v[2 * i] = __uint_as_float(gpk[k][i] << 16);
-            v[2 * i + 1] = __uint_as_float(gpk[k][i] & 0xFFFF0000u);
-          }
-          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl1 * BN + c * 32), v2);
-          if (k == MYCH - 1) release(sl1);
-        } else {
-          tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl0 * BN + c * 32), v);
-          if (k == MYCH - 1) release(sl0);
-        }
+        tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl0 * BN + c * 32), v);
+        if (k == MYCH - 1) release(sl0);
         uint8_t* ent = epi + e * E::NT * E::SUB_BYTES + q * E::WARP_BYTES;
         // this row holds some of the ragged columns [N8, N) (fp32 partials need none)
         const bool tail = EK != K_PART && row_ok && col0 + EPI_N > pr.N8 && col0 < N;
@@ -899,21 +1053,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
           if (tail) {
             store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, v);
             if (pr.out_mask & 2) store_tail_bf16(pr.out[1], pr.ldo[1], row, col0, pr.N8, N, h);
-          }
-        } else if constexpr (EK == K_SWIGLU) {
-          float m[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            v2[i] = round_to<__nv_bfloat16>(v2[i]);
-            m[i] = __fmul_rn(silu_fast(v[i]), v2[i]);
-          }
-          smem_row_store_bf16(ent, lane, v);
-          smem_row_store_bf16(ent + E::SUB_BYTES, lane, v2);
-          smem_row_store_bf16(ent + 2 * E::SUB_BYTES, lane, m);
-          if (tail) {
-            if (pr.out_mask & 1) store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, v);
-            if (pr.out_mask & 2) store_tail_bf16(pr.out[1], pr.ldo[1], row, col0, pr.N8, N, v2);
-            store_tail_bf16(pr.out[2], pr.ldo[2], row, col0, pr.N8, N, m);
           }
         } else if constexpr (EK == K_RESID) {
           float r[32];
