@@ -95,6 +95,10 @@ void prof_start(Ctx& c);
 // Call right after a kernel launch: counts it, records a launch error, and
 // closes its timing record with the launch's algorithmic FLOPs and bytes.
 void note_launch(Ctx& c, int kind, int epi, double flops, double bytes);
+// keep the first launch error of a sequence
+inline void track(Ctx& c, cudaError_t e) {
+  if (e != cudaSuccess && c.err == cudaSuccess) c.err = e;
+}
 
 // Algorithmic work of one GEMM launch: 2 M N K FLOPs per operand pair, every
 // operand and epilogue input read once, every output written once.

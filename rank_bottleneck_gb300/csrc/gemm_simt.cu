@@ -71,6 +71,7 @@ __device__ __forceinline__ void dot2_step(float& s, float& c, float a, float b) 
 
 template <int EK>
 __global__ void __launch_bounds__(THREADS) simt_kernel(const __grid_constant__ Params P) {
+  grid_dependency_sync();
   const Prob& pr = P.p[blockIdx.z];
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TM, n0 = static_cast<int64_t>(blockIdx.x) * TN;
   if (m0 >= pr.M || n0 >= pr.N) return;
@@ -205,8 +206,8 @@ static Op make_op(const Operand& o) {
 }
 
 template <int EK>
-static void go(const Params& P, dim3 grid, cudaStream_t s) {
-  simt_kernel<EK><<<grid, THREADS, 0, s>>>(P);
+static cudaError_t go(const Params& P, dim3 grid, cudaStream_t s) {
+  return launch_pdl(simt_kernel<EK>, grid, THREADS, 0, s, P);
 }
 
 }  // namespace simt
@@ -246,14 +247,14 @@ void gemm_simt(Ctx& c, const GemmLaunch& g) {
   gemm_work(g, 4, flops, bytes);
   prof_start(c);
   switch (g.epi) {
-    case EPI_STORE: go<EPI_STORE>(P, grid, c.stream); break;
-    case EPI_SIGMA: go<EPI_SIGMA>(P, grid, c.stream); break;
-    case EPI_NORM: go<EPI_NORM>(P, grid, c.stream); break;
-    case EPI_RESID: go<EPI_RESID>(P, grid, c.stream); break;
-    case EPI_SWIGLU: go<EPI_SWIGLU>(P, grid, c.stream); break;
-    case EPI_DSIGMA: go<EPI_DSIGMA>(P, grid, c.stream); break;
-    case EPI_DSWIGLU: go<EPI_DSWIGLU>(P, grid, c.stream); break;
-    case EPI_STORE_CHAIN: go<EPI_STORE_CHAIN>(P, grid, c.stream); break;
+    case EPI_STORE: track(c, go<EPI_STORE>(P, grid, c.stream)); break;
+    case EPI_SIGMA: track(c, go<EPI_SIGMA>(P, grid, c.stream)); break;
+    case EPI_NORM: track(c, go<EPI_NORM>(P, grid, c.stream)); break;
+    case EPI_RESID: track(c, go<EPI_RESID>(P, grid, c.stream)); break;
+    case EPI_SWIGLU: track(c, go<EPI_SWIGLU>(P, grid, c.stream)); break;
+    case EPI_DSIGMA: track(c, go<EPI_DSIGMA>(P, grid, c.stream)); break;
+    case EPI_DSWIGLU: track(c, go<EPI_DSWIGLU>(P, grid, c.stream)); break;
+    case EPI_STORE_CHAIN: track(c, go<EPI_STORE_CHAIN>(P, grid, c.stream)); break;
   }
   note_launch(c, KK_GEMM_FFMA, static_cast<int>(g.epi), flops, bytes);
 }

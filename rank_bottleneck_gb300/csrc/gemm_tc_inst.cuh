@@ -14,7 +14,7 @@ void go(const Params& P, int units, int num_sms, cudaStream_t s) {
   auto k = gemm_kernel<BN, EK, AMN, BMN, CG>;
   constexpr int SMEM = Cfg<BN, EK, CG>::SMEM_BYTES;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(kernel_threads<EK>(), 1, 1);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = s;
@@ -44,6 +44,11 @@ void go(const Params& P, int units, int num_sms, cudaStream_t s) {
   });
   const int groups = units < max_groups ? units : max_groups;
   cfg.gridDim = dim3(groups * CG, 1, 1);
+  // programmatic dependent launch (see grid_dependency_sync)
+  attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs += 1;
   cudaLaunchKernelEx(&cfg, k, P);
 }
 

@@ -588,6 +588,9 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // setup above touches no global memory; from here on the previous kernel's
+  // results are read and its inputs may be overwritten
+  grid_dependency_sync();
   const uint32_t tmem = *tmem_slot;
   const int nseg = num_segments<EK>(P);
 

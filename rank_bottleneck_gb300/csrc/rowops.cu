@@ -18,6 +18,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) stats_kernel(const T* __restrict__ x, int64_t rows, int d,
                                                     int S, float eps, float* __restrict__ ss,
                                                     float* __restrict__ rstd) {
+  grid_dependency_sync();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
   if (row >= rows) return;
@@ -44,7 +45,8 @@ void launch_stats(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float eps,
                   float* rstd) {
   const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
   prof_start(c);
-  stats_kernel<T><<<grid, 256, 0, c.stream>>>(x, rows, static_cast<int>(d), S, eps, ss, rstd);
+  track(c, launch_pdl(stats_kernel<T>, grid, 256, 0, c.stream, x, rows, static_cast<int>(d), S, eps,
+                      ss, rstd));
   note_launch(c, KK_STATS, -1, 2.0 * rows * d, static_cast<double>(rows) * (d * sizeof(T) + 4 * S + 4));
 }
 
@@ -54,6 +56,7 @@ void launch_stats(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float eps,
 template <typename T>
 __global__ void fold_cols_kernel(const T* __restrict__ A, const T* __restrict__ w, int64_t rows,
                                  int64_t cols, T* __restrict__ out) {
+  grid_dependency_sync();
   const int64_t nvec = cols / 8;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows * nvec;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -72,7 +75,7 @@ void launch_fold_cols(Ctx& c, const T* A, const T* w, int64_t rows, int64_t cols
   const int64_t n = rows * (cols / 8);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 8));
   prof_start(c);
-  fold_cols_kernel<T><<<grid, 256, 0, c.stream>>>(A, w, rows, cols, out);
+  track(c, launch_pdl(fold_cols_kernel<T>, grid, 256, 0, c.stream, A, w, rows, cols, out));
   note_launch(c, KK_FOLD, -1, 1.0 * rows * cols, (2.0 * rows * cols + cols) * sizeof(T));
 }
 
@@ -120,6 +123,7 @@ __global__ void __launch_bounds__(kNormBwdMaxWarps * 32, 2)
     norm_bwd_kernel(const T* __restrict__ dn, const T* __restrict__ x, const T* __restrict__ w,
                     const float* __restrict__ rstd, const T* __restrict__ dres, int64_t rows,
                     int d, T* __restrict__ dx, float* __restrict__ part) {
+  grid_dependency_sync();
   // [warps][d + d/8] column sums; column c lives at c + c/8, so the 8 columns a
   // lane owns are 9 floats apart from the next lane's: no bank conflicts
   extern __shared__ float acc[];
@@ -201,6 +205,7 @@ __global__ void __launch_bounds__(kNormBwdMaxWarps * 32, 2)
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ part, int nblk, int d,
                                                      T* __restrict__ out) {
+  grid_dependency_sync();
   __shared__ float red[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col = blockIdx.x * 32 + lane;
@@ -237,13 +242,13 @@ void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* r
   }();
   (void)attr;
   prof_start(c);
-  norm_bwd_kernel<T><<<nblk, nw * 32, smem, c.stream>>>(
-      dn, x, w, rstd, dres, rows, static_cast<int>(d), dx, part);
+  track(c, launch_pdl(norm_bwd_kernel<T>, nblk, nw * 32, smem, c.stream, dn, x, w, rstd, dres, rows,
+                      static_cast<int>(d), dx, part));
   note_launch(c, KK_NORM_BWD, -1, 8.0 * rows * d,
               4.0 * rows * d * sizeof(T) + d * sizeof(T) + 4.0 * rows + 4.0 * nblk * d);
   prof_start(c);
-  colsum_kernel<T><<<static_cast<unsigned>((d + 31) / 32), 256, 0, c.stream>>>(
-      part, nblk, static_cast<int>(d), dw);
+  track(c, launch_pdl(colsum_kernel<T>, static_cast<unsigned>((d + 31) / 32), 256, 0, c.stream,
+                      part, nblk, static_cast<int>(d), dw));
   note_launch(c, KK_COLSUM, -1, 1.0 * nblk * d, 4.0 * nblk * d + d * sizeof(T));
 }
 
@@ -254,6 +259,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
                                      int64_t plane_rows, int64_t N, int64_t ldp,
                                      const bf16* __restrict__ colv, bf16* __restrict__ out,
                                      int64_t ldo) {
+  grid_dependency_sync();
   const int64_t nvec = (N + 7) / 8;
   const int64_t plane = plane_rows * ldp;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M * nvec;
@@ -286,8 +292,8 @@ void launch_splitk_reduce(Ctx& c, const float* part, int splits, int64_t M, int6
   const int64_t n = M * ((N + 7) / 8);
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 8));
   prof_start(c);
-  splitk_reduce_kernel<<<grid, 256, 0, c.stream>>>(part, splits, M, plane_rows, N, ldp, colv, out,
-                                                   ldo);
+  track(c, launch_pdl(splitk_reduce_kernel, grid, 256, 0, c.stream, part, splits, M, plane_rows, N,
+                      ldp, colv, out, ldo));
   note_launch(c, KK_SPLITK_REDUCE, -1, 1.0 * splits * M * N, (4.0 * splits + 2.0) * M * N);
 }
 
@@ -298,6 +304,7 @@ template <typename T, int OP>  // OP 0: h = sigma(z); 1: m = SiLU(G) U; 2: out =
 __global__ void ew_kernel(const T* __restrict__ a, int64_t lda, const T* __restrict__ b,
                           int64_t rows, int64_t cols, const float* __restrict__ rowv, int sigma,
                           T* __restrict__ out, int64_t ldo) {
+  grid_dependency_sync();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows * cols;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = i / cols, col = i - r * cols;
@@ -319,7 +326,8 @@ static void launch_ew(Ctx& c, const T* a, int64_t lda, const T* b, int64_t rows,
   const int64_t n = rows * cols;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 16));
   prof_start(c);
-  ew_kernel<T, OP><<<grid, 256, 0, c.stream>>>(a, lda, b, rows, cols, rowv, sigma, out, ldo);
+  track(c, launch_pdl(ew_kernel<T, OP>, grid, 256, 0, c.stream, a, lda, b, rows, cols, rowv, sigma,
+                      out, ldo));
   note_launch(c, KK_ELEMENTWISE, OP, 4.0 * n, (OP == 1 ? 3.0 : 2.0) * n * sizeof(T));
 }
 
