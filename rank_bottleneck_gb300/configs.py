@@ -8,6 +8,9 @@ WORKLOADS = {
     "mlp-f32-T256-d256-r64-dff688": dict(T=256, d=256, r=64, d_ff=688, S=4, dtype="f32", kind="mlp"),
     # 1B shape: micro-batch 4 x sequence 4096
     "1b-T16384-d2048-r512-dff5461": dict(T=16384, d=2048, r=512, d_ff=5461, S=4),
+    # the 1B block at a quarter of the tokens: small enough for multi-pass profiler
+    # captures, its d_ff-wide activations still larger than L2
+    "1b-T4096-d2048-r512-dff5461": dict(T=4096, d=2048, r=512, d_ff=5461, S=4),
     "7b-T16384-d4096-r1024-dff11008": dict(T=16384, d=4096, r=1024, d_ff=11008, S=8),
     "13b-ckpt-T16384-d5120-r1280-dff13824": dict(T=16384, d=5120, r=1280, d_ff=13824, S=8,
                                                   checkpoint=True),

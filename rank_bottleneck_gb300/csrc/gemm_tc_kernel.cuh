@@ -63,8 +63,10 @@ struct EpiShape {
   static constexpr int ELEM = (EK == K_PART) ? 4 : 2;        // output element bytes
   static constexpr int SUB_BYTES = BM * EPI_N * ELEM;        // one 128 x 32 subtile
   static constexpr int WARP_BYTES = 32 * EPI_N * ELEM;       // one warp's 32 rows of it
-  // ring entries: kinds that read epilogue inputs keep several subtiles of them in flight
-  static constexpr int NE = (EK == K_PART) ? 2 : (NT == 1 || NIN > 0) ? 8 : 4;
+  // ring entries: kinds that read epilogue inputs keep several subtiles of them in
+  // flight; the others only need each warp's previous store to have left shared
+  // memory, and leave the rest to operand stages
+  static constexpr int NE = (EK == K_PART) ? 2 : (NIN > 0) ? 8 : 4;
   static constexpr int BYTES = NE * NT * SUB_BYTES;
 };
 
@@ -372,6 +374,18 @@ __device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const float* v)
       "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
       "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32u_nowait(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
@@ -834,18 +848,75 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         const float rms_g = sqrtf(tot / static_cast<float>(pr.K) + P.eps);
         const uint32_t tR = tmem + lane_base + static_cast<uint32_t>(sl0 * BN);
         const uint32_t tP = tmem + lane_base + static_cast<uint32_t>(slp * BN);
-        for (int s = 0; s < S; ++s) {
+        uint32_t zpk[MYCH][16];  // z = R after the last shard, as bf16 pairs
+        // waits for shard s's product and gives its local normalisation 1 / rms_s
+        // and per-row correction alpha_s = rms_s / rms_g
+        auto shard = [&](int s, float& inv_local, float& alpha) -> bool {
           const int sl = (s == 0) ? sl0 : slp;
-          if (!acquire(sl, norm_ph[sl])) {
-            ok = false;
-            break;
-          }
+          if (!acquire(sl, norm_ph[sl])) return false;
           norm_ph[sl] ^= 1u;
           const float ss_s = row_ok ? ss[s] : 0.f;
           const float rms_s = sqrtf(ss_s / shard_w + P.eps);
-          const float inv_local = 1.0f / rms_s;  // local normalisation
-          const float alpha = rms_s / rms_g;     // per-row correction
+          inv_local = 1.0f / rms_s;
+          alpha = rms_s / rms_g;
+          return true;
+        };
+        for (int s = 0; s + 1 < S; ++s) {
+          float inv_local, alpha;
+          if (!shard(s, inv_local, alpha)) {
+            ok = false;
+            break;
+          }
+          // two chunks per TMEM round trip: all loads in flight, then one wait; the
+          // new running sum overwrites the loaded one in place
 #pragma unroll 1
+          for (int k = 0; k < MYCH; k += 2) {
+            const uint32_t c0 = static_cast<uint32_t>((k * EPI_GROUPS + grp) * 32);
+            const uint32_t c1 = static_cast<uint32_t>(((k + 1) * EPI_GROUPS + grp) * 32);
+            uint32_t r0[32], r1[32];
+            if (s == 0) {
+              tmem_ld32_nowait(tR + c0, r0);
+              tmem_ld32_nowait(tR + c1, r1);
+              tmem_wait_ld2(r0, r1);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                r0[i] = __float_as_uint(alpha * (__uint_as_float(r0[i]) * inv_local));
+                r1[i] = __float_as_uint(alpha * (__uint_as_float(r1[i]) * inv_local));
+              }
+            } else {
+              uint32_t p0[32], p1[32];
+              tmem_ld32_nowait(tP + c0, p0);
+              tmem_ld32_nowait(tR + c0, r0);
+              tmem_ld32_nowait(tP + c1, p1);
+              tmem_ld32_nowait(tR + c1, r1);
+              tmem_wait_ld2(p0, r0);
+              tie32(p1);
+              tie32(r1);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                r0[i] = __float_as_uint(
+                    fmaf(alpha, __uint_as_float(p0[i]) * inv_local, __uint_as_float(r0[i])));
+                r1[i] = __float_as_uint(
+                    fmaf(alpha, __uint_as_float(p1[i]) * inv_local, __uint_as_float(r1[i])));
+              }
+            }
+            tmem_st32u_nowait(tR + c0, r0);
+            tmem_st32u_nowait(tR + c1, r1);
+          }
+          tmem_wait_st();  // R is complete before it is read again or P's slot is refilled
+          if (s > 0) release(slp);
+        }
+        if (!ok) break;
+        {
+          // last shard: z goes to registers (it is rounded to bf16 anyway), and both
+          // TMEM slots are free for the next tile before z and sigma(z) are stored
+          const int s = S - 1;
+          float inv_local, alpha;
+          if (!shard(s, inv_local, alpha)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
           for (int k = 0; k < MYCH; ++k) {
             const uint32_t col = static_cast<uint32_t>((k * EPI_GROUPS + grp) * 32);
             float v[32];
@@ -854,7 +925,6 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = alpha * (v[i] * inv_local);
             } else {
-              // both loads in flight, one wait
               uint32_t pv[32], rv[32];
               tmem_ld32_nowait(tP + col, pv);
               tmem_ld32_nowait(tR + col, rv);
@@ -863,12 +933,65 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
               for (int i = 0; i < 32; ++i)
                 v[i] = fmaf(alpha, __uint_as_float(pv[i]) * inv_local, __uint_as_float(rv[i]));
             }
-            tmem_st32_nowait(tR + col, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+              zpk[k][i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
           }
-          tmem_wait_st();  // R is complete before it is read again or P's slot is refilled
           if (s > 0) release(slp);
+          release(sl0);
         }
         if (!ok) break;
+        const int rt = static_cast<int>(w.m0) + row_off + q * 32;
+#pragma unroll
+        for (int k = 0; k < MYCH; ++k) {
+          const int c = k * EPI_GROUPS + grp;
+          const int64_t col0 = n0 + c * EPI_N;
+          const int e = static_cast<int>((tile_no * NCH + c) % E::NE);
+          uint8_t* ent = epi + e * E::NT * E::SUB_BYTES + q * E::WARP_BYTES;
+          uint32_t hpk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float z0 = __uint_as_float(zpk[k][i] << 16);
+            const float z1 = __uint_as_float(zpk[k][i] & 0xFFFF0000u);
+            const __nv_bfloat162 h = __floats2bfloat162_rn(act_fast(z0, P.sigma), act_fast(z1, P.sigma));
+            hpk[i] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          smem_row_store_packed(ent, lane, zpk[k]);
+          smem_row_store_packed(ent + E::SUB_BYTES, lane, hpk);
+          if (row_ok && col0 + EPI_N > pr.N8 && col0 < N) {
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              f[2 * i] = __uint_as_float(zpk[k][i] << 16);
+              f[2 * i + 1] = __uint_as_float(zpk[k][i] & 0xFFFF0000u);
+            }
+            if (pr.out_mask & 1) store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, f);
+            if (pr.out_mask & 2) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                f[2 * i] = __uint_as_float(hpk[i] << 16);
+                f[2 * i + 1] = __uint_as_float(hpk[i] & 0xFFFF0000u);
+              }
+              store_tail_bf16(pr.out[1], pr.ldo[1], row, col0, pr.N8, N, f);
+            }
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            if (rt < M && col0 < pr.N8) {
+              if (pr.out_mask & 1)
+                tma_store_2d(&pr.mo[0], smem_u32(ent), static_cast<int>(col0), rt);
+              if (pr.out_mask & 2)
+                tma_store_2d(&pr.mo[1], smem_u32(ent + E::SUB_BYTES), static_cast<int>(col0), rt);
+            }
+            bulk_commit();
+            bulk_wait_read<E::NE / EPI_GROUPS - 1>();
+          }
+          __syncwarp();
+        }
+        continue;  // the tile is done
       } else if constexpr (EK == K_SWIGLU) {
         // G first: keep this warp's columns of it as bf16 pairs and free its slot
         // at once, so the MMAs of the next tile's G overlap this tile's epilogue
