@@ -268,13 +268,22 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
   }
   note_launch(c, KK_GEMM_TC, static_cast<int>(g.epi), flops, bytes);
   if (split) {
+    SplitkReduce r;
+    r.nprob = g.nprob;
     for (int i = 0; i < g.nprob; ++i) {
       const Prob& p = P.p[i];
-      launch_splitk_reduce(c, static_cast<const float*>(part_ptr[i]), p.splits, p.M, part_rows[i],
-                           p.N, part_ld[i],
-                           static_cast<const __nv_bfloat16*>(g.p[i].colv),
-                           static_cast<__nv_bfloat16*>(g.p[i].out[0]), g.p[i].ldo[0]);
+      SplitkProb& q = r.p[i];
+      q.part = static_cast<const float*>(part_ptr[i]);
+      q.splits = p.splits;
+      q.M = p.M;
+      q.plane_rows = part_rows[i];
+      q.N = p.N;
+      q.ldp = part_ld[i];
+      q.colv = static_cast<const __nv_bfloat16*>(g.p[i].colv);
+      q.out = static_cast<__nv_bfloat16*>(g.p[i].out[0]);
+      q.ldo = g.p[i].ldo[0];
     }
+    launch_splitk_reduce(c, r);
   }
 }
 

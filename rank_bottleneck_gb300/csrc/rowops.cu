@@ -253,48 +253,64 @@ void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* r
 }
 
 // ---------------------------------------------------------------------------
-// split-K reduction (fixed order over splits)
+// split-K reduction (fixed order over splits), all problems of a launch at once
 // ---------------------------------------------------------------------------
-__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int64_t M,
-                                     int64_t plane_rows, int64_t N, int64_t ldp,
-                                     const bf16* __restrict__ colv, bf16* __restrict__ out,
-                                     int64_t ldo) {
+__global__ void splitk_reduce_kernel(const SplitkReduce R) {
   grid_dependency_sync();
-  const int64_t nvec = (N + 7) / 8;
-  const int64_t plane = plane_rows * ldp;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M * nvec;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < R.total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / nvec, c0 = (i - r * nvec) * 8;
+    int pi = 0;
+    while (pi + 1 < R.nprob && i >= R.p[pi + 1].begin) ++pi;
+    const SplitkProb& q = R.p[pi];
+    const int64_t nvec = (q.N + 7) / 8;
+    const int64_t li = i - q.begin;
+    const int64_t r = li / nvec, c0 = (li - r * nvec) * 8;
+    const int64_t plane = q.plane_rows * q.ldp;
+    const float* src = q.part + r * q.ldp + c0;
     float a[8];
-    Vec8<float>::load(part + r * ldp + c0, a);
-    for (int s = 1; s < splits; ++s) {
-      float b[8];
-      Vec8<float>::load(part + s * plane + r * ldp + c0, b);
+    Vec8<float>::load(src, a);
+    // four splits' loads in flight at a time; the adds keep split order
+    for (int s = 1; s < q.splits; s += 4) {
+      float b[4][8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) a[k] += b[k];
+      for (int u = 0; u < 4; ++u)
+        if (s + u < q.splits) Vec8<float>::load(src + (s + u) * plane, b[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (s + u < q.splits) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) a[k] += b[u][k];
+        }
     }
-    if (colv != nullptr) {
+    if (q.colv != nullptr) {
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (c0 + k < N) a[k] *= __bfloat162float(colv[c0 + k]);
+        if (c0 + k < q.N) a[k] *= __bfloat162float(q.colv[c0 + k]);
     }
-    bf16* o = out + r * ldo + c0;
-    if (c0 + 8 <= N) {
+    bf16* o = q.out + r * q.ldo + c0;
+    if (c0 + 8 <= q.N) {
       Vec8<bf16>::store(o, a);
     } else {
-      for (int k = 0; c0 + k < N; ++k) o[k] = __float2bfloat16_rn(a[k]);
+      for (int k = 0; c0 + k < q.N; ++k) o[k] = __float2bfloat16_rn(a[k]);
     }
   }
 }
 
-void launch_splitk_reduce(Ctx& c, const float* part, int splits, int64_t M, int64_t plane_rows,
-                          int64_t N, int64_t ldp, const bf16* colv, bf16* out, int64_t ldo) {
-  const int64_t n = M * ((N + 7) / 8);
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 8));
+void launch_splitk_reduce(Ctx& c, SplitkReduce& R) {
+  double flops = 0, bytes = 0;
+  R.total = 0;
+  for (int i = 0; i < R.nprob; ++i) {
+    SplitkProb& q = R.p[i];
+    q.begin = R.total;
+    R.total += q.M * ((q.N + 7) / 8);
+    flops += 1.0 * q.splits * q.M * q.N;
+    bytes += (4.0 * q.splits + 2.0) * q.M * q.N;
+  }
+  const unsigned grid =
+      static_cast<unsigned>(std::min<int64_t>((R.total + 255) / 256, c.num_sms * 8));
   prof_start(c);
-  track(c, launch_pdl(splitk_reduce_kernel, grid, 256, 0, c.stream, part, splits, M, plane_rows, N,
-                      ldp, colv, out, ldo));
-  note_launch(c, KK_SPLITK_REDUCE, -1, 1.0 * splits * M * N, (4.0 * splits + 2.0) * M * N);
+  track(c, launch_pdl(splitk_reduce_kernel, grid, 256, 0, c.stream, R));
+  note_launch(c, KK_SPLITK_REDUCE, -1, flops, bytes);
 }
 
 // ---------------------------------------------------------------------------

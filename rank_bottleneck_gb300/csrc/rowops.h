@@ -26,10 +26,24 @@ void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* r
                      const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw);
 int norm_bwd_blocks(int num_sms);
 
-// out[i, j] = colv[j] * sum_s part[s * plane_rows + i][j] (fixed order over s), bf16 output.
-void launch_splitk_reduce(Ctx& c, const float* part, int splits, int64_t M, int64_t plane_rows,
-                          int64_t N, int64_t ldp, const __nv_bfloat16* colv, __nv_bfloat16* out,
-                          int64_t ldo);
+// Split-K reduction of up to three problems in one launch: per problem
+// out[i, j] = colv[j] * sum_s part[s * plane_rows + i][j] (fixed order over s),
+// bf16 output; colv may be null.
+struct SplitkProb {
+  const float* part;
+  int splits;
+  int64_t M, plane_rows, N, ldp;
+  const __nv_bfloat16* colv;
+  __nv_bfloat16* out;
+  int64_t ldo;
+  int64_t begin;  // set by the launcher: first work item of this problem
+};
+struct SplitkReduce {
+  SplitkProb p[3];
+  int nprob = 0;
+  int64_t total = 0;  // set by the launcher
+};
+void launch_splitk_reduce(Ctx& c, SplitkReduce& r);
 
 // h = sigma(z) elementwise, rounded exactly like the GEMM epilogues round it.
 template <typename T>
