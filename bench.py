@@ -317,7 +317,7 @@ def run_ours(args, rank, local_rank, world):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": f"{peak_src} HBM copy"}
     roof.update(kernel=dom, launches_per_step=dk["launches"] / nprof,
-                ms_per_launch=dk["ms"] / dk["launches"], traffic=traffic_for(dom),
+                ms_per_launch=dk["ms"] / dk["launches"], traffic=traffic_for(dom, args.workload),
                 flops_per_launch=dk["flops"] / dk["launches"],
                 bytes_per_launch=dk["bytes"] / dk["launches"])
 
@@ -361,9 +361,9 @@ def run_ours(args, rank, local_rank, world):
         print(json.dumps(line), flush=True)
 
 
-def traffic_for(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if it matches the
-    current kernel source; None otherwise."""
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    this workload with the current kernel source; None otherwise."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -371,7 +371,7 @@ def traffic_for(kernel):
     except (OSError, ValueError):
         return None
     entry = t.get(kernel)
-    if not entry:
+    if not entry or entry.get("workload") != workload:
         return None
     import hashlib
     src = os.path.join(ROOT, "rank_bottleneck_gb300", "csrc", entry["source"])
