@@ -156,16 +156,17 @@ int bn_profile_stop(bn_launch_record* out, int max_records);
 /* Weight gradient without any caller-provided scratch: for callers that cannot
  * allocate GPU memory (their memory is reserved up front by their own pool, or
  * a cudaMalloc is forbidden or would synchronise where they run). The paper has
- * no counterpart; this is the split-K weight-gradient GEMM of bn_block_backward
+ * no counterpart; this is the weight-gradient GEMM of bn_block_backward
  * (dA = dz^T X, dB = dY^T h) offered on its own.
  *   dW[i, j] = colscale[j] * sum_{t < T} A[t, i] * B[t, j],  i < M, j < N
  * A [T, lda] and B [T, ldb] are row-major bf16 (token rows), dW [M, ldw] bf16;
  * colscale (bf16, N values) may be NULL; fp32 accumulation on the tensor cores.
  * Pointers 16-byte aligned, leading dimensions multiples of 8.
  * Scratch: a 32 MiB array inside the library (held on every GPU that loads
- * it until the process exits) holds the fp32 partial sums of the K split;
- * sizes with M * round_up(N, 8) * 8 bytes > 32 MiB - 256 return
- * BN_ERR_UNSUPPORTED. No device memory is allocated. The first call on each
+ * it until the process exits) holds the status word and the fp32 partial
+ * tiles of the K split: at most one 128 x 256 tile per SM, whatever M, N and T
+ * are (a GPU with more than 255 SMs returns BN_ERR_UNSUPPORTED). No device
+ * memory is allocated. The first call on each
  * device looks the array's device address up (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture. All calls
  * share the array, which keeps the last call's contents: calls whose kernels

@@ -48,9 +48,10 @@ typedef struct {
   const float* rowv; const void* colv;
 } bn_gemm_problem;
 
-/* Launch 1..3 problems of one epilogue in one engine launch. dtype: bn_dtype.
- * allow_split lets the tensor-core engine split K for STORE (fp32 partials in
- * `scratch` after its 256-byte status word, reduced in a fixed order).
+/* Launch 1..16 problems of one epilogue in one engine launch. dtype: bn_dtype.
+ * allow_split lets the tensor-core engine cut the STORE tiles left over after
+ * whole rounds of CTA groups into K ranges (fp32 partial tiles in `scratch`
+ * after its 256-byte status word, summed in a fixed order by a second kernel).
  * Pointers are device pointers, 16-byte aligned. Asynchronous on `stream`. */
 bn_status bn_testing_gemm(int32_t dtype, int32_t epi, int32_t sigma, int32_t S, float eps,
                           int32_t allow_split, int32_t nprob, const bn_gemm_problem* probs,

@@ -77,33 +77,6 @@ int device_sms() {
   return cache[dev];
 }
 
-// Largest M x ldp(N) summed over the problems of one weight-gradient launch.
-int64_t max_wgrad_elems(const Shape& s) {
-  auto ldp = [](int64_t n) { return (n + 7) / 8 * 8; };
-  auto rows = [](int64_t m) { return (m + 255) / 256 * 256; };  // split planes hold whole tiles
-  int64_t best = 0;
-  auto cand = [&](int64_t v) { best = std::max(best, v); };
-  if (s.dense) {
-    cand(rows(s.d) * ldp(s.d_ff));
-    cand(2 * rows(s.d_ff) * ldp(s.d));
-    if (s.full()) {
-      cand(rows(s.d) * ldp(s.d));
-      cand(3 * rows(s.d) * ldp(s.d));
-    }
-  } else {
-    cand(rows(s.d) * ldp(s.r));
-    cand(rows(s.r) * ldp(s.d_ff));
-    cand(2 * rows(s.d_ff) * ldp(s.r));
-    cand(2 * rows(s.r) * ldp(s.d));
-    if (s.full()) {
-      cand(rows(s.r) * ldp(s.d));
-      cand(3 * rows(s.d) * ldp(s.r));
-      cand(3 * rows(s.r) * ldp(s.d));
-    }
-  }
-  return best;
-}
-
 void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
           size_t* saved_bytes, size_t* scratch_bytes) {
   Bump sv(saved_base), sc(scratch_base);
@@ -159,8 +132,7 @@ void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
   B.nblk = norm_bwd_blocks(device_sms());
   B.dw_part = static_cast<float*>(sc.take(static_cast<size_t>(B.nblk) * s.d * 4));
   if (s.dtype == BN_BF16) {
-    B.partial_bytes = std::min<size_t>(static_cast<size_t>(8) * max_wgrad_elems(s) * 4,
-                                       static_cast<size_t>(1) << 30);
+    B.partial_bytes = gemm_tc_partial_bytes(device_sms());
     B.partial = static_cast<float*>(sc.take(B.partial_bytes));
   }
   if (saved_bytes) *saved_bytes = sv.off;
@@ -274,6 +246,20 @@ GemmProblem wgrad(int64_t M, int64_t N, int64_t T, const void* a, int64_t lda, c
   p.ldo[0] = ldo;
   p.colv = colv;
   return p;
+}
+
+// The weight gradients of a backward pass, gathered and launched together at its
+// end: they read only tensors the backward has already written (nothing later
+// overwrites them), and one launch over all their tiles fills whole rounds of
+// the CTA groups, with only the last few tiles split along K.
+struct Wgrads {
+  GemmProblem p[kMaxProblems];
+  int n = 0;
+};
+void flush_wgrads(Ctx& c, const Shape& s, Wgrads& w);
+void add_wgrad(Ctx& c, const Shape& s, Wgrads& w, const GemmProblem& q) {
+  if (w.n == kMaxProblems) flush_wgrads(c, s, w);
+  w.p[w.n++] = q;
 }
 
 #define DT_CALL(s, FN, ...)                                          \
@@ -589,32 +575,31 @@ void dx_gemm(Ctx& c, const Shape& s, const void* dz, int64_t K, const void* A, i
   gemm(c, s, g);
 }
 
+void flush_wgrads(Ctx& c, const Shape& s, Wgrads& w) {
+  if (w.n == 0) return;
+  GemmLaunch g = launch(EPI_STORE, s);
+  g.allow_split = true;
+  g.nprob = w.n;
+  for (int i = 0; i < w.n; ++i) g.p[i] = w.p[i];
+  gemm(c, s, g);
+  w.n = 0;
+}
+
 void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const void* x,
                       const void* dy, const void* dq, const void* dk, void* dx,
                       const bn_block_params* dW, const Acts& A, const Tmp& B) {
   const int64_t T = s.T, d = s.d, r = s.r;
+  Wgrads wg;
   const void* x1 = s.full() ? A.x1 : x;
   // ---- down bottleneck: y = x1 + B_d sigma(A_d m)
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    g.nprob = 1;
-    g.p[0] = wgrad(d, r, T, dy, d, A.h_d, r, dW->B_d, r);
-    gemm(c, s, g);
-  }
+  add_wgrad(c, s, wg, wgrad(d, r, T, dy, d, A.h_d, r, dW->B_d, r));
   {
     GemmLaunch g = launch(EPI_DSIGMA, s);
     g.nprob = 1;
     g.p[0] = dsigma(s, dy, d, d, W->B_d, A.z_d, r, B.dz_d, nullptr);
     gemm(c, s, g);
   }
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    g.nprob = 1;
-    g.p[0] = wgrad(r, s.d_ff, T, B.dz_d, r, A.m, s.ld_act, dW->A_d, s.ld_ff);
-    gemm(c, s, g);
-  }
+  add_wgrad(c, s, wg, wgrad(r, s.d_ff, T, B.dz_d, r, A.m, s.ld_act, dW->A_d, s.ld_ff));
   {
     // dm = dz_d A_d, then the SwiGLU backward in the epilogue
     GemmLaunch g = launch(EPI_DSWIGLU, s);
@@ -634,14 +619,8 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
     gemm(c, s, g);
   }
   // ---- gate / up bottlenecks
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    g.nprob = 2;
-    g.p[0] = wgrad(s.d_ff, r, T, B.dG, s.ld_act, A.h_gu, 2 * r, dW->B_g, r);
-    g.p[1] = wgrad(s.d_ff, r, T, B.dU, s.ld_act, at(A.h_gu, r, s), 2 * r, dW->B_u, r);
-    gemm(c, s, g);
-  }
+  add_wgrad(c, s, wg, wgrad(s.d_ff, r, T, B.dG, s.ld_act, A.h_gu, 2 * r, dW->B_g, r));
+  add_wgrad(c, s, wg, wgrad(s.d_ff, r, T, B.dU, s.ld_act, at(A.h_gu, r, s), 2 * r, dW->B_u, r));
   {
     GemmLaunch g = launch(EPI_DSIGMA, s);
     g.nprob = 2;
@@ -650,56 +629,35 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
                     at(B.dz_gu, r, s), A.rstd2);
     gemm(c, s, g);
   }
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    g.nprob = 1;
-    g.p[0] = wgrad(2 * r, d, T, B.dz_gu, 2 * r, x1, d, dW->A_gu, d, W->w_norm2);
-    gemm(c, s, g);
-  }
+  add_wgrad(c, s, wg, wgrad(2 * r, d, T, B.dz_gu, 2 * r, x1, d, dW->A_gu, d, W->w_norm2));
   dx_gemm(c, s, B.dz_gu, 2 * r, W->A_gu, d, d, B.dn, d);
   void* dx1 = s.full() ? B.dx1 : dx;
   DT_CALL(s, normbwd, c, s, B, B.dn, x1, W->w_norm2, A.rstd2, dy, dx1, dW->w_norm2);
-  if (!s.full()) return;
+  if (!s.full()) {
+    flush_wgrads(c, s, wg);
+    return;
+  }
 
   // ---- O bottleneck: x1 = x + B_o sigma(A_o V)
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    g.nprob = 1;
-    g.p[0] = wgrad(d, r, T, dx1, d, A.h_o, r, dW->B_o, r);
-    gemm(c, s, g);
-  }
+  add_wgrad(c, s, wg, wgrad(d, r, T, dx1, d, A.h_o, r, dW->B_o, r));
   {
     GemmLaunch g = launch(EPI_DSIGMA, s);
     g.nprob = 1;
     g.p[0] = dsigma(s, dx1, d, d, W->B_o, A.z_o, r, B.dz_o, nullptr);
     gemm(c, s, g);
   }
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    g.nprob = 1;
-    g.p[0] = wgrad(r, d, T, B.dz_o, r, A.V, d, dW->A_o, d);
-    gemm(c, s, g);
-  }
+  add_wgrad(c, s, wg, wgrad(r, d, T, B.dz_o, r, A.V, d, dW->A_o, d));
   dx_gemm(c, s, B.dz_o, r, W->A_o, d, d, B.dV, d);
 
   // ---- Q / K / V bottlenecks
   const void* dQKV[3] = {dq, dk, B.dV};
   const void* Bup[3] = {W->B_q, W->B_k, W->B_v};
   void* dB[3] = {dW->B_q, dW->B_k, dW->B_v};
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    for (int i = 0; i < 3; ++i) {
-      if (dQKV[i] == nullptr) {
-        zero2d(c, dB[i], r * s.E, r * s.E, d);
-        continue;
-      }
-      g.p[g.nprob++] = wgrad(d, r, T, dQKV[i], d, at(A.h_qkv, i * r, s), 3 * r, dB[i], r);
-    }
-    gemm(c, s, g);
+  for (int i = 0; i < 3; ++i) {
+    if (dQKV[i] == nullptr)
+      zero2d(c, dB[i], r * s.E, r * s.E, d);
+    else
+      add_wgrad(c, s, wg, wgrad(d, r, T, dQKV[i], d, at(A.h_qkv, i * r, s), 3 * r, dB[i], r));
   }
   {
     GemmLaunch g = launch(EPI_DSIGMA, s);
@@ -713,15 +671,10 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
     }
     gemm(c, s, g);
   }
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    g.nprob = 1;
-    g.p[0] = wgrad(3 * r, d, T, B.dz_qkv, 3 * r, x, d, dW->A_qkv, d, W->w_norm1);
-    gemm(c, s, g);
-  }
+  add_wgrad(c, s, wg, wgrad(3 * r, d, T, B.dz_qkv, 3 * r, x, d, dW->A_qkv, d, W->w_norm1));
   dx_gemm(c, s, B.dz_qkv, 3 * r, W->A_qkv, d, d, B.dn, d);
   DT_CALL(s, normbwd, c, s, B, B.dn, x, W->w_norm1, A.rstd1, dx1, dx, dW->w_norm1);
+  flush_wgrads(c, s, wg);
 }
 
 void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void* x,
@@ -729,13 +682,8 @@ void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void
                     const bn_block_params* dW, const Acts& A, const Tmp& B) {
   const int64_t T = s.T, d = s.d, dff = s.d_ff;
   const void* x1 = s.full() ? A.x1 : x;
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    g.nprob = 1;
-    g.p[0] = wgrad(d, dff, T, dy, d, A.m, s.ld_act, dW->A_d, s.ld_ff);
-    gemm(c, s, g);
-  }
+  Wgrads wg;
+  add_wgrad(c, s, wg, wgrad(d, dff, T, dy, d, A.m, s.ld_act, dW->A_d, s.ld_ff));
   {
     // dm = dy W_d with the SwiGLU backward; rows scaled by rstd2 for the norm GEMMs
     GemmLaunch g = launch(EPI_DSWIGLU, s);
@@ -755,14 +703,8 @@ void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void
     p.rowv = A.rstd2;
     gemm(c, s, g);
   }
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    g.nprob = 2;
-    g.p[0] = wgrad(dff, d, T, B.dG, s.ld_act, x1, d, dW->A_gu, d, W->w_norm2);
-    g.p[1] = wgrad(dff, d, T, B.dU, s.ld_act, x1, d, at(dW->A_gu, dff * d, s), d, W->w_norm2);
-    gemm(c, s, g);
-  }
+  add_wgrad(c, s, wg, wgrad(dff, d, T, B.dG, s.ld_act, x1, d, dW->A_gu, d, W->w_norm2));
+  add_wgrad(c, s, wg, wgrad(dff, d, T, B.dU, s.ld_act, x1, d, at(dW->A_gu, dff * d, s), d, W->w_norm2));
   {
     GemmLaunch g = launch(EPI_STORE_CHAIN, s);
     g.nprob = 1;
@@ -780,26 +722,18 @@ void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void
   }
   void* dx1 = s.full() ? B.dx1 : dx;
   DT_CALL(s, normbwd, c, s, B, B.dn, x1, W->w_norm2, A.rstd2, dy, dx1, dW->w_norm2);
-  if (!s.full()) return;
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    g.nprob = 1;
-    g.p[0] = wgrad(d, d, T, dx1, d, A.V, d, dW->A_o, d);
-    gemm(c, s, g);
+  if (!s.full()) {
+    flush_wgrads(c, s, wg);
+    return;
   }
+  add_wgrad(c, s, wg, wgrad(d, d, T, dx1, d, A.V, d, dW->A_o, d));
   DT_CALL(s, rowscale, c, s, dq, d, A.rstd1, d, B.dqkv, 3 * d);
   DT_CALL(s, rowscale, c, s, dk, d, A.rstd1, d, at(B.dqkv, d, s), 3 * d);
   dx_gemm(c, s, dx1, d, W->A_o, d, d, at(B.dqkv, 2 * d, s), 3 * d, A.rstd1);
-  {
-    GemmLaunch g = launch(EPI_STORE, s);
-    g.allow_split = true;
-    g.nprob = 1;
-    g.p[0] = wgrad(3 * d, d, T, B.dqkv, 3 * d, x, d, dW->A_qkv, d, W->w_norm1);
-    gemm(c, s, g);
-  }
+  add_wgrad(c, s, wg, wgrad(3 * d, d, T, B.dqkv, 3 * d, x, d, dW->A_qkv, d, W->w_norm1));
   dx_gemm(c, s, B.dqkv, 3 * d, W->A_qkv, d, d, B.dn, d);
   DT_CALL(s, normbwd, c, s, B, B.dn, x, W->w_norm1, A.rstd1, dx1, dx, dW->w_norm1);
+  flush_wgrads(c, s, wg);
 }
 
 Ctx make_ctx(void* scratch, bn_stream_t stream, const Tmp& B) {

@@ -40,6 +40,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Most GEMM problems in one engine launch (the block's weight gradients go out
+// together: 11 of them).
+constexpr int kMaxProblems = 16;
+
 // Device status word bits (first word of the caller's scratch buffer).
 constexpr int kStatusTimeout = 1;
 

@@ -8,11 +8,14 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "common.cuh"
+
 namespace bn {
 
 enum Epi : int {
   // out0 = acc * rowv[i] * colv[j]  (rowv fp32, colv element type; each optional).
-  // The tensor-core engine may split K across CTAs for it when allow_split is set.
+  // With allow_split the tensor-core engine may cut the tiles left over after
+  // whole rounds of CTA groups into K ranges, summed by a reduction kernel.
   EPI_STORE = 0,
   // out0 = z = acc; out1 = h = sigma(z), sigma evaluated on z as stored.
   EPI_SIGMA = 1,
@@ -63,7 +66,7 @@ struct GemmLaunch {
   float eps = 1e-5f;
   bool allow_split = false;  // EPI_STORE only: K may be split (deterministic reduction)
   int nprob = 0;
-  GemmProblem p[3];
+  GemmProblem p[kMaxProblems];
 };
 
 struct Ctx {
@@ -81,7 +84,7 @@ struct Ctx {
 enum KernelKind : int {
   KK_GEMM_TC = 0,        // tcgen05 GEMM engine
   KK_GEMM_FFMA = 1,      // fp32 GEMM engine
-  KK_SPLITK_REDUCE = 2,  // split-K reduction
+  KK_SPLITK_REDUCE = 2,  // reduction of K-split tiles
   KK_STATS = 3,          // Online RMSNorm shard statistics
   KK_FOLD = 4,           // norm weight folded into a down-projection
   KK_NORM_BWD = 5,       // RMSNorm backward
@@ -124,7 +127,8 @@ inline void gemm_work(const GemmLaunch& g, int esize, double& flops, double& byt
 void gemm_tc(Ctx& c, const GemmLaunch& g);    // bf16 operands, tcgen05
 void gemm_simt(Ctx& c, const GemmLaunch& g);  // fp32 operands, FFMA
 
-// Largest split-K workspace gemm_tc may use for a GEMM of this size.
-size_t gemm_tc_partial_bytes(int64_t M, int64_t N, int num_sms);
+// fp32 partial tiles gemm_tc may use (Ctx::partial) for a K split on a GPU with
+// num_sms SMs; with less, it runs whole tiles only.
+size_t gemm_tc_partial_bytes(int num_sms);
 
 }  // namespace bn

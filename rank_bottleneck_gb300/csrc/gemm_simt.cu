@@ -35,7 +35,7 @@ struct Prob {
   const float* colv;
 };
 struct Params {
-  Prob p[3];
+  Prob p[kMaxProblems];
   int S, sigma;
   float eps;
 };

@@ -1,8 +1,9 @@
-// Host side of the tcgen05 GEMM engine: tensor-map encoding, tile-width and
-// split-K choice, launch, and the deterministic split-K reduction.
+// Host side of the tcgen05 GEMM engine: tensor-map encoding, tile width, the
+// K split of left-over tiles, launch, and the deterministic partial-tile reduction.
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -74,37 +75,12 @@ static int epi_kind(Epi e) {
 }
 
 static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-static int64_t ldp_of(int64_t N) { return cdiv(N, 8) * 8; }
-
-// Split count minimising rounds x (k-blocks per split) plus the reduction's
-// HBM traffic, all in units of one 128 x BN x 64 k-block on one SM.
-static int choose_splits(int64_t tiles, int64_t nkb, int64_t MN_total, int grid, int BN,
-                         size_t cap_bytes) {
-  const double t_kb_us = 2.0 * 128 * BN * 64 / (1.6e15 / grid) * 1e6;
-  double best = 1e300;
-  int best_s = 1;
-  for (int s = 1; s <= 16; ++s) {
-    const int64_t per = cdiv(nkb, s);
-    if (s > 1 && per < 4) break;
-    const int64_t eff = cdiv(nkb, per);
-    if (eff != s) continue;
-    if (s > 1 && static_cast<size_t>(s) * MN_total * 4 > cap_bytes) break;
-    const double rounds = static_cast<double>(cdiv(tiles * s, grid));
-    double t = rounds * per * t_kb_us;
-    if (s > 1) t += (8.0 * s + 2.0) * MN_total / 6.0e12 * 1e6;
-    if (t < best * 0.97) {
-      best = t;
-      best_s = s;
-    }
-  }
-  return best_s;
-}
 
 }  // namespace tc
 
-size_t gemm_tc_partial_bytes(int64_t M, int64_t N, int num_sms) {
-  (void)num_sms;
-  return static_cast<size_t>(16) * tc::cdiv(M, 2 * tc::BM) * 2 * tc::BM * tc::ldp_of(N) * 4;
+size_t gemm_tc_partial_bytes(int num_sms) {
+  // at most one split unit per CTA group, each a [CG x 128][256] fp32 tile
+  return static_cast<size_t>(num_sms) * tc::BM * 256 * 4;
 }
 
 namespace {
@@ -125,7 +101,7 @@ int cta_group_for(const GemmLaunch& g) {
 void gemm_tc(Ctx& c, const GemmLaunch& g) {
   using namespace tc;
   int ek = epi_kind(g.epi);
-  if (ek < 0 || g.nprob < 1 || g.nprob > 3) {
+  if (ek < 0 || g.nprob < 1 || g.nprob > kMaxProblems) {
     c.bad = 1;
     return;
   }
@@ -150,7 +126,8 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
   P.status = c.status;
 
   const bool a_mn = g.p[0].a[0].mn_major, b_mn = g.p[0].b[0].mn_major;
-  int64_t tiles_total = 0, mn_total = 0, nkb_max = 0;
+  int64_t tiles_total = 0, nkb_min = INT64_MAX;
+  bool plain = true;  // no row scale: the reduction kernel applies only colv
   for (int i = 0; i < g.nprob; ++i) {
     const GemmProblem& q = g.p[i];
     if (q.M <= 0 || q.N <= 0 || q.K <= 0 || q.a[0].mn_major != a_mn || q.b[0].mn_major != b_mn) {
@@ -158,24 +135,30 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
       return;
     }
     tiles_total += cdiv(q.M, BMP) * cdiv(q.N, BN);
-    mn_total += cdiv(q.M, BMP) * BMP * ldp_of(q.N);
-    nkb_max = std::max(nkb_max, cdiv(q.K, BK));
+    nkb_min = std::min(nkb_min, cdiv(q.K, BK));
+    plain = plain && q.rowv == nullptr;
   }
-  int splits = 1;
-  if (ek == K_STORE && g.allow_split) {
-    bool plain = true;
-    for (int i = 0; i < g.nprob; ++i) plain = plain && g.p[i].rowv == nullptr;
-    if (plain)
-      splits = choose_splits(tiles_total, nkb_max, mn_total, c.num_sms / CG, BN * CG,
-                             c.partial_bytes);
+  // K split (weight gradients, K = T): whole tiles fill complete rounds of the CTA
+  // groups; the tiles left over are each cut into rem_split k-ranges of at least
+  // 8 k-blocks that share one last round.
+  const int groups = c.num_sms / CG;
+  int64_t rem = 0;
+  int rem_split = 1;
+  if (ek == K_STORE && g.allow_split && plain) {
+    rem = tiles_total % groups;
+    if (rem > 0) {
+      rem_split = static_cast<int>(std::min<int64_t>(groups / rem, nkb_min / 8));
+      const size_t need = static_cast<size_t>(rem) * rem_split * BMP * BN * 4;
+      if (rem_split < 2 || c.partial == nullptr || need > c.partial_bytes) rem_split = 1;
+    }
   }
-  const bool split = splits > 1;
-  if (split) ek = K_PART;
+  if (rem_split == 1) rem = 0;
+  const bool split = rem > 0;
+  P.full_units = static_cast<int>(tiles_total - rem);
+  P.rem_split = rem_split;
+  P.part = split ? c.partial : nullptr;
 
   int units = 0;
-  size_t part_off = 0;
-  void* part_ptr[3] = {nullptr, nullptr, nullptr};
-  int64_t part_ld[3] = {0, 0, 0}, part_rows[3] = {0, 0, 0};
   for (int i = 0; i < g.nprob; ++i) {
     const GemmProblem& q = g.p[i];
     Prob& p = P.p[i];
@@ -231,26 +214,10 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     p.colv = q.colv;
     p.tiles_m = static_cast<int>(cdiv(q.M, BMP));
     p.tiles_n = static_cast<int>(cdiv(q.N, BN));
-    p.kb_per_split = static_cast<int>(cdiv(p.nkb[0], splits));
-    p.splits = static_cast<int>(cdiv(p.nkb[0], p.kb_per_split));
-    if (split) {
-      // fp32 partials: split s of this problem is rows [s M, (s + 1) M) of one tensor
-      // split s of this problem owns rows [s * Mp, (s + 1) * Mp), Mp = M rounded up to 128
-      const int64_t Mp = static_cast<int64_t>(p.tiles_m) * BMP;
-      part_ptr[i] = reinterpret_cast<char*>(c.partial) + part_off;
-      part_ld[i] = ldp_of(q.N);
-      part_rows[i] = Mp;
-      part_off += static_cast<size_t>(p.splits) * Mp * part_ld[i] * 4;
-      if (part_off > c.partial_bytes ||
-          !encode(&p.mo[0], part_ptr[i], q.N, Mp * p.splits, part_ld[i], 32, 32,
-                  CU_TENSOR_MAP_SWIZZLE_128B, 4)) {
-        c.bad = 4;
-        return;
-      }
-    }
-    p.unit_begin = units;
-    units += p.tiles_m * p.tiles_n * (split ? p.splits : 1);
+    p.tile_begin = units;
+    units += p.tiles_m * p.tiles_n;
   }
+  units = P.full_units + static_cast<int>(rem) * rem_split;
   P.total_units = units;
   double flops, bytes;
   gemm_work(g, 2, flops, bytes);
@@ -268,22 +235,26 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
   }
   note_launch(c, KK_GEMM_TC, static_cast<int>(g.epi), flops, bytes);
   if (split) {
-    SplitkReduce r;
+    TileReduce r;
     r.nprob = g.nprob;
+    r.full_units = P.full_units;
+    r.rem_split = rem_split;
+    r.rem_tiles = static_cast<int>(rem);
+    r.tile_rows = BMP;
+    r.BN = BN;
+    r.part = c.partial;
     for (int i = 0; i < g.nprob; ++i) {
       const Prob& p = P.p[i];
-      SplitkProb& q = r.p[i];
-      q.part = static_cast<const float*>(part_ptr[i]);
-      q.splits = p.splits;
+      TileReduceProb& q = r.p[i];
       q.M = p.M;
-      q.plane_rows = part_rows[i];
       q.N = p.N;
-      q.ldp = part_ld[i];
+      q.tiles_n = p.tiles_n;
+      q.tile_begin = p.tile_begin;
       q.colv = static_cast<const __nv_bfloat16*>(g.p[i].colv);
       q.out = static_cast<__nv_bfloat16*>(g.p[i].out[0]);
       q.ldo = g.p[i].ldo[0];
     }
-    launch_splitk_reduce(c, r);
+    launch_tile_reduce(c, r);
   }
 }
 

@@ -64,7 +64,6 @@ bool BN_CAT(launch_bn, GEMM_BN, BN_CAT(_cg, GEMM_CG, ))(int ek, bool a_mn, bool 
     case K_STORE * 4 + 0: go<K_STORE, false, false>(P, units, num_sms, s); return true;
     case K_STORE * 4 + 1: go<K_STORE, false, true>(P, units, num_sms, s); return true;
     case K_STORE * 4 + 3: go<K_STORE, true, true>(P, units, num_sms, s); return true;
-    case K_PART * 4 + 3: go<K_PART, true, true>(P, units, num_sms, s); return true;
     case K_SIGMA * 4 + 0: go<K_SIGMA, false, false>(P, units, num_sms, s); return true;
     case K_RESID * 4 + 0: go<K_RESID, false, false>(P, units, num_sms, s); return true;
     case K_DSIGMA * 4 + 1: go<K_DSIGMA, false, true>(P, units, num_sms, s); return true;

@@ -50,7 +50,7 @@ constexpr int EPI_N = 32;  // columns per epilogue subtile
 
 // epilogue kinds of the kernel template
 enum : int {
-  K_STORE = 0, K_PART = 1, K_SIGMA = 2, K_NORM = 3, K_RESID = 4, K_SWIGLU = 5,
+  K_STORE = 0, K_SIGMA = 2, K_NORM = 3, K_RESID = 4, K_SWIGLU = 5,
   K_DSIGMA = 6, K_DSWIGLU = 7, K_CHAIN = 8
 };
 
@@ -60,13 +60,13 @@ struct EpiShape {
   static constexpr int NOUT =
       (EK == K_SWIGLU) ? 3 : (EK == K_SIGMA || EK == K_NORM || EK == K_DSWIGLU) ? 2 : 1;
   static constexpr int NT = NIN > NOUT ? NIN : NOUT;         // subtiles per ring entry
-  static constexpr int ELEM = (EK == K_PART) ? 4 : 2;        // output element bytes
+  static constexpr int ELEM = 2;                             // output element bytes (bf16)
   static constexpr int SUB_BYTES = BM * EPI_N * ELEM;        // one 128 x 32 subtile
   static constexpr int WARP_BYTES = 32 * EPI_N * ELEM;       // one warp's 32 rows of it
   // ring entries: kinds that read epilogue inputs keep several subtiles of them in
   // flight; the others only need each warp's previous store to have left shared
   // memory, and leave the rest to operand stages
-  static constexpr int NE = (EK == K_PART) ? 2 : (NIN > 0) ? 8 : 4;
+  static constexpr int NE = (NIN > 0) ? 8 : 4;
   static constexpr int BYTES = NE * NT * SUB_BYTES;
 };
 
@@ -104,17 +104,24 @@ struct Prob {
   int64_t ldo[3];
   const float* rowv;
   const void* colv;
-  int tiles_m, tiles_n, unit_begin;
+  int tiles_m, tiles_n;
+  int tile_begin;     // tiles of the problems before this one
   int nkb[2];         // k-blocks of operand pair 0 / 1
-  int splits, kb_per_split;
   int out_mask;       // bit k: output k is written
 };
 
 struct Params {
-  Prob p[3];
+  Prob p[kMaxProblems];
   int nprob, total_units, S, sigma;
   float eps;
   int* status;
+  // Units [0, full_units) are whole tiles, in tile order over the problems,
+  // dealt round-robin to the CTA groups. Each remaining tile (STORE with K split)
+  // is cut into rem_split k-ranges, units full_units + rem_split t + s, whose
+  // fp32 partial tiles go to `part` and are summed by a reduction kernel: the
+  // whole tiles fill complete rounds and the split tiles one last round.
+  int full_units, rem_split;
+  float* part;  // per split unit j: [CG x 128][BN] fp32 at j * CG * 128 * BN
 };
 
 // ---------------------------------------------------------------------------
@@ -468,12 +475,6 @@ __device__ __forceinline__ void smem_row_load_bf16(const uint8_t* blk, int t, fl
     }
   }
 }
-__device__ __forceinline__ void smem_row_store_f32(uint8_t* blk, int t, const float* v) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    *reinterpret_cast<float4*>(blk + t * 128 + ((c ^ (t & 7)) << 4)) =
-        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-}
 // Columns [max(col0, N8), min(col0 + 32, N)) of one row, written directly: TMA
 // bounds the innermost dimension in 16-byte units, so the maps stop at N8 and
 // this covers the last (N mod 8) columns.
@@ -502,24 +503,35 @@ __device__ __forceinline__ void ld_vec_bf16(const __nv_bfloat16* p, int64_t col0
 // work decomposition
 // ---------------------------------------------------------------------------
 struct Work {
-  int pi, split;
+  int pi;
   int64_t m0, nb;
+  int kb0, kb1;   // k-blocks [kb0, kb1)
+  int part_slot;  // -1: a whole tile; else its fp32 partial goes to this slot
 };
 
-// Unit u -> problem, split, first row m0 of the (CG x 128)-row tile, n-block.
+// Unit u -> problem, first row m0 of the (CG x 128)-row tile, n-block, k-range.
 template <int CG>
 __device__ __forceinline__ Work decode(const Params& P, int u) {
-  int pi = 0;
-  while (pi + 1 < P.nprob && u >= P.p[pi + 1].unit_begin) ++pi;
-  const Prob& pr = P.p[pi];
-  const int local = u - pr.unit_begin;
-  const int tiles = pr.tiles_m * pr.tiles_n;
   Work w;
+  int t = u;
+  int sp = 0;
+  w.part_slot = -1;
+  if (u >= P.full_units) {
+    const int j = u - P.full_units;
+    t = P.full_units + j / P.rem_split;
+    sp = j % P.rem_split;
+    w.part_slot = j;
+  }
+  int pi = 0;
+  while (pi + 1 < P.nprob && t >= P.p[pi + 1].tile_begin) ++pi;
+  const Prob& pr = P.p[pi];
+  const int local = t - pr.tile_begin;
   w.pi = pi;
-  w.split = local / tiles;
-  const int t = local - w.split * tiles;
-  w.m0 = static_cast<int64_t>(t / pr.tiles_n) * BM * CG;
-  w.nb = t % pr.tiles_n;  // n-block index; the kernel scales it by BN
+  w.m0 = static_cast<int64_t>(local / pr.tiles_n) * BM * CG;
+  w.nb = local % pr.tiles_n;  // n-block index; the kernel scales it by BN
+  const int nkb = pr.nkb[0];
+  w.kb0 = (w.part_slot < 0) ? 0 : sp * nkb / P.rem_split;
+  w.kb1 = (w.part_slot < 0) ? nkb : (sp + 1) * nkb / P.rem_split;
   return w;
 }
 
@@ -529,7 +541,7 @@ __device__ __forceinline__ int num_segments(const Params& P) {
 }
 // k-block range and operand pair of segment s of a unit
 template <int EK>
-__device__ __forceinline__ void segment(const Params& P, const Prob& pr, int split, int s,
+__device__ __forceinline__ void segment(const Params& P, const Prob& pr, const Work& w, int s,
                                         int& kb0, int& nkb, int& pair) {
   if (EK == K_NORM) {
     const int per = pr.nkb[0] / P.S;
@@ -541,8 +553,8 @@ __device__ __forceinline__ void segment(const Params& P, const Prob& pr, int spl
     nkb = pr.nkb[s];
     pair = s;
   } else {
-    kb0 = split * pr.kb_per_split;
-    nkb = min(pr.kb_per_split, pr.nkb[0] - kb0);
+    kb0 = w.kb0;
+    nkb = w.kb1 - w.kb0;
     pair = 0;
   }
 }
@@ -626,7 +638,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         const int n0 = static_cast<int>(w.nb) * BN + static_cast<int>(rank) * (BN / CG);  // B rows
         for (int s = 0; ok && s < nseg; ++s) {
           int kb0, nkb, opair;
-          segment<EK>(P, pr, w.split, s, kb0, nkb, opair);
+          segment<EK>(P, pr, w, s, kb0, nkb, opair);
           const CUtensorMap* ma = &pr.ma[opair];
           const CUtensorMap* mb = &pr.mb[opair];
           for (int kb = kb0; kb < kb0 + nkb; ++kb) {
@@ -698,7 +710,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         const Prob& pr = P.p[w.pi];
         for (int s = 0; ok && s < nseg; ++s) {
           int kb0, nkb, opair;
-          segment<EK>(P, pr, w.split, s, kb0, nkb, opair);
+          segment<EK>(P, pr, w, s, kb0, nkb, opair);
           const bool fresh = !(EK == K_CHAIN && s == 1);
           if (EK == K_NORM) {
             slot = static_cast<int>(tile_no & 1) ^ (s == 0 ? 0 : 1);
@@ -1150,11 +1162,41 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl0 * BN + c * 32), v);
         if (k == MYCH - 1) release(sl0);
         uint8_t* ent = epi + e * E::NT * E::SUB_BYTES + q * E::WARP_BYTES;
-        // this row holds some of the ragged columns [N8, N) (fp32 partials need none)
-        const bool tail = EK != K_PART && row_ok && col0 + EPI_N > pr.N8 && col0 < N;
-        if constexpr (EK == K_PART) {
-          smem_row_store_f32(ent, lane, v);
-        } else if constexpr (EK == K_STORE || EK == K_CHAIN) {
+        if (EK == K_STORE && w.part_slot >= 0) {
+          // fp32 partial tile of a split unit, written in whole 128-byte rows: this
+          // warp's 32 x 32 block goes through its ring entry, 16 rows at a time,
+          // transposed so that lane = column. A split unit issues no TMA stores;
+          // the ones still reading the ring from earlier units are waited for once.
+          if (k == 0) {
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+          }
+          float* dst = P.part + (static_cast<int64_t>(w.part_slot) * CG * BM + row_off + q * 32) * BN +
+                       c * 32 + lane;
+          auto cell = [&](int rr, int col) -> float* {  // row rr, column col of the block
+            return reinterpret_cast<float*>(ent + rr * 128 + ((((col >> 2) ^ (rr & 7)) << 4) |
+                                                              ((col & 3) << 2)));
+          };
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            if ((lane >> 4) == h) {
+              const int rr = lane & 15;
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                *reinterpret_cast<float4*>(cell(rr, 4 * i)) =
+                    make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr)
+              dst[static_cast<int64_t>(h * 16 + rr) * BN] = *cell(rr, lane);
+            __syncwarp();
+          }
+          continue;  // summed, scaled and stored by the reduction kernel
+        }
+        // this row holds some of the ragged columns [N8, N)
+        const bool tail = row_ok && col0 + EPI_N > pr.N8 && col0 < N;
+        if constexpr (EK == K_STORE || EK == K_CHAIN) {
           if (pr.colv != nullptr) {
             float cv[32];
             ld_vec_bf16(static_cast<const __nv_bfloat16*>(pr.colv), col0, N, cv);
@@ -1217,14 +1259,11 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         if (lane == 0) {
           const uint32_t src = smem_u32(ent);
           const int rt = static_cast<int>(w.m0) + row_off + q * 32;  // row within the problem
-          // split-K partials: split s owns rows [s * Mp, (s + 1) * Mp), Mp = tiles_m * 128 CG
-          const int r0 = rt + (EK == K_PART ? w.split * pr.tiles_m * BM * CG : 0);
-          const int64_t lim = (EK == K_PART) ? N : pr.N8;  // extent of the output maps
-          if (rt < M && col0 < lim) {  // boxes partly outside the tensor are clipped by TMA
+          if (rt < M && col0 < pr.N8) {  // boxes partly outside the tensor are clipped by TMA
 #pragma unroll
             for (int o = 0; o < E::NOUT; ++o)
               if (pr.out_mask & (1 << o))
-                tma_store_2d(&pr.mo[o], src + o * E::SUB_BYTES, static_cast<int>(col0), r0);
+                tma_store_2d(&pr.mo[o], src + o * E::SUB_BYTES, static_cast<int>(col0), rt);
           }
           bulk_commit();
           // a warp reuses a ring entry every NE / EPI_GROUPS of its own subtiles: the

@@ -5,8 +5,8 @@
 // Who needs it: code that must not allocate GPU memory at all, e.g. a caller
 // whose memory is fully reserved up front by its own pool, or code that runs
 // where a cudaMalloc would synchronise the device or is forbidden. Those callers
-// still own and pass every input and output; only the temporary fp32 partial
-// sums of the K split (and the device status word) live here.
+// still own and pass every input and output; only the fp32 partial tiles of
+// the K split (and the device status word) live here.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -17,8 +17,9 @@
 namespace bn {
 namespace {
 
-// Fixed scratch: 256 bytes of status word, then the fp32 partial sums.
-// Every GPU that loads this library holds these bytes until the process exits.
+// Fixed scratch: 256 bytes of status word, then the fp32 partial tiles (at most
+// one 128 x 256 tile per SM, whatever the problem's size). Every GPU that loads
+// this library holds these bytes until the process exits.
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
 constexpr size_t kStatusBytes = 256;
 
@@ -59,15 +60,12 @@ extern "C" bn_status bn_weight_grad_noalloc(int64_t M, int64_t N, int64_t T, con
   const uintptr_t mis = reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
                         reinterpret_cast<uintptr_t>(dW) | reinterpret_cast<uintptr_t>(colscale);
   if ((mis & 15) || (lda % 8) || (ldb % 8) || (ldw % 8)) return BN_ERR_ALIGNMENT;
-  // at least a two-way split of K must fit: M x round_up(N, 8) fp32 partials each
-  const size_t plane = static_cast<size_t>(M) * static_cast<size_t>((N + 7) / 8 * 8) * 4;
-  if (2 * plane > kNoAllocScratchBytes - kStatusBytes) return BN_ERR_UNSUPPORTED;
 
   void* scratch = nullptr;
   bn_status st = scratch_address(&scratch);
   if (st != BN_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the status word must start at zero; the partial sums are fully overwritten
+  // the status word must start at zero; the partial tiles are fully overwritten
   if (cudaMemsetAsync(scratch, 0, kStatusBytes, s) != cudaSuccess) return BN_ERR_CUDA;
 
   GemmLaunch g;
@@ -97,6 +95,7 @@ extern "C" bn_status bn_weight_grad_noalloc(int64_t M, int64_t N, int64_t T, con
     c.num_sms = nsm;
   c.partial = reinterpret_cast<float*>(static_cast<char*>(scratch) + kStatusBytes);
   c.partial_bytes = kNoAllocScratchBytes - kStatusBytes;
+  if (c.partial_bytes < gemm_tc_partial_bytes(c.num_sms)) return BN_ERR_UNSUPPORTED;
   gemm_tc(c, g);
   if (c.bad) return BN_ERR_UNSUPPORTED;
   if (c.err != cudaSuccess) return BN_ERR_CUDA;

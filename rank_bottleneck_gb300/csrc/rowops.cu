@@ -253,64 +253,68 @@ void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* r
 }
 
 // ---------------------------------------------------------------------------
-// split-K reduction (fixed order over splits), all problems of a launch at once
+// reduction of the GEMM's split tiles (fixed order over the k-ranges)
 // ---------------------------------------------------------------------------
-__global__ void splitk_reduce_kernel(const SplitkReduce R) {
+// grid: (split tile, slab of 256 / (BN / 8) rows: one row per BN / 8 threads); 256
+// threads, 8 columns each
+__global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduce r) {
   grid_dependency_sync();
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < R.total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    int pi = 0;
-    while (pi + 1 < R.nprob && i >= R.p[pi + 1].begin) ++pi;
-    const SplitkProb& q = R.p[pi];
-    const int64_t nvec = (q.N + 7) / 8;
-    const int64_t li = i - q.begin;
-    const int64_t r = li / nvec, c0 = (li - r * nvec) * 8;
-    const int64_t plane = q.plane_rows * q.ldp;
-    const float* src = q.part + r * q.ldp + c0;
-    float a[8];
-    Vec8<float>::load(src, a);
-    // four splits' loads in flight at a time; the adds keep split order
-    for (int s = 1; s < q.splits; s += 4) {
+  const int rt = blockIdx.x;
+  const int t = r.full_units + rt;
+  int pi = 0;
+  while (pi + 1 < r.nprob && t >= r.p[pi + 1].tile_begin) ++pi;
+  const TileReduceProb& q = r.p[pi];
+  const int tl = t - q.tile_begin;
+  const int64_t m0 = static_cast<int64_t>(tl / q.tiles_n) * r.tile_rows;
+  const int64_t n0 = static_cast<int64_t>(tl % q.tiles_n) * r.BN;
+  const int per_row = r.BN / 8;
+  const int c8 = (threadIdx.x % per_row) * 8;
+  const int64_t col = n0 + c8;
+  if (col >= q.N) return;
+  float cv[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    cv[k] = (q.colv != nullptr && col + k < q.N) ? __bfloat162float(q.colv[col + k]) : 1.f;
+  const int64_t slot_elems = static_cast<int64_t>(r.tile_rows) * r.BN;
+  const float* base = r.part + static_cast<int64_t>(rt) * r.rem_split * slot_elems + c8;
+  {
+    const int rr = blockIdx.y * (256 / per_row) + threadIdx.x / per_row;
+    const int64_t row = m0 + rr;
+    if (row >= q.M) return;
+    const float* src = base + static_cast<int64_t>(rr) * r.BN;
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // four k-ranges' loads in flight at a time; the adds keep k order
+    for (int s = 0; s < r.rem_split; s += 4) {
       float b[4][8];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (s + u < q.splits) Vec8<float>::load(src + (s + u) * plane, b[u]);
+        if (s + u < r.rem_split) Vec8<float>::load(src + (s + u) * slot_elems, b[u]);
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (s + u < q.splits) {
+        if (s + u < r.rem_split) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) a[k] += b[u][k];
         }
     }
-    if (q.colv != nullptr) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (c0 + k < q.N) a[k] *= __bfloat162float(q.colv[c0 + k]);
-    }
-    bf16* o = q.out + r * q.ldo + c0;
-    if (c0 + 8 <= q.N) {
+    for (int k = 0; k < 8; ++k) a[k] *= cv[k];
+    bf16* o = q.out + row * q.ldo + col;
+    if (col + 8 <= q.N) {
       Vec8<bf16>::store(o, a);
     } else {
-      for (int k = 0; c0 + k < q.N; ++k) o[k] = __float2bfloat16_rn(a[k]);
+      for (int k = 0; col + k < q.N; ++k) o[k] = __float2bfloat16_rn(a[k]);
     }
   }
 }
 
-void launch_splitk_reduce(Ctx& c, SplitkReduce& R) {
-  double flops = 0, bytes = 0;
-  R.total = 0;
-  for (int i = 0; i < R.nprob; ++i) {
-    SplitkProb& q = R.p[i];
-    q.begin = R.total;
-    R.total += q.M * ((q.N + 7) / 8);
-    flops += 1.0 * q.splits * q.M * q.N;
-    bytes += (4.0 * q.splits + 2.0) * q.M * q.N;
-  }
-  const unsigned grid =
-      static_cast<unsigned>(std::min<int64_t>((R.total + 255) / 256, c.num_sms * 8));
+void launch_tile_reduce(Ctx& c, const TileReduce& r) {
+  const dim3 grid(static_cast<unsigned>(r.rem_tiles),
+                  static_cast<unsigned>(r.tile_rows / (256 / (r.BN / 8))));
+  const double elems = static_cast<double>(r.rem_tiles) * r.tile_rows * r.BN;
   prof_start(c);
-  track(c, launch_pdl(splitk_reduce_kernel, grid, 256, 0, c.stream, R));
-  note_launch(c, KK_SPLITK_REDUCE, -1, flops, bytes);
+  track(c, launch_pdl(tile_reduce_kernel, grid, 256, 0, c.stream, r));
+  note_launch(c, KK_SPLITK_REDUCE, -1, elems * r.rem_split,
+              elems * (4.0 * r.rem_split + 2.0));
 }
 
 // ---------------------------------------------------------------------------

@@ -26,24 +26,25 @@ void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* r
                      const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw);
 int norm_bwd_blocks(int num_sms);
 
-// Split-K reduction of up to three problems in one launch: per problem
-// out[i, j] = colv[j] * sum_s part[s * plane_rows + i][j] (fixed order over s),
-// bf16 output; colv may be null.
-struct SplitkProb {
-  const float* part;
-  int splits;
-  int64_t M, plane_rows, N, ldp;
+// Reduction of the GEMM's split tiles. Tiles [0, full_units) of the launch were
+// whole; tile full_units + t (t < rem_tiles) was cut into rem_split k-ranges
+// whose fp32 partial tiles sit in slots rem_split t + s, each [tile_rows][BN].
+// For those tiles out[i, j] = colv[j] * sum_s partial_s[i, j] (fixed order over
+// s, bf16 output, colv optional), clipped to the problem's M x N.
+struct TileReduceProb {
+  int64_t M, N;
+  int tiles_n, tile_begin;
   const __nv_bfloat16* colv;
   __nv_bfloat16* out;
   int64_t ldo;
-  int64_t begin;  // set by the launcher: first work item of this problem
 };
-struct SplitkReduce {
-  SplitkProb p[3];
+struct TileReduce {
+  TileReduceProb p[kMaxProblems];
   int nprob = 0;
-  int64_t total = 0;  // set by the launcher
+  int full_units = 0, rem_split = 0, rem_tiles = 0, tile_rows = 0, BN = 0;
+  const float* part = nullptr;
 };
-void launch_splitk_reduce(Ctx& c, SplitkReduce& r);
+void launch_tile_reduce(Ctx& c, const TileReduce& r);
 
 // h = sigma(z) elementwise, rounded exactly like the GEMM epilogues round it.
 template <typename T>

@@ -11,7 +11,7 @@ extern "C" bn_status bn_testing_gemm(int32_t dtype, int32_t epi, int32_t sigma, 
                                      float eps, int32_t allow_split, int32_t nprob,
                                      const bn_gemm_problem* probs, void* scratch,
                                      size_t scratch_bytes, bn_stream_t stream) {
-  if (probs == nullptr || nprob < 1 || nprob > 3 || epi < 0 || epi > 7 || S < 1 || S > 16 ||
+  if (probs == nullptr || nprob < 1 || nprob > kMaxProblems || epi < 0 || epi > 7 || S < 1 || S > 16 ||
       (dtype != BN_F32 && dtype != BN_BF16) || scratch == nullptr || scratch_bytes < 256)
     return BN_ERR_INVALID_ARG;
   GemmLaunch g;

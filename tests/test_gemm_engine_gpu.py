@@ -1,6 +1,6 @@
 """Unit tests of the GEMM engine behind the block (tensor-core bf16 and FFMA fp32):
 every fused epilogue, every operand layout the block uses, ragged and tiny
-shapes, split-K, grouped launches. Reference: the same op in numpy float64 on
+shapes, K split of left-over tiles, grouped launches. Reference: the same op in numpy float64 on
 the exact (bf16-rounded) inputs. Padding around every operand and output holds
 NaN, so any read or write outside the logical bounds fails the test."""
 import zlib
@@ -133,15 +133,50 @@ def test_store_split_k_with_row_and_column_scales(lib, dtype):
     assert err(host(q2["out0"], 136), ref2) <= TOL[dtype]
 
 
+# K split of the tiles left over after whole rounds of CTA groups (76 pairs on a
+# 152-SM GB300): fewer tiles than groups (all split), more tiles with a
+# remainder, an exact multiple (no split), and a launch of many problems like
+# the block's gathered weight gradients (ragged shapes, with and without a
+# column scale).
+SPLIT_CASES = {
+    "fewer-tiles": [(1536, 2048, 16384)],
+    "remainder": [(2816, 2048, 8192)],
+    "exact-rounds": [(4864, 1024, 4096)],
+    "eleven-problems": [(512, 5464, 4096), (520, 264, 4096), (2048, 512, 4096), (512, 2048, 4096),
+                        (5461, 512, 4096), (5461, 512, 4096), (1024, 2048, 4096), (2048, 512, 4096),
+                        (2048, 512, 4096), (2048, 512, 4096), (512, 2048, 4096)],
+}
+
+
+@pytest.mark.parametrize("case", list(SPLIT_CASES))
+def test_store_split_remainder(lib, case):
+    from _gemmhook import run
+    rng = np.random.default_rng(zlib.crc32(case.encode()))
+    qs, refs = [], []
+    for i, (M, N, K) in enumerate(SPLIT_CASES[case]):
+        q, r = problem(rng, M, N, K, True, True, "bf16")
+        ref = r["A"] @ r["B"].T
+        if i % 2:
+            colv = rnd(rng, (N,), "bf16") + 1
+            q["colv"] = torch.from_numpy(colv).to("cuda", torch.bfloat16)
+            ref = ref * colv.astype(np.float64)[None]
+        q["out0"], q["ldo"] = out_buf(M, N, "bf16")
+        qs.append(q)
+        refs.append(ref)
+    run(lib, "store", qs, dtype="bf16", allow_split=True)
+    for q, ref, (M, N, K) in zip(qs, refs, SPLIT_CASES[case]):
+        assert err(host(q["out0"], N), ref) <= TOL["bf16"]
+
+
 def test_split_k_is_deterministic(lib):
     from _gemmhook import run
     rng = np.random.default_rng(8)
-    q, _ = problem(rng, 512, 512, 16384, True, True, "bf16")
+    q, _ = problem(rng, 2816, 2048, 8192, True, True, "bf16")  # whole rounds + split tiles
     outs = []
     for _ in range(2):
-        q["out0"], q["ldo"] = out_buf(512, 512, "bf16")
+        q["out0"], q["ldo"] = out_buf(2816, 2048, "bf16")
         run(lib, "store", [q], dtype="bf16", allow_split=True)
-        outs.append(q["out0"][:, :512].clone())
+        outs.append(q["out0"][:, :2048].clone())
     assert torch.equal(outs[0], outs[1])
 
 
