@@ -14,6 +14,34 @@ using bf16 = __nv_bfloat16;
 // ---------------------------------------------------------------------------
 // F0: per-row, per-shard sums of squares (one warp per row)
 // ---------------------------------------------------------------------------
+// 8 elements of T kept packed in registers (16 bytes of bf16, 32 of fp32),
+// unpacked element by element where they are used.
+template <typename T> struct Pack8;
+template <> struct Pack8<__nv_bfloat16> {
+  uint4 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) {
+    v = *reinterpret_cast<const uint4*>(p);
+  }
+  __device__ __forceinline__ void zero() { v = make_uint4(0, 0, 0, 0); }
+  __device__ __forceinline__ float operator[](int i) const {
+    const uint32_t w = (i < 2) ? v.x : (i < 4) ? v.y : (i < 6) ? v.z : v.w;
+    return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+};
+template <> struct Pack8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = *reinterpret_cast<const float4*>(p);
+    b = *reinterpret_cast<const float4*>(p + 4);
+  }
+  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ float operator[](int i) const {
+    const float4& q = (i < 4) ? a : b;
+    const int j = i & 3;
+    return j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
+  }
+};
+
 template <typename T>
 __global__ void __launch_bounds__(256) stats_kernel(const T* __restrict__ x, int64_t rows, int d,
                                                     int S, float eps, float* __restrict__ ss,
@@ -90,36 +118,13 @@ constexpr int kNormBwdMaxWarps = 8;
 constexpr int kNormBwdUnroll = 4;
 constexpr size_t kNormBwdSmemLimit = 200 * 1024;
 
-// 8 elements of T kept packed in registers (16 bytes of bf16, 32 of fp32),
-// unpacked element by element where they are used.
-template <typename T> struct Pack8;
-template <> struct Pack8<__nv_bfloat16> {
-  uint4 v;
-  __device__ __forceinline__ void load(const __nv_bfloat16* p) {
-    v = *reinterpret_cast<const uint4*>(p);
-  }
-  __device__ __forceinline__ void zero() { v = make_uint4(0, 0, 0, 0); }
-  __device__ __forceinline__ float operator[](int i) const {
-    const uint32_t w = (i < 2) ? v.x : (i < 4) ? v.y : (i < 6) ? v.z : v.w;
-    return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
-  }
-};
-template <> struct Pack8<float> {
-  float4 a, b;
-  __device__ __forceinline__ void load(const float* p) {
-    a = *reinterpret_cast<const float4*>(p);
-    b = *reinterpret_cast<const float4*>(p + 4);
-  }
-  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
-  __device__ __forceinline__ float operator[](int i) const {
-    const float4& q = (i < 4) ? a : b;
-    const int j = i & 3;
-    return j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
-  }
-};
 
-template <typename T>
-__global__ void __launch_bounds__(kNormBwdMaxWarps * 32, 2)
+// NP > 0: rows of exactly NP * 256 bf16 elements, held in registers for the
+// whole row (dn, x and dres all loaded up front: one memory round trip per row;
+// one block per SM for the registers). NP = 0: any d, two passes over the row
+// (the second one mostly from L1/L2), two blocks per SM.
+template <typename T, int NP>
+__global__ void __launch_bounds__(kNormBwdMaxWarps * 32, NP > 0 ? 1 : 2)
     norm_bwd_kernel(const T* __restrict__ dn, const T* __restrict__ x, const T* __restrict__ w,
                     const float* __restrict__ rstd, const T* __restrict__ dres, int64_t rows,
                     int d, T* __restrict__ dx, float* __restrict__ part) {
@@ -139,6 +144,43 @@ __global__ void __launch_bounds__(kNormBwdMaxWarps * 32, 2)
        row += static_cast<int64_t>(gridDim.x) * nw) {
     const T* dnr = dn + row * d;
     const T* xr = x + row * d;
+    if constexpr (NP > 0) {
+      const T* dr = dres + row * d;
+      Pack8<T> a[NP], b[NP], g[NP];
+#pragma unroll
+      for (int u = 0; u < NP; ++u) {
+        const int c = lane * 8 + u * 256;
+        a[u].load(dnr + c);
+        b[u].load(xr + c);
+        g[u].load(dr + c);
+      }
+      float s = 0.f;
+#pragma unroll
+      for (int u = 0; u < NP; ++u) {
+        Pack8<T> ww;
+        ww.load(w + lane * 8 + u * 256);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s = fmaf(a[u][i] * ww[i], b[u][i], s);
+      }
+      s = warp_sum(s);
+      const float r = rstd[row];
+      const float coef = r * r * s * inv_d;
+      T* o = dx + row * d;
+#pragma unroll
+      for (int u = 0; u < NP; ++u) {
+        const int c = lane * 8 + u * 256;
+        Pack8<T> ww;
+        ww.load(w + c);
+        float out[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          out[i] = g[u][i] + (a[u][i] * ww[i] - b[u][i] * coef);
+          my[c + c / 8 + i] = fmaf(a[u][i], b[u][i], my[c + c / 8 + i]);
+        }
+        Vec8<T>::store(o + c, out);
+      }
+      continue;
+    }
     float s = 0.f;
     for (int base = lane * 8; base < d; base += 256 * U) {
       Pack8<T> a[U], b[U], ww[U];
@@ -235,14 +277,21 @@ void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* r
   const int nw = static_cast<int>(std::max<size_t>(
       1, std::min<size_t>(kNormBwdMaxWarps, kNormBwdSmemLimit / row_bytes)));
   const size_t smem = row_bytes * nw;
+  // bf16 rows of 1024 or 2048 elements stay in registers
+  constexpr bool kResident = sizeof(T) == 2;  // register-resident rows for bf16 only
+  constexpr int kNP4 = kResident ? 4 : 0, kNP8 = kResident ? 8 : 0;
+  auto kern = norm_bwd_kernel<T, 0>;
+  if (kResident && d == 2048) kern = norm_bwd_kernel<T, kNP8>;
+  if (kResident && d == 1024) kern = norm_bwd_kernel<T, kNP4>;
   static const bool attr = [] {
-    cudaFuncSetAttribute(norm_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(kNormBwdSmemLimit));
+    for (auto k : {norm_bwd_kernel<T, 0>, norm_bwd_kernel<T, kNP4>, norm_bwd_kernel<T, kNP8>})
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kNormBwdSmemLimit));
     return true;
   }();
   (void)attr;
   prof_start(c);
-  track(c, launch_pdl(norm_bwd_kernel<T>, nblk, nw * 32, smem, c.stream, dn, x, w, rstd, dres, rows,
+  track(c, launch_pdl(kern, nblk, nw * 32, smem, c.stream, dn, x, w, rstd, dres, rows,
                       static_cast<int>(d), dx, part));
   note_launch(c, KK_NORM_BWD, -1, 8.0 * rows * d,
               4.0 * rows * d * sizeof(T) + d * sizeof(T) + 4.0 * rows + 4.0 * nblk * d);
