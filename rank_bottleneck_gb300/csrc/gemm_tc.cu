@@ -181,7 +181,7 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     p.K = q.K;
     // epilogue outputs: 32 x 32 boxes (bf16, 64-byte swizzle; fp32 partials, 128-byte)
     const int nout = (ek == K_SWIGLU) ? 3 : (ek == K_SIGMA || ek == K_NORM || ek == K_DSWIGLU) ? 2 : 1;
-    const int nin = (ek == K_RESID || ek == K_DSIGMA) ? 1 : (ek == K_DSWIGLU) ? 2 : 0;
+    const int nin = (ek == K_RESID) ? 1 : (ek == K_DSWIGLU) ? 2 : 0;  // through the TMA ring
     p.out_mask = 0;
     p.N8 = q.N / 8 * 8;
     for (int j = 0; j < 3; ++j) {
@@ -212,6 +212,8 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     }
     p.rowv = q.rowv;
     p.colv = q.colv;
+    p.in_raw = (ek == K_DSIGMA) ? q.in[0] : nullptr;
+    p.ldi_raw = q.ldi[0];
     p.tiles_m = static_cast<int>(cdiv(q.M, BMP));
     p.tiles_n = static_cast<int>(cdiv(q.N, BN));
     p.tile_begin = units;

@@ -56,7 +56,10 @@ enum : int {
 
 template <int EK>
 struct EpiShape {
-  static constexpr int NIN = (EK == K_RESID || EK == K_DSIGMA) ? 1 : (EK == K_DSWIGLU) ? 2 : 0;
+  // epilogue inputs staged through the ring by the input warp (the sigma-backward's
+  // z is instead read straight into registers: its GEMMs are long in K, so the
+  // read hides behind the next tile's MMAs, and the ring's space goes to stages)
+  static constexpr int NIN = (EK == K_RESID) ? 1 : (EK == K_DSWIGLU) ? 2 : 0;
   static constexpr int NOUT =
       (EK == K_SWIGLU) ? 3 : (EK == K_SIGMA || EK == K_NORM || EK == K_DSWIGLU) ? 2 : 1;
   static constexpr int NT = NIN > NOUT ? NIN : NOUT;         // subtiles per ring entry
@@ -108,6 +111,8 @@ struct Prob {
   int tile_begin;     // tiles of the problems before this one
   int nkb[2];         // k-blocks of operand pair 0 / 1
   int out_mask;       // bit k: output k is written
+  const void* in_raw; // sigma-backward: z, read directly (row stride ldi_raw)
+  int64_t ldi_raw;
 };
 
 struct Params {
@@ -485,6 +490,20 @@ __device__ __forceinline__ void store_tail_bf16(void* base, int64_t ld, int64_t 
   for (int i = 0; i < 32; ++i) {
     const int64_t col = col0 + i;
     if (col >= N8 && col < N) p[col] = __float2bfloat16_rn(v[i]);
+  }
+}
+// Row `row`, columns [col0, col0 + 32) of a bf16 matrix with row stride ld and N
+// columns, zero beyond N or when the row is outside the matrix.
+__device__ __forceinline__ void ld_row32_bf16(const __nv_bfloat16* p, int64_t ld, int64_t row,
+                                              bool row_ok, int64_t col0, int64_t N, float* v) {
+  const __nv_bfloat16* r = p + (row_ok ? row : 0) * ld;
+  if (row_ok && col0 + 32 <= N) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) Vec8<__nv_bfloat16>::load(r + col0 + 8 * i, v + 8 * i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      v[i] = (row_ok && col0 + i < N) ? __bfloat162float(r[col0 + i]) : 0.f;
   }
 }
 // 32 bf16 values starting at column col0 of a vector of length N (zero beyond N)
@@ -1158,6 +1177,10 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
             break;
           }
         }
+        float zin[EK == K_DSIGMA ? 32 : 1];
+        if constexpr (EK == K_DSIGMA)  // issued first: in flight during the TMEM load
+          ld_row32_bf16(static_cast<const __nv_bfloat16*>(pr.in_raw), pr.ldi_raw, row, row_ok,
+                        col0, N, zin);
         float v[32];
         tmem_ld32(tmem + lane_base + static_cast<uint32_t>(sl0 * BN + c * 32), v);
         if (k == MYCH - 1) release(sl0);
@@ -1230,10 +1253,8 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
           smem_row_store_bf16(ent, lane, v);
           if (tail) store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, v);
         } else if constexpr (EK == K_DSIGMA) {
-          float z[32];
-          smem_row_load_bf16(ent, lane, z);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = (v[i] * act_grad_fast(z[i], P.sigma)) * rs;
+          for (int i = 0; i < 32; ++i) v[i] = (v[i] * act_grad_fast(zin[i], P.sigma)) * rs;
           smem_row_store_bf16(ent, lane, v);
           if (tail) store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, v);
         } else if constexpr (EK == K_DSWIGLU) {
