@@ -44,7 +44,7 @@ struct Tmp {
   void *A1f = nullptr, *A2f = nullptr;  // down-projections with the norm weight folded in
   void *dz_d = nullptr, *dG = nullptr, *dU = nullptr, *dz_gu = nullptr, *dn = nullptr;
   void *dx1 = nullptr, *dz_o = nullptr, *dV = nullptr, *dz_qkv = nullptr, *dqkv = nullptr;
-  float* dw_part = nullptr;
+  float *dw_part1 = nullptr, *dw_part2 = nullptr;  // RMSNorm dw partial column sums
   float* partial = nullptr;
   size_t partial_bytes = 0;
   int nblk = 0;
@@ -130,7 +130,8 @@ void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
     }
   }
   B.nblk = norm_bwd_blocks(device_sms());
-  B.dw_part = static_cast<float*>(sc.take(static_cast<size_t>(B.nblk) * s.d * 4));
+  B.dw_part2 = static_cast<float*>(sc.take(static_cast<size_t>(B.nblk) * s.d * 4));
+  if (s.full()) B.dw_part1 = static_cast<float*>(sc.take(static_cast<size_t>(B.nblk) * s.d * 4));
   if (s.dtype == BN_BF16) {
     B.partial_bytes = gemm_tc_partial_bytes(device_sms());
     B.partial = static_cast<float*>(sc.take(B.partial_bytes));
@@ -252,11 +253,15 @@ GemmProblem wgrad(int64_t M, int64_t N, int64_t T, const void* a, int64_t lda, c
 // end: they read only tensors the backward has already written (nothing later
 // overwrites them), and one launch over all their tiles fills whole rounds of
 // the CTA groups, with only the last few tiles split along K.
+// The RMSNorm dw column sums of a bf16 backward go out in the same final
+// launch as the reduction of the weight-gradient GEMM's split tiles.
 struct Wgrads {
   GemmProblem p[kMaxProblems];
   int n = 0;
+  ColsumJob col[2];
+  int ncol = 0;
 };
-void flush_wgrads(Ctx& c, const Shape& s, Wgrads& w);
+void flush_wgrads(Ctx& c, const Shape& s, Wgrads& w, bool final = false);
 void add_wgrad(Ctx& c, const Shape& s, Wgrads& w, const GemmProblem& q) {
   if (w.n == kMaxProblems) flush_wgrads(c, s, w);
   w.p[w.n++] = q;
@@ -274,17 +279,46 @@ template <typename T>
 void stats(Ctx& c, const void* x, const Shape& s, float* ss, float* rstd) {
   launch_stats<T>(c, static_cast<const T*>(x), s.T, s.d, s.S, s.eps, ss, rstd);
 }
+// a norm weight folded into a down-projection: out = A diag(w), A [rows, cols]
+struct Fold {
+  const void* A = nullptr;
+  const void* w = nullptr;
+  int64_t rows = 0, cols = 0;
+  void* out = nullptr;
+};
+// stats(x) and up to two weight folds in one launch
 template <typename T>
-void fold(Ctx& c, const void* A, const void* w, int64_t rows, int64_t cols, void* out) {
-  launch_fold_cols<T>(c, static_cast<const T*>(A), static_cast<const T*>(w), rows, cols,
-                      static_cast<T*>(out));
+void stats_fold(Ctx& c, const void* x, const Shape& s, float* ss, float* rstd, const Fold& a,
+                const Fold& b) {
+  auto job = [](const Fold& f) {
+    FoldJob<T> j;
+    j.A = static_cast<const T*>(f.A);
+    j.w = static_cast<const T*>(f.w);
+    j.rows = f.rows;
+    j.cols = f.cols;
+    j.out = static_cast<T*>(f.out);
+    return j;
+  };
+  launch_stats_fold<T>(c, static_cast<const T*>(x), s.T, s.d, s.S, s.eps, ss, rstd, job(a), job(b));
 }
+// RMSNorm backward; `part` holds its dw partial sums until they are summed
+// (bf16: in the backward's final launch, see Wgrads)
 template <typename T>
-void normbwd(Ctx& c, const Shape& s, const Tmp& B, const void* dn, const void* x, const void* w,
-             const float* rstd, const void* dres, void* dx, void* dw) {
-  launch_norm_bwd<T>(c, static_cast<const T*>(dn), static_cast<const T*>(x),
-                     static_cast<const T*>(w), rstd, static_cast<const T*>(dres), s.T, s.d,
-                     static_cast<T*>(dx), B.dw_part, B.nblk, static_cast<T*>(dw));
+void normbwd(Ctx& c, const Shape& s, const Tmp& B, Wgrads& wg, float* part, const void* dn,
+             const void* x, const void* w, const float* rstd, const void* dres, void* dx,
+             void* dw) {
+  const bool defer = s.dtype == BN_BF16;
+  const int rows_written = launch_norm_bwd<T>(
+      c, static_cast<const T*>(dn), static_cast<const T*>(x), static_cast<const T*>(w), rstd,
+      static_cast<const T*>(dres), s.T, s.d, static_cast<T*>(dx), part, B.nblk,
+      static_cast<T*>(dw), !defer);
+  if (defer) {
+    ColsumJob& j = wg.col[wg.ncol++];
+    j.part = part;
+    j.nblk = rows_written;
+    j.d = static_cast<int>(s.d);
+    j.out = static_cast<bf16*>(dw);
+  }
 }
 template <typename T>
 void sigma_ew(Ctx& c, const Shape& s, const void* z, int64_t cols, int64_t ld, void* h) {
@@ -436,17 +470,19 @@ void plain_down(Ctx& c, const Shape& s, const void* X, int64_t K, int64_t ldx, c
 void forward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, void* y,
                      void* q, void* k, const Acts& A, const Tmp& B) {
   const void* x1 = x;
+  const Fold f2{W->A_gu, W->w_norm2, 2 * s.r, s.d, B.A2f};
   if (s.full()) {
-    DT_CALL(s, stats, c, x, s, A.ss1, A.rstd1);
-    DT_CALL(s, fold, c, W->A_qkv, W->w_norm1, 3 * s.r, s.d, B.A1f);
+    const Fold f1{W->A_qkv, W->w_norm1, 3 * s.r, s.d, B.A1f};
+    DT_CALL(s, stats_fold, c, x, s, A.ss1, A.rstd1, f1, f2);
     norm_down(c, s, x, A.ss1, B.A1f, 3 * s.r, A.z_qkv, A.h_qkv);
     qkv_up(c, s, W, A, q, k);
     plain_down(c, s, A.V, s.d, s.d, W->A_o, s.d, A.z_o, A.h_o);
     o_up(c, s, W, x, A);
     x1 = A.x1;
+    DT_CALL(s, stats, c, x1, s, A.ss2, A.rstd2);
+  } else {
+    DT_CALL(s, stats_fold, c, x1, s, A.ss2, A.rstd2, f2, Fold{});
   }
-  DT_CALL(s, stats, c, x1, s, A.ss2, A.rstd2);
-  DT_CALL(s, fold, c, W->A_gu, W->w_norm2, 2 * s.r, s.d, B.A2f);
   norm_down(c, s, x1, A.ss2, B.A2f, 2 * s.r, A.z_gu, A.h_gu);
   gu_up(c, s, W, A, !s.ckpt);
   plain_down(c, s, A.m, s.d_ff, s.ld_act, W->A_d, s.ld_ff, A.z_d, A.h_d);
@@ -456,9 +492,10 @@ void forward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const voi
 void forward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, void* y,
                    void* q, void* k, const Acts& A, const Tmp& B) {
   const void* x1 = x;
+  const Fold f2{W->A_gu, W->w_norm2, 2 * s.d_ff, s.d, B.A2f};
   if (s.full()) {
-    DT_CALL(s, stats, c, x, s, A.ss1, A.rstd1);
-    DT_CALL(s, fold, c, W->A_qkv, W->w_norm1, 3 * s.d, s.d, B.A1f);
+    const Fold f1{W->A_qkv, W->w_norm1, 3 * s.d, s.d, B.A1f};
+    DT_CALL(s, stats_fold, c, x, s, A.ss1, A.rstd1, f1, f2);
     GemmLaunch g = launch(EPI_NORM, s);
     void* outs[3] = {q, k, A.V};
     for (int i = 0; i < 3; ++i) {
@@ -487,9 +524,10 @@ void forward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void*
     p.ldo[0] = s.d;
     gemm(c, s, o);
     x1 = A.x1;
+    DT_CALL(s, stats, c, x1, s, A.ss2, A.rstd2);
+  } else {
+    DT_CALL(s, stats_fold, c, x1, s, A.ss2, A.rstd2, f2, Fold{});
   }
-  DT_CALL(s, stats, c, x1, s, A.ss2, A.rstd2);
-  DT_CALL(s, fold, c, W->A_gu, W->w_norm2, 2 * s.d_ff, s.d, B.A2f);
   GemmLaunch g = launch(EPI_NORM, s);
   void* outs[2] = {A.G, A.U};
   for (int i = 0; i < 2; ++i) {
@@ -575,14 +613,22 @@ void dx_gemm(Ctx& c, const Shape& s, const void* dz, int64_t K, const void* A, i
   gemm(c, s, g);
 }
 
-void flush_wgrads(Ctx& c, const Shape& s, Wgrads& w) {
-  if (w.n == 0) return;
-  GemmLaunch g = launch(EPI_STORE, s);
-  g.allow_split = true;
-  g.nprob = w.n;
-  for (int i = 0; i < w.n; ++i) g.p[i] = w.p[i];
-  gemm(c, s, g);
-  w.n = 0;
+void flush_wgrads(Ctx& c, const Shape& s, Wgrads& w, bool final) {
+  TileReduce tr;
+  if (w.n > 0) {
+    GemmLaunch g = launch(EPI_STORE, s);
+    g.allow_split = true;
+    if (final) g.finish = &tr;
+    g.nprob = w.n;
+    for (int i = 0; i < w.n; ++i) g.p[i] = w.p[i];
+    gemm(c, s, g);
+    w.n = 0;
+  }
+  if (!final) return;
+  for (int j = 0; j < w.ncol; ++j) tr.col[j] = w.col[j];
+  tr.ncol = w.ncol;
+  w.ncol = 0;
+  launch_finish(c, tr);
 }
 
 void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const void* x,
@@ -632,9 +678,10 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
   add_wgrad(c, s, wg, wgrad(2 * r, d, T, B.dz_gu, 2 * r, x1, d, dW->A_gu, d, W->w_norm2));
   dx_gemm(c, s, B.dz_gu, 2 * r, W->A_gu, d, d, B.dn, d);
   void* dx1 = s.full() ? B.dx1 : dx;
-  DT_CALL(s, normbwd, c, s, B, B.dn, x1, W->w_norm2, A.rstd2, dy, dx1, dW->w_norm2);
+  DT_CALL(s, normbwd, c, s, B, wg, B.dw_part2, B.dn, x1, W->w_norm2, A.rstd2, dy, dx1,
+          dW->w_norm2);
   if (!s.full()) {
-    flush_wgrads(c, s, wg);
+    flush_wgrads(c, s, wg, true);
     return;
   }
 
@@ -673,8 +720,9 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
   }
   add_wgrad(c, s, wg, wgrad(3 * r, d, T, B.dz_qkv, 3 * r, x, d, dW->A_qkv, d, W->w_norm1));
   dx_gemm(c, s, B.dz_qkv, 3 * r, W->A_qkv, d, d, B.dn, d);
-  DT_CALL(s, normbwd, c, s, B, B.dn, x, W->w_norm1, A.rstd1, dx1, dx, dW->w_norm1);
-  flush_wgrads(c, s, wg);
+  DT_CALL(s, normbwd, c, s, B, wg, B.dw_part1, B.dn, x, W->w_norm1, A.rstd1, dx1, dx,
+          dW->w_norm1);
+  flush_wgrads(c, s, wg, true);
 }
 
 void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void* x,
@@ -721,9 +769,10 @@ void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void
     gemm(c, s, g);
   }
   void* dx1 = s.full() ? B.dx1 : dx;
-  DT_CALL(s, normbwd, c, s, B, B.dn, x1, W->w_norm2, A.rstd2, dy, dx1, dW->w_norm2);
+  DT_CALL(s, normbwd, c, s, B, wg, B.dw_part2, B.dn, x1, W->w_norm2, A.rstd2, dy, dx1,
+          dW->w_norm2);
   if (!s.full()) {
-    flush_wgrads(c, s, wg);
+    flush_wgrads(c, s, wg, true);
     return;
   }
   add_wgrad(c, s, wg, wgrad(d, d, T, dx1, d, A.V, d, dW->A_o, d));
@@ -732,8 +781,9 @@ void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void
   dx_gemm(c, s, dx1, d, W->A_o, d, d, at(B.dqkv, 2 * d, s), 3 * d, A.rstd1);
   add_wgrad(c, s, wg, wgrad(3 * d, d, T, B.dqkv, 3 * d, x, d, dW->A_qkv, d, W->w_norm1));
   dx_gemm(c, s, B.dqkv, 3 * d, W->A_qkv, d, d, B.dn, d);
-  DT_CALL(s, normbwd, c, s, B, B.dn, x, W->w_norm1, A.rstd1, dx1, dx, dW->w_norm1);
-  flush_wgrads(c, s, wg);
+  DT_CALL(s, normbwd, c, s, B, wg, B.dw_part1, B.dn, x, W->w_norm1, A.rstd1, dx1, dx,
+          dW->w_norm1);
+  flush_wgrads(c, s, wg, true);
 }
 
 Ctx make_ctx(void* scratch, bn_stream_t stream, const Tmp& B) {

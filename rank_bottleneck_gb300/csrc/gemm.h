@@ -59,12 +59,17 @@ struct GemmProblem {
   const void* colv = nullptr;
 };
 
+struct TileReduce;
+
 struct GemmLaunch {
   Epi epi = EPI_STORE;
   int sigma = 0;      // bn_sigma
   int S = 1;          // shards of the online norm
   float eps = 1e-5f;
   bool allow_split = false;  // EPI_STORE only: K may be split (deterministic reduction)
+  // tcgen05 engine: when set, the reduction of split tiles is described here
+  // (rem_tiles = 0: none) for the caller to launch (launch_finish), not launched
+  TileReduce* finish = nullptr;
   int nprob = 0;
   GemmProblem p[kMaxProblems];
 };

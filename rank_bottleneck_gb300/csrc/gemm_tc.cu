@@ -236,8 +236,10 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     return;
   }
   note_launch(c, KK_GEMM_TC, static_cast<int>(g.epi), flops, bytes);
+  TileReduce local;
+  TileReduce& r = g.finish ? *g.finish : local;
+  r.rem_tiles = 0;
   if (split) {
-    TileReduce r;
     r.nprob = g.nprob;
     r.full_units = P.full_units;
     r.rem_split = rem_split;
@@ -256,7 +258,7 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
       q.out = static_cast<__nv_bfloat16*>(g.p[i].out[0]);
       q.ldo = g.p[i].ldo[0];
     }
-    launch_tile_reduce(c, r);
+    if (g.finish == nullptr) launch_finish(c, r);
   }
 }
 

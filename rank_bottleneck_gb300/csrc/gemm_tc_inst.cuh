@@ -9,7 +9,7 @@ namespace tc {
 namespace {
 
 template <int EK, bool AMN, bool BMN>
-void go(const Params& P, int units, int num_sms, cudaStream_t s) {
+bool go(const Params& P, int units, int num_sms, cudaStream_t s) {
   constexpr int BN = GEMM_BN, CG = GEMM_CG;
   auto k = gemm_kernel<BN, EK, AMN, BMN, CG>;
   constexpr int SMEM = Cfg<BN, EK, CG>::SMEM_BYTES;
@@ -28,9 +28,18 @@ void go(const Params& P, int units, int num_sms, cudaStream_t s) {
   }
   // persistent grid: as many CTAs (pairs) as can be resident at once
   static int max_groups = 0;
+  static bool usable = true;
   static std::once_flag once;
   std::call_once(once, [&] {
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (EK == K_NORM) {
+      // its warpgroups trade registers (setmaxnreg) on the assumption that every
+      // thread is launched with kNormRegsLaunch of them: with fewer the trade
+      // could not complete, so the kernel is not launched at all
+      cudaFuncAttributes fa;
+      usable = cudaFuncGetAttributes(&fa, k) == cudaSuccess && fa.numRegs == kNormRegsLaunch;
+      cudaGetLastError();
+    }
     int n = 0;
     if (CG == 2) {
       cudaLaunchConfig_t q = cfg;
@@ -42,6 +51,7 @@ void go(const Params& P, int units, int num_sms, cudaStream_t s) {
     }
     max_groups = n;
   });
+  if (!usable) return false;
   const int groups = units < max_groups ? units : max_groups;
   cfg.gridDim = dim3(groups * CG, 1, 1);
   // programmatic dependent launch (see grid_dependency_sync)
@@ -50,6 +60,7 @@ void go(const Params& P, int units, int num_sms, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs += 1;
   cudaLaunchKernelEx(&cfg, k, P);
+  return true;
 }
 
 }  // namespace
@@ -61,16 +72,16 @@ bool BN_CAT(launch_bn, GEMM_BN, BN_CAT(_cg, GEMM_CG, ))(int ek, bool a_mn, bool 
                                                         cudaStream_t s) {
   const int key = ek * 4 + (a_mn ? 2 : 0) + (b_mn ? 1 : 0);
   switch (key) {
-    case K_STORE * 4 + 0: go<K_STORE, false, false>(P, units, num_sms, s); return true;
-    case K_STORE * 4 + 1: go<K_STORE, false, true>(P, units, num_sms, s); return true;
-    case K_STORE * 4 + 3: go<K_STORE, true, true>(P, units, num_sms, s); return true;
-    case K_SIGMA * 4 + 0: go<K_SIGMA, false, false>(P, units, num_sms, s); return true;
-    case K_RESID * 4 + 0: go<K_RESID, false, false>(P, units, num_sms, s); return true;
-    case K_DSIGMA * 4 + 1: go<K_DSIGMA, false, true>(P, units, num_sms, s); return true;
-    case K_DSWIGLU * 4 + 1: go<K_DSWIGLU, false, true>(P, units, num_sms, s); return true;
-    case K_CHAIN * 4 + 1: go<K_CHAIN, false, true>(P, units, num_sms, s); return true;
-    case K_NORM * 4 + 0: go<K_NORM, false, false>(P, units, num_sms, s); return true;
-    case K_SWIGLU * 4 + 0: go<K_SWIGLU, false, false>(P, units, num_sms, s); return true;
+    case K_STORE * 4 + 0: return go<K_STORE, false, false>(P, units, num_sms, s);
+    case K_STORE * 4 + 1: return go<K_STORE, false, true>(P, units, num_sms, s);
+    case K_STORE * 4 + 3: return go<K_STORE, true, true>(P, units, num_sms, s);
+    case K_SIGMA * 4 + 0: return go<K_SIGMA, false, false>(P, units, num_sms, s);
+    case K_RESID * 4 + 0: return go<K_RESID, false, false>(P, units, num_sms, s);
+    case K_DSIGMA * 4 + 1: return go<K_DSIGMA, false, true>(P, units, num_sms, s);
+    case K_DSWIGLU * 4 + 1: return go<K_DSWIGLU, false, true>(P, units, num_sms, s);
+    case K_CHAIN * 4 + 1: return go<K_CHAIN, false, true>(P, units, num_sms, s);
+    case K_NORM * 4 + 0: return go<K_NORM, false, false>(P, units, num_sms, s);
+    case K_SWIGLU * 4 + 0: return go<K_SWIGLU, false, false>(P, units, num_sms, s);
     default: return false;
   }
 }

@@ -20,14 +20,17 @@
 //   warp 10       epilogue-input producer: TMA loads of the tensors an
 //                 epilogue reads (residual, z, G and U) into the same
 //                 subtile ring, ahead of the epilogue.
+// Online RMSNorm's kernel moves the epilogue to warps 4..11 (warps 2 and 3 are
+// idle) and shifts registers to it with setmaxnreg: it keeps each row's running
+// sum over the shards in registers.
 // The epilogue works on 128 x 32 subtiles; warp w owns rows 32 (w % 4) .. +31
 // of each and stores them as one 32 x 32 TMA box, so every global access is a
 // bulk copy and the threads only touch conflict-free swizzled shared memory.
 //
 // A work unit is one 128 x BN output tile (or one K split of it), a sequence
 // of segments; each segment is a K range, possibly of another operand pair,
-// accumulated in its own TMEM slot: this is how Online RMSNorm sees each
-// emulated shard's partial product and how SwiGLU sees G and U side by side.
+// accumulated in the next TMEM slot of the ring: this is how Online RMSNorm sees
+// each emulated shard's partial product and how SwiGLU sees G and U side by side.
 //
 // Every mbarrier wait is bounded by wall time (kWaitLimitNs). On expiry the
 // thread sets a CTA-wide abort flag and the device status word, all roles
@@ -73,12 +76,35 @@ struct EpiShape {
   static constexpr int BYTES = NE * NT * SUB_BYTES;
 };
 
+// First epilogue warp. Online RMSNorm keeps each row's running sum in the
+// epilogue's registers, so its epilogue warps form whole warpgroups (4..11)
+// that take registers from warpgroup 0 (warps 0..3: the producer, the MMA
+// issuer and two idle warps) with setmaxnreg, which acts per warpgroup.
+template <int EK>
+constexpr int epi_warp0() {
+  return EK == K_NORM ? 4 : 2;
+}
 // threads of a CTA: kinds without epilogue inputs leave out the input-producer
 // warp, which leaves the epilogue more registers
 template <int EK>
 constexpr int kernel_threads() {
-  return EpiShape<EK>::NIN > 0 ? NUM_THREADS : NUM_THREADS - 32;
+  return EK == K_NORM ? 32 * (4 + NUM_EPI_WARPS)
+                      : (EpiShape<EK>::NIN > 0 ? NUM_THREADS : NUM_THREADS - 32);
 }
+// Online RMSNorm register split. At launch, 12 warps get 168 registers a thread
+// (3 warps per SM sub-partition): 384 x 168 = 64512 in all. Warpgroup 0 drops to
+// kNormRegsLow and the two epilogue warpgroups rise to kNormRegsHigh:
+// 128 x 56 + 256 x 224 = 64512, no more than the launch's total, and 56 + 2 x 224
+// = 504 of the 512 a sub-partition holds per lane. That increase is the only one:
+// it asks for exactly what warpgroup 0 gives up, whatever the order in which the
+// warps get there. At the end the epilogue drops to kNormRegsLow too (a decrease
+// never waits), so every warp reaches the common exit path with the same count.
+constexpr int kNormRegsLaunch = 168;
+constexpr int kNormRegsLow = 56;
+constexpr int kNormRegsHigh = 224;
+static_assert(128 * kNormRegsLow + 256 * kNormRegsHigh <= 384 * kNormRegsLaunch,
+              "register split too large");
+static_assert(kNormRegsLow + 2 * kNormRegsHigh <= 512, "register split exceeds a sub-partition");
 
 template <int BN, int EK, int CG = 1>
 struct Cfg {
@@ -157,7 +183,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase of `bar` with parity `parity` to complete.
-static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity,
+static __device__ __forceinline__ bool wait_bar_inline(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag, int* status,
                                              unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -173,6 +199,22 @@ static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity,
       }
     }
   }
+}
+// Out of line (fewer registers at the call sites) except in Online RMSNorm's
+// kernel: its warpgroups run at different register counts, and one called
+// function cannot serve both.
+static __device__ __noinline__ bool wait_bar_call(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, int* status,
+                                                  unsigned long long limit_ns) {
+  return wait_bar_inline(bar, parity, abort_flag, status, limit_ns);
+}
+template <int EK>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status, unsigned long long limit_ns = kWaitLimitNs) {
+  if constexpr (EK == K_NORM)
+    return wait_bar_inline(bar, parity, abort_flag, status, limit_ns);
+  else
+    return wait_bar_call(bar, parity, abort_flag, status, limit_ns);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
@@ -236,6 +278,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
       : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -639,6 +690,11 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
   const uint32_t tmem = *tmem_slot;
   const int nseg = num_segments<EK>(P);
 
+  // Online RMSNorm's register split is made per warpgroup, in one place for
+  // each: a point where the register count differs between the branches
+  // cannot be shared code.
+  if (warp == 0 || warp == 1 || warp == epi_warp0<EK>() + NUM_EPI_WARPS || (EK == K_NORM && warp < 4)) {
+  if constexpr (EK == K_NORM) setmaxnreg_dec<kNormRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ operand producer
     if (lane == 0) {
@@ -661,7 +717,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
           const CUtensorMap* ma = &pr.ma[opair];
           const CUtensorMap* mb = &pr.mb[opair];
           for (int kb = kb0; kb < kb0 + nkb; ++kb) {
-            if (!wait_bar(smem_u32(&empty[stage]), ph ^ 1u, abort_flag, P.status)) {
+            if (!wait_bar<EK>(smem_u32(&empty[stage]), ph ^ 1u, abort_flag, P.status)) {
               ok = false;
               break;
             }
@@ -707,7 +763,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
             st = C::STAGES - 1;
             p ^= 1u;
           }
-          wait_bar(smem_u32(&full[st]), p, abort_flag, P.status, 50ull * 1000 * 1000);
+          wait_bar<EK>(smem_u32(&full[st]), p, abort_flag, P.status, 50ull * 1000 * 1000);
         }
       }
     }
@@ -719,24 +775,16 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
       uint32_t ph = 0;
       int slot = 0;
       uint32_t sph = 0;
-      // Online RMSNorm keeps a tile's running sum in one slot (tile t: slot t % 2)
-      // while the shards' partial products land in the other
-      uint32_t norm_ph[2] = {0u, 0u};
-      int64_t tile_no = 0;
       bool ok = true;
-      for (int u = pair; ok && u < P.total_units; u += npairs, ++tile_no) {
+      for (int u = pair; ok && u < P.total_units; u += npairs) {
         const Work w = decode<CG>(P, u);
         const Prob& pr = P.p[w.pi];
         for (int s = 0; ok && s < nseg; ++s) {
           int kb0, nkb, opair;
           segment<EK>(P, pr, w, s, kb0, nkb, opair);
           const bool fresh = !(EK == K_CHAIN && s == 1);
-          if (EK == K_NORM) {
-            slot = static_cast<int>(tile_no & 1) ^ (s == 0 ? 0 : 1);
-            sph = norm_ph[slot];
-          }
           if (fresh) {
-            if (!wait_bar(smem_u32(&acce[slot]), sph ^ 1u, abort_flag, P.status)) {
+            if (!wait_bar<EK>(smem_u32(&acce[slot]), sph ^ 1u, abort_flag, P.status)) {
               ok = false;
               break;
             }
@@ -744,7 +792,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
           }
           const uint32_t d_tmem = tmem + static_cast<uint32_t>(slot * BN);
           for (int i = 0; i < nkb; ++i) {
-            if (!wait_bar(smem_u32(&full[stage]), ph, abort_flag, P.status)) {
+            if (!wait_bar<EK>(smem_u32(&full[stage]), ph, abort_flag, P.status)) {
               ok = false;
               break;
             }
@@ -765,10 +813,10 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
           }
           if (!ok) break;
           if (!(EK == K_CHAIN && s == 0)) {
+            // each segment's accumulator (for Online RMSNorm: each shard's partial
+            // product) takes the next slot of the ring
             mma_commit<CG>(smem_u32(&accf[slot]));
-            if (EK == K_NORM) {
-              norm_ph[slot] ^= 1u;
-            } else if (++slot == C::NSLOT) {
+            if (++slot == C::NSLOT) {
               slot = 0;
               sph ^= 1u;
             }
@@ -777,9 +825,9 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
       }
       // every MMA issued must complete before TMEM is released
       mma_commit_local<CG>(smem_u32(drain));
-      wait_bar(smem_u32(drain), 0, abort_flag, P.status, ok ? kWaitLimitNs : 50ull * 1000 * 1000);
+      wait_bar<EK>(smem_u32(drain), 0, abort_flag, P.status, ok ? kWaitLimitNs : 50ull * 1000 * 1000);
     }
-  } else if (warp == 2 + NUM_EPI_WARPS) {
+  } else if (warp == epi_warp0<EK>() + NUM_EPI_WARPS) {
     // ------------------------------------------------------------ epilogue-input producer
     if (E::NIN > 0 && lane == 0) {
       int e = 0;
@@ -792,7 +840,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         const int m0 = static_cast<int>(w.m0) + row_off;
         const int n0 = static_cast<int>(w.nb) * BN;
         for (int c = 0; c < NCH; ++c) {
-          if (!wait_bar(smem_u32(&epi_empty[e]), eph ^ 1u, abort_flag, P.status)) {
+          if (!wait_bar<EK>(smem_u32(&epi_empty[e]), eph ^ 1u, abort_flag, P.status)) {
             ok = false;
             break;
           }
@@ -818,24 +866,25 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
             st = E::NE - 1;
             p ^= 1u;
           }
-          wait_bar(smem_u32(&epi_full[st]), p, abort_flag, P.status, 50ull * 1000 * 1000);
+          wait_bar<EK>(smem_u32(&epi_full[st]), p, abort_flag, P.status, 50ull * 1000 * 1000);
         }
       }
     }
+  }  // Online RMSNorm: warps 2 and 3 only lend their registers
   } else {
     // ------------------------------------------------------------ epilogue
+    if constexpr (EK == K_NORM) setmaxnreg_inc<kNormRegsHigh>();
     const int q = warp & 3;                 // TMEM lane quarter = tile rows 32q .. 32q + 31
-    const int grp = (warp - 2) >> 2;        // this warp's subtiles: c % EPI_GROUPS == grp
+    const int grp = (warp - epi_warp0<EK>()) >> 2;  // this warp's subtiles: c % EPI_GROUPS == grp
     constexpr int MYCH = NCH / EPI_GROUPS;  // subtiles per warp per tile
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int slot = 0;
     uint32_t sph = 0;
-    uint32_t norm_ph[2] = {0u, 0u};         // Online RMSNorm: per-slot phases (see the MMA warp)
     int prev_e = 0, mine = 0;
     int64_t tile_no = 0;                    // tiles this CTA has finished
     bool ok = true;
     auto acquire = [&](int sl, uint32_t p) -> bool {
-      if (!wait_bar(smem_u32(&accf[sl]), p, abort_flag, P.status)) return false;
+      if (!wait_bar<EK>(smem_u32(&accf[sl]), p, abort_flag, P.status)) return false;
       tc_fence_after();
       return true;
     };
@@ -865,113 +914,44 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
       uint32_t gpk[EK == K_SWIGLU ? MYCH : 1][16];  // SwiGLU: this warp's G, bf16 pairs
       int sl0 = slot, sl1 = slot;  // TMEM slot(s) of this tile's accumulator(s)
       if constexpr (EK == K_NORM) {
-        // Online RMSNorm. The running sum R lives in TMEM slot sl0 = tile % 2; each
-        // shard's partial product P_s arrives in the other slot and is folded as
+        // Online RMSNorm. Shard s's partial product P_s arrives in the next TMEM
+        // slot of the ring; the epilogue folds it into the running sum R, kept in
+        // registers (this thread's row, this group's columns), as
         // R += alpha_s * (P_s / rms_s): local normalisation, then the per-row
-        // correction alpha_s = rms_s / rms_g.
-        sl0 = static_cast<int>(tile_no & 1);
-        const int slp = sl0 ^ 1;
+        // correction alpha_s = rms_s / rms_g. The slot is free again as soon as
+        // P_s is in registers, so the MMAs of shard s + 1 run during the fold.
         const int S = P.S;
         const float* ss = pr.rowv + (row_ok ? row : 0) * S;
         float tot = 0.f;
         for (int s = 0; s < S; ++s) tot += row_ok ? ss[s] : 0.f;
         const float shard_w = static_cast<float>(pr.K / S);
         const float rms_g = sqrtf(tot / static_cast<float>(pr.K) + P.eps);
-        const uint32_t tR = tmem + lane_base + static_cast<uint32_t>(sl0 * BN);
-        const uint32_t tP = tmem + lane_base + static_cast<uint32_t>(slp * BN);
-        uint32_t zpk[MYCH][16];  // z = R after the last shard, as bf16 pairs
-        // waits for shard s's product and gives its local normalisation 1 / rms_s
-        // and per-row correction alpha_s = rms_s / rms_g
-        auto shard = [&](int s, float& inv_local, float& alpha) -> bool {
-          const int sl = (s == 0) ? sl0 : slp;
-          if (!acquire(sl, norm_ph[sl])) return false;
-          norm_ph[sl] ^= 1u;
+        float R[MYCH][32];
+        for (int s = 0; s < S; ++s) {
+          const int sl = slot;
+          if (!acquire(sl, sph)) {
+            ok = false;
+            break;
+          }
+          advance();
           const float ss_s = row_ok ? ss[s] : 0.f;
           const float rms_s = sqrtf(ss_s / shard_w + P.eps);
-          inv_local = 1.0f / rms_s;
-          alpha = rms_s / rms_g;
-          return true;
-        };
-        for (int s = 0; s + 1 < S; ++s) {
-          float inv_local, alpha;
-          if (!shard(s, inv_local, alpha)) {
-            ok = false;
-            break;
-          }
-          // two chunks per TMEM round trip: all loads in flight, then one wait; the
-          // new running sum overwrites the loaded one in place
-#pragma unroll 1
-          for (int k = 0; k < MYCH; k += 2) {
-            const uint32_t c0 = static_cast<uint32_t>((k * EPI_GROUPS + grp) * 32);
-            const uint32_t c1 = static_cast<uint32_t>(((k + 1) * EPI_GROUPS + grp) * 32);
-            uint32_t r0[32], r1[32];
-            if (s == 0) {
-              tmem_ld32_nowait(tR + c0, r0);
-              tmem_ld32_nowait(tR + c1, r1);
-              tmem_wait_ld2(r0, r1);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                r0[i] = __float_as_uint(alpha * (__uint_as_float(r0[i]) * inv_local));
-                r1[i] = __float_as_uint(alpha * (__uint_as_float(r1[i]) * inv_local));
-              }
-            } else {
-              uint32_t p0[32], p1[32];
-              tmem_ld32_nowait(tP + c0, p0);
-              tmem_ld32_nowait(tR + c0, r0);
-              tmem_ld32_nowait(tP + c1, p1);
-              tmem_ld32_nowait(tR + c1, r1);
-              tmem_wait_ld2(p0, r0);
-              tie32(p1);
-              tie32(r1);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                r0[i] = __float_as_uint(
-                    fmaf(alpha, __uint_as_float(p0[i]) * inv_local, __uint_as_float(r0[i])));
-                r1[i] = __float_as_uint(
-                    fmaf(alpha, __uint_as_float(p1[i]) * inv_local, __uint_as_float(r1[i])));
-              }
-            }
-            tmem_st32u_nowait(tR + c0, r0);
-            tmem_st32u_nowait(tR + c1, r1);
-          }
-          tmem_wait_st();  // R is complete before it is read again or P's slot is refilled
-          if (s > 0) release(slp);
-        }
-        if (!ok) break;
-        {
-          // last shard: z goes to registers (it is rounded to bf16 anyway), and both
-          // TMEM slots are free for the next tile before z and sigma(z) are stored
-          const int s = S - 1;
-          float inv_local, alpha;
-          if (!shard(s, inv_local, alpha)) {
-            ok = false;
-            break;
-          }
+          const float inv_local = 1.0f / rms_s;
+          const float alpha = rms_s / rms_g;
+          const uint32_t tP = tmem + lane_base + static_cast<uint32_t>(sl * BN);
 #pragma unroll
           for (int k = 0; k < MYCH; ++k) {
-            const uint32_t col = static_cast<uint32_t>((k * EPI_GROUPS + grp) * 32);
             float v[32];
+            tmem_ld32(tP + static_cast<uint32_t>((k * EPI_GROUPS + grp) * 32), v);
+            if (k == MYCH - 1) release(sl);  // every column of P_s is in registers
             if (s == 0) {
-              tmem_ld32(tR + col, v);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = alpha * (v[i] * inv_local);
+              for (int i = 0; i < 32; ++i) R[k][i] = alpha * (v[i] * inv_local);
             } else {
-              uint32_t pv[32], rv[32];
-              tmem_ld32_nowait(tP + col, pv);
-              tmem_ld32_nowait(tR + col, rv);
-              tmem_wait_ld2(pv, rv);
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                v[i] = fmaf(alpha, __uint_as_float(pv[i]) * inv_local, __uint_as_float(rv[i]));
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-              zpk[k][i] = *reinterpret_cast<const uint32_t*>(&h);
+              for (int i = 0; i < 32; ++i) R[k][i] = fmaf(alpha, v[i] * inv_local, R[k][i]);
             }
           }
-          if (s > 0) release(slp);
-          release(sl0);
         }
         if (!ok) break;
         const int rt = static_cast<int>(w.m0) + row_off + q * 32;
@@ -981,22 +961,27 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
           const int64_t col0 = n0 + c * EPI_N;
           const int e = static_cast<int>((tile_no * NCH + c) % E::NE);
           uint8_t* ent = epi + e * E::NT * E::SUB_BYTES + q * E::WARP_BYTES;
-          uint32_t hpk[16];
+          uint32_t zpk[16], hpk[16];  // z = R rounded to bf16, h = sigma(z): bf16 pairs
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float z0 = __uint_as_float(zpk[k][i] << 16);
-            const float z1 = __uint_as_float(zpk[k][i] & 0xFFFF0000u);
+            const __nv_bfloat162 h = __floats2bfloat162_rn(R[k][2 * i], R[k][2 * i + 1]);
+            zpk[i] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float z0 = __uint_as_float(zpk[i] << 16);
+            const float z1 = __uint_as_float(zpk[i] & 0xFFFF0000u);
             const __nv_bfloat162 h = __floats2bfloat162_rn(act_fast(z0, P.sigma), act_fast(z1, P.sigma));
             hpk[i] = *reinterpret_cast<const uint32_t*>(&h);
           }
-          smem_row_store_packed(ent, lane, zpk[k]);
+          smem_row_store_packed(ent, lane, zpk);
           smem_row_store_packed(ent + E::SUB_BYTES, lane, hpk);
           if (row_ok && col0 + EPI_N > pr.N8 && col0 < N) {
             float f[32];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              f[2 * i] = __uint_as_float(zpk[k][i] << 16);
-              f[2 * i + 1] = __uint_as_float(zpk[k][i] & 0xFFFF0000u);
+              f[2 * i] = __uint_as_float(zpk[i] << 16);
+              f[2 * i + 1] = __uint_as_float(zpk[i] & 0xFFFF0000u);
             }
             if (pr.out_mask & 1) store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, f);
             if (pr.out_mask & 2) {
@@ -1172,7 +1157,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         const int e = static_cast<int>(j % E::NE);
         const uint32_t eph = static_cast<uint32_t>((j / E::NE) & 1);
         if (E::NIN > 0) {
-          if (!wait_bar(smem_u32(&epi_full[e]), eph, abort_flag, P.status)) {
+          if (!wait_bar<EK>(smem_u32(&epi_full[e]), eph, abort_flag, P.status)) {
             ok = false;
             break;
           }
@@ -1303,6 +1288,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
       bulk_wait_all();
     }
     __syncwarp();
+    if constexpr (EK == K_NORM) setmaxnreg_dec<kNormRegsLow>();
   }
 
   tc_fence_before();

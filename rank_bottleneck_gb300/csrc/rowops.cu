@@ -42,69 +42,168 @@ template <> struct Pack8<float> {
   }
 };
 
+// Statistics of one row from chunks already in registers: chunk u of a batch
+// covers columns base + 256 u + 8 lane .. +7 (zero past d). Shards are whole
+// multiples of 8 columns, so a chunk lies in one shard; each shard's sum is
+// reduced across the warp once per batch it intersects and added in shard
+// order. cur / cur_s / tot carry a shard that continues into the next batch.
+template <typename T, int U>
+__device__ __forceinline__ void stats_batch(const Pack8<T> (&v)[U], int base, int d, int w,
+                                            float* __restrict__ ss_row, int lane, float& cur,
+                                            int& cur_s, float& tot) {
+  float q[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    float a = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = fmaf(v[u][i], v[u][i], a);
+    q[u] = a;
+  }
+  const int last = min(d, base + 256 * U) - 1;
+  for (int s = base / w; s <= last / w; ++s) {
+    const int lo = s * w, hi = lo + w;  // the shard's columns
+    float a = 0.f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = base + 256 * u + 8 * lane;
+      if (c >= lo && c < hi) a += q[u];  // chunks past d are zero and past hi
+    }
+    a = warp_sum(a);
+    if (s != cur_s) {
+      if (lane == 0) ss_row[cur_s] = cur;
+      cur_s = s;
+      cur = 0.f;
+    }
+    cur += a;
+    tot += a;
+  }
+}
+
+template <typename T, int U>
+__device__ __forceinline__ void load_batch(Pack8<T> (&v)[U], const T* __restrict__ xr, int base,
+                                           int d, int lane) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int c = base + 256 * u + 8 * lane;
+    if (c < d)
+      v[u].load(xr + c);
+    else
+      v[u].zero();
+  }
+}
+
+// Rows [warp0, rows) with stride `stride`, one warp each. Rows of at most 2048
+// columns are one batch: the next row's loads are issued before this row is
+// reduced, so two rows per warp are in flight. Longer rows go batch by batch.
+template <typename T>
+__device__ __forceinline__ void stats_rows(const T* __restrict__ x, int64_t rows, int d, int S,
+                                           float eps, float* __restrict__ ss,
+                                           float* __restrict__ rstd, int64_t row0,
+                                           int64_t stride, int lane) {
+  constexpr int U = 8;
+  const int w = d / S;
+  if (d <= 256 * U) {
+    Pack8<T> v[U], nx[U];
+    if (row0 < rows) load_batch<T, U>(v, x + row0 * d, 0, d, lane);
+    for (int64_t row = row0; row < rows; row += stride) {
+      const int64_t next = row + stride;
+      if (next < rows) load_batch<T, U>(nx, x + next * d, 0, d, lane);
+      float cur = 0.f, tot = 0.f;
+      int cur_s = 0;
+      stats_batch<T, U>(v, 0, d, w, ss + row * S, lane, cur, cur_s, tot);
+      if (lane == 0) {
+        ss[row * S + cur_s] = cur;
+        rstd[row] = 1.0f / sqrtf(tot / static_cast<float>(d) + eps);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = nx[u];
+    }
+    return;
+  }
+  for (int64_t row = row0; row < rows; row += stride) {
+    const T* xr = x + row * d;
+    float cur = 0.f, tot = 0.f;
+    int cur_s = 0;
+    for (int base = 0; base < d; base += 256 * U) {
+      Pack8<T> v[U];
+      load_batch<T, U>(v, xr, base, d, lane);
+      stats_batch<T, U>(v, base, d, w, ss + row * S, lane, cur, cur_s, tot);
+    }
+    if (lane == 0) {
+      ss[row * S + cur_s] = cur;
+      rstd[row] = 1.0f / sqrtf(tot / static_cast<float>(d) + eps);
+    }
+  }
+}
+
+// out = A diag(w) on block b of the nb blocks given to the job
+template <typename T>
+__device__ __forceinline__ void fold_blocks(const FoldJob<T>& f, int b, int nb) {
+  const int64_t nvec = f.cols / 8;
+  for (int64_t i = b * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < f.rows * nvec;
+       i += static_cast<int64_t>(nb) * blockDim.x) {
+    const int64_t r = i / nvec, c = (i - r * nvec) * 8;
+    float a[8], ww[8];
+    Vec8<T>::load(f.A + r * f.cols + c, a);
+    Vec8<T>::load(f.w + c, ww);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] *= ww[k];
+    Vec8<T>::store(f.out + r * f.cols + c, a);
+  }
+}
+
+// Blocks [0, stat_blocks): the row statistics, each of their warps taking rows
+// warp, warp + 8 stat_blocks, ... The blocks after them fold norm weights into
+// down-projections: job 0 on the next fold_blocks0 blocks, job 1 on the rest.
 template <typename T>
 __global__ void __launch_bounds__(256) stats_kernel(const T* __restrict__ x, int64_t rows, int d,
                                                     int S, float eps, float* __restrict__ ss,
-                                                    float* __restrict__ rstd) {
+                                                    float* __restrict__ rstd, int stat_blocks,
+                                                    const FoldJob<T> f0, int fold_blocks0,
+                                                    const FoldJob<T> f1) {
   grid_dependency_sync();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-  if (row >= rows) return;
-  const T* xr = x + row * d;
-  const int w = d / S;
-  float tot = 0.f;
-  for (int s = 0; s < S; ++s) {
-    float acc = 0.f;
-    for (int c = s * w + lane * 8; c < (s + 1) * w; c += 256) {
-      float v[8];
-      Vec8<T>::load(xr + c, v);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc = fmaf(v[i], v[i], acc);
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) ss[row * S + s] = acc;
-    tot += acc;
+  const int b = static_cast<int>(blockIdx.x);
+  if (b >= stat_blocks) {
+    const int fb = b - stat_blocks;
+    if (fb < fold_blocks0)
+      fold_blocks(f0, fb, fold_blocks0);
+    else
+      fold_blocks(f1, fb - fold_blocks0, static_cast<int>(gridDim.x) - stat_blocks - fold_blocks0);
+    return;
   }
-  if (lane == 0) rstd[row] = 1.0f / sqrtf(tot / static_cast<float>(d) + eps);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  stats_rows(x, rows, d, S, eps, ss, rstd, static_cast<int64_t>(b) * 8 + warp,
+             static_cast<int64_t>(stat_blocks) * 8, lane);
+}
+
+template <typename T>
+static unsigned fold_grid(const Ctx& c, const FoldJob<T>& f) {
+  if (f.A == nullptr || f.rows * f.cols == 0) return 0;
+  const int64_t n = f.rows * (f.cols / 8);
+  return static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 4));
+}
+
+template <typename T>
+void launch_stats_fold(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float eps, float* ss,
+                       float* rstd, const FoldJob<T>& f0, const FoldJob<T>& f1) {
+  // three blocks of 8 warps per SM (80 registers a thread for bf16), each warp
+  // looping over rows
+  const unsigned sb = static_cast<unsigned>(std::min<int64_t>((rows + 7) / 8, c.num_sms * 3));
+  const unsigned g0 = fold_grid(c, f0), g1 = fold_grid(c, f1);
+  const double fold_elems = static_cast<double>(g0 ? f0.rows * f0.cols : 0) +
+                            static_cast<double>(g1 ? f1.rows * f1.cols : 0);
+  prof_start(c);
+  track(c, launch_pdl(stats_kernel<T>, sb + g0 + g1, 256, 0, c.stream, x, rows, static_cast<int>(d),
+                      S, eps, ss, rstd, static_cast<int>(sb), f0, static_cast<int>(g0), f1));
+  note_launch(c, KK_STATS, -1, 2.0 * rows * d + fold_elems,
+              static_cast<double>(rows) * (d * sizeof(T) + 4 * S + 4) +
+                  2.0 * fold_elems * sizeof(T));
 }
 
 template <typename T>
 void launch_stats(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float eps, float* ss,
                   float* rstd) {
-  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
-  prof_start(c);
-  track(c, launch_pdl(stats_kernel<T>, grid, 256, 0, c.stream, x, rows, static_cast<int>(d), S, eps,
-                      ss, rstd));
-  note_launch(c, KK_STATS, -1, 2.0 * rows * d, static_cast<double>(rows) * (d * sizeof(T) + 4 * S + 4));
-}
-
-// ---------------------------------------------------------------------------
-// weight fold: out = A diag(w)
-// ---------------------------------------------------------------------------
-template <typename T>
-__global__ void fold_cols_kernel(const T* __restrict__ A, const T* __restrict__ w, int64_t rows,
-                                 int64_t cols, T* __restrict__ out) {
-  grid_dependency_sync();
-  const int64_t nvec = cols / 8;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows * nvec;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / nvec, c = (i - r * nvec) * 8;
-    float a[8], ww[8];
-    Vec8<T>::load(A + r * cols + c, a);
-    Vec8<T>::load(w + c, ww);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) a[k] *= ww[k];
-    Vec8<T>::store(out + r * cols + c, a);
-  }
-}
-
-template <typename T>
-void launch_fold_cols(Ctx& c, const T* A, const T* w, int64_t rows, int64_t cols, T* out) {
-  const int64_t n = rows * (cols / 8);
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 8));
-  prof_start(c);
-  track(c, launch_pdl(fold_cols_kernel<T>, grid, 256, 0, c.stream, A, w, rows, cols, out));
-  note_launch(c, KK_FOLD, -1, 1.0 * rows * cols, (2.0 * rows * cols + cols) * sizeof(T));
+  launch_stats_fold<T>(c, x, rows, d, S, eps, ss, rstd, FoldJob<T>{}, FoldJob<T>{});
 }
 
 // ---------------------------------------------------------------------------
@@ -114,7 +213,6 @@ void launch_fold_cols(Ctx& c, const T* A, const T* w, int64_t rows, int64_t cols
 // a row of `part`; colsum_kernel adds the rows in a fixed order, so dw is
 // bit-reproducible.
 // ---------------------------------------------------------------------------
-constexpr int kNormBwdMaxWarps = 8;
 constexpr int kNormBwdUnroll = 4;
 constexpr size_t kNormBwdSmemLimit = 200 * 1024;
 
@@ -123,8 +221,13 @@ constexpr size_t kNormBwdSmemLimit = 200 * 1024;
 // whole row (dn, x and dres all loaded up front: one memory round trip per row;
 // one block per SM for the registers). NP = 0: any d, two passes over the row
 // (the second one mostly from L1/L2), two blocks per SM.
+// Register-resident rows run 12 warps in one block per SM (up to 168 registers a
+// thread); the two-pass form runs two blocks of 8 warps per SM.
+template <int NP>
+constexpr int norm_bwd_warps() { return NP > 0 ? 12 : 8; }
+
 template <typename T, int NP>
-__global__ void __launch_bounds__(kNormBwdMaxWarps * 32, NP > 0 ? 1 : 2)
+__global__ void __launch_bounds__(norm_bwd_warps<NP>() * 32, NP > 0 ? 1 : 2)
     norm_bwd_kernel(const T* __restrict__ dn, const T* __restrict__ x, const T* __restrict__ w,
                     const float* __restrict__ rstd, const T* __restrict__ dres, int64_t rows,
                     int d, T* __restrict__ dx, float* __restrict__ part) {
@@ -135,7 +238,9 @@ __global__ void __launch_bounds__(kNormBwdMaxWarps * 32, NP > 0 ? 1 : 2)
   const int nw = blockDim.x >> 5;
   const int dp = d + d / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* wsm = acc + nw * dp;  // the norm weight as fp32, read by every row
   for (int i = threadIdx.x; i < nw * dp; i += blockDim.x) acc[i] = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) wsm[i] = to_f<T>(w[i]);
   __syncthreads();
   float* my = acc + warp * dp;
   const float inv_d = 1.0f / static_cast<float>(d);
@@ -146,19 +251,20 @@ __global__ void __launch_bounds__(kNormBwdMaxWarps * 32, NP > 0 ? 1 : 2)
     const T* xr = x + row * d;
     if constexpr (NP > 0) {
       const T* dr = dres + row * d;
-      Pack8<T> a[NP], b[NP], g[NP];
+      Pack8<T> a[NP], b[NP];
 #pragma unroll
       for (int u = 0; u < NP; ++u) {
         const int c = lane * 8 + u * 256;
         a[u].load(dnr + c);
         b[u].load(xr + c);
-        g[u].load(dr + c);
       }
       float s = 0.f;
 #pragma unroll
       for (int u = 0; u < NP; ++u) {
-        Pack8<T> ww;
-        ww.load(w + lane * 8 + u * 256);
+        const int c = lane * 8 + u * 256;
+        const float4 w0 = *reinterpret_cast<const float4*>(wsm + c);
+        const float4 w1 = *reinterpret_cast<const float4*>(wsm + c + 4);
+        const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) s = fmaf(a[u][i] * ww[i], b[u][i], s);
       }
@@ -169,12 +275,15 @@ __global__ void __launch_bounds__(kNormBwdMaxWarps * 32, NP > 0 ? 1 : 2)
 #pragma unroll
       for (int u = 0; u < NP; ++u) {
         const int c = lane * 8 + u * 256;
-        Pack8<T> ww;
-        ww.load(w + c);
+        const float4 w0 = *reinterpret_cast<const float4*>(wsm + c);
+        const float4 w1 = *reinterpret_cast<const float4*>(wsm + c + 4);
+        const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        Pack8<T> g;  // the residual gradient, read only here: fewer registers live
+        g.load(dr + c);
         float out[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          out[i] = g[u][i] + (a[u][i] * ww[i] - b[u][i] * coef);
+          out[i] = g[i] + (a[u][i] * ww[i] - b[u][i] * coef);
           my[c + c / 8 + i] = fmaf(a[u][i], b[u][i], my[c + c / 8 + i]);
         }
         Vec8<T>::store(o + c, out);
@@ -242,15 +351,15 @@ __global__ void __launch_bounds__(kNormBwdMaxWarps * 32, NP > 0 ? 1 : 2)
   }
 }
 
-// dw[col] = sum over blocks b of part[b][col]: 32 columns per block, each of the
-// 8 warps sums a fixed contiguous range of b, the 8 sums are added in warp order.
+// dw[col] = sum over blocks b of part[b][col] for the 32 columns of block `cb`:
+// each of the 8 warps sums a fixed contiguous range of b, the 8 sums are added
+// in warp order.
 template <typename T>
-__global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ part, int nblk, int d,
-                                                     T* __restrict__ out) {
-  grid_dependency_sync();
+__device__ __forceinline__ void colsum_block(const float* __restrict__ part, int nblk, int d,
+                                             T* __restrict__ out, int cb) {
   __shared__ float red[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col = blockIdx.x * 32 + lane;
+  const int col = cb * 32 + lane;
   const int per = (nblk + 7) / 8;
   const int b0 = warp * per, b1 = min(nblk, b0 + per);
   float v = 0.f;
@@ -267,19 +376,31 @@ __global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ p
   }
 }
 
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ part, int nblk, int d,
+                                                     T* __restrict__ out) {
+  grid_dependency_sync();
+  colsum_block(part, nblk, d, out, static_cast<int>(blockIdx.x));
+}
+
 int norm_bwd_blocks(int num_sms) { return 2 * num_sms; }
 
 template <typename T>
-void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rstd,
-                     const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw) {
-  // as many warps (<= 8) as their column sums fit in shared memory
-  const size_t row_bytes = sizeof(float) * static_cast<size_t>(d + d / 8);
-  const int nw = static_cast<int>(std::max<size_t>(
-      1, std::min<size_t>(kNormBwdMaxWarps, kNormBwdSmemLimit / row_bytes)));
-  const size_t smem = row_bytes * nw;
+int launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rstd,
+                    const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw,
+                    bool colsum) {
   // bf16 rows of 1024 or 2048 elements stay in registers
   constexpr bool kResident = sizeof(T) == 2;  // register-resident rows for bf16 only
   constexpr int kNP4 = kResident ? 4 : 0, kNP8 = kResident ? 8 : 0;
+  const bool resident = kResident && (d == 2048 || d == 1024);
+  if (resident) nblk = std::min(nblk, c.num_sms);  // one block per SM
+  // as many warps as their column sums fit in shared memory, beside the weight
+  const size_t row_bytes = sizeof(float) * static_cast<size_t>(d + d / 8);
+  const size_t w_bytes = sizeof(float) * static_cast<size_t>(d);
+  const int max_warps = resident ? norm_bwd_warps<4>() : norm_bwd_warps<0>();
+  const int nw = static_cast<int>(std::max<size_t>(
+      1, std::min<size_t>(max_warps, (kNormBwdSmemLimit - w_bytes) / row_bytes)));
+  const size_t smem = row_bytes * nw + w_bytes;
   auto kern = norm_bwd_kernel<T, 0>;
   if (kResident && d == 2048) kern = norm_bwd_kernel<T, kNP8>;
   if (kResident && d == 1024) kern = norm_bwd_kernel<T, kNP4>;
@@ -295,20 +416,21 @@ void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* r
                       static_cast<int>(d), dx, part));
   note_launch(c, KK_NORM_BWD, -1, 8.0 * rows * d,
               4.0 * rows * d * sizeof(T) + d * sizeof(T) + 4.0 * rows + 4.0 * nblk * d);
+  if (!colsum) return nblk;  // the caller sums `part` later (launch_finish)
   prof_start(c);
   track(c, launch_pdl(colsum_kernel<T>, static_cast<unsigned>((d + 31) / 32), 256, 0, c.stream,
                       part, nblk, static_cast<int>(d), dw));
   note_launch(c, KK_COLSUM, -1, 1.0 * nblk * d, 4.0 * nblk * d + d * sizeof(T));
+  return nblk;
 }
 
 // ---------------------------------------------------------------------------
-// reduction of the GEMM's split tiles (fixed order over the k-ranges)
+// end of a bf16 backward: reduction of the GEMM's split tiles (fixed order over
+// the k-ranges) and the RMSNorm dw column sums, in one launch
 // ---------------------------------------------------------------------------
-// grid: (split tile, slab of 256 / (BN / 8) rows: one row per BN / 8 threads); 256
-// threads, 8 columns each
-__global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduce r) {
-  grid_dependency_sync();
-  const int rt = blockIdx.x;
+// Split tile rt, slab y of 256 / (BN / 8) rows (one row per BN / 8 threads, 8
+// columns per thread).
+__device__ __forceinline__ void tile_reduce_block(const TileReduce& r, int rt, int y) {
   const int t = r.full_units + rt;
   int pi = 0;
   while (pi + 1 < r.nprob && t >= r.p[pi + 1].tile_begin) ++pi;
@@ -326,44 +448,74 @@ __global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduce r) {
     cv[k] = (q.colv != nullptr && col + k < q.N) ? __bfloat162float(q.colv[col + k]) : 1.f;
   const int64_t slot_elems = static_cast<int64_t>(r.tile_rows) * r.BN;
   const float* base = r.part + static_cast<int64_t>(rt) * r.rem_split * slot_elems + c8;
-  {
-    const int rr = blockIdx.y * (256 / per_row) + threadIdx.x / per_row;
-    const int64_t row = m0 + rr;
-    if (row >= q.M) return;
-    const float* src = base + static_cast<int64_t>(rr) * r.BN;
-    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    // four k-ranges' loads in flight at a time; the adds keep k order
-    for (int s = 0; s < r.rem_split; s += 4) {
-      float b[4][8];
+  const int rr = y * (256 / per_row) + threadIdx.x / per_row;
+  const int64_t row = m0 + rr;
+  if (row >= q.M) return;
+  const float* src = base + static_cast<int64_t>(rr) * r.BN;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  // four k-ranges' loads in flight at a time; the adds keep k order
+  for (int s = 0; s < r.rem_split; s += 4) {
+    float b[4][8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (s + u < r.rem_split) Vec8<float>::load(src + (s + u) * slot_elems, b[u]);
+    for (int u = 0; u < 4; ++u)
+      if (s + u < r.rem_split) Vec8<float>::load(src + (s + u) * slot_elems, b[u]);
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (s + u < r.rem_split) {
+    for (int u = 0; u < 4; ++u)
+      if (s + u < r.rem_split) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) a[k] += b[u][k];
-        }
-    }
+        for (int k = 0; k < 8; ++k) a[k] += b[u][k];
+      }
+  }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) a[k] *= cv[k];
-    bf16* o = q.out + row * q.ldo + col;
-    if (col + 8 <= q.N) {
-      Vec8<bf16>::store(o, a);
-    } else {
-      for (int k = 0; col + k < q.N; ++k) o[k] = __float2bfloat16_rn(a[k]);
-    }
+  for (int k = 0; k < 8; ++k) a[k] *= cv[k];
+  bf16* o = q.out + row * q.ldo + col;
+  if (col + 8 <= q.N) {
+    Vec8<bf16>::store(o, a);
+  } else {
+    for (int k = 0; col + k < q.N; ++k) o[k] = __float2bfloat16_rn(a[k]);
   }
 }
 
-void launch_tile_reduce(Ctx& c, const TileReduce& r) {
-  const dim3 grid(static_cast<unsigned>(r.rem_tiles),
-                  static_cast<unsigned>(r.tile_rows / (256 / (r.BN / 8))));
-  const double elems = static_cast<double>(r.rem_tiles) * r.tile_rows * r.BN;
+static int reduce_slabs(const TileReduce& r) { return r.tile_rows / (256 / (r.BN / 8)); }
+
+// blocks [0, rem_tiles x slabs): split tiles; then (d + 31) / 32 blocks per dw job
+__global__ void __launch_bounds__(256) finish_kernel(const TileReduce r) {
+  grid_dependency_sync();
+  int b = static_cast<int>(blockIdx.x);
+  const int slabs = r.rem_tiles > 0 ? r.tile_rows / (256 / (r.BN / 8)) : 1;
+  const int nred = r.rem_tiles * slabs;
+  if (b < nred) {
+    tile_reduce_block(r, b / slabs, b % slabs);
+    return;
+  }
+  b -= nred;
+  for (int j = 0; j < r.ncol; ++j) {
+    const int nb = (r.col[j].d + 31) / 32;
+    if (b < nb) {
+      colsum_block(r.col[j].part, r.col[j].nblk, r.col[j].d, r.col[j].out, b);
+      return;
+    }
+    b -= nb;
+  }
+}
+
+void launch_finish(Ctx& c, const TileReduce& r) {
+  int blocks = r.rem_tiles > 0 ? r.rem_tiles * reduce_slabs(r) : 0;
+  double flops = 0, bytes = 0;
+  if (r.rem_tiles > 0) {
+    const double elems = static_cast<double>(r.rem_tiles) * r.tile_rows * r.BN;
+    flops += elems * r.rem_split;
+    bytes += elems * (4.0 * r.rem_split + 2.0);
+  }
+  for (int j = 0; j < r.ncol; ++j) {
+    blocks += static_cast<int>((r.col[j].d + 31) / 32);
+    flops += static_cast<double>(r.col[j].nblk) * r.col[j].d;
+    bytes += (4.0 * r.col[j].nblk + 2.0) * r.col[j].d;
+  }
+  if (blocks == 0) return;
   prof_start(c);
-  track(c, launch_pdl(tile_reduce_kernel, grid, 256, 0, c.stream, r));
-  note_launch(c, KK_SPLITK_REDUCE, -1, elems * r.rem_split,
-              elems * (4.0 * r.rem_split + 2.0));
+  track(c, launch_pdl(finish_kernel, static_cast<unsigned>(blocks), 256, 0, c.stream, r));
+  note_launch(c, r.rem_tiles > 0 ? KK_SPLITK_REDUCE : KK_COLSUM, -1, flops, bytes);
 }
 
 // ---------------------------------------------------------------------------
@@ -418,9 +570,10 @@ void launch_rowscale(Ctx& c, const T* in, int64_t ldi, const float* rowv, int64_
 
 #define BN_INSTANTIATE(T)                                                                        \
   template void launch_stats<T>(Ctx&, const T*, int64_t, int64_t, int, float, float*, float*);   \
-  template void launch_fold_cols<T>(Ctx&, const T*, const T*, int64_t, int64_t, T*);             \
-  template void launch_norm_bwd<T>(Ctx&, const T*, const T*, const T*, const float*, const T*,   \
-                                   int64_t, int64_t, T*, float*, int, T*);                       \
+  template void launch_stats_fold<T>(Ctx&, const T*, int64_t, int64_t, int, float, float*, float*, \
+                                     const FoldJob<T>&, const FoldJob<T>&);                    \
+  template int launch_norm_bwd<T>(Ctx&, const T*, const T*, const T*, const float*, const T*,   \
+                                  int64_t, int64_t, T*, float*, int, T*, bool);                  \
   template void launch_sigma<T>(Ctx&, const T*, int64_t, int64_t, int64_t, T*, int64_t, int);    \
   template void launch_swiglu<T>(Ctx&, const T*, const T*, int64_t, int64_t, int64_t, T*,        \
                                  int64_t);                                                       \

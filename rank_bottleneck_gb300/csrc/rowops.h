@@ -12,25 +12,43 @@ template <typename T>
 void launch_stats(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float eps, float* ss,
                   float* rstd);
 
-// out[j, k] = A[j, k] * w[k]: the RMSNorm weight folded into a down-projection.
+// out[j, k] = A[j, k] * w[k] for j < rows, k < cols (row stride cols): a norm
+// weight folded into a down-projection. A null A is no job.
 template <typename T>
-void launch_fold_cols(Ctx& c, const T* A, const T* w, int64_t rows, int64_t cols, T* out);
+struct FoldJob {
+  const T* A = nullptr;
+  const T* w = nullptr;
+  int64_t rows = 0, cols = 0;
+  T* out = nullptr;
+};
+
+// launch_stats and, in the same launch, up to two weight folds.
+template <typename T>
+void launch_stats_fold(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float eps, float* ss,
+                       float* rstd, const FoldJob<T>& f0, const FoldJob<T>& f1);
 
 // RMSNorm backward from dn' = rstd * dn (the gradient of the normalised input
 // times the row's 1/rms):
 //   dx[t, j] = dres[t, j] + dn'[t, j] w[j] - x[t, j] rstd[t]^2 sum_k(dn' w x)[t, k] / d
 //   dw[j]    = sum_t dn'[t, j] x[t, j]
-// dw is reduced deterministically through `part` (nblk x d fp32).
+// dw is reduced deterministically through `part` (nblk x d fp32): in a second
+// launch when `colsum`, else by the caller (launch_finish). Returns the rows of
+// `part` written (at most nblk).
 template <typename T>
-void launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rstd,
-                     const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw);
+int launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rstd,
+                    const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw,
+                    bool colsum);
 int norm_bwd_blocks(int num_sms);
 
-// Reduction of the GEMM's split tiles. Tiles [0, full_units) of the launch were
-// whole; tile full_units + t (t < rem_tiles) was cut into rem_split k-ranges
-// whose fp32 partial tiles sit in slots rem_split t + s, each [tile_rows][BN].
-// For those tiles out[i, j] = colv[j] * sum_s partial_s[i, j] (fixed order over
-// s, bf16 output, colv optional), clipped to the problem's M x N.
+// End of a bf16 backward, one launch: the reduction of the GEMM's split tiles
+// and the RMSNorm dw column sums.
+// Tiles [0, full_units) of the GEMM launch were whole; tile full_units + t
+// (t < rem_tiles) was cut into rem_split k-ranges whose fp32 partial tiles sit
+// in slots rem_split t + s, each [tile_rows][BN]. For those tiles
+// out[i, j] = colv[j] * sum_s partial_s[i, j] (fixed order over s, bf16
+// output, colv optional), clipped to the problem's M x N.
+// Column-sum job j: out[col] = sum_b part[b][col] over nblk rows of d columns
+// (what launch_norm_bwd leaves in `part` when it is told not to sum it).
 struct TileReduceProb {
   int64_t M, N;
   int tiles_n, tile_begin;
@@ -38,13 +56,20 @@ struct TileReduceProb {
   __nv_bfloat16* out;
   int64_t ldo;
 };
+struct ColsumJob {
+  const float* part = nullptr;
+  int nblk = 0, d = 0;
+  __nv_bfloat16* out = nullptr;
+};
 struct TileReduce {
   TileReduceProb p[kMaxProblems];
   int nprob = 0;
   int full_units = 0, rem_split = 0, rem_tiles = 0, tile_rows = 0, BN = 0;
   const float* part = nullptr;
+  ColsumJob col[2];
+  int ncol = 0;
 };
-void launch_tile_reduce(Ctx& c, const TileReduce& r);
+void launch_finish(Ctx& c, const TileReduce& r);
 
 // h = sigma(z) elementwise, rounded exactly like the GEMM epilogues round it.
 template <typename T>

@@ -216,6 +216,27 @@ def test_online_norm(lib, dtype, S):
     assert err(host(q["out1"], N), silu(z)) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("S", [4, 8])
+def test_online_norm_many_tiles(lib, S):
+    """More 256-row tiles than CTA pairs, with a ragged last tile: every pair runs
+    several tiles, so each shard's partial product cycles through the TMEM slot
+    ring across tile boundaries."""
+    from _gemmhook import run
+    rng = np.random.default_rng(40 + S)
+    M, N, K, eps = 5156, 1024, 1024, 1e-5
+    q, r = problem(rng, M, N, K, False, False, "bf16")
+    A = r["A"]
+    ss = np.stack([np.sum(A[:, s * K // S:(s + 1) * K // S] ** 2, axis=1) for s in range(S)], 1)
+    q["rowv"] = torch.from_numpy(ss.astype(np.float32)).cuda()
+    q["out0"], q["ldo"] = out_buf(M, N, "bf16")
+    q["out1"], _ = out_buf(M, N, "bf16")
+    run(lib, "norm", [q], dtype="bf16", S=S, eps=eps)
+    rms = np.sqrt(np.sum(ss, 1) / K + eps)
+    z = (A @ r["B"].T) / rms[:, None]
+    assert err(host(q["out0"], N), z) <= TOL["bf16"]
+    assert err(host(q["out1"], N), silu(z)) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_resid_and_grouped(lib, dtype):
     from _gemmhook import run
