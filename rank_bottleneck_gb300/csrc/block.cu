@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -48,7 +49,14 @@ struct Tmp {
   float* partial = nullptr;
   size_t partial_bytes = 0;
   int nblk = 0;
+  int* chain = nullptr;  // counters of the chained launches (ChainLink), kChainLinks links
 };
+
+// Chained launch pairs: an r-wide GEMM (the producer, whose tile count leaves
+// part of the GPU idle in its last round) and the up-projection that reads its
+// output. Links 0..3 are the forward's, 4..7 the backward's.
+constexpr int kChainLinks = 8;
+int64_t chain_stride(const Shape& s) { return 32 + (s.T + 127) / 128 / 32 * 32 + 32; }
 
 struct Bump {
   char* base;
@@ -135,6 +143,7 @@ void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
   if (s.dtype == BN_BF16) {
     B.partial_bytes = gemm_tc_partial_bytes(device_sms());
     B.partial = static_cast<float*>(sc.take(B.partial_bytes));
+    B.chain = static_cast<int*>(sc.take(kChainLinks * chain_stride(s) * 4));
   }
   if (saved_bytes) *saved_bytes = sv.off;
   if (scratch_bytes) *scratch_bytes = sc.off;
@@ -219,10 +228,46 @@ void* at(void* p, int64_t elems, const Shape& s) {
 }
 
 void gemm(Ctx& c, const Shape& s, const GemmLaunch& g) {
-  if (s.dtype == BN_BF16)
+  if (s.dtype == BN_BF16) {
     gemm_tc(c, g);
-  else
+  } else {
+    c.chain_out = ChainLink{};
+    c.chain_in = ChainLink{};
     gemm_simt(c, g);
+  }
+}
+
+// Chained launches (ChainLink). BN_GEMM_CHAIN=0 in the environment turns them off.
+bool chains_on(const Shape& s, const Tmp& B) {
+  static const bool off = [] {
+    const char* v = std::getenv("BN_GEMM_CHAIN");
+    return v != nullptr && v[0] == '0';
+  }();
+  return !off && s.dtype == BN_BF16 && B.chain != nullptr;
+}
+ChainLink chain_link(const Shape& s, const Tmp& B, int i) {
+  ChainLink l;
+  l.entered = B.chain + i * chain_stride(s);
+  l.rows = l.entered + 32;
+  return l;
+}
+// zero links [first, first + n) before the launches that use them
+void chain_reset(Ctx& c, const Shape& s, const Tmp& B, int first, int n) {
+  if (!chains_on(s, B)) return;
+  track(c, cudaMemsetAsync(B.chain + first * chain_stride(s), 0,
+                           static_cast<size_t>(n * chain_stride(s)) * 4, c.stream));
+}
+// the next GEMM launch produces rows for link i
+void produce(Ctx& c, const Shape& s, const Tmp& B, int i) {
+  if (chains_on(s, B)) c.chain_out = chain_link(s, B, i);
+}
+// the next GEMM launch consumes link i, filled by the launch just before it
+void consume(Ctx& c, const Shape& s, const Tmp& B, int i) {
+  if (!chains_on(s, B) || c.chain_rows_target <= 0) return;
+  ChainLink l = chain_link(s, B, i);
+  l.entered_target = c.chain_entered_target;
+  l.rows_target = c.chain_rows_target;
+  c.chain_in = l;
 }
 
 GemmLaunch launch(Epi e, const Shape& s) {
@@ -471,21 +516,30 @@ void forward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const voi
                      void* q, void* k, const Acts& A, const Tmp& B) {
   const void* x1 = x;
   const Fold f2{W->A_gu, W->w_norm2, 2 * s.r, s.d, B.A2f};
+  chain_reset(c, s, B, 0, 4);
   if (s.full()) {
     const Fold f1{W->A_qkv, W->w_norm1, 3 * s.r, s.d, B.A1f};
     DT_CALL(s, stats_fold, c, x, s, A.ss1, A.rstd1, f1, f2);
+    produce(c, s, B, 0);
     norm_down(c, s, x, A.ss1, B.A1f, 3 * s.r, A.z_qkv, A.h_qkv);
+    consume(c, s, B, 0);
     qkv_up(c, s, W, A, q, k);
+    produce(c, s, B, 1);
     plain_down(c, s, A.V, s.d, s.d, W->A_o, s.d, A.z_o, A.h_o);
+    consume(c, s, B, 1);
     o_up(c, s, W, x, A);
     x1 = A.x1;
     DT_CALL(s, stats, c, x1, s, A.ss2, A.rstd2);
   } else {
     DT_CALL(s, stats_fold, c, x1, s, A.ss2, A.rstd2, f2, Fold{});
   }
+  produce(c, s, B, 2);
   norm_down(c, s, x1, A.ss2, B.A2f, 2 * s.r, A.z_gu, A.h_gu);
+  consume(c, s, B, 2);
   gu_up(c, s, W, A, !s.ckpt);
+  produce(c, s, B, 3);
   plain_down(c, s, A.m, s.d_ff, s.ld_act, W->A_d, s.ld_ff, A.z_d, A.h_d);
+  consume(c, s, B, 3);
   down_up(c, s, W, A, x1, y);
 }
 
@@ -637,15 +691,18 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
   const int64_t T = s.T, d = s.d, r = s.r;
   Wgrads wg;
   const void* x1 = s.full() ? A.x1 : x;
+  chain_reset(c, s, B, 4, 4);
   // ---- down bottleneck: y = x1 + B_d sigma(A_d m)
   add_wgrad(c, s, wg, wgrad(d, r, T, dy, d, A.h_d, r, dW->B_d, r));
   {
     GemmLaunch g = launch(EPI_DSIGMA, s);
     g.nprob = 1;
     g.p[0] = dsigma(s, dy, d, d, W->B_d, A.z_d, r, B.dz_d, nullptr);
+    produce(c, s, B, 4);
     gemm(c, s, g);
   }
   add_wgrad(c, s, wg, wgrad(r, s.d_ff, T, B.dz_d, r, A.m, s.ld_act, dW->A_d, s.ld_ff));
+  consume(c, s, B, 4);
   {
     // dm = dz_d A_d, then the SwiGLU backward in the epilogue
     GemmLaunch g = launch(EPI_DSWIGLU, s);
@@ -673,9 +730,11 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
     g.p[0] = dsigma(s, B.dG, s.ld_act, s.d_ff, W->B_g, A.z_gu, 2 * r, B.dz_gu, A.rstd2);
     g.p[1] = dsigma(s, B.dU, s.ld_act, s.d_ff, W->B_u, at(A.z_gu, r, s), 2 * r,
                     at(B.dz_gu, r, s), A.rstd2);
+    produce(c, s, B, 5);
     gemm(c, s, g);
   }
   add_wgrad(c, s, wg, wgrad(2 * r, d, T, B.dz_gu, 2 * r, x1, d, dW->A_gu, d, W->w_norm2));
+  consume(c, s, B, 5);
   dx_gemm(c, s, B.dz_gu, 2 * r, W->A_gu, d, d, B.dn, d);
   void* dx1 = s.full() ? B.dx1 : dx;
   DT_CALL(s, normbwd, c, s, B, wg, B.dw_part2, B.dn, x1, W->w_norm2, A.rstd2, dy, dx1,
@@ -691,9 +750,11 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
     GemmLaunch g = launch(EPI_DSIGMA, s);
     g.nprob = 1;
     g.p[0] = dsigma(s, dx1, d, d, W->B_o, A.z_o, r, B.dz_o, nullptr);
+    produce(c, s, B, 6);
     gemm(c, s, g);
   }
   add_wgrad(c, s, wg, wgrad(r, d, T, B.dz_o, r, A.V, d, dW->A_o, d));
+  consume(c, s, B, 6);
   dx_gemm(c, s, B.dz_o, r, W->A_o, d, d, B.dV, d);
 
   // ---- Q / K / V bottlenecks
@@ -716,9 +777,12 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
       g.p[g.nprob++] = dsigma(s, dQKV[i], d, d, Bup[i], at(A.z_qkv, i * r, s), 3 * r,
                               at(B.dz_qkv, i * r, s), A.rstd1);
     }
+    // with a zeroed slice (dq or dk absent) not every row block is counted
+    if (g.nprob == 3) produce(c, s, B, 7);
     gemm(c, s, g);
   }
   add_wgrad(c, s, wg, wgrad(3 * r, d, T, B.dz_qkv, 3 * r, x, d, dW->A_qkv, d, W->w_norm1));
+  consume(c, s, B, 7);
   dx_gemm(c, s, B.dz_qkv, 3 * r, W->A_qkv, d, d, B.dn, d);
   DT_CALL(s, normbwd, c, s, B, wg, B.dw_part1, B.dn, x, W->w_norm1, A.rstd1, dx1, dx,
           dW->w_norm1);

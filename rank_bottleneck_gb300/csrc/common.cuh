@@ -44,6 +44,21 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // together: 11 of them).
 constexpr int kMaxProblems = 16;
 
+// Chained launches (tcgen05 engine). A producer launch counts, per row block of
+// its tiles (CG x 128 rows), the epilogue warps whose output stores of that
+// block have landed (`rows`), and its CTAs once past their grid-dependency wait
+// (`entered`). The launch right after it on the stream, the consumer, then
+// reads the producer's output as its A operand without waiting for the whole
+// producer grid: it waits for `entered` to reach entered_target (so every
+// earlier kernel is complete) and, per tile, for its row block's count to reach
+// rows_target. Its CTAs start on the SMs the producer's last round leaves idle.
+// The producer must not read what the consumer writes. Counters start at zero.
+struct ChainLink {
+  int* entered = nullptr;
+  int* rows = nullptr;
+  int entered_target = 0, rows_target = 0;
+};
+
 // Device status word bits (first word of the caller's scratch buffer).
 constexpr int kStatusTimeout = 1;
 

@@ -81,6 +81,10 @@ struct Ctx {
   float* partial = nullptr;    // split-K workspace (fp32)
   size_t partial_bytes = 0;
   int launches = 0;
+  // targets a consumer of the last tcgen05 launch waits for (ChainLink)
+  int chain_entered_target = 0, chain_rows_target = 0;
+  // links for the next tcgen05 launch (taken and cleared by it)
+  ChainLink chain_out, chain_in;
   cudaError_t err = cudaSuccess;
   int bad = 0;                 // a bn_status other than BN_OK raised inside a launcher
 };

@@ -100,6 +100,12 @@ int cta_group_for(const GemmLaunch& g) {
 
 void gemm_tc(Ctx& c, const GemmLaunch& g) {
   using namespace tc;
+  // this launch's chain links, if any (none carry over to a later launch)
+  const ChainLink chain_out = c.chain_out, chain_in = c.chain_in;
+  c.chain_out = ChainLink{};
+  c.chain_in = ChainLink{};
+  c.chain_entered_target = 0;
+  c.chain_rows_target = 0;
   int ek = epi_kind(g.epi);
   if (ek < 0 || g.nprob < 1 || g.nprob > kMaxProblems) {
     c.bad = 1;
@@ -223,18 +229,35 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
   P.total_units = units;
   double flops, bytes;
   gemm_work(g, 2, flops, bytes);
+  // chained launches: kinds that take part, every problem spanning the same row blocks
+  const bool producer = ek == K_NORM || ek == K_SIGMA || ek == K_DSIGMA;
+  const bool consumer = ek == K_STORE || ek == K_RESID || ek == K_SWIGLU || ek == K_DSWIGLU;
+  P.out = producer ? chain_out : ChainLink{};
+  P.in = consumer ? chain_in : ChainLink{};
+  int tiles_per_row_block = 0;
+  for (int i = 0; i < g.nprob; ++i) {
+    if (g.p[i].M != g.p[0].M) {
+      P.out = ChainLink{};
+      P.in = ChainLink{};
+    }
+    tiles_per_row_block += P.p[i].tiles_n;
+  }
   prof_start(c);
-  bool ok;
+  int ctas;
   if (CG == 2)
-    ok = (BN == 256) ? launch_bn256_cg2(ek, a_mn, b_mn, P, units, c.num_sms, c.stream)
-                     : launch_bn128_cg2(ek, a_mn, b_mn, P, units, c.num_sms, c.stream);
+    ctas = (BN == 256) ? launch_bn256_cg2(ek, a_mn, b_mn, P, units, c.num_sms, c.stream)
+                       : launch_bn128_cg2(ek, a_mn, b_mn, P, units, c.num_sms, c.stream);
   else
-    ok = (BN == 256) ? launch_bn256_cg1(ek, a_mn, b_mn, P, units, c.num_sms, c.stream)
-                     : launch_bn128_cg1(ek, a_mn, b_mn, P, units, c.num_sms, c.stream);
-  if (!ok) {
+    ctas = (BN == 256) ? launch_bn256_cg1(ek, a_mn, b_mn, P, units, c.num_sms, c.stream)
+                       : launch_bn128_cg1(ek, a_mn, b_mn, P, units, c.num_sms, c.stream);
+  if (ctas == 0) {
     c.bad = 5;
     return;
   }
+  // what a consumer of this launch waits for: all its CTAs past their dependency
+  // wait, and per row block one count from each epilogue warp of each tile
+  c.chain_entered_target = P.out.rows ? ctas : 0;
+  c.chain_rows_target = P.out.rows ? tiles_per_row_block * NUM_EPI_WARPS * CG : 0;
   note_launch(c, KK_GEMM_TC, static_cast<int>(g.epi), flops, bytes);
   TileReduce local;
   TileReduce& r = g.finish ? *g.finish : local;

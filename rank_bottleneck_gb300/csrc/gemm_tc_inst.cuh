@@ -9,7 +9,7 @@ namespace tc {
 namespace {
 
 template <int EK, bool AMN, bool BMN>
-bool go(const Params& P, int units, int num_sms, cudaStream_t s) {
+int go(const Params& P, int units, int num_sms, cudaStream_t s) {
   constexpr int BN = GEMM_BN, CG = GEMM_CG;
   auto k = gemm_kernel<BN, EK, AMN, BMN, CG>;
   constexpr int SMEM = Cfg<BN, EK, CG>::SMEM_BYTES;
@@ -51,7 +51,7 @@ bool go(const Params& P, int units, int num_sms, cudaStream_t s) {
     }
     max_groups = n;
   });
-  if (!usable) return false;
+  if (!usable) return 0;
   const int groups = units < max_groups ? units : max_groups;
   cfg.gridDim = dim3(groups * CG, 1, 1);
   // programmatic dependent launch (see grid_dependency_sync)
@@ -60,14 +60,14 @@ bool go(const Params& P, int units, int num_sms, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs += 1;
   cudaLaunchKernelEx(&cfg, k, P);
-  return true;
+  return groups * CG;
 }
 
 }  // namespace
 
 #define BN_CAT2(a, b, c) a##b##c
 #define BN_CAT(a, b, c) BN_CAT2(a, b, c)
-bool BN_CAT(launch_bn, GEMM_BN, BN_CAT(_cg, GEMM_CG, ))(int ek, bool a_mn, bool b_mn,
+int BN_CAT(launch_bn, GEMM_BN, BN_CAT(_cg, GEMM_CG, ))(int ek, bool a_mn, bool b_mn,
                                                         const Params& P, int units, int num_sms,
                                                         cudaStream_t s) {
   const int key = ek * 4 + (a_mn ? 2 : 0) + (b_mn ? 1 : 0);
@@ -82,7 +82,7 @@ bool BN_CAT(launch_bn, GEMM_BN, BN_CAT(_cg, GEMM_CG, ))(int ek, bool a_mn, bool 
     case K_CHAIN * 4 + 1: return go<K_CHAIN, false, true>(P, units, num_sms, s);
     case K_NORM * 4 + 0: return go<K_NORM, false, false>(P, units, num_sms, s);
     case K_SWIGLU * 4 + 0: return go<K_SWIGLU, false, false>(P, units, num_sms, s);
-    default: return false;
+    default: return 0;
   }
 }
 

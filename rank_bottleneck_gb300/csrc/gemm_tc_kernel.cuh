@@ -76,6 +76,18 @@ struct EpiShape {
   static constexpr int BYTES = NE * NT * SUB_BYTES;
 };
 
+// Chained launches (ChainLink): the kinds that may produce rows for the next
+// launch (the r-wide GEMMs) and the kinds that may consume the previous
+// launch's rows (the up-projections and the dX GEMMs).
+template <int EK>
+constexpr bool can_produce() {
+  return EK == K_NORM || EK == K_SIGMA || EK == K_DSIGMA;
+}
+template <int EK>
+constexpr bool can_consume() {
+  return EK == K_STORE || EK == K_RESID || EK == K_SWIGLU || EK == K_DSWIGLU;
+}
+
 // First epilogue warp. Online RMSNorm keeps each row's running sum in the
 // epilogue's registers, so its epilogue warps form whole warpgroups (4..11)
 // that take registers from warpgroup 0 (warps 0..3: the producer, the MMA
@@ -153,11 +165,44 @@ struct Params {
   // whole tiles fill complete rounds and the split tiles one last round.
   int full_units, rem_split;
   float* part;  // per split unit j: [CG x 128][BN] fp32 at j * CG * 128 * BN
+  ChainLink out;  // this launch produces rows for the next launch (counts them)
+  ChainLink in;   // this launch consumes the previous launch's rows (waits on them)
 };
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// orders this thread's generic-proxy accesses with its async-proxy (TMA)
+// accesses of global memory
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Bounded wait until *p >= target (acquire). On expiry: abort flag and
+// timeout status, as for the barrier waits.
+static __device__ __noinline__ bool wait_count(const int* p, int target, volatile int* abort_flag,
+                                               int* status) {
+  if (ld_acquire(p) >= target) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (ld_acquire(p) >= target) return true;
+    if ((n & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -686,7 +731,16 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
   tc_fence_after();
   // setup above touches no global memory; from here on the previous kernel's
   // results are read and its inputs may be overwritten
-  grid_dependency_sync();
+  // A chained consumer starts during its producer's last round: it triggers its
+  // own dependents but does not wait for the producer grid to finish; its roles
+  // wait below for the producer's CTAs to be past their own dependency wait
+  // (so every earlier kernel is complete) and, per tile, for the rows they read.
+  if (!can_consume<EK>() || P.in.rows == nullptr)
+    grid_dependency_sync();
+  else
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if constexpr (can_produce<EK>())
+    if (P.out.entered != nullptr && threadIdx.x == 0) red_release_add(P.out.entered, 1);
   const uint32_t tmem = *tmem_slot;
   const int nseg = num_segments<EK>(P);
 
@@ -705,10 +759,19 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
       int stage = 0;
       uint32_t ph = 0;
       int issued = 0;
-      bool ok = true;
+      bool ok = !can_consume<EK>() || P.in.entered == nullptr ||
+                wait_count(P.in.entered, P.in.entered_target, abort_flag, P.status);
       for (int u = pair; ok && u < P.total_units; u += npairs) {
         const Work w = decode<CG>(P, u);
         const Prob& pr = P.p[w.pi];
+        if (can_consume<EK>() && P.in.rows != nullptr) {
+          // the producer's tiles of these rows have all been stored
+          if (!wait_count(P.in.rows + w.m0 / (BM * CG), P.in.rows_target, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+        }
         const int m0 = static_cast<int>(w.m0) + row_off;                  // this CTA's A rows
         const int n0 = static_cast<int>(w.nb) * BN + static_cast<int>(rank) * (BN / CG);  // B rows
         for (int s = 0; ok && s < nseg; ++s) {
@@ -833,7 +896,9 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
       int e = 0;
       uint32_t eph = 0;
       int issued = 0;
-      bool ok = true;
+      bool ok = !can_consume<EK>() || P.in.entered == nullptr ||
+                wait_count(P.in.entered, P.in.entered_target, abort_flag, P.status);
+      if (can_consume<EK>() && ok && P.in.entered != nullptr) fence_proxy_async_global();
       for (int u = pair; ok && u < P.total_units; u += npairs) {
         const Work w = decode<CG>(P, u);
         const Prob& pr = P.p[w.pi];
@@ -904,6 +969,29 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         sph ^= 1u;
       }
     };
+    // Chained producer: once this warp's stores of a tile have landed, count
+    // them for the tile's row block (the next launch reads those rows). Online
+    // RMSNorm's epilogue, which must drain the next tile's shards while the MMAs
+    // run on, counts a tile when it is about to store the next one (or exits),
+    // by when the stores have long landed; the other kinds wait for their
+    // stores at the end of the tile, hidden behind the next tile's long K loop.
+    int64_t pending_rb = -1;
+    auto signal_pending = [&]() {
+      if (!can_produce<EK>() || pending_rb < 0) return;
+      if (lane == 0) {
+        bulk_wait_all();
+        fence_proxy_async_global();
+        red_release_add(P.out.rows + pending_rb, 1);
+      }
+      __syncwarp();
+      pending_rb = -1;
+    };
+    auto signal_rows = [&](const Work& w) {
+      if (can_produce<EK>() && P.out.rows != nullptr) pending_rb = w.m0 / (BM * CG);
+    };
+    // (a chained consumer's epilogue needs no wait of its own: it touches global
+    // memory only after its accumulators are complete, i.e. after the operand
+    // producer's waits)
     for (int u = pair; ok && u < P.total_units; u += npairs, ++tile_no) {
       const Work w = decode<CG>(P, u);
       const Prob& pr = P.p[w.pi];
@@ -954,6 +1042,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
           }
         }
         if (!ok) break;
+        signal_pending();
         const int rt = static_cast<int>(w.m0) + row_off + q * 32;
 #pragma unroll
         for (int k = 0; k < MYCH; ++k) {
@@ -1007,6 +1096,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
           }
           __syncwarp();
         }
+        signal_rows(w);
         continue;  // the tile is done
       } else if constexpr (EK == K_SWIGLU) {
         // G first: keep this warp's columns of it as bf16 pairs and free its slot
@@ -1281,7 +1371,12 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         prev_e = e;
         ++mine;
       }
+      if (ok) {
+        signal_rows(w);
+        signal_pending();
+      }
     }
+    if (ok) signal_pending();
     if (lane == 0) {
       bulk_wait_read<0>();
       if (E::NIN > 0 && mine > 0) mbar_arrive(smem_u32(&epi_empty[prev_e]));
