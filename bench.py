@@ -330,6 +330,16 @@ def run_ours(args, rank, local_rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg)
 
+    # activation memory: what the forward keeps for the backward (`saved`), the
+    # backward's temporaries (`scratch`), and the process's peak device allocation
+    n_saved, n_scratch = B.workspace_size(cfg)
+    act = {"saved_bytes": n_saved, "scratch_bytes": n_scratch,
+           "peak_allocated_bytes": torch.cuda.max_memory_allocated(dev)}
+    if cfg.checkpoint:
+        import dataclasses
+        act["saved_bytes_without_checkpoint"] = B.workspace_size(
+            dataclasses.replace(cfg, checkpoint=False))[0]
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -348,6 +358,7 @@ def run_ours(args, rank, local_rank, world):
                                  "nominal_dense_2250": 100 * tflops / NOMINAL_BF16_TFLOPS,
                                  "source": peak_src},
             "roofline": roof,
+            "activation_bytes": act,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": (launches[0] + launches[1]) * args.steps,
