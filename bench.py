@@ -348,7 +348,7 @@ def run_ours(args, rank, local_rank, world):
             "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) factors)",
             "config": {"workload": args.workload, "T": cfg.T, "d": cfg.d, "r": cfg.r,
                        "d_ff": cfg.d_ff, "S": cfg.S, "sigma": cfg.sigma, "kind": cfg.kind,
-                       "dense": cfg.dense, "checkpoint": cfg.checkpoint,
+                       "dense": cfg.dense, "checkpoint": cfg.checkpoint, "btp": cfg.btp,
                        "l2": "flushed before every timed step (256 MiB write, outside the step events)",
                        "parallelism": "replica per GPU" if world > 1 else "single GPU"},
             "tflops": tflops, "model_tflop_per_step": mflops / 1e12,

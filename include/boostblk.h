@@ -89,6 +89,15 @@ typedef struct {
   int32_t dense;  /* 1 = full-rank baseline block: A_* hold the dense W, B_* are NULL */
   int32_t checkpoint; /* 1 = save only the r-wide pre-activations (factorised block only) */
   float eps;      /* RMSNorm epsilon, e.g. 1e-5 */
+  /* 1 = bottleneck-aware tensor parallelism emulated over the S shards (factorised
+   * block only; BOOST page, "Move the chunk boundary to the bottleneck"): every
+   * row-parallel down-projection (also the O and down-projection ones) and every
+   * up-projection's input gradient sums S per-shard partial products in its
+   * epilogue, in shard order -- the chunk's r-wide all-reduce, 7r values per
+   * token and pass. The d_ff shards are whole 64-column blocks (the last ones one
+   * block shorter when 64 S does not divide d_ff). Results equal the plain
+   * block's up to rounding. 0 = each of those GEMMs sums over all of K at once. */
+  int32_t btp;
 } bn_block_desc;
 
 /* Parameters (forward) or their gradients (backward). Shapes, low-rank block:

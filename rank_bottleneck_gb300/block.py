@@ -32,7 +32,8 @@ class _Desc(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int64), ("r", ctypes.c_int64),
                 ("d_ff", ctypes.c_int64), ("ld_ff", ctypes.c_int64), ("S", ctypes.c_int32),
                 ("sigma", ctypes.c_int32), ("dtype", ctypes.c_int32), ("kind", ctypes.c_int32),
-                ("dense", ctypes.c_int32), ("checkpoint", ctypes.c_int32), ("eps", ctypes.c_float)]
+                ("dense", ctypes.c_int32), ("checkpoint", ctypes.c_int32), ("eps", ctypes.c_float),
+                ("btp", ctypes.c_int32)]
 
 
 class _Params(ctypes.Structure):
@@ -98,6 +99,7 @@ class BlockConfig:
     dense: bool = False
     checkpoint: bool = False
     eps: float = 1e-5
+    btp: bool = False  # bottleneck-aware tensor parallelism emulated over the S shards
 
     def __post_init__(self):
         if self.ld_ff is None:
@@ -110,7 +112,7 @@ class BlockConfig:
     def desc(self) -> _Desc:
         return _Desc(self.T, self.d, self.r, self.d_ff, self.ld_ff, self.S, SIGMAS[self.sigma],
                      BN_BF16 if self.dtype == "bf16" else BN_F32, KINDS[self.kind],
-                     int(self.dense), int(self.checkpoint), self.eps)
+                     int(self.dense), int(self.checkpoint), self.eps, int(self.btp))
 
     def param_shapes(self):
         """Logical shape of each parameter (A_d has ld_ff-strided rows)."""

@@ -26,7 +26,7 @@ thread_local char g_cuda_err[256] = "no error";
 struct Shape {
   int64_t T, d, r, d_ff, ld_ff;
   int64_t ld_act;  // row stride of the [T, d_ff] activations G, U, m, dG, dU: whole 128-byte lines
-  int S, sigma, dtype, kind, dense, ckpt;
+  int S, sigma, dtype, kind, dense, ckpt, btp;
   float eps;
   int64_t E;  // bytes per element
   bool full() const { return kind == BN_BLOCK_FULL; }
@@ -164,10 +164,12 @@ bn_status check_desc(const bn_block_desc* D, Shape& s) {
   s.dense = D->dense;
   s.ckpt = D->checkpoint;
   s.eps = D->eps;
+  s.btp = D->btp;
   if (s.dtype != BN_F32 && s.dtype != BN_BF16) return BN_ERR_INVALID_ARG;
   if (s.sigma != BN_SIGMA_IDENTITY && s.sigma != BN_SIGMA_SILU) return BN_ERR_INVALID_ARG;
   if (s.kind != BN_BLOCK_FULL && s.kind != BN_BLOCK_MLP) return BN_ERR_INVALID_ARG;
-  if ((s.dense != 0 && s.dense != 1) || (s.ckpt != 0 && s.ckpt != 1)) return BN_ERR_INVALID_ARG;
+  if ((s.dense != 0 && s.dense != 1) || (s.ckpt != 0 && s.ckpt != 1) || (s.btp != 0 && s.btp != 1))
+    return BN_ERR_INVALID_ARG;
   if (s.T < 1 || s.d < 1 || s.d_ff < 1 || s.ld_ff < s.d_ff || s.S < 1 || s.S > 16)
     return BN_ERR_INVALID_ARG;
   if (!(s.eps >= 0.f) || s.eps > 1.f) return BN_ERR_INVALID_ARG;
@@ -179,6 +181,9 @@ bn_status check_desc(const bn_block_desc* D, Shape& s) {
   if (s.d % s.S != 0 || (s.d / s.S) % 8 != 0) return BN_ERR_INVALID_ARG;
   if (s.ld_ff % 8 != 0 || (!s.dense && s.r % 8 != 0)) return BN_ERR_ALIGNMENT;
   if (s.dense && s.ckpt) return BN_ERR_UNSUPPORTED;
+  // tensor-parallel emulation of the factorised block; each shard of d_ff gets
+  // at least one 64-column block
+  if (s.btp && (s.dense || (s.d_ff + 63) / 64 < s.S)) return BN_ERR_UNSUPPORTED;
   if (s.dtype == BN_BF16 && (s.d / s.S) % 64 != 0) return BN_ERR_UNSUPPORTED;
   s.E = (s.dtype == BN_BF16) ? 2 : 4;
   return BN_OK;
@@ -491,10 +496,12 @@ void norm_down(Ctx& c, const Shape& s, const void* x, const float* ss, const voi
   gemm(c, s, g);
 }
 
-// z = X A^T, h = sigma(z)   (X [T, K] with leading dimension ldx)
+// z = X A^T, h = sigma(z)   (X [T, K] with leading dimension ldx). Emulated
+// bottleneck-aware TP: a row-parallel down-projection, the S shards' partial
+// products summed in the epilogue (the chunk's all-reduce).
 void plain_down(Ctx& c, const Shape& s, const void* X, int64_t K, int64_t ldx, const void* Adown,
                 int64_t lda, void* z, void* h) {
-  GemmLaunch g = launch(EPI_SIGMA, s);
+  GemmLaunch g = launch(s.btp ? EPI_NORM : EPI_SIGMA, s);  // EPI_NORM with no rowv: shard sum
   g.nprob = 1;
   GemmProblem& p = g.p[0];
   p.M = s.T;
@@ -633,6 +640,12 @@ void recompute(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, 
 // ---------------------------------------------------------------------------
 // backward
 // ---------------------------------------------------------------------------
+// The sigma-backward of a low-rank layer: dh = dY Bup summed over all of dY's
+// columns at once, or (emulated bottleneck-aware TP) over the S shards of the
+// column-parallel up-projection's outputs, summed in the epilogue (the
+// backward's r-wide all-reduce).
+Epi dsigma_epi(const Shape& s) { return s.btp ? EPI_SHARD_DSIGMA : EPI_DSIGMA; }
+
 // dz = (dY Bup) * sigma'(z) * rowv: one problem of a grouped DSIGMA launch
 GemmProblem dsigma(const Shape& s, const void* dY, int64_t ldy, int64_t K, const void* Bup,
                    const void* z, int64_t ldz, void* dz, const float* rowv) {
@@ -695,7 +708,7 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
   // ---- down bottleneck: y = x1 + B_d sigma(A_d m)
   add_wgrad(c, s, wg, wgrad(d, r, T, dy, d, A.h_d, r, dW->B_d, r));
   {
-    GemmLaunch g = launch(EPI_DSIGMA, s);
+    GemmLaunch g = launch(dsigma_epi(s), s);
     g.nprob = 1;
     g.p[0] = dsigma(s, dy, d, d, W->B_d, A.z_d, r, B.dz_d, nullptr);
     produce(c, s, B, 4);
@@ -725,7 +738,7 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
   add_wgrad(c, s, wg, wgrad(s.d_ff, r, T, B.dG, s.ld_act, A.h_gu, 2 * r, dW->B_g, r));
   add_wgrad(c, s, wg, wgrad(s.d_ff, r, T, B.dU, s.ld_act, at(A.h_gu, r, s), 2 * r, dW->B_u, r));
   {
-    GemmLaunch g = launch(EPI_DSIGMA, s);
+    GemmLaunch g = launch(dsigma_epi(s), s);
     g.nprob = 2;
     g.p[0] = dsigma(s, B.dG, s.ld_act, s.d_ff, W->B_g, A.z_gu, 2 * r, B.dz_gu, A.rstd2);
     g.p[1] = dsigma(s, B.dU, s.ld_act, s.d_ff, W->B_u, at(A.z_gu, r, s), 2 * r,
@@ -747,7 +760,7 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
   // ---- O bottleneck: x1 = x + B_o sigma(A_o V)
   add_wgrad(c, s, wg, wgrad(d, r, T, dx1, d, A.h_o, r, dW->B_o, r));
   {
-    GemmLaunch g = launch(EPI_DSIGMA, s);
+    GemmLaunch g = launch(dsigma_epi(s), s);
     g.nprob = 1;
     g.p[0] = dsigma(s, dx1, d, d, W->B_o, A.z_o, r, B.dz_o, nullptr);
     produce(c, s, B, 6);
@@ -768,7 +781,7 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
       add_wgrad(c, s, wg, wgrad(d, r, T, dQKV[i], d, at(A.h_qkv, i * r, s), 3 * r, dB[i], r));
   }
   {
-    GemmLaunch g = launch(EPI_DSIGMA, s);
+    GemmLaunch g = launch(dsigma_epi(s), s);
     for (int i = 0; i < 3; ++i) {
       if (dQKV[i] == nullptr) {
         zero2d(c, at(B.dz_qkv, i * r, s), 3 * r * s.E, r * s.E, T);

@@ -20,7 +20,9 @@ enum Epi : int {
   // out0 = z = acc; out1 = h = sigma(z), sigma evaluated on z as stored.
   EPI_SIGMA = 1,
   // Online RMSNorm over S emulated shards of K (see ONLINE NORM below), then as
-  // EPI_SIGMA; out1 may be null (no sigma: the dense block).
+  // EPI_SIGMA; out1 may be null (no sigma: the dense block). With rowv null: the
+  // S shards' partial products are summed with no normalisation (a row-parallel
+  // down-projection of bottleneck-aware tensor parallelism), then as EPI_SIGMA.
   EPI_NORM = 2,
   // out0 = in0 + acc (residual add).
   EPI_RESID = 3,
@@ -33,6 +35,10 @@ enum Epi : int {
   EPI_DSWIGLU = 6,
   // Two segments accumulated into one sum (K split over two operand pairs), then as EPI_STORE.
   EPI_STORE_CHAIN = 7,
+  // As EPI_DSIGMA, with K (the output dimension of the up-projection B) cut into S
+  // emulated shards whose partial products are summed in the epilogue: the
+  // r-wide all-reduce of bottleneck-aware tensor parallelism.
+  EPI_SHARD_DSIGMA = 8,
 };
 // ONLINE NORM. rowv = ss [M, S] fp32 holds each row's sum of squares over each
 // of S equal shards of K (the raw input, before the norm weight). For shard s:

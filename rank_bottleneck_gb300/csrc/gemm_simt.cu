@@ -84,14 +84,14 @@ __global__ void __launch_bounds__(THREADS) simt_kernel(const __grid_constant__ P
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = cmp[i][j] = R[i][j] = 0.f;
 
-  const int nseg = (EK == EPI_NORM) ? P.S : (EK == EPI_SWIGLU || EK == EPI_STORE_CHAIN) ? 2 : 1;
+  constexpr bool kFold = EK == EPI_NORM || EK == EPI_SHARD_DSIGMA;  // shard-summed kinds
+  const int nseg = kFold ? P.S : (EK == EPI_SWIGLU || EK == EPI_STORE_CHAIN) ? 2 : 1;
   for (int s = 0; s < nseg; ++s) {
     const int pair = (EK == EPI_SWIGLU || EK == EPI_STORE_CHAIN) ? s : 0;
     int k_lo = 0, k_hi = static_cast<int>(pr.K);
-    if (EK == EPI_NORM) {
-      const int w = static_cast<int>(pr.K) / P.S;
-      k_lo = s * w;
-      k_hi = k_lo + w;
+    if (kFold) {  // emulated shard s of K
+      k_lo = static_cast<int>(s * pr.K / P.S);
+      k_hi = static_cast<int>((s + 1) * pr.K / P.S);
     }
     if (!(EK == EPI_STORE_CHAIN && s == 1)) {
 #pragma unroll
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(THREADS) simt_kernel(const __grid_constant__ P
         acc[i][j] = __fadd_rn(acc[i][j], cmp[i][j]);
         cmp[i][j] = 0.f;
       }
-    if (EK == EPI_NORM) {
+    if (EK == EPI_NORM && pr.rowv != nullptr) {
       // Online RMSNorm: local normalisation, then the per-row correction alpha
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -145,6 +145,12 @@ __global__ void __launch_bounds__(THREADS) simt_kernel(const __grid_constant__ P
           R[i][j] = (s == 0) ? alpha * local : fmaf(alpha, local, R[i][j]);
         }
       }
+    } else if (kFold) {
+      // the shards' partial products summed in shard order (emulated all-reduce)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) R[i][j] = (s == 0) ? acc[i][j] : __fadd_rn(R[i][j], acc[i][j]);
     } else if (EK == EPI_SWIGLU && s == 0) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -179,9 +185,10 @@ __global__ void __launch_bounds__(THREADS) simt_kernel(const __grid_constant__ P
         if (pr.out[0] != nullptr) pr.out[0][row * pr.ldo[0] + col] = G;
         if (pr.out[1] != nullptr) pr.out[1][row * pr.ldo[1] + col] = U;
         pr.out[2][row * pr.ldo[2] + col] = __fmul_rn(silu_f(G), U);
-      } else if (EK == EPI_DSIGMA) {
+      } else if (EK == EPI_DSIGMA || EK == EPI_SHARD_DSIGMA) {
         const float z = pr.in[0][row * pr.ldi[0] + col];
-        pr.out[0][row * pr.ldo[0] + col] = (v * act_grad_f(z, P.sigma)) * rs;
+        const float dh = (EK == EPI_SHARD_DSIGMA) ? R[i][j] : v;
+        pr.out[0][row * pr.ldo[0] + col] = (dh * act_grad_f(z, P.sigma)) * rs;
       } else if (EK == EPI_DSWIGLU) {
         const float G = pr.in[0][row * pr.ldi[0] + col];
         const float U = pr.in[1][row * pr.ldi[1] + col];
@@ -255,6 +262,7 @@ void gemm_simt(Ctx& c, const GemmLaunch& g) {
     case EPI_DSIGMA: track(c, go<EPI_DSIGMA>(P, grid, c.stream)); break;
     case EPI_DSWIGLU: track(c, go<EPI_DSWIGLU>(P, grid, c.stream)); break;
     case EPI_STORE_CHAIN: track(c, go<EPI_STORE_CHAIN>(P, grid, c.stream)); break;
+    case EPI_SHARD_DSIGMA: track(c, go<EPI_SHARD_DSIGMA>(P, grid, c.stream)); break;
   }
   note_launch(c, KK_GEMM_FFMA, static_cast<int>(g.epi), flops, bytes);
 }

@@ -70,6 +70,7 @@ static int epi_kind(Epi e) {
     case EPI_DSIGMA: return K_DSIGMA;
     case EPI_DSWIGLU: return K_DSWIGLU;
     case EPI_STORE_CHAIN: return K_CHAIN;
+    case EPI_SHARD_DSIGMA: return K_SDSIGMA;
   }
   return -1;
 }
@@ -178,7 +179,10 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
       }
       p.nkb[j] = static_cast<int>(cdiv(q.K, BK));
     }
-    if (ek == K_NORM && (q.K % (BK * g.S) != 0)) {
+    // Online RMSNorm's shards are equal, whole k-blocks; a plain shard sum needs
+    // at least one k-block per shard
+    if ((ek == K_NORM && q.rowv != nullptr && q.K % (BK * g.S) != 0) ||
+        ((ek == K_NORM || ek == K_SDSIGMA) && (g.S < 1 || cdiv(q.K, BK) < g.S))) {
       c.bad = 3;
       return;
     }
@@ -218,7 +222,7 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     }
     p.rowv = q.rowv;
     p.colv = q.colv;
-    p.in_raw = (ek == K_DSIGMA) ? q.in[0] : nullptr;
+    p.in_raw = (ek == K_DSIGMA || ek == K_SDSIGMA) ? q.in[0] : nullptr;
     p.ldi_raw = q.ldi[0];
     p.tiles_m = static_cast<int>(cdiv(q.M, BMP));
     p.tiles_n = static_cast<int>(cdiv(q.N, BN));
@@ -230,7 +234,7 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
   double flops, bytes;
   gemm_work(g, 2, flops, bytes);
   // chained launches: kinds that take part, every problem spanning the same row blocks
-  const bool producer = ek == K_NORM || ek == K_SIGMA || ek == K_DSIGMA;
+  const bool producer = ek == K_NORM || ek == K_SIGMA || ek == K_DSIGMA || ek == K_SDSIGMA;
   const bool consumer = ek == K_STORE || ek == K_RESID || ek == K_SWIGLU || ek == K_DSWIGLU;
   P.out = producer ? chain_out : ChainLink{};
   P.in = consumer ? chain_in : ChainLink{};

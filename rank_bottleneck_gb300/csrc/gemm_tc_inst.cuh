@@ -32,7 +32,7 @@ int go(const Params& P, int units, int num_sms, cudaStream_t s) {
   static std::once_flag once;
   std::call_once(once, [&] {
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (EK == K_NORM) {
+    if (is_fold<EK>()) {
       // its warpgroups trade registers (setmaxnreg) on the assumption that every
       // thread is launched with kNormRegsLaunch of them: with fewer the trade
       // could not complete, so the kernel is not launched at all
@@ -81,6 +81,7 @@ int BN_CAT(launch_bn, GEMM_BN, BN_CAT(_cg, GEMM_CG, ))(int ek, bool a_mn, bool b
     case K_DSWIGLU * 4 + 1: return go<K_DSWIGLU, false, true>(P, units, num_sms, s);
     case K_CHAIN * 4 + 1: return go<K_CHAIN, false, true>(P, units, num_sms, s);
     case K_NORM * 4 + 0: return go<K_NORM, false, false>(P, units, num_sms, s);
+    case K_SDSIGMA * 4 + 1: return go<K_SDSIGMA, false, true>(P, units, num_sms, s);
     case K_SWIGLU * 4 + 0: return go<K_SWIGLU, false, false>(P, units, num_sms, s);
     default: return 0;
   }

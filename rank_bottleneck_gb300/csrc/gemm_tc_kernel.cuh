@@ -54,8 +54,19 @@ constexpr int EPI_N = 32;  // columns per epilogue subtile
 // epilogue kinds of the kernel template
 enum : int {
   K_STORE = 0, K_SIGMA = 2, K_NORM = 3, K_RESID = 4, K_SWIGLU = 5,
-  K_DSIGMA = 6, K_DSWIGLU = 7, K_CHAIN = 8
+  K_DSIGMA = 6, K_DSWIGLU = 7, K_CHAIN = 8, K_SDSIGMA = 9
 };
+// Shard-summed kinds: K is cut into S segments (emulated shards), each
+// segment's partial product goes to the next TMEM slot and the epilogue sums
+// them in registers -- the emulated all-reduce. K_NORM applies Online RMSNorm's
+// per-shard normalisation and correction while summing (or none, for a plain
+// row-parallel down-projection, when rowv is null) and stores z and sigma(z);
+// K_SDSIGMA sums dY B over the shards of B's output dimension and stores
+// dz = sum * sigma'(z) * rowv.
+template <int EK>
+constexpr bool is_fold() {
+  return EK == K_NORM || EK == K_SDSIGMA;
+}
 
 template <int EK>
 struct EpiShape {
@@ -81,7 +92,7 @@ struct EpiShape {
 // launch's rows (the up-projections and the dX GEMMs).
 template <int EK>
 constexpr bool can_produce() {
-  return EK == K_NORM || EK == K_SIGMA || EK == K_DSIGMA;
+  return EK == K_NORM || EK == K_SIGMA || EK == K_DSIGMA || EK == K_SDSIGMA;
 }
 template <int EK>
 constexpr bool can_consume() {
@@ -94,13 +105,13 @@ constexpr bool can_consume() {
 // issuer and two idle warps) with setmaxnreg, which acts per warpgroup.
 template <int EK>
 constexpr int epi_warp0() {
-  return EK == K_NORM ? 4 : 2;
+  return is_fold<EK>() ? 4 : 2;
 }
 // threads of a CTA: kinds without epilogue inputs leave out the input-producer
 // warp, which leaves the epilogue more registers
 template <int EK>
 constexpr int kernel_threads() {
-  return EK == K_NORM ? 32 * (4 + NUM_EPI_WARPS)
+  return is_fold<EK>() ? 32 * (4 + NUM_EPI_WARPS)
                       : (EpiShape<EK>::NIN > 0 ? NUM_THREADS : NUM_THREADS - 32);
 }
 // Online RMSNorm register split. At launch, 12 warps get 168 registers a thread
@@ -256,7 +267,7 @@ static __device__ __noinline__ bool wait_bar_call(uint32_t bar, uint32_t parity,
 template <int EK>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          int* status, unsigned long long limit_ns = kWaitLimitNs) {
-  if constexpr (EK == K_NORM)
+  if constexpr (is_fold<EK>())
     return wait_bar_inline(bar, parity, abort_flag, status, limit_ns);
   else
     return wait_bar_call(bar, parity, abort_flag, status, limit_ns);
@@ -652,16 +663,17 @@ __device__ __forceinline__ Work decode(const Params& P, int u) {
 
 template <int EK>
 __device__ __forceinline__ int num_segments(const Params& P) {
-  return EK == K_NORM ? P.S : (EK == K_SWIGLU || EK == K_CHAIN) ? 2 : 1;
+  return is_fold<EK>() ? P.S : (EK == K_SWIGLU || EK == K_CHAIN) ? 2 : 1;
 }
 // k-block range and operand pair of segment s of a unit
 template <int EK>
 __device__ __forceinline__ void segment(const Params& P, const Prob& pr, const Work& w, int s,
                                         int& kb0, int& nkb, int& pair) {
-  if (EK == K_NORM) {
-    const int per = pr.nkb[0] / P.S;
-    kb0 = s * per;
-    nkb = per;
+  if (is_fold<EK>()) {
+    // S segments of k-blocks (equal when S divides the k-blocks, as Online
+    // RMSNorm's shards require; otherwise the first ones one shorter)
+    kb0 = s * pr.nkb[0] / P.S;
+    nkb = (s + 1) * pr.nkb[0] / P.S - kb0;
     pair = 0;
   } else if (EK == K_SWIGLU || EK == K_CHAIN) {
     kb0 = 0;
@@ -747,8 +759,9 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
   // Online RMSNorm's register split is made per warpgroup, in one place for
   // each: a point where the register count differs between the branches
   // cannot be shared code.
-  if (warp == 0 || warp == 1 || warp == epi_warp0<EK>() + NUM_EPI_WARPS || (EK == K_NORM && warp < 4)) {
-  if constexpr (EK == K_NORM) setmaxnreg_dec<kNormRegsLow>();
+  if (warp == 0 || warp == 1 || warp == epi_warp0<EK>() + NUM_EPI_WARPS ||
+      (is_fold<EK>() && warp < 4)) {
+  if constexpr (is_fold<EK>()) setmaxnreg_dec<kNormRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------ operand producer
     if (lane == 0) {
@@ -938,7 +951,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
   }  // Online RMSNorm: warps 2 and 3 only lend their registers
   } else {
     // ------------------------------------------------------------ epilogue
-    if constexpr (EK == K_NORM) setmaxnreg_inc<kNormRegsHigh>();
+    if constexpr (is_fold<EK>()) setmaxnreg_inc<kNormRegsHigh>();
     const int q = warp & 3;                 // TMEM lane quarter = tile rows 32q .. 32q + 31
     const int grp = (warp - epi_warp0<EK>()) >> 2;  // this warp's subtiles: c % EPI_GROUPS == grp
     constexpr int MYCH = NCH / EPI_GROUPS;  // subtiles per warp per tile
@@ -1001,17 +1014,21 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
       const bool row_ok = row < M;
       uint32_t gpk[EK == K_SWIGLU ? MYCH : 1][16];  // SwiGLU: this warp's G, bf16 pairs
       int sl0 = slot, sl1 = slot;  // TMEM slot(s) of this tile's accumulator(s)
-      if constexpr (EK == K_NORM) {
-        // Online RMSNorm. Shard s's partial product P_s arrives in the next TMEM
-        // slot of the ring; the epilogue folds it into the running sum R, kept in
-        // registers (this thread's row, this group's columns), as
-        // R += alpha_s * (P_s / rms_s): local normalisation, then the per-row
-        // correction alpha_s = rms_s / rms_g. The slot is free again as soon as
-        // P_s is in registers, so the MMAs of shard s + 1 run during the fold.
+      if constexpr (is_fold<EK>()) {
+        // Shard s's partial product P_s arrives in the next TMEM slot of the
+        // ring; the epilogue folds it into the running sum R, kept in registers
+        // (this thread's row, this group's columns). Online RMSNorm (K_NORM with
+        // the sums of squares in rowv) folds R += alpha_s * (P_s / rms_s): local
+        // normalisation, then the per-row correction alpha_s = rms_s / rms_g.
+        // Otherwise R += P_s: the plain sum of the shards' partials. The slot is
+        // free again as soon as P_s is in registers, so the MMAs of shard s + 1
+        // run during the fold.
         const int S = P.S;
-        const float* ss = pr.rowv + (row_ok ? row : 0) * S;
+        const bool norm = EK == K_NORM && pr.rowv != nullptr;
+        const float* ss = norm ? pr.rowv + (row_ok ? row : 0) * S : nullptr;
         float tot = 0.f;
-        for (int s = 0; s < S; ++s) tot += row_ok ? ss[s] : 0.f;
+        if (norm)
+          for (int s = 0; s < S; ++s) tot += row_ok ? ss[s] : 0.f;
         const float shard_w = static_cast<float>(pr.K / S);
         const float rms_g = sqrtf(tot / static_cast<float>(pr.K) + P.eps);
         float R[MYCH][32];
@@ -1022,10 +1039,13 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
             break;
           }
           advance();
-          const float ss_s = row_ok ? ss[s] : 0.f;
-          const float rms_s = sqrtf(ss_s / shard_w + P.eps);
-          const float inv_local = 1.0f / rms_s;
-          const float alpha = rms_s / rms_g;
+          float inv_local = 1.f, alpha = 1.f;
+          if (norm) {
+            const float ss_s = row_ok ? ss[s] : 0.f;
+            const float rms_s = sqrtf(ss_s / shard_w + P.eps);
+            inv_local = 1.0f / rms_s;
+            alpha = rms_s / rms_g;
+          }
           const uint32_t tP = tmem + lane_base + static_cast<uint32_t>(sl * BN);
 #pragma unroll
           for (int k = 0; k < MYCH; ++k) {
@@ -1044,6 +1064,39 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         if (!ok) break;
         signal_pending();
         const int rt = static_cast<int>(w.m0) + row_off + q * 32;
+        if constexpr (EK == K_SDSIGMA) {
+          // dz = (sum over shards of dY_s B_s) * sigma'(z) * rowv
+          const float rs = (pr.rowv != nullptr && row_ok) ? pr.rowv[row] : 1.f;
+#pragma unroll
+          for (int k = 0; k < MYCH; ++k) {
+            // one chunk's z at a time: its loads stay below the previous chunk's
+            // stores (the running sum already holds 128 registers)
+            asm volatile("" ::: "memory");
+            const int c = k * EPI_GROUPS + grp;
+            const int64_t col0 = n0 + c * EPI_N;
+            const int e = static_cast<int>((tile_no * NCH + c) % E::NE);
+            uint8_t* ent = epi + e * E::NT * E::SUB_BYTES + q * E::WARP_BYTES;
+            float v[32];  // z, then dz in place
+            ld_row32_bf16(static_cast<const __nv_bfloat16*>(pr.in_raw), pr.ldi_raw, row, row_ok,
+                          col0, N, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = (R[k][i] * act_grad_fast(v[i], P.sigma)) * rs;
+            smem_row_store_bf16(ent, lane, v);
+            if (row_ok && col0 + EPI_N > pr.N8 && col0 < N)
+              store_tail_bf16(pr.out[0], pr.ldo[0], row, col0, pr.N8, N, v);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+              if (rt < M && col0 < pr.N8)
+                tma_store_2d(&pr.mo[0], smem_u32(ent), static_cast<int>(col0), rt);
+              bulk_commit();
+              bulk_wait_read<E::NE / EPI_GROUPS - 1>();
+            }
+            __syncwarp();
+          }
+          signal_rows(w);
+          continue;  // the tile is done
+        }
 #pragma unroll
         for (int k = 0; k < MYCH; ++k) {
           const int c = k * EPI_GROUPS + grp;
@@ -1383,7 +1436,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
       bulk_wait_all();
     }
     __syncwarp();
-    if constexpr (EK == K_NORM) setmaxnreg_dec<kNormRegsLow>();
+    if constexpr (is_fold<EK>()) setmaxnreg_dec<kNormRegsLow>();
   }
 
   tc_fence_before();

@@ -59,6 +59,8 @@ def test_workspace_sizes_and_checkpoint_saving():
     (dict(dense=True, checkpoint=True), 3),
     (dict(S=64), 1),
     (dict(d=512, S=16), 3),               # bf16 shards narrower than 64 columns
+    (dict(dense=True, btp=True), 3),      # the TP emulation is of the factorised block
+    (dict(d_ff=100, ld_ff=128, d=1024, S=4, btp=True), 3),  # fewer 64-column blocks than shards
 ])
 def test_bad_descriptors_are_rejected(lib, bad, code):
     from rank_bottleneck_gb300.block import workspace_size
