@@ -35,7 +35,7 @@ that name):
 * the pages give no backward pass; the gradients here are the plain
   derivatives of the forward definition above.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 eps = 1e-5 inside the square root of both the local and the global RMS;
 SwiGLU m = SiLU(G) * U; sigma on every factorised layer (including the gate
 and up bottlenecks, with SwiGLU's own SiLU on G on top); checkpoint mode saves

@@ -21,7 +21,7 @@ sum over shards of slice products, and ``_Comm`` counts what each all-reduce
 carries. It must reach exactly (up to fp64 rounding) what the plain block of
 ``oracle/block.py`` computes.
 
-Readings where the pages are silent (also in the design doc):
+Readings where the pages are silent:
 * the backward is the plain derivative of the same layout: a column-parallel
   up-projection's input gradient is an r-wide all-reduce of per-shard partials,
   a row-parallel down-projection's input gradient is local;

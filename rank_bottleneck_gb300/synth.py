@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the low-rank bottleneck decoder block.
+"""Seeded synthetic inputs for the low-rank bottleneck decoder block and its
+attention core.
 
 This module only draws random numbers and rounds them to the storage precision.
 It holds none of the block's arithmetic, so both the CUDA path and the fp64 CPU
@@ -72,4 +73,18 @@ def make_block_inputs(T, d, r, d_ff, *, kind="full", dense=False, dtype="bf16", 
         if dtype == "bf16":
             v = round_to_bf16(v)
         out[name] = v
+    return out
+
+
+def make_attention_inputs(B, L, H, d_head, *, seed=0, q_scale=1.0):
+    """Draw q, k, v and the upstream gradient do of the attention core, each
+    [B * L, H * d_head] ~ N(0, 1) (q times q_scale: larger values sharpen the
+    softmax), rounded to bf16. Returns {name: float32 ndarray}."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = {}
+    for name in ("q", "k", "v", "do"):
+        v = rng.standard_normal((B * L, H * d_head), dtype=np.float32)
+        if name == "q":
+            v *= np.float32(q_scale)
+        out[name] = round_to_bf16(v)
     return out
