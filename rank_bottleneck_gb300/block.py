@@ -46,7 +46,7 @@ class LaunchRecord(ctypes.Structure):
 
 
 KERNEL_NAMES = ("gemm_tcgen05", "gemm_fp32", "splitk_reduce", "norm_stats", "norm_weight_fold",
-                "rmsnorm_backward", "dw_colsum", "elementwise")
+                "rmsnorm_backward", "dw_colsum", "elementwise", "attention")
 
 _lib = None
 

@@ -1,0 +1,848 @@
+// Attention core on the tcgen05 tensor cores (sm_103a): exact multi-head
+// softmax attention, causal or not, forward and backward, d_head = 128.
+//
+// The project page of BOOST places the attention core between the grouped
+// Q/K/V up-projection and the O projection of the decoder block (section
+// "Move the chunk boundary to the bottleneck", the decoder-block figure); the
+// paper summary page cites FlashAttention for it. The arithmetic is the
+// FlashAttention one: the forward keeps a running row maximum and sum (online
+// softmax) and writes the row log-sum-exp; the backward recomputes the
+// probabilities from it.
+//
+// One kernel template, three modes, all built on one tile shape: a stationary
+// 128-row tile (one row per TMEM lane and per epilogue thread) and a stream of
+// 64-row blocks of the other side, both d_head = 128 wide.
+//   FWD   stationary Q;        blocks K_j, V_j.   S = Q K_j^T (TMEM), online
+//         softmax in registers, P (bf16) to shared memory, PV = P V_j (TMEM),
+//         O = O alpha + PV in registers.
+//   BKV   stationary K and V;  blocks Q_i, dO_i.  S^T = K Q_i^T, dP^T = V dO_i^T,
+//         P^T and dS^T (bf16) to shared memory, dV += P^T dO_i and
+//         dK += dS^T Q_i accumulated in TMEM.
+//   BQ    stationary Q and dO; blocks K_j, V_j.   S = Q K_j^T, dP = dO V_j^T,
+//         dS to shared memory, dQ += dS K_j in TMEM.
+// Per CTA (192 threads, persistent over the tiles, one CTA per SM):
+//   warp 0      TMA producer: the stationary tile(s), then a ring of NSTAGE
+//               stages of streamed blocks (plus, in BKV, the blocks' row terms);
+//   warp 1      TMEM owner (512 columns) and, from one thread, the MMA issuer;
+//   warps 2..5  elementwise: warp w owns TMEM lanes 32 (w % 4) .. + 31, one
+//               tile row per thread.
+// TMEM columns: S (and the forward's rows of P V) double-buffered so that the
+// next block's S = Q K^T runs while the current block's softmax does:
+//   [0, 128)   S of block buffers 0 and 1 (64 columns each)
+//   FWD  [128, 384)  P V of block buffers 0 and 1 (128 columns each)
+//   BKV, BQ  [128, 256)  dP of block buffers 0 and 1; [256, 384) dV; [384, 512) dK or dQ.
+// Every operand is bf16 in 128-byte-swizzled shared memory: K-major for the
+// S and dP products (rows of 64 elements per 128-byte line), and the streamed
+// blocks' same bytes read MN-major for the accumulating products (the 64
+// d_head columns of a line are the N dimension, the block's rows are K).
+// Every mbarrier wait is bounded (kWaitLimitNs): on expiry the kernel records
+// a timeout in the status word and every role unwinds.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/boostattn.h"
+#include "gemm.h"
+#include "tc_ptx.cuh"
+
+namespace bn {
+namespace attn {
+
+using namespace tc;
+
+constexpr int DH = 128;      // head width
+constexpr int BR = 128;      // rows of the stationary tile
+constexpr int BC = 64;       // rows of a streamed block
+constexpr int NSTAGE = 3;    // streamed-block ring
+constexpr int NTHREADS = 192;
+constexpr int SUB_R = BR * 128;          // one 64-column half of a stationary tile: 16 KB
+constexpr int SUB_C = BC * 128;          // one 64-column half of a streamed block: 8 KB
+constexpr int XTILE = 2 * SUB_R;         // a stationary tile: 32 KB
+constexpr int STAGE = 2 * 2 * SUB_C;     // two streamed blocks: 32 KB
+constexpr int AUX = 512;                 // BKV: 64 l2 + 64 D floats per stage
+constexpr int EBUF = BR * 128;           // a 128 x 64 bf16 elementwise tile: 16 KB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+enum Mode : int { FWD = 0, BKV = 1, BQ = 2 };
+
+template <int MODE>
+struct Lay {
+  static constexpr int NX = (MODE == FWD) ? 1 : 2;   // stationary tiles
+  static constexpr int NE = (MODE == BKV) ? 2 : 1;   // elementwise tiles (each double-buffered)
+  static constexpr int X_OFF = 0;
+  static constexpr int Y_OFF = X_OFF + NX * XTILE;
+  static constexpr int E_OFF = Y_OFF + NSTAGE * STAGE;
+  static constexpr int AUX_OFF = E_OFF + NE * 2 * EBUF;
+  static constexpr int BAR_OFF = AUX_OFF + ((MODE == BKV) ? NSTAGE * AUX : 0);
+  static constexpr int BYTES = BAR_OFF + 256;
+  static constexpr int SMEM = 1024 + BYTES;
+  static_assert(E_OFF % 1024 == 0, "elementwise tiles must be 1024-byte aligned");
+  static_assert(SMEM <= 232448, "shared memory over the per-CTA limit");
+};
+
+struct Params {
+  CUtensorMap mx[2];  // stationary operands: boxes of 64 columns x 128 rows
+  CUtensorMap my[2];  // streamed operands: boxes of 64 columns x 64 rows
+  int B, L, H, Lp;
+  int causal;
+  int ntiles;
+  float scale;        // 1 / sqrt(d_head)
+  float scale_log2;   // scale * log2(e)
+  __nv_bfloat16* out0;  // FWD: o; BKV: dv
+  __nv_bfloat16* out1;  // BKV: dk; BQ: dq
+  float* lse;           // FWD: [B H, Lp]
+  const float* l2;      // backward: lse * log2(e), [B H, Lp]
+  const float* dd;      // backward: D = rowsum(dO * O), [B H, Lp]
+  int* status;
+};
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// contiguous global -> shared copy (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                     int* status, unsigned long long limit = kWaitLimitNs) {
+  return wait_bar_call(bar, parity, abort_flag, status, limit);
+}
+
+// Tile u -> (stationary tile index, sequence*head). Causal tiles are dealt
+// heaviest first: query tiles from the end of the sequence, key tiles from
+// its start.
+template <int MODE>
+__device__ __forceinline__ void decode(const Params& P, int u, int& t, int& bh) {
+  const int BH = P.B * P.H;
+  const int nt = (P.L + BR - 1) / BR;
+  bh = u % BH;
+  t = (MODE == BKV) ? u / BH : nt - 1 - u / BH;
+}
+// streamed blocks [first, last) of tile t
+template <int MODE>
+__device__ __forceinline__ void blocks(const Params& P, int t, int& first, int& last) {
+  const int nb = (P.L + BC - 1) / BC;
+  if (MODE == BKV) {
+    first = P.causal ? (t * BR) / BC : 0;
+    last = nb;
+  } else {
+    first = 0;
+    last = P.causal ? min(nb, (t * BR + BR) / BC) : nb;
+  }
+}
+
+// One thread's 32 bf16 values (16 packed pairs) into row r, 16-byte chunks
+// 4 h .. 4 h + 3, of a 128-row x 128-byte tile with the 128-byte swizzle.
+__device__ __forceinline__ void put_row32(uint8_t* tile, int r, int h, const uint32_t* pk) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(tile + r * 128 + (((4 * h + c) ^ (r & 7)) << 4)) =
+        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// 32 fp32 values as bf16 to global memory (16-byte aligned)
+__device__ __forceinline__ void store32(__nv_bfloat16* dst, const float* v, float s) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 u;
+    u.x = pack2(v[8 * c] * s, v[8 * c + 1] * s);
+    u.y = pack2(v[8 * c + 2] * s, v[8 * c + 3] * s);
+    u.z = pack2(v[8 * c + 4] * s, v[8 * c + 5] * s);
+    u.w = pack2(v[8 * c + 6] * s, v[8 * c + 7] * s);
+    *reinterpret_cast<uint4*>(dst + 8 * c) = u;
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant__ Params P) {
+  using LY = Lay<MODE>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sX = smem + LY::X_OFF;
+  uint8_t* sY = smem + LY::Y_OFF;
+  float* sAux = reinterpret_cast<float*>(smem + LY::AUX_OFF);
+  uint8_t* sE = smem + LY::E_OFF;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
+  uint64_t* x_full = bars;
+  uint64_t* x_empty = bars + 1;
+  uint64_t* y_full = bars + 2;                // [NSTAGE]
+  uint64_t* y_empty = y_full + NSTAGE;        // [NSTAGE]
+  uint64_t* s_full = y_empty + NSTAGE;        // [2]
+  uint64_t* s_empty = s_full + 2;             // [2]
+  uint64_t* e_full = s_empty + 2;             // [2]
+  uint64_t* e_empty = e_full + 2;             // [2]  backward: accumulating MMAs done with E
+  uint64_t* a_full = e_empty + 2;             // FWD [2]: P V ready; backward [1]: tile's sums done
+  uint64_t* a_empty = a_full + 2;             // FWD [2]: P V read;  backward [1]: sums read out
+  uint64_t* drain = a_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(x_full), 1);
+    mbar_init(smem_u32(x_empty), 1);
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(smem_u32(&y_full[i]), 1);
+      mbar_init(smem_u32(&y_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s_full[i]), 1);
+      mbar_init(smem_u32(&s_empty[i]), 4);
+      mbar_init(smem_u32(&e_full[i]), 4);
+      mbar_init(smem_u32(&e_empty[i]), 1);
+      mbar_init(smem_u32(&a_full[i]), 1);
+      mbar_init(smem_u32(&a_empty[i]), 4);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc<1>(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  grid_dependency_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int i = 0; i < LY::NX; ++i) tma_prefetch_desc(&P.mx[i]);
+      for (int i = 0; i < 2; ++i) tma_prefetch_desc(&P.my[i]);
+      bool ok = true;
+      uint32_t tn = 0, jn = 0;
+      uint32_t x_loads = 0;
+      for (int u = blockIdx.x; ok && u < P.ntiles; u += gridDim.x, ++tn) {
+        int t, bh, first, last;
+        decode<MODE>(P, u, t, bh);
+        blocks<MODE>(P, t, first, last);
+        const int b = bh / P.H, col = (bh % P.H) * DH;
+        if (!bwait(smem_u32(x_empty), (tn & 1u) ^ 1u, abort_flag, P.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t xb = smem_u32(x_full);
+        mbar_expect_tx(xb, LY::NX * XTILE);
+        for (int i = 0; i < LY::NX; ++i)
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(smem_u32(sX + i * XTILE + c * SUB_R), &P.mx[i], col + 64 * c, t * BR, b, xb);
+        ++x_loads;
+        for (int j = first; j < last; ++j, ++jn) {
+          const int st = jn % NSTAGE;
+          if (!bwait(smem_u32(&y_empty[st]), ((jn / NSTAGE) & 1u) ^ 1u, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t yb = smem_u32(&y_full[st]);
+          mbar_expect_tx(yb, STAGE + (MODE == BKV ? AUX : 0));
+          uint8_t* stg = sY + st * STAGE;
+          for (int i = 0; i < 2; ++i)
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d(smem_u32(stg + i * 2 * SUB_C + c * SUB_C), &P.my[i], col + 64 * c,
+                          j * BC, b, yb);
+          if constexpr (MODE == BKV) {
+            const int64_t off = static_cast<int64_t>(bh) * P.Lp + j * BC;
+            bulk_load(smem_u32(sAux + st * (AUX / 4)), P.l2 + off, BC * 4, yb);
+            bulk_load(smem_u32(sAux + st * (AUX / 4) + BC), P.dd + off, BC * 4, yb);
+          }
+        }
+      }
+      if (!ok) {
+        // the copies in flight must land before the CTA exits
+        const unsigned long long lim = 50ull * 1000 * 1000;
+        for (uint32_t i = 0; i < NSTAGE && i < jn; ++i) {
+          const uint32_t k = jn - 1 - i;
+          bwait(smem_u32(&y_full[k % NSTAGE]), (k / NSTAGE) & 1u, abort_flag, P.status, lim);
+        }
+        if (x_loads > 0) bwait(smem_u32(x_full), (x_loads - 1) & 1u, abort_flag, P.status, lim);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_S = instr_desc(128, BC, false, false);   // S, dP: K-major B
+      constexpr uint32_t ID_A = instr_desc(128, DH, false, true);    // sums: MN-major B
+      bool ok = true;
+      uint32_t tn = 0, jn = 0;
+      // S (and dP) of streamed block number n into TMEM buffer n & 1
+      auto issue_sd = [&](uint32_t n) -> bool {
+        const int st = n % NSTAGE, bf = n & 1;
+        if (!bwait(smem_u32(&y_full[st]), (n / NSTAGE) & 1u, abort_flag, P.status)) return false;
+        if (!bwait(smem_u32(&s_empty[bf]), ((n >> 1) & 1u) ^ 1u, abort_flag, P.status)) return false;
+        tc_fence_after();
+        const uint32_t y = smem_u32(sY + st * STAGE);
+        const uint32_t x = smem_u32(sX);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16<1>(tmem + bf * BC, smem_desc(x + c * SUB_R + kk * 32, false),
+                        smem_desc(y + c * SUB_C + kk * 32, false), ID_S, (c | kk) ? 1u : 0u);
+        if constexpr (MODE != FWD) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16<1>(tmem + 128 + bf * BC,
+                          smem_desc(x + XTILE + c * SUB_R + kk * 32, false),
+                          smem_desc(y + 2 * SUB_C + c * SUB_C + kk * 32, false), ID_S,
+                          (c | kk) ? 1u : 0u);
+        }
+        mma_commit<1>(smem_u32(&s_full[bf]));
+        return true;
+      };
+      for (int u = blockIdx.x; ok && u < P.ntiles; u += gridDim.x, ++tn) {
+        int t, bh, first, last;
+        decode<MODE>(P, u, t, bh);
+        blocks<MODE>(P, t, first, last);
+        if (!bwait(smem_u32(x_full), tn & 1u, abort_flag, P.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int nblk = last - first;
+        if (!issue_sd(jn)) {
+          ok = false;
+          break;
+        }
+        for (int i = 0; i < nblk; ++i, ++jn) {
+          if (i + 1 < nblk && !issue_sd(jn + 1)) {
+            ok = false;
+            break;
+          }
+          const int st = jn % NSTAGE, bf = jn & 1;
+          if (!bwait(smem_u32(&e_full[bf]), (jn >> 1) & 1u, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          if constexpr (MODE == FWD) {
+            if (!bwait(smem_u32(&a_empty[bf]), ((jn >> 1) & 1u) ^ 1u, abort_flag, P.status)) {
+              ok = false;
+              break;
+            }
+          } else {
+            if (i == 0 && !bwait(smem_u32(&a_empty[0]), (tn & 1u) ^ 1u, abort_flag, P.status)) {
+              ok = false;
+              break;
+            }
+          }
+          tc_fence_after();
+          const uint32_t y = smem_u32(sY + st * STAGE);
+          const uint32_t e = smem_u32(sE + bf * EBUF);
+          if constexpr (MODE == FWD) {
+            // P V_j: A = P [128 x 64 keys], B = V_j read MN-major [d_head x 64 keys]
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16<1>(tmem + 128 + bf * DH, smem_desc(e + kk * 32, false),
+                          smem_desc(y + 2 * SUB_C + kk * 2048, true), ID_A, kk ? 1u : 0u);
+            mma_commit<1>(smem_u32(&a_full[bf]));
+          } else {
+            const uint32_t acc = (i > 0) ? 1u : 0u;
+            if constexpr (MODE == BKV) {
+              // dV += P^T dO_i ; dK += dS^T Q_i
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16<1>(tmem + 256, smem_desc(e + kk * 32, false),
+                            smem_desc(y + 2 * SUB_C + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16<1>(tmem + 384, smem_desc(e + 2 * EBUF + kk * 32, false),
+                            smem_desc(y + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
+            } else {
+              // dQ += dS K_j
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16<1>(tmem + 384, smem_desc(e + kk * 32, false),
+                            smem_desc(y + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
+            }
+            mma_commit<1>(smem_u32(&e_empty[bf]));
+          }
+          mma_commit<1>(smem_u32(&y_empty[st]));
+        }
+        if (!ok) break;
+        if constexpr (MODE != FWD) mma_commit<1>(smem_u32(&a_full[0]));
+        mma_commit<1>(smem_u32(x_empty));
+      }
+      // every MMA issued must complete before TMEM is released
+      mma_commit<1>(smem_u32(drain));
+      bwait(smem_u32(drain), 0, abort_flag, P.status, ok ? kWaitLimitNs : 50ull * 1000 * 1000);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise
+    const int q = warp & 3;
+    const int r = 32 * q + lane;  // this thread's tile row
+    const uint32_t lb = static_cast<uint32_t>(32 * q) << 16;
+    bool ok = true;
+    uint32_t tn = 0, jn = 0;
+    auto arrive4 = [&](uint64_t* bar) {
+      if (lane == 0) mbar_arrive(smem_u32(bar));
+    };
+    for (int u = blockIdx.x; ok && u < P.ntiles; u += gridDim.x, ++tn) {
+      int t, bh, first, last;
+      decode<MODE>(P, u, t, bh);
+      blocks<MODE>(P, t, first, last);
+      const int b = bh / P.H, col = (bh % P.H) * DH;
+      const int row = t * BR + r;                 // this thread's query (FWD, BQ) or key (BKV)
+      const int64_t grow = static_cast<int64_t>(b) * P.L + row;  // its token row
+      const bool row_ok = row < P.L;
+      if constexpr (MODE == FWD) {
+        float O[DH];
+#pragma unroll
+        for (int i = 0; i < DH; ++i) O[i] = 0.f;
+        float m = -INFINITY, l = 0.f, alpha_prev = 0.f;
+        // O = O * a + (P V of block number n)
+        auto accumulate = [&](uint32_t n, float a) -> bool {
+          const int bf = n & 1;
+          if (!bwait(smem_u32(&a_full[bf]), (n >> 1) & 1u, abort_flag, P.status)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+            tmem_ld32(tmem + lb + 128 + bf * DH + 32 * c, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) O[32 * c + i] = fmaf(O[32 * c + i], a, v[i]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          arrive4(&a_empty[bf]);
+          return true;
+        };
+        for (int j = first; j < last; ++j, ++jn) {
+          const int bf = jn & 1;
+          if (!bwait(smem_u32(&s_full[bf]), (jn >> 1) & 1u, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int k0 = j * BC;
+          const bool mask = (P.causal && k0 + BC - 1 > t * BR) || k0 + BC > P.L;
+          float mx = -INFINITY;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float v[32];
+            tmem_ld32(tmem + lb + bf * BC + 32 * h, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int key = k0 + 32 * h + i;
+              const bool vis = !mask || (key < P.L && (!P.causal || key <= row));
+              mx = vis ? fmaxf(mx, v[i] * P.scale_log2) : mx;
+            }
+          }
+          const float m_new = fmaxf(m, mx);
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+          const float alpha = exp2f(m - m_use);
+          float rs = 0.f;
+          uint8_t* e = sE + bf * EBUF;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float v[32];
+            tmem_ld32(tmem + lb + bf * BC + 32 * h, v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const int key = k0 + 32 * h + i;
+              const bool v0 = !mask || (key < P.L && (!P.causal || key <= row));
+              const bool v1 = !mask || (key + 1 < P.L && (!P.causal || key + 1 <= row));
+              const float p0 = v0 ? exp2f(fmaf(v[i], P.scale_log2, -m_use)) : 0.f;
+              const float p1 = v1 ? exp2f(fmaf(v[i + 1], P.scale_log2, -m_use)) : 0.f;
+              rs += p0 + p1;
+              pk[i / 2] = pack2(p0, p1);
+            }
+            put_row32(e, r, h, pk);
+          }
+          fence_proxy_async();
+          tc_fence_before();
+          __syncwarp();
+          arrive4(&e_full[bf]);
+          arrive4(&s_empty[bf]);
+          l = fmaf(l, alpha, rs);
+          m = m_new;
+          if (j > first && !accumulate(jn - 1, alpha_prev)) {
+            ok = false;
+            break;
+          }
+          alpha_prev = alpha;
+        }
+        if (!ok || !accumulate(jn - 1, alpha_prev)) {
+          ok = false;
+          break;
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (row_ok) {
+          __nv_bfloat16* dst = P.out0 + grow * (static_cast<int64_t>(P.H) * DH) + col;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) store32(dst + 32 * c, O + 32 * c, inv);
+        }
+        P.lse[static_cast<int64_t>(bh) * P.Lp + row] =
+            l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      } else {
+        // backward: per-row terms of the stationary rows (BQ) come from global memory
+        float lr = 0.f, dr = 0.f;
+        if constexpr (MODE == BQ) {
+          lr = P.l2[static_cast<int64_t>(bh) * P.Lp + row];
+          dr = P.dd[static_cast<int64_t>(bh) * P.Lp + row];
+        }
+        for (int j = first; j < last; ++j, ++jn) {
+          const int bf = jn & 1, st = jn % NSTAGE;
+          if (!bwait(smem_u32(&s_full[bf]), (jn >> 1) & 1u, abort_flag, P.status) ||
+              !bwait(smem_u32(&e_empty[bf]), ((jn >> 1) & 1u) ^ 1u, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          if constexpr (MODE == BKV) {
+            // the block's row terms arrived with its stage
+            if (!bwait(smem_u32(&y_full[st]), (jn / NSTAGE) & 1u, abort_flag, P.status)) {
+              ok = false;
+              break;
+            }
+          }
+          tc_fence_after();
+          const int c0 = j * BC;  // first column (query in BKV, key in BQ) of the block
+          const bool mask = (MODE == BKV)
+                                ? ((P.causal && c0 < t * BR + BR - 1) || c0 + BC > P.L ||
+                                   t * BR + BR > P.L)
+                                : ((P.causal && c0 + BC - 1 > t * BR) || c0 + BC > P.L ||
+                                   t * BR + BR > P.L);
+          const float* al = sAux + st * (AUX / 4);
+          uint8_t* e1 = sE + bf * EBUF;
+          uint8_t* e2 = sE + (LY::NE - 1) * 2 * EBUF + bf * EBUF;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float s[32], dp[32];
+            tmem_ld32(tmem + lb + bf * BC + 32 * h, s);
+            tmem_ld32(tmem + lb + 128 + bf * BC + 32 * h, dp);
+            uint32_t pp[16], pd[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float p[2], ds[2];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int cc = c0 + 32 * h + i + k;  // the other side's index
+                bool vis;
+                float lv, dv;
+                if constexpr (MODE == BKV) {
+                  vis = !mask || (cc < P.L && row_ok && (!P.causal || row <= cc));
+                  lv = al[32 * h + i + k];
+                  dv = al[BC + 32 * h + i + k];
+                } else {
+                  vis = !mask || (cc < P.L && row_ok && (!P.causal || cc <= row));
+                  lv = lr;
+                  dv = dr;
+                }
+                p[k] = vis ? exp2f(fmaf(s[i + k], P.scale_log2, -lv)) : 0.f;
+                ds[k] = p[k] * (dp[i + k] - dv);
+              }
+              pp[i / 2] = pack2(p[0], p[1]);
+              pd[i / 2] = pack2(ds[0], ds[1]);
+            }
+            if constexpr (MODE == BKV) put_row32(e1, r, h, pp);
+            put_row32(e2, r, h, pd);
+          }
+          fence_proxy_async();
+          tc_fence_before();
+          __syncwarp();
+          arrive4(&e_full[bf]);
+          arrive4(&s_empty[bf]);
+        }
+        if (!ok) break;
+        if (!bwait(smem_u32(&a_full[0]), tn & 1u, abort_flag, P.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int64_t ld = static_cast<int64_t>(P.H) * DH;
+        if constexpr (MODE == BKV) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+            tmem_ld32(tmem + lb + 256 + 32 * c, v);
+            if (row_ok) store32(P.out0 + grow * ld + col + 32 * c, v, 1.f);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(tmem + lb + 384 + 32 * c, v);
+          if (row_ok) store32(P.out1 + grow * ld + col + 32 * c, v, P.scale);
+        }
+        tc_fence_before();
+        __syncwarp();
+        arrive4(&a_empty[0]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<1>(tmem, 512);
+  }
+}
+
+// D[bh, i] = sum_e dO[i, h, e] O[i, h, e] (0 for L <= i < Lp) and
+// l2[bh, i] = lse[bh, i] log2(e): one warp per (token row, head).
+__global__ void attn_rows_kernel(const __nv_bfloat16* __restrict__ o,
+                                 const __nv_bfloat16* __restrict__ dout,
+                                 const float* __restrict__ lse, float* __restrict__ dd,
+                                 float* __restrict__ l2, int B, int L, int H, int Lp) {
+  grid_dependency_sync();
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t total = static_cast<int64_t>(B) * H * Lp;
+  if (w >= total) return;
+  const int i = static_cast<int>(w % Lp);
+  const int64_t bh = w / Lp;
+  const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
+  float acc = 0.f;
+  if (i < L) {
+    const int64_t off = (static_cast<int64_t>(b) * L + i) * (static_cast<int64_t>(H) * DH) +
+                        h * DH + lane * 4;
+    const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+    const uint2 g = *reinterpret_cast<const uint2*>(dout + off);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float2 fa = __bfloat1622float2(a2[k]), fg = __bfloat1622float2(g2[k]);
+      acc = fmaf(fa.x, fg.x, acc);
+      acc = fmaf(fa.y, fg.y, acc);
+    }
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) {
+    dd[w] = acc;
+    l2[w] = lse[w] * kLog2e;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 3-D map over [B, L, H d_head] bf16: boxes of 64 columns x `rows` token rows
+// of one sequence (rows past L read as zero), 128-byte swizzle.
+bool encode3(CUtensorMap* m, const void* ptr, const bn_attn_desc& d, uint32_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t D = static_cast<cuuint64_t>(d.H * d.d_head);
+  cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(d.L), static_cast<cuuint64_t>(d.B)};
+  cuuint64_t strides[2] = {D * 2, D * 2 * static_cast<cuuint64_t>(d.L)};
+  cuuint32_t box[3] = {64, rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sms() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+template <int MODE>
+cudaError_t launch(Ctx& c, const Params& P, double flops, double bytes) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Lay<MODE>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int grid = P.ntiles < c.num_sms ? P.ntiles : c.num_sms;
+  prof_start(c);
+  cudaError_t e = launch_pdl(attn_kernel<MODE>, dim3(grid), dim3(NTHREADS), Lay<MODE>::SMEM,
+                             c.stream, P);
+  note_launch(c, KK_ATTN, MODE, flops, bytes);
+  return e;
+}
+
+thread_local char g_err[256] = "no error";
+
+bn_status check(const bn_attn_desc* d) {
+  if (d == nullptr || d->B < 1 || d->L < 1 || d->H < 1 || d->d_head < 1 ||
+      (d->causal != 0 && d->causal != 1))
+    return BN_ERR_INVALID_ARG;
+  if (d->d_head != DH) return BN_ERR_UNSUPPORTED;
+  // 32-bit tile indices and TMA coordinates
+  const int64_t Lp = bn_attn_lse_stride(d->L);
+  if (d->B * d->H * Lp >= (int64_t(1) << 31) || d->L >= (int64_t(1) << 31) ||
+      d->H * DH >= (int64_t(1) << 24))
+    return BN_ERR_UNSUPPORTED;
+  return BN_OK;
+}
+bool aligned(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// algorithmic FLOPs of the matrix products: 4 B H d_head x (visible (i, j) pairs)
+// forward (S and P V), twice that plus the recomputed S in the backward
+double visible_pairs(const bn_attn_desc& d) {
+  const double L = static_cast<double>(d.L);
+  return static_cast<double>(d.B * d.H) * (d.causal ? L * (L + 1) / 2 : L * L);
+}
+
+}  // namespace attn
+}  // namespace bn
+
+using namespace bn;
+using namespace bn::attn;
+
+extern "C" int64_t bn_attn_lse_stride(int64_t L) { return L <= 0 ? 0 : (L + 127) / 128 * 128; }
+
+extern "C" bn_status bn_attn_workspace_size(const bn_attn_desc* d, size_t* lse_bytes,
+                                            size_t* scratch_bytes) {
+  bn_status s = check(d);
+  if (s != BN_OK) return s;
+  const size_t rows = static_cast<size_t>(d->B * d->H * bn_attn_lse_stride(d->L));
+  if (lse_bytes) *lse_bytes = rows * 4;
+  if (scratch_bytes) *scratch_bytes = 256 + 2 * rows * 4;
+  return BN_OK;
+}
+
+extern "C" bn_status bn_attn_forward(const bn_attn_desc* d, const void* q, const void* k,
+                                     const void* v, void* o, float* lse, void* scratch,
+                                     bn_stream_t stream) {
+  bn_status s = check(d);
+  if (s != BN_OK) return s;
+  for (const void* p : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(lse),
+                        static_cast<const void*>(scratch)})
+    if (!aligned(p)) return p == nullptr ? BN_ERR_INVALID_ARG : BN_ERR_ALIGNMENT;
+  Params P = {};
+  if (!encode3(&P.mx[0], q, *d, BR) || !encode3(&P.my[0], k, *d, BC) ||
+      !encode3(&P.my[1], v, *d, BC))
+    return BN_ERR_CUDA;
+  P.B = static_cast<int>(d->B);
+  P.L = static_cast<int>(d->L);
+  P.H = static_cast<int>(d->H);
+  P.Lp = static_cast<int>(bn_attn_lse_stride(d->L));
+  P.causal = d->causal;
+  P.ntiles = static_cast<int>(d->B * d->H * (P.Lp / BR));
+  P.scale = 1.f / sqrtf(static_cast<float>(DH));
+  P.scale_log2 = P.scale * kLog2e;
+  P.out0 = static_cast<__nv_bfloat16*>(o);
+  P.lse = lse;
+  P.status = static_cast<int*>(scratch);
+  Ctx c;
+  c.stream = reinterpret_cast<cudaStream_t>(stream);
+  c.num_sms = sms();
+  const double elems = static_cast<double>(d->B * d->L * d->H * DH);
+  cudaError_t e = launch<FWD>(c, P, 4.0 * DH * visible_pairs(*d),
+                              4.0 * elems * 2 + static_cast<double>(d->B * d->H * P.Lp) * 4);
+  if (e != cudaSuccess) {
+    std::snprintf(g_err, sizeof(g_err), "%s", cudaGetErrorString(e));
+    return BN_ERR_CUDA;
+  }
+  return BN_OK;
+}
+
+extern "C" bn_status bn_attn_backward(const bn_attn_desc* d, const void* q, const void* k,
+                                      const void* v, const void* o, const float* lse,
+                                      const void* dout, void* dq, void* dk, void* dv,
+                                      void* scratch, bn_stream_t stream) {
+  bn_status s = check(d);
+  if (s != BN_OK) return s;
+  for (const void* p : {q, k, v, o, static_cast<const void*>(lse), dout,
+                        static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv), static_cast<const void*>(scratch)})
+    if (!aligned(p)) return p == nullptr ? BN_ERR_INVALID_ARG : BN_ERR_ALIGNMENT;
+  const int Lp = static_cast<int>(bn_attn_lse_stride(d->L));
+  const int64_t rows = d->B * d->H * Lp;
+  float* dd = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + 256);
+  float* l2 = dd + rows;
+  Params P = {};
+  P.B = static_cast<int>(d->B);
+  P.L = static_cast<int>(d->L);
+  P.H = static_cast<int>(d->H);
+  P.Lp = Lp;
+  P.causal = d->causal;
+  P.ntiles = static_cast<int>(d->B * d->H * (Lp / BR));
+  P.scale = 1.f / sqrtf(static_cast<float>(DH));
+  P.scale_log2 = P.scale * kLog2e;
+  P.l2 = l2;
+  P.dd = dd;
+  P.status = static_cast<int*>(scratch);
+  Ctx c;
+  c.stream = reinterpret_cast<cudaStream_t>(stream);
+  c.num_sms = sms();
+  const double elems = static_cast<double>(d->B * d->L * d->H * DH);
+  const double pairs = visible_pairs(*d);
+  cudaError_t e;
+  {
+    const int64_t threads = rows * 32;
+    prof_start(c);
+    e = launch_pdl(attn_rows_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256),
+                   0, c.stream, static_cast<const __nv_bfloat16*>(o),
+                   static_cast<const __nv_bfloat16*>(dout), lse, dd, l2, P.B, P.L, P.H, Lp);
+    note_launch(c, KK_ATTN, 3, 2.0 * elems, 2.0 * elems * 2 + 3.0 * rows * 4);
+  }
+  if (e == cudaSuccess) {
+    Params K = P;
+    if (!encode3(&K.mx[0], k, *d, BR) || !encode3(&K.mx[1], v, *d, BR) ||
+        !encode3(&K.my[0], q, *d, BC) || !encode3(&K.my[1], dout, *d, BC))
+      return BN_ERR_CUDA;
+    K.out0 = static_cast<__nv_bfloat16*>(dv);
+    K.out1 = static_cast<__nv_bfloat16*>(dk);
+    e = launch<BKV>(c, K, 8.0 * DH * pairs, 6.0 * elems * 2 + 2.0 * rows * 4);
+  }
+  if (e == cudaSuccess) {
+    Params Q = P;
+    if (!encode3(&Q.mx[0], q, *d, BR) || !encode3(&Q.mx[1], dout, *d, BR) ||
+        !encode3(&Q.my[0], k, *d, BC) || !encode3(&Q.my[1], v, *d, BC))
+      return BN_ERR_CUDA;
+    Q.out1 = static_cast<__nv_bfloat16*>(dq);
+    e = launch<BQ>(c, Q, 6.0 * DH * pairs, 5.0 * elems * 2 + 2.0 * rows * 4);
+  }
+  if (e != cudaSuccess) {
+    std::snprintf(g_err, sizeof(g_err), "%s", cudaGetErrorString(e));
+    return BN_ERR_CUDA;
+  }
+  return BN_OK;
+}

@@ -105,6 +105,7 @@ enum KernelKind : int {
   KK_NORM_BWD = 5,       // RMSNorm backward
   KK_COLSUM = 6,         // dw column reduction
   KK_ELEMENTWISE = 7,    // sigma recompute / SwiGLU / row scaling
+  KK_ATTN = 8,           // attention core (epi: 0 forward, 1 dK/dV, 2 dQ, 3 row terms)
 };
 
 // Call right before a kernel launch: starts its timing record when the

@@ -8,7 +8,7 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "boostblk.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("boostblk.h", "boostattn.h")]
 
 
 @pytest.fixture(scope="module")
@@ -20,14 +20,17 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(bn_[a-z_0-9]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(bn_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_exports_every_declared_function(lib):
     names = declared_functions()
     assert "bn_block_forward" in names and "bn_block_backward" in names
+    assert "bn_attn_forward" in names and "bn_attn_backward" in names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -111,3 +114,51 @@ def test_status_strings(lib):
     for code, name in enumerate([b"BN_OK", b"BN_ERR_INVALID_ARG", b"BN_ERR_ALIGNMENT",
                                  b"BN_ERR_UNSUPPORTED", b"BN_ERR_CUDA", b"BN_ERR_TIMEOUT"]):
         assert lib.bn_status_string(code) == name
+
+
+# ---------------------------------------------------------------------------
+# attention core (include/boostattn.h)
+# ---------------------------------------------------------------------------
+
+def test_attention_workspace_sizes(lib):
+    from rank_bottleneck_gb300.attention import AttnConfig, workspace_size
+    c = AttnConfig(B=4, L=4096, H=16)
+    assert c.lse_stride == 4096
+    assert AttnConfig(B=1, L=1000, H=2).lse_stride == 1024
+    n_lse, n_scratch = workspace_size(c)
+    assert n_lse == 4 * 16 * 4096 * 4
+    assert n_scratch == 256 + 2 * n_lse
+
+
+@pytest.mark.parametrize("bad, code", [
+    (dict(B=0), 1), (dict(L=0), 1), (dict(H=0), 1), (dict(causal=2), 1),
+    (dict(d_head=64), 3),                 # only d_head = 128 is built
+])
+def test_attention_bad_descriptors(lib, bad, code):
+    from rank_bottleneck_gb300 import attention as A
+    base = dict(B=2, L=256, H=2, d_head=128, causal=1)
+    base.update(bad)
+    d = A._AttnDesc(base["B"], base["L"], base["H"], base["d_head"], base["causal"])
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert A._lib().bn_attn_workspace_size(ctypes.byref(d), ctypes.byref(a), ctypes.byref(b)) == code
+    fake = [ctypes.c_void_p(4096 * (i + 1)) for i in range(7)]
+    assert A._lib().bn_attn_forward(ctypes.byref(d), *fake) == code
+
+
+def test_attention_bad_pointers_rejected_before_launch(lib):
+    from rank_bottleneck_gb300 import attention as A
+    d = A.AttnConfig(B=2, L=256, H=2).desc()
+    ok = [ctypes.c_void_p(4096 * (i + 1)) for i in range(11)]
+    f, bw = A._lib().bn_attn_forward, A._lib().bn_attn_backward
+    for i in range(6):                    # q, k, v, o, lse, scratch
+        args = list(ok[:7])
+        args[i] = None
+        assert f(ctypes.byref(d), *args) == 1
+        args[i] = ctypes.c_void_p(4096 * 9 + 8)
+        assert f(ctypes.byref(d), *args) == 2
+    for i in range(10):                   # q, k, v, o, lse, dout, dq, dk, dv, scratch
+        args = list(ok[:11])
+        args[i] = None
+        assert bw(ctypes.byref(d), *args) == 1
+        args[i] = ctypes.c_void_p(4096 * 20 + 4)
+        assert bw(ctypes.byref(d), *args) == 2
