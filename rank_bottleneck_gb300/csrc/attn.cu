@@ -56,7 +56,7 @@ constexpr int DH = 128;      // head width
 constexpr int BR = 128;      // rows of the stationary tile
 constexpr int BC = 64;       // rows of a streamed block
 constexpr int NSTAGE = 3;    // streamed-block ring
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 elementwise
 constexpr int SUB_R = BR * 128;          // one 64-column half of a stationary tile: 16 KB
 constexpr int SUB_C = BC * 128;          // one 64-column half of a streamed block: 8 KB
 constexpr int XTILE = 2 * SUB_R;         // a stationary tile: 32 KB
@@ -76,7 +76,9 @@ struct Lay {
   static constexpr int Y_OFF = X_OFF + NX * XTILE;
   static constexpr int E_OFF = Y_OFF + NSTAGE * STAGE;
   static constexpr int AUX_OFF = E_OFF + NE * 2 * EBUF;
-  static constexpr int BAR_OFF = AUX_OFF + ((MODE == BKV) ? NSTAGE * AUX : 0);
+  static constexpr int XCH_OFF = AUX_OFF + ((MODE == BKV) ? NSTAGE * AUX : 0);
+  // FWD: row sums exchanged between the two warps of a row, [2 tile parity][2 half][128]
+  static constexpr int BAR_OFF = XCH_OFF + ((MODE == FWD) ? 2 * 2 * BR * 4 : 0);
   static constexpr int BYTES = BAR_OFF + 256;
   static constexpr int SMEM = 1024 + BYTES;
   static_assert(E_OFF % 1024 == 0, "elementwise tiles must be 1024-byte aligned");
@@ -115,6 +117,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
           "r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+// 2^x with the hardware approximation (flush-to-zero; 2^-inf = 0)
+__device__ __forceinline__ float ex2f_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                      int* status, unsigned long long limit = kWaitLimitNs) {
@@ -191,7 +199,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
   uint64_t* a_full = e_empty + 2;             // FWD [2]: P V ready; backward [1]: tile's sums done
   uint64_t* a_empty = a_full + 2;             // FWD [2]: P V read;  backward [1]: sums read out
   uint64_t* drain = a_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* lx = drain + 1;                   // FWD [4 row quarters][2 tile parity]: row sums exchanged
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lx + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -205,13 +214,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_empty[i]), 4);
-      mbar_init(smem_u32(&e_full[i]), 4);
+      mbar_init(smem_u32(&s_empty[i]), 8);
+      mbar_init(smem_u32(&e_full[i]), 8);
       mbar_init(smem_u32(&e_empty[i]), 1);
       mbar_init(smem_u32(&a_full[i]), 1);
-      mbar_init(smem_u32(&a_empty[i]), 4);
+      mbar_init(smem_u32(&a_empty[i]), 8);
     }
     mbar_init(smem_u32(drain), 1);
+    for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&lx[i]), 64);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -334,48 +344,43 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             ok = false;
             break;
           }
-          if constexpr (MODE == FWD) {
-            if (!bwait(smem_u32(&a_empty[bf]), ((jn >> 1) & 1u) ^ 1u, abort_flag, P.status)) {
-              ok = false;
-              break;
-            }
-          } else {
-            if (i == 0 && !bwait(smem_u32(&a_empty[0]), (tn & 1u) ^ 1u, abort_flag, P.status)) {
-              ok = false;
-              break;
-            }
+          // the first accumulating product of a tile overwrites its TMEM sums: they
+          // must have been read out (FWD: O alternates between two buffers by tile)
+          const int ab = (MODE == FWD) ? static_cast<int>(tn & 1u) : 0;
+          const uint32_t apar = ((MODE == FWD) ? ((tn >> 1) & 1u) : (tn & 1u)) ^ 1u;
+          if (i == 0 && !bwait(smem_u32(&a_empty[ab]), apar, abort_flag, P.status)) {
+            ok = false;
+            break;
           }
           tc_fence_after();
           const uint32_t y = smem_u32(sY + st * STAGE);
           const uint32_t e = smem_u32(sE + bf * EBUF);
+          const uint32_t acc = (i > 0) ? 1u : 0u;
           if constexpr (MODE == FWD) {
-            // P V_j: A = P [128 x 64 keys], B = V_j read MN-major [d_head x 64 keys]
+            // O += P V_j: A = P [128 x 64 keys], B = V_j read MN-major [d_head x 64 keys]
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16<1>(tmem + 128 + bf * DH, smem_desc(e + kk * 32, false),
-                          smem_desc(y + 2 * SUB_C + kk * 2048, true), ID_A, kk ? 1u : 0u);
-            mma_commit<1>(smem_u32(&a_full[bf]));
+              mma_bf16<1>(tmem + 128 + ab * DH, smem_desc(e + kk * 32, false),
+                          smem_desc(y + 2 * SUB_C + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
+          } else if constexpr (MODE == BKV) {
+            // dV += P^T dO_i ; dK += dS^T Q_i
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16<1>(tmem + 256, smem_desc(e + kk * 32, false),
+                          smem_desc(y + 2 * SUB_C + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16<1>(tmem + 384, smem_desc(e + 2 * EBUF + kk * 32, false),
+                          smem_desc(y + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
           } else {
-            const uint32_t acc = (i > 0) ? 1u : 0u;
-            if constexpr (MODE == BKV) {
-              // dV += P^T dO_i ; dK += dS^T Q_i
+            // dQ += dS K_j
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_bf16<1>(tmem + 256, smem_desc(e + kk * 32, false),
-                            smem_desc(y + 2 * SUB_C + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_bf16<1>(tmem + 384, smem_desc(e + 2 * EBUF + kk * 32, false),
-                            smem_desc(y + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
-            } else {
-              // dQ += dS K_j
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_bf16<1>(tmem + 384, smem_desc(e + kk * 32, false),
-                            smem_desc(y + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
-            }
-            mma_commit<1>(smem_u32(&e_empty[bf]));
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16<1>(tmem + 384, smem_desc(e + kk * 32, false),
+                          smem_desc(y + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
           }
+          // the E tiles of this buffer are free, and (FWD) O holds block i
+          mma_commit<1>(smem_u32(&e_empty[bf]));
           mma_commit<1>(smem_u32(&y_empty[st]));
         }
         if (!ok) break;
@@ -388,112 +393,141 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
     }
   } else {
     // ------------------------------------------------------------ elementwise
+    // Eight warps: warp w owns TMEM lanes 32 (w % 4) .. + 31 (tile rows) and
+    // column half hf of every block and of every TMEM sum. The forward's two
+    // warps of a row (w and w + 4) both read the whole block for its maximum and
+    // exchange their partial row sums once per tile (mbarrier lx).
     const int q = warp & 3;
-    const int r = 32 * q + lane;  // this thread's tile row
+    const int hf = (warp - 2) >> 2;
+    const int r = 32 * q + lane;
     const uint32_t lb = static_cast<uint32_t>(32 * q) << 16;
     bool ok = true;
     uint32_t tn = 0, jn = 0;
-    auto arrive4 = [&](uint64_t* bar) {
+    auto arrive = [&](uint64_t* bar) {
       if (lane == 0) mbar_arrive(smem_u32(bar));
     };
+    // Every lane waits; the warp goes on only if all of them saw the phase, so
+    // that no lane can reach a warp-collective tcgen05 instruction alone.
+    auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool r = bwait(smem_u32(bar), parity, abort_flag, P.status);
+      return __all_sync(0xffffffffu, r);
+    };
+    const int64_t ld = static_cast<int64_t>(P.H) * DH;
     for (int u = blockIdx.x; ok && u < P.ntiles; u += gridDim.x, ++tn) {
       int t, bh, first, last;
       decode<MODE>(P, u, t, bh);
       blocks<MODE>(P, t, first, last);
-      const int b = bh / P.H, col = (bh % P.H) * DH;
+      const int b = bh / P.H, col = (bh % P.H) * DH + 64 * hf;
       const int row = t * BR + r;                 // this thread's query (FWD, BQ) or key (BKV)
       const int64_t grow = static_cast<int64_t>(b) * P.L + row;  // its token row
       const bool row_ok = row < P.L;
+      // visibility of the other side's index c: lo <= c <= hi
+      int lo, hi;
+      if constexpr (MODE == BKV) {
+        lo = row_ok ? (P.causal ? row : 0) : P.L;
+        hi = P.L - 1;
+      } else {
+        lo = 0;
+        hi = (MODE == BQ && !row_ok) ? -1 : (P.causal ? min(row, P.L - 1) : P.L - 1);
+      }
       if constexpr (MODE == FWD) {
-        float O[DH];
-#pragma unroll
-        for (int i = 0; i < DH; ++i) O[i] = 0.f;
-        float m = -INFINITY, l = 0.f, alpha_prev = 0.f;
-        // O = O * a + (P V of block number n)
-        auto accumulate = [&](uint32_t n, float a) -> bool {
-          const int bf = n & 1;
-          if (!bwait(smem_u32(&a_full[bf]), (n >> 1) & 1u, abort_flag, P.status)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float v[32];
-            tmem_ld32(tmem + lb + 128 + bf * DH + 32 * c, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) O[32 * c + i] = fmaf(O[32 * c + i], a, v[i]);
-          }
-          tc_fence_before();
-          __syncwarp();
-          arrive4(&a_empty[bf]);
-          return true;
-        };
+        float* xl = reinterpret_cast<float*>(smem + LY::XCH_OFF);  // [2 tile parity][2 half][128]
+        const int ob = static_cast<int>(tn & 1u);                    // this tile's O buffer
+        const uint32_t ocol = 128 + ob * DH + 64 * hf;
+        float m = -INFINITY, l = 0.f;
         for (int j = first; j < last; ++j, ++jn) {
           const int bf = jn & 1;
-          if (!bwait(smem_u32(&s_full[bf]), (jn >> 1) & 1u, abort_flag, P.status)) {
+          if (!wwait(&s_full[bf], (jn >> 1) & 1u) ||
+              !wwait(&e_empty[bf], ((jn >> 1) & 1u) ^ 1u)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const int k0 = j * BC;
-          const bool mask = (P.causal && k0 + BC - 1 > t * BR) || k0 + BC > P.L;
-          float mx = -INFINITY;
+          const int c0 = j * BC + 32 * hf, c1 = j * BC + 32 * (1 - hf);
+          float x[32], y[32];
+          tmem_ld32(tmem + lb + bf * BC + 32 * hf, x);
+          tmem_ld32(tmem + lb + bf * BC + 32 * (1 - hf), y);
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float v[32];
-            tmem_ld32(tmem + lb + bf * BC + 32 * h, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int key = k0 + 32 * h + i;
-              const bool vis = !mask || (key < P.L && (!P.causal || key <= row));
-              mx = vis ? fmaxf(mx, v[i] * P.scale_log2) : mx;
-            }
+          for (int i = 0; i < 32; ++i) {
+            x[i] = (c0 + i >= lo && c0 + i <= hi) ? x[i] * P.scale_log2 : -INFINITY;
+            const float yv = (c1 + i >= lo && c1 + i <= hi) ? y[i] * P.scale_log2 : -INFINITY;
+            mx[i & 3] = fmaxf(mx[i & 3], fmaxf(x[i], yv));
           }
-          const float m_new = fmaxf(m, mx);
-          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-          const float alpha = exp2f(m - m_use);
-          float rs = 0.f;
-          uint8_t* e = sE + bf * EBUF;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float v[32];
-            tmem_ld32(tmem + lb + bf * BC + 32 * h, v);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int key = k0 + 32 * h + i;
-              const bool v0 = !mask || (key < P.L && (!P.causal || key <= row));
-              const bool v1 = !mask || (key + 1 < P.L && (!P.causal || key + 1 <= row));
-              const float p0 = v0 ? exp2f(fmaf(v[i], P.scale_log2, -m_use)) : 0.f;
-              const float p1 = v1 ? exp2f(fmaf(v[i + 1], P.scale_log2, -m_use)) : 0.f;
-              rs += p0 + p1;
-              pk[i / 2] = pack2(p0, p1);
+          const float bm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          const float m_new = fmaxf(m, bm);
+          // (a warp-wide decision: the TMEM accesses below are warp-collective;
+          // the row's other warp sees the same rows and decides the same)
+          const bool rescale = __any_sync(0xffffffffu, m_new > m + 8.f);
+          if (j == first) {
+            m = m_new;
+          } else if (rescale) {
+            // Lazy rescale: p = 2^(x - m) stays below 2^8 while the running maximum
+            // m lags the true one by at most 8; past that, O (in TMEM, complete
+            // through the previous block) and l move to the new maximum.
+            const uint32_t pj = jn - 1;
+            if (!wwait(&e_empty[pj & 1u], (pj >> 1) & 1u)) {
+              ok = false;
+              break;
             }
-            put_row32(e, r, h, pk);
+            tc_fence_after();
+            const float a = ex2f_approx(m - m_new);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              float o[32];
+              tmem_ld32(tmem + lb + ocol + 32 * c, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= a;
+              tmem_st32(tmem + lb + ocol + 32 * c, o);
+            }
+            l *= a;
+            m = m_new;
           }
+          float rs[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float p0 = ex2f_approx(x[i] - m), p1 = ex2f_approx(x[i + 1] - m);
+            rs[(i >> 1) & 3] += p0 + p1;
+            pk[i / 2] = pack2(p0, p1);
+          }
+          l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+          put_row32(sE + bf * EBUF, r, hf, pk);
           fence_proxy_async();
           tc_fence_before();
           __syncwarp();
-          arrive4(&e_full[bf]);
-          arrive4(&s_empty[bf]);
-          l = fmaf(l, alpha, rs);
-          m = m_new;
-          if (j > first && !accumulate(jn - 1, alpha_prev)) {
-            ok = false;
-            break;
-          }
-          alpha_prev = alpha;
+          arrive(&e_full[bf]);
+          arrive(&s_empty[bf]);
         }
-        if (!ok || !accumulate(jn - 1, alpha_prev)) {
+        if (!ok) break;
+        // O is complete once the tile's last product has committed
+        const uint32_t pj = jn - 1;
+        if (!wwait(&e_empty[pj & 1u], (pj >> 1) & 1u)) {
           ok = false;
           break;
         }
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        if (row_ok) {
-          __nv_bfloat16* dst = P.out0 + grow * (static_cast<int64_t>(P.H) * DH) + col;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) store32(dst + 32 * c, O + 32 * c, inv);
+        tc_fence_after();
+        float* ls = xl + ob * 2 * BR;
+        ls[hf * BR + r] = l;
+        mbar_arrive(smem_u32(&lx[2 * q + ob]));
+        if (!wwait(&lx[2 * q + ob], (tn >> 1) & 1u)) {
+          ok = false;
+          break;
         }
-        P.lse[static_cast<int64_t>(bh) * P.Lp + row] =
-            l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        const float lt = l + ls[(1 - hf) * BR + r];
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float o[32];
+          tmem_ld32(tmem + lb + ocol + 32 * c, o);
+          if (row_ok) store32(P.out0 + grow * ld + col + 32 * c, o, inv);
+        }
+        if (hf == 0)
+          P.lse[static_cast<int64_t>(bh) * P.Lp + row] =
+              lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
+        tc_fence_before();
+        __syncwarp();
+        arrive(&a_empty[ob]);
       } else {
         // backward: per-row terms of the stationary rows (BQ) come from global memory
         float lr = 0.f, dr = 0.f;
@@ -503,90 +537,84 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
         }
         for (int j = first; j < last; ++j, ++jn) {
           const int bf = jn & 1, st = jn % NSTAGE;
-          if (!bwait(smem_u32(&s_full[bf]), (jn >> 1) & 1u, abort_flag, P.status) ||
-              !bwait(smem_u32(&e_empty[bf]), ((jn >> 1) & 1u) ^ 1u, abort_flag, P.status)) {
+          if (!wwait(&s_full[bf], (jn >> 1) & 1u) ||
+              !wwait(&e_empty[bf], ((jn >> 1) & 1u) ^ 1u)) {
             ok = false;
             break;
           }
           if constexpr (MODE == BKV) {
             // the block's row terms arrived with its stage
-            if (!bwait(smem_u32(&y_full[st]), (jn / NSTAGE) & 1u, abort_flag, P.status)) {
+            if (!wwait(&y_full[st], (jn / NSTAGE) & 1u)) {
               ok = false;
               break;
             }
           }
           tc_fence_after();
-          const int c0 = j * BC;  // first column (query in BKV, key in BQ) of the block
-          const bool mask = (MODE == BKV)
-                                ? ((P.causal && c0 < t * BR + BR - 1) || c0 + BC > P.L ||
-                                   t * BR + BR > P.L)
-                                : ((P.causal && c0 + BC - 1 > t * BR) || c0 + BC > P.L ||
-                                   t * BR + BR > P.L);
-          const float* al = sAux + st * (AUX / 4);
-          uint8_t* e1 = sE + bf * EBUF;
-          uint8_t* e2 = sE + (LY::NE - 1) * 2 * EBUF + bf * EBUF;
+          const int c0 = j * BC + 32 * hf;  // first column (query in BKV, key in BQ) of the half
+          uint32_t sr[32], dr32[32];
+          tmem_ld32_nowait(tmem + lb + bf * BC + 32 * hf, sr);
+          tmem_ld32_nowait(tmem + lb + 128 + bf * BC + 32 * hf, dr32);
+          tmem_wait_ld2(sr, dr32);
+          uint32_t pp[16], pd[16];
+          const float* al = sAux + st * (AUX / 4) + 32 * hf;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float s[32], dp[32];
-            tmem_ld32(tmem + lb + bf * BC + 32 * h, s);
-            tmem_ld32(tmem + lb + 128 + bf * BC + 32 * h, dp);
-            uint32_t pp[16], pd[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              float p[2], ds[2];
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int cc = c0 + 32 * h + i + k;  // the other side's index
-                bool vis;
-                float lv, dv;
-                if constexpr (MODE == BKV) {
-                  vis = !mask || (cc < P.L && row_ok && (!P.causal || row <= cc));
-                  lv = al[32 * h + i + k];
-                  dv = al[BC + 32 * h + i + k];
-                } else {
-                  vis = !mask || (cc < P.L && row_ok && (!P.causal || cc <= row));
-                  lv = lr;
-                  dv = dr;
-                }
-                p[k] = vis ? exp2f(fmaf(s[i + k], P.scale_log2, -lv)) : 0.f;
-                ds[k] = p[k] * (dp[i + k] - dv);
-              }
-              pp[i / 2] = pack2(p[0], p[1]);
-              pd[i / 2] = pack2(ds[0], ds[1]);
+          for (int i = 0; i < 32; i += 4) {
+            float lv[4], dv[4];
+            if constexpr (MODE == BKV) {
+              const float4 a = *reinterpret_cast<const float4*>(al + i);
+              const float4 d4 = *reinterpret_cast<const float4*>(al + BC + i);
+              lv[0] = a.x; lv[1] = a.y; lv[2] = a.z; lv[3] = a.w;
+              dv[0] = d4.x; dv[1] = d4.y; dv[2] = d4.z; dv[3] = d4.w;
+            } else {
+              lv[0] = lv[1] = lv[2] = lv[3] = lr;
+              dv[0] = dv[1] = dv[2] = dv[3] = dr;
             }
-            if constexpr (MODE == BKV) put_row32(e1, r, h, pp);
-            put_row32(e2, r, h, pd);
+            float p[4], ds[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int c = c0 + i + k;
+              const float xs = (c >= lo && c <= hi)
+                                   ? fmaf(__uint_as_float(sr[i + k]), P.scale_log2, -lv[k])
+                                   : -INFINITY;
+              p[k] = ex2f_approx(xs);
+              ds[k] = p[k] * (__uint_as_float(dr32[i + k]) - dv[k]);
+            }
+            pp[i / 2] = pack2(p[0], p[1]);
+            pp[i / 2 + 1] = pack2(p[2], p[3]);
+            pd[i / 2] = pack2(ds[0], ds[1]);
+            pd[i / 2 + 1] = pack2(ds[2], ds[3]);
           }
+          if constexpr (MODE == BKV) put_row32(sE + bf * EBUF, r, hf, pp);
+          put_row32(sE + (LY::NE - 1) * 2 * EBUF + bf * EBUF, r, hf, pd);
           fence_proxy_async();
           tc_fence_before();
           __syncwarp();
-          arrive4(&e_full[bf]);
-          arrive4(&s_empty[bf]);
+          arrive(&e_full[bf]);
+          arrive(&s_empty[bf]);
         }
         if (!ok) break;
-        if (!bwait(smem_u32(&a_full[0]), tn & 1u, abort_flag, P.status)) {
+        if (!wwait(&a_full[0], tn & 1u)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int64_t ld = static_cast<int64_t>(P.H) * DH;
         if constexpr (MODE == BKV) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             float v[32];
-            tmem_ld32(tmem + lb + 256 + 32 * c, v);
+            tmem_ld32(tmem + lb + 256 + 64 * hf + 32 * c, v);
             if (row_ok) store32(P.out0 + grow * ld + col + 32 * c, v, 1.f);
           }
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           float v[32];
-          tmem_ld32(tmem + lb + 384 + 32 * c, v);
+          tmem_ld32(tmem + lb + 384 + 64 * hf + 32 * c, v);
           if (row_ok) store32(P.out1 + grow * ld + col + 32 * c, v, P.scale);
         }
         tc_fence_before();
         __syncwarp();
-        arrive4(&a_empty[0]);
+        arrive(&a_empty[0]);
       }
     }
   }
