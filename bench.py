@@ -161,16 +161,19 @@ def oracle_step(cfg, inp):
     f = {k: v.astype(np.float64) for k, v in inp.items()}
     p = {k: f[k] for k in cfg.param_shapes()}
     oc = dict(kind=cfg.kind, dense=cfg.dense, sigma=cfg.sigma, eps=cfg.eps,
-              checkpoint=cfg.checkpoint)
+              checkpoint=cfg.checkpoint, attn=cfg.attn, seq_len=cfg.seq_len or None)
     out, saved = O.block_forward(p, f["x"], oc)
-    O.block_backward(p, f["x"], saved, f["dy"], f.get("dq"), f.get("dk"), oc)
+    dq, dk = (None, None) if cfg.attn else (f.get("dq"), f.get("dk"))
+    O.block_backward(p, f["x"], saved, f["dy"], dq, dk, oc)
 
 
 def oracle_sample_cfg(cfg, rows):
+    """The workload on `rows` token rows; with the attention core inside, one
+    sequence of `rows` tokens (the oracle's attention holds rows^2 scores per head)."""
     from rank_bottleneck_gb300.block import BlockConfig
     kw = {k: getattr(cfg, k) for k in ("d", "r", "d_ff", "S", "sigma", "dtype", "kind", "dense",
-                                       "checkpoint", "eps")}
-    return BlockConfig(T=rows, **kw)
+                                       "checkpoint", "eps", "attn")}
+    return BlockConfig(T=rows, seq_len=rows if cfg.attn else 0, **kw)
 
 
 def time_oracle(cfg, rows, seed=0):
@@ -189,10 +192,13 @@ def cpu_baseline(cfg, target_s=15.0):
     t = time_oracle(cfg, rows)
     rows = int(min(max(rows * target_s / max(t, 1e-3), 128), cfg.T))
     rows = max(64, rows // 64 * 64)
+    if cfg.attn:
+        rows = min(rows, 1024)
     t = time_oracle(cfg, rows)
     return {"value": rows / t, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"{rows} of the workload's {cfg.T} token rows, one fp64 forward+backward "
-                      f"({t:.1f} s)"}
+                      f"({t:.1f} s)" + (f"; attention over one sequence of {rows} tokens (the "
+                                        f"workload's are {cfg.seq_len})" if cfg.attn else "")}
 
 
 # ---------------------------------------------------------------------------
@@ -221,12 +227,15 @@ def run_ours(args, rank, local_rank, world):
             params[n].copy_(t)
         else:
             params[n] = t
-    act_names = ["x", "dy"] + (["dq", "dk"] if cfg.kind == "full" else [])
+    # q and k leave the block (and dq, dk enter it) only when the attention core
+    # runs outside it
+    qk_io = cfg.kind == "full" and not cfg.attn
+    act_names = ["x", "dy"] + (["dq", "dk"] if qk_io else [])
     acts = {n: torch.from_numpy(inp[n]).to(dev, dt) for n in act_names}
     ws = B.Workspace(cfg, dev)
     y = torch.empty_like(acts["x"])
-    q = torch.empty_like(acts["x"]) if cfg.kind == "full" else None
-    k = torch.empty_like(acts["x"]) if cfg.kind == "full" else None
+    q = torch.empty_like(acts["x"]) if qk_io else None
+    k = torch.empty_like(acts["x"]) if qk_io else None
     dx = torch.empty_like(acts["x"])
     grads = {n: B.empty_param(cfg, n, dev) for n in cfg.param_shapes()}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -305,7 +314,7 @@ def run_ours(args, rank, local_rank, world):
             "gbs": v["bytes"] / (v["ms"] / 1e3) / 1e9 if v["ms"] > 0 else None}
     dom = max(kernels, key=lambda n: kernels[n]["ms"])
     dk = kernels[dom]
-    if dom.startswith("gemm"):
+    if dom.startswith("gemm") or dom == "attention":
         achieved = dk["flops"] / (dk["ms"] / 1e3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -349,6 +358,7 @@ def run_ours(args, rank, local_rank, world):
             "config": {"workload": args.workload, "T": cfg.T, "d": cfg.d, "r": cfg.r,
                        "d_ff": cfg.d_ff, "S": cfg.S, "sigma": cfg.sigma, "kind": cfg.kind,
                        "dense": cfg.dense, "checkpoint": cfg.checkpoint, "btp": cfg.btp,
+                       "attn": cfg.attn, "seq_len": cfg.seq_len if cfg.attn else None,
                        "l2": "flushed before every timed step (256 MiB write, outside the step events)",
                        "parallelism": "replica per GPU" if world > 1 else "single GPU"},
             "tflops": tflops, "model_tflop_per_step": mflops / 1e12,
@@ -408,7 +418,7 @@ def run_e2e(args, cfg, inp, params, ws, act_names, dev, stream, world):
                for _ in range(NB)]
     dev_in = [{n: torch.empty(host_in[0][n].shape, dtype=dt, device=dev) for n in act_names}
               for _ in range(NB)]
-    full = cfg.kind == "full"
+    full = cfg.kind == "full" and not cfg.attn
     dev_out = [{"y": torch.empty(cfg.T, cfg.d, dtype=dt, device=dev),
                 "dx": torch.empty(cfg.T, cfg.d, dtype=dt, device=dev),
                 "q": torch.empty(cfg.T, cfg.d, dtype=dt, device=dev) if full else None,
@@ -486,6 +496,8 @@ def run_reference(args, rank, world):
     t64 = time_oracle(cfg, 64)
     budget = 120.0 / max(1, args.steps + args.warmup)
     rows = int(max(8, min(cfg.T, 64 * budget / max(t64, 1e-3))))
+    if cfg.attn:
+        rows = min(rows, 1024)  # one sequence of `rows` tokens
     c = oracle_sample_cfg(cfg, rows)
     inp = make_block_inputs(c.T, c.d, c.r, c.d_ff, kind=c.kind, dense=c.dense, dtype=c.dtype, seed=0)
     for _ in range(args.warmup):

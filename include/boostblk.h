@@ -11,7 +11,8 @@
  * The block (full kind), with sigma = SiLU or identity:
  *   z_qkv = OnlineRMSNorm_S(x; w_norm1) . A_qkv^T         [T, 3r]  grouped Q/K/V down
  *   Q, K, V = sigma(z_q) B_q^T, sigma(z_k) B_k^T, sigma(z_v) B_v^T   [T, d] each
- *   x1 = x + sigma(V A_o^T) B_o^T                          (attention core excluded)
+ *   x1 = x + sigma(V A_o^T) B_o^T        (attention core outside the block; with
+ *                                          desc.attn = 1, O = attention(Q, K, V) replaces V)
  *   z_gu = OnlineRMSNorm_S(x1; w_norm2) . A_gu^T           [T, 2r]  grouped gate/up down
  *   G, U = sigma(z_g) B_g^T, sigma(z_u) B_u^T              [T, d_ff]
  *   m = SiLU(G) * U ;  y = x1 + sigma(m A_d^T) B_d^T
@@ -98,6 +99,16 @@ typedef struct {
    * block shorter when 64 S does not divide d_ff). Results equal the plain
    * block's up to rounding. 0 = each of those GEMMs sums over all of K at once. */
   int32_t btp;
+  /* 1 = the attention core runs inside the block (full kind, bf16, d a multiple
+   * of 128; see boostattn.h): T = (T / seq_len) causal sequences of seq_len
+   * tokens, d / 128 heads of 128; the O projection reads
+   * O = softmax(Q K^T / sqrt(128) + causal mask) V instead of V. The block is
+   * then the whole decoder layer: q_out, k_out (forward) and dq, dk (backward)
+   * must be NULL, and Q, K, O and the attention's row log-sum-exp join the saved
+   * activations (recomputed in checkpoint mode). 0 = the attention core runs
+   * outside: the O projection reads V, Q and K leave through q_out and k_out. */
+  int32_t attn;
+  int32_t seq_len; /* tokens per sequence when attn = 1 (T % seq_len == 0); else ignored */
 } bn_block_desc;
 
 /* Parameters (forward) or their gradients (backward). Shapes, low-rank block:
@@ -146,7 +157,8 @@ int bn_last_launch_count(void);
  * every kernel the library launches from this thread is bracketed by two CUDA
  * events on its stream and recorded with its kind (0 tcgen05 GEMM, 1 fp32 GEMM,
  * 2 split-K reduction, 3 norm statistics, 4 weight fold, 5 RMSNorm backward,
- * 6 dw column sum, 7 elementwise), its GEMM epilogue (or -1) and its
+ * 6 dw column sum, 7 elementwise, 8 attention core with epi 0 forward, 1 dK/dV,
+ * 2 dQ, 3 row terms), its GEMM epilogue (or -1) and its
  * algorithmic FLOPs and bytes (each input read once, each output written once).
  * bn_profile_stop() ends recording, waits for the recorded events, copies up to
  * max_records records (device time in ms) into `out` (host memory) and returns

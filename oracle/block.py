@@ -18,8 +18,11 @@ that name):
   Q/K/V, O, residual, pre-RMSNorm, gate/up, SwiGLU, down, residual
   -- BOOST, same section, the decoder-block figure and its caption; the layer
   set is fixed by the all-reduce volume table (3r + r + 2r + r = 7r down
-  widths, 5d + 2 d_ff up widths). The attention core is not part of the path:
-  the O projection reads V directly.
+  widths, 5d + 2 d_ff up widths). By default the attention core is not part
+  of the path and the O projection reads V directly; with cfg["attn"] the
+  causal attention core of ``oracle.attention`` runs between them (sequences
+  of cfg["seq_len"] tokens, cfg["heads"] heads, d / 128 unless given) and the
+  O projection reads its output.
 * RMSNorm is the plain definition n = x * w / sqrt(mean(x^2) + eps). Online
   RMSNorm reaches this result exactly -- BOOST, "Three supporting changes" ->
   Online RMSNorm ("gives the exact result"), and BOOST-MLSys26, core method ->
@@ -46,6 +49,8 @@ never rounded again.
 from __future__ import annotations
 
 import numpy as np
+
+from .attention import attention_backward, attention_forward
 
 EPS = 1e-5
 
@@ -180,7 +185,8 @@ def swiglu_backward(dm, G, U):
 # ----------------------------------------------------------------------------
 
 def _cfg(cfg):
-    c = dict(kind="full", dense=False, sigma="silu", eps=EPS, checkpoint=False)
+    c = dict(kind="full", dense=False, sigma="silu", eps=EPS, checkpoint=False, attn=False,
+             seq_len=None, heads=None)
     c.update(cfg or {})
     if c["dense"] and c["checkpoint"]:
         raise ValueError("low-rank activation checkpointing applies to the factorised block only")
@@ -216,6 +222,21 @@ def _down_up(p, x1, z_d, c):
     return dict(h_d=h_d, y=x1 + h_d @ p["B_d"].T)
 
 
+def _attn_shape(c, x):
+    T, d = x.shape
+    L = c["seq_len"]
+    H = c["heads"] if c["heads"] else d // 128
+    if not L or T % L or d % H:
+        raise ValueError("attn needs T % seq_len == 0 and d % heads == 0")
+    return T // L, L, H
+
+
+def _attention(a, c, x):
+    """O (and lse) from q, k, v: the attention core, when it is inside the block."""
+    Bs, L, H = _attn_shape(c, x)
+    a["o"], a["lse"] = attention_forward(a["q"], a["k"], a["v"], Bs, L, H, causal=True)
+
+
 def block_forward(p, x, cfg=None):
     """Forward of one block. Returns (outputs, saved).
 
@@ -231,11 +252,16 @@ def block_forward(p, x, cfg=None):
         if c["dense"]:
             qkv = n1 @ p["A_qkv"].T
             q, k, v = _split(qkv, 3)
-            a.update(q=q, k=k, v=v, x1=x + v @ p["A_o"].T)
+            a.update(q=q, k=k, v=v)
+            if c["attn"]:
+                _attention(a, c, x)
+            a["x1"] = x + a["o" if c["attn"] else "v"] @ p["A_o"].T
         else:
             a["z_qkv"] = n1 @ p["A_qkv"].T
             a.update(_qkv_up(p, a["z_qkv"], c))
-            a["z_o"] = a["v"] @ p["A_o"].T
+            if c["attn"]:
+                _attention(a, c, x)
+            a["z_o"] = a["o" if c["attn"] else "v"] @ p["A_o"].T
             a.update(_o_up(p, x, a["z_o"], c))
     elif c["kind"] == "mlp":
         a["x1"] = x
@@ -254,7 +280,7 @@ def block_forward(p, x, cfg=None):
         a["z_d"] = a["m"] @ p["A_d"].T
         a.update(_down_up(p, a["x1"], a["z_d"], c))
     outputs = {"y": a["y"]}
-    if c["kind"] == "full":
+    if c["kind"] == "full" and not c["attn"]:
         outputs.update(q=a["q"], k=a["k"])
     if c["checkpoint"]:
         keep = ("z_qkv", "z_o", "z_gu", "z_d") if c["kind"] == "full" else ("z_gu", "z_d")
@@ -278,6 +304,8 @@ def recompute(p, x, saved, cfg=None):
         n1, rstd1 = rmsnorm(x, p["w_norm1"], c["eps"])
         a.update(n1=n1, rstd1=rstd1)
         a.update(_qkv_up(p, a["z_qkv"], c))
+        if c["attn"]:
+            _attention(a, c, x)
         a.update(_o_up(p, x, a["z_o"], c))
     else:
         a["x1"] = x
@@ -324,18 +352,30 @@ def block_backward(p, x, saved, dy, dq=None, dk=None, cfg=None):
     if c["kind"] == "mlp":
         return dx1, g
 
-    # attention-projection half: x1 = x + O(V), V = Vproj(n1), n1 = RMSNorm(x)
+    # attention-projection half: x1 = x + O(V) (or O(attention(Q, K, V))),
+    # Q, K, V = projections of n1 = RMSNorm(x)
     dq = np.zeros((T, x.shape[1])) if dq is None else dq
     dk = np.zeros((T, x.shape[1])) if dk is None else dk
+    X_o = a["o" if c["attn"] else "v"]
+
+    def core_backward(dX):
+        """dV from the O projection's input gradient; with the attention core
+        inside, its backward gives dQ, dK, dV (dq, dk from outside are 0)."""
+        if not c["attn"]:
+            return dq, dk, dX
+        Bs, L, H = _attn_shape(c, x)
+        return attention_backward(a["q"], a["k"], a["v"], dX, Bs, L, H, causal=True)
+
     if c["dense"]:
-        g["A_o"] = dx1.T @ a["v"]
-        dv = dx1 @ p["A_o"]
+        g["A_o"] = dx1.T @ X_o
+        dq, dk, dv = core_backward(dx1 @ p["A_o"])
         dqkv = np.concatenate([dq, dk, dv], axis=1)
         g["A_qkv"] = dqkv.T @ a["n1"]
         dn1 = dqkv @ p["A_qkv"]
     else:
-        dv, g["A_o"], g["B_o"] = lowrank_backward(dx1, a["v"], a["z_o"], a["h_o"],
+        dX, g["A_o"], g["B_o"] = lowrank_backward(dx1, X_o, a["z_o"], a["h_o"],
                                                   p["A_o"], p["B_o"], s)
+        dq, dk, dv = core_backward(dX)
         A_q, A_k, A_v = np.split(p["A_qkv"], 3, axis=0)
         z_q, z_k, z_v = _split(a["z_qkv"], 3)
         h_q, h_k, h_v = _split(a["h_qkv"], 3)

@@ -33,7 +33,7 @@ class _Desc(ctypes.Structure):
                 ("d_ff", ctypes.c_int64), ("ld_ff", ctypes.c_int64), ("S", ctypes.c_int32),
                 ("sigma", ctypes.c_int32), ("dtype", ctypes.c_int32), ("kind", ctypes.c_int32),
                 ("dense", ctypes.c_int32), ("checkpoint", ctypes.c_int32), ("eps", ctypes.c_float),
-                ("btp", ctypes.c_int32)]
+                ("btp", ctypes.c_int32), ("attn", ctypes.c_int32), ("seq_len", ctypes.c_int32)]
 
 
 class _Params(ctypes.Structure):
@@ -100,6 +100,8 @@ class BlockConfig:
     checkpoint: bool = False
     eps: float = 1e-5
     btp: bool = False  # bottleneck-aware tensor parallelism emulated over the S shards
+    attn: bool = False  # the causal attention core inside the block (heads of 128)
+    seq_len: int = 0    # tokens per sequence when attn
 
     def __post_init__(self):
         if self.ld_ff is None:
@@ -112,7 +114,8 @@ class BlockConfig:
     def desc(self) -> _Desc:
         return _Desc(self.T, self.d, self.r, self.d_ff, self.ld_ff, self.S, SIGMAS[self.sigma],
                      BN_BF16 if self.dtype == "bf16" else BN_F32, KINDS[self.kind],
-                     int(self.dense), int(self.checkpoint), self.eps, int(self.btp))
+                     int(self.dense), int(self.checkpoint), self.eps, int(self.btp),
+                     int(self.attn), int(self.seq_len))
 
     def param_shapes(self):
         """Logical shape of each parameter (A_d has ld_ff-strided rows)."""
@@ -192,8 +195,9 @@ def _params_struct(cfg: BlockConfig, params) -> _Params:
 
 
 def forward(cfg: BlockConfig, params, x, ws: Workspace, y=None, q=None, k=None, stream=None):
-    """Forward pass; returns {"y": y} (+ "q", "k" for the full block)."""
-    full = cfg.kind == "full"
+    """Forward pass; returns {"y": y} (+ "q", "k" for the full block whose attention
+    core runs outside it)."""
+    full = cfg.kind == "full" and not cfg.attn
     y = torch.empty_like(x) if y is None else y
     if full:
         q = torch.empty_like(x) if q is None else q

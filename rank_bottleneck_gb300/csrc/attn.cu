@@ -43,8 +43,7 @@
 #include <cstdio>
 #include <mutex>
 
-#include "../../include/boostattn.h"
-#include "gemm.h"
+#include "attn.h"
 #include "tc_ptx.cuh"
 
 namespace bn {
@@ -757,7 +756,82 @@ double visible_pairs(const bn_attn_desc& d) {
   return static_cast<double>(d.B * d.H) * (d.causal ? L * (L + 1) / 2 : L * L);
 }
 
+
 }  // namespace attn
+
+bn_status attn_check(const bn_attn_desc& d) { return attn::check(&d); }
+size_t attn_scratch_floats(const bn_attn_desc& d) {
+  return static_cast<size_t>(2 * d.B * d.H * bn_attn_lse_stride(d.L));
+}
+
+cudaError_t attn_forward(Ctx& c, const bn_attn_desc& d, const void* q, const void* k,
+                         const void* v, void* o, float* lse, int* status) {
+  using namespace attn;
+  Params P = {};
+  if (!encode3(&P.mx[0], q, d, BR) || !encode3(&P.my[0], k, d, BC) || !encode3(&P.my[1], v, d, BC))
+    return cudaErrorInvalidValue;
+  P.B = static_cast<int>(d.B);
+  P.L = static_cast<int>(d.L);
+  P.H = static_cast<int>(d.H);
+  P.Lp = static_cast<int>(bn_attn_lse_stride(d.L));
+  P.causal = d.causal;
+  P.ntiles = static_cast<int>(d.B * d.H * (P.Lp / BR));
+  P.scale = 1.f / sqrtf(static_cast<float>(DH));
+  P.scale_log2 = P.scale * kLog2e;
+  P.out0 = static_cast<__nv_bfloat16*>(o);
+  P.lse = lse;
+  P.status = status;
+  const double elems = static_cast<double>(d.B * d.L * d.H * DH);
+  return launch<FWD>(c, P, 4.0 * DH * visible_pairs(d),
+                     4.0 * elems * 2 + static_cast<double>(d.B * d.H * P.Lp) * 4);
+}
+
+cudaError_t attn_backward(Ctx& c, const bn_attn_desc& d, const void* q, const void* k,
+                          const void* v, const void* o, const float* lse, const void* dout,
+                          void* dq, void* dk, void* dv, float* rows_scratch, int* status) {
+  using namespace attn;
+  const int Lp = static_cast<int>(bn_attn_lse_stride(d.L));
+  const int64_t rows = d.B * d.H * Lp;
+  float* dd = rows_scratch;
+  float* l2 = dd + rows;
+  Params P = {};
+  P.B = static_cast<int>(d.B);
+  P.L = static_cast<int>(d.L);
+  P.H = static_cast<int>(d.H);
+  P.Lp = Lp;
+  P.causal = d.causal;
+  P.ntiles = static_cast<int>(d.B * d.H * (Lp / BR));
+  P.scale = 1.f / sqrtf(static_cast<float>(DH));
+  P.scale_log2 = P.scale * kLog2e;
+  P.l2 = l2;
+  P.dd = dd;
+  P.status = status;
+  const double elems = static_cast<double>(d.B * d.L * d.H * DH);
+  const double pairs = visible_pairs(d);
+  const int64_t threads = rows * 32;
+  prof_start(c);
+  cudaError_t e = launch_pdl(attn_rows_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)),
+                             dim3(256), 0, c.stream, static_cast<const __nv_bfloat16*>(o),
+                             static_cast<const __nv_bfloat16*>(dout), lse, dd, l2, P.B, P.L, P.H,
+                             Lp);
+  note_launch(c, KK_ATTN, 3, 2.0 * elems, 2.0 * elems * 2 + 3.0 * rows * 4);
+  if (e != cudaSuccess) return e;
+  Params K = P;
+  if (!encode3(&K.mx[0], k, d, BR) || !encode3(&K.mx[1], v, d, BR) ||
+      !encode3(&K.my[0], q, d, BC) || !encode3(&K.my[1], dout, d, BC))
+    return cudaErrorInvalidValue;
+  K.out0 = static_cast<__nv_bfloat16*>(dv);
+  K.out1 = static_cast<__nv_bfloat16*>(dk);
+  e = launch<BKV>(c, K, 8.0 * DH * pairs, 6.0 * elems * 2 + 2.0 * rows * 4);
+  if (e != cudaSuccess) return e;
+  Params Q = P;
+  if (!encode3(&Q.mx[0], q, d, BR) || !encode3(&Q.mx[1], dout, d, BR) ||
+      !encode3(&Q.my[0], k, d, BC) || !encode3(&Q.my[1], v, d, BC))
+    return cudaErrorInvalidValue;
+  Q.out1 = static_cast<__nv_bfloat16*>(dq);
+  return launch<BQ>(c, Q, 6.0 * DH * pairs, 5.0 * elems * 2 + 2.0 * rows * 4);
+}
+
 }  // namespace bn
 
 using namespace bn;
@@ -783,27 +857,10 @@ extern "C" bn_status bn_attn_forward(const bn_attn_desc* d, const void* q, const
   for (const void* p : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(lse),
                         static_cast<const void*>(scratch)})
     if (!aligned(p)) return p == nullptr ? BN_ERR_INVALID_ARG : BN_ERR_ALIGNMENT;
-  Params P = {};
-  if (!encode3(&P.mx[0], q, *d, BR) || !encode3(&P.my[0], k, *d, BC) ||
-      !encode3(&P.my[1], v, *d, BC))
-    return BN_ERR_CUDA;
-  P.B = static_cast<int>(d->B);
-  P.L = static_cast<int>(d->L);
-  P.H = static_cast<int>(d->H);
-  P.Lp = static_cast<int>(bn_attn_lse_stride(d->L));
-  P.causal = d->causal;
-  P.ntiles = static_cast<int>(d->B * d->H * (P.Lp / BR));
-  P.scale = 1.f / sqrtf(static_cast<float>(DH));
-  P.scale_log2 = P.scale * kLog2e;
-  P.out0 = static_cast<__nv_bfloat16*>(o);
-  P.lse = lse;
-  P.status = static_cast<int*>(scratch);
   Ctx c;
   c.stream = reinterpret_cast<cudaStream_t>(stream);
   c.num_sms = sms();
-  const double elems = static_cast<double>(d->B * d->L * d->H * DH);
-  cudaError_t e = launch<FWD>(c, P, 4.0 * DH * visible_pairs(*d),
-                              4.0 * elems * 2 + static_cast<double>(d->B * d->H * P.Lp) * 4);
+  const cudaError_t e = attn_forward(c, *d, q, k, v, o, lse, static_cast<int*>(scratch));
   if (e != cudaSuccess) {
     std::snprintf(g_err, sizeof(g_err), "%s", cudaGetErrorString(e));
     return BN_ERR_CUDA;
@@ -821,53 +878,12 @@ extern "C" bn_status bn_attn_backward(const bn_attn_desc* d, const void* q, cons
                         static_cast<const void*>(dq), static_cast<const void*>(dk),
                         static_cast<const void*>(dv), static_cast<const void*>(scratch)})
     if (!aligned(p)) return p == nullptr ? BN_ERR_INVALID_ARG : BN_ERR_ALIGNMENT;
-  const int Lp = static_cast<int>(bn_attn_lse_stride(d->L));
-  const int64_t rows = d->B * d->H * Lp;
-  float* dd = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + 256);
-  float* l2 = dd + rows;
-  Params P = {};
-  P.B = static_cast<int>(d->B);
-  P.L = static_cast<int>(d->L);
-  P.H = static_cast<int>(d->H);
-  P.Lp = Lp;
-  P.causal = d->causal;
-  P.ntiles = static_cast<int>(d->B * d->H * (Lp / BR));
-  P.scale = 1.f / sqrtf(static_cast<float>(DH));
-  P.scale_log2 = P.scale * kLog2e;
-  P.l2 = l2;
-  P.dd = dd;
-  P.status = static_cast<int*>(scratch);
   Ctx c;
   c.stream = reinterpret_cast<cudaStream_t>(stream);
   c.num_sms = sms();
-  const double elems = static_cast<double>(d->B * d->L * d->H * DH);
-  const double pairs = visible_pairs(*d);
-  cudaError_t e;
-  {
-    const int64_t threads = rows * 32;
-    prof_start(c);
-    e = launch_pdl(attn_rows_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)), dim3(256),
-                   0, c.stream, static_cast<const __nv_bfloat16*>(o),
-                   static_cast<const __nv_bfloat16*>(dout), lse, dd, l2, P.B, P.L, P.H, Lp);
-    note_launch(c, KK_ATTN, 3, 2.0 * elems, 2.0 * elems * 2 + 3.0 * rows * 4);
-  }
-  if (e == cudaSuccess) {
-    Params K = P;
-    if (!encode3(&K.mx[0], k, *d, BR) || !encode3(&K.mx[1], v, *d, BR) ||
-        !encode3(&K.my[0], q, *d, BC) || !encode3(&K.my[1], dout, *d, BC))
-      return BN_ERR_CUDA;
-    K.out0 = static_cast<__nv_bfloat16*>(dv);
-    K.out1 = static_cast<__nv_bfloat16*>(dk);
-    e = launch<BKV>(c, K, 8.0 * DH * pairs, 6.0 * elems * 2 + 2.0 * rows * 4);
-  }
-  if (e == cudaSuccess) {
-    Params Q = P;
-    if (!encode3(&Q.mx[0], q, *d, BR) || !encode3(&Q.mx[1], dout, *d, BR) ||
-        !encode3(&Q.my[0], k, *d, BC) || !encode3(&Q.my[1], v, *d, BC))
-      return BN_ERR_CUDA;
-    Q.out1 = static_cast<__nv_bfloat16*>(dq);
-    e = launch<BQ>(c, Q, 6.0 * DH * pairs, 5.0 * elems * 2 + 2.0 * rows * 4);
-  }
+  float* rows = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + 256);
+  const cudaError_t e = attn_backward(c, *d, q, k, v, o, lse, dout, dq, dk, dv, rows,
+                                      static_cast<int*>(scratch));
   if (e != cudaSuccess) {
     std::snprintf(g_err, sizeof(g_err), "%s", cudaGetErrorString(e));
     return BN_ERR_CUDA;

@@ -12,6 +12,7 @@
 
 #include "../../include/boostblk.h"
 #include "common.cuh"
+#include "attn.h"
 #include "gemm.h"
 #include "rowops.h"
 
@@ -27,6 +28,8 @@ struct Shape {
   int64_t T, d, r, d_ff, ld_ff;
   int64_t ld_act;  // row stride of the [T, d_ff] activations G, U, m, dG, dU: whole 128-byte lines
   int S, sigma, dtype, kind, dense, ckpt, btp;
+  int attn;        // the attention core runs inside the block (H heads of 128, sequences of L)
+  int64_t L, H;
   float eps;
   int64_t E;  // bytes per element
   bool full() const { return kind == BN_BLOCK_FULL; }
@@ -38,6 +41,8 @@ struct Acts {
   void *z_qkv = nullptr, *h_qkv = nullptr, *V = nullptr, *z_o = nullptr, *h_o = nullptr;
   void *x1 = nullptr, *z_gu = nullptr, *h_gu = nullptr, *G = nullptr, *U = nullptr, *m = nullptr;
   void *z_d = nullptr, *h_d = nullptr;
+  void *Q = nullptr, *K = nullptr, *O = nullptr;  // attention core: its inputs and output
+  float* lse = nullptr;                            // and its row log-sum-exp
 };
 // temporaries in `scratch`
 struct Tmp {
@@ -46,6 +51,8 @@ struct Tmp {
   void *dz_d = nullptr, *dG = nullptr, *dU = nullptr, *dz_gu = nullptr, *dn = nullptr;
   void *dx1 = nullptr, *dz_o = nullptr, *dV = nullptr, *dz_qkv = nullptr, *dqkv = nullptr;
   float *dw_part1 = nullptr, *dw_part2 = nullptr;  // RMSNorm dw partial column sums
+  void *dO = nullptr, *dQ = nullptr, *dK = nullptr;  // attention core gradients
+  float* attn_rows = nullptr;                        // and its backward's row terms
   float* partial = nullptr;
   size_t partial_bytes = 0;
   int nblk = 0;
@@ -85,6 +92,17 @@ int device_sms() {
   return cache[dev];
 }
 
+// the attention core's shapes: T / L causal sequences of L tokens, d / 128 heads
+bn_attn_desc attn_desc(const Shape& s) {
+  bn_attn_desc a;
+  a.B = s.L > 0 ? s.T / s.L : 0;
+  a.L = s.L;
+  a.H = s.H;
+  a.d_head = 128;
+  a.causal = 1;
+  return a;
+}
+
 void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
           size_t* saved_bytes, size_t* scratch_bytes) {
   Bump sv(saved_base), sc(scratch_base);
@@ -104,6 +122,13 @@ void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
     }
     A.V = rest.take(T * s.d * E);
     A.x1 = rest.take(T * s.d * E);
+    if (s.attn) {
+      A.Q = rest.take(T * s.d * E);
+      A.K = rest.take(T * s.d * E);
+      A.O = rest.take(T * s.d * E);
+      const bn_attn_desc a = attn_desc(s);
+      A.lse = static_cast<float*>(rest.take(static_cast<size_t>(a.B * a.H * bn_attn_lse_stride(a.L)) * 4));
+    }
   }
   A.ss2 = static_cast<float*>(rest.take(T * s.S * 4));
   A.rstd2 = static_cast<float*>(rest.take(T * 4));
@@ -137,6 +162,13 @@ void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
       B.dz_qkv = sc.take(T * 3 * s.r * E);
     }
   }
+  if (s.attn) {
+    B.dO = sc.take(T * s.d * E);
+    B.dQ = sc.take(T * s.d * E);
+    B.dK = sc.take(T * s.d * E);
+    if (s.dense) B.dV = sc.take(T * s.d * E);
+    B.attn_rows = static_cast<float*>(sc.take(attn_scratch_floats(attn_desc(s)) * 4));
+  }
   B.nblk = norm_bwd_blocks(device_sms());
   B.dw_part2 = static_cast<float*>(sc.take(static_cast<size_t>(B.nblk) * s.d * 4));
   if (s.full()) B.dw_part1 = static_cast<float*>(sc.take(static_cast<size_t>(B.nblk) * s.d * 4));
@@ -165,11 +197,22 @@ bn_status check_desc(const bn_block_desc* D, Shape& s) {
   s.ckpt = D->checkpoint;
   s.eps = D->eps;
   s.btp = D->btp;
+  s.attn = D->attn;
+  s.L = D->seq_len;
+  s.H = s.d / 128;
   if (s.dtype != BN_F32 && s.dtype != BN_BF16) return BN_ERR_INVALID_ARG;
   if (s.sigma != BN_SIGMA_IDENTITY && s.sigma != BN_SIGMA_SILU) return BN_ERR_INVALID_ARG;
   if (s.kind != BN_BLOCK_FULL && s.kind != BN_BLOCK_MLP) return BN_ERR_INVALID_ARG;
-  if ((s.dense != 0 && s.dense != 1) || (s.ckpt != 0 && s.ckpt != 1) || (s.btp != 0 && s.btp != 1))
+  if ((s.dense != 0 && s.dense != 1) || (s.ckpt != 0 && s.ckpt != 1) || (s.btp != 0 && s.btp != 1) ||
+      (s.attn != 0 && s.attn != 1))
     return BN_ERR_INVALID_ARG;
+  if (s.attn) {
+    // the attention core: full kind, bf16, heads of 128, whole sequences
+    if (s.kind != BN_BLOCK_FULL || s.L < 1 || s.T % s.L != 0) return BN_ERR_INVALID_ARG;
+    if (s.dtype != BN_BF16 || s.d % 128 != 0) return BN_ERR_UNSUPPORTED;
+    const bn_status a = attn_check(attn_desc(s));
+    if (a != BN_OK) return a;
+  }
   if (s.T < 1 || s.d < 1 || s.d_ff < 1 || s.ld_ff < s.d_ff || s.S < 1 || s.S > 16)
     return BN_ERR_INVALID_ARG;
   if (!(s.eps >= 0.f) || s.eps > 1.f) return BN_ERR_INVALID_ARG;
@@ -404,6 +447,11 @@ bn_status finish(Ctx& c) {
 // forward pieces (shared by the forward and the checkpoint recompute)
 // ---------------------------------------------------------------------------
 
+// O = causal softmax attention of (Q, K, V), and its row log-sum-exp
+void attention(Ctx& c, const Shape& s, const Acts& A, const Tmp& B) {
+  track(c, attn_forward(c, attn_desc(s), A.Q, A.K, A.V, A.O, A.lse, B.status));
+}
+
 // V (and Q, K when wanted) = sigma(z) B^T for the grouped Q/K/V bottlenecks.
 void qkv_up(Ctx& c, const Shape& s, const bn_block_params* W, const Acts& A, void* q, void* k) {
   GemmLaunch g = launch(EPI_STORE, s);
@@ -530,9 +578,10 @@ void forward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const voi
     produce(c, s, B, 0);
     norm_down(c, s, x, A.ss1, B.A1f, 3 * s.r, A.z_qkv, A.h_qkv);
     consume(c, s, B, 0);
-    qkv_up(c, s, W, A, q, k);
+    qkv_up(c, s, W, A, s.attn ? A.Q : q, s.attn ? A.K : k);
+    if (s.attn) attention(c, s, A, B);
     produce(c, s, B, 1);
-    plain_down(c, s, A.V, s.d, s.d, W->A_o, s.d, A.z_o, A.h_o);
+    plain_down(c, s, s.attn ? A.O : A.V, s.d, s.d, W->A_o, s.d, A.z_o, A.h_o);
     consume(c, s, B, 1);
     o_up(c, s, W, x, A);
     x1 = A.x1;
@@ -558,7 +607,7 @@ void forward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void*
     const Fold f1{W->A_qkv, W->w_norm1, 3 * s.d, s.d, B.A1f};
     DT_CALL(s, stats_fold, c, x, s, A.ss1, A.rstd1, f1, f2);
     GemmLaunch g = launch(EPI_NORM, s);
-    void* outs[3] = {q, k, A.V};
+    void* outs[3] = {s.attn ? A.Q : q, s.attn ? A.K : k, A.V};
     for (int i = 0; i < 3; ++i) {
       GemmProblem& p = g.p[g.nprob++];
       p.M = s.T;
@@ -571,13 +620,14 @@ void forward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void*
       p.ldo[0] = s.d;
     }
     gemm(c, s, g);
+    if (s.attn) attention(c, s, A, B);
     GemmLaunch o = launch(EPI_RESID, s);
     o.nprob = 1;
     GemmProblem& p = o.p[0];
     p.M = s.T;
     p.N = s.d;
     p.K = s.d;
-    p.a[0] = op(A.V, s.d, KM);
+    p.a[0] = op(s.attn ? A.O : A.V, s.d, KM);
     p.b[0] = op(W->A_o, s.d, KM);
     p.in[0] = x;
     p.ldi[0] = s.d;
@@ -621,12 +671,14 @@ void forward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void*
 
 // Checkpoint mode: rebuild every activation the backward reads from the saved
 // pre-activations, with the same kernels (bit-identical to the forward).
-void recompute(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, const Acts& A) {
+void recompute(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, const Acts& A,
+               const Tmp& B) {
   const void* x1 = x;
   if (s.full()) {
     DT_CALL(s, stats, c, x, s, A.ss1, A.rstd1);
     DT_CALL(s, sigma_ew, c, s, A.z_qkv, 3 * s.r, 3 * s.r, A.h_qkv);
-    qkv_up(c, s, W, A, nullptr, nullptr);
+    qkv_up(c, s, W, A, s.attn ? A.Q : nullptr, s.attn ? A.K : nullptr);
+    if (s.attn) attention(c, s, A, B);  // O for the O bottleneck's backward
     DT_CALL(s, sigma_ew, c, s, A.z_o, s.r, s.r, A.h_o);
     o_up(c, s, W, x, A);
     x1 = A.x1;
@@ -766,12 +818,15 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
     produce(c, s, B, 6);
     gemm(c, s, g);
   }
-  add_wgrad(c, s, wg, wgrad(r, d, T, B.dz_o, r, A.V, d, dW->A_o, d));
+  add_wgrad(c, s, wg, wgrad(r, d, T, B.dz_o, r, s.attn ? A.O : A.V, d, dW->A_o, d));
   consume(c, s, B, 6);
-  dx_gemm(c, s, B.dz_o, r, W->A_o, d, d, B.dV, d);
+  dx_gemm(c, s, B.dz_o, r, W->A_o, d, d, s.attn ? B.dO : B.dV, d);
+  if (s.attn)
+    track(c, attn_backward(c, attn_desc(s), A.Q, A.K, A.V, A.O, A.lse, B.dO, B.dQ, B.dK, B.dV,
+                           B.attn_rows, B.status));
 
   // ---- Q / K / V bottlenecks
-  const void* dQKV[3] = {dq, dk, B.dV};
+  const void* dQKV[3] = {s.attn ? B.dQ : dq, s.attn ? B.dK : dk, B.dV};
   const void* Bup[3] = {W->B_q, W->B_k, W->B_v};
   void* dB[3] = {dW->B_q, dW->B_k, dW->B_v};
   for (int i = 0; i < 3; ++i) {
@@ -852,10 +907,19 @@ void backward_dense(Ctx& c, const Shape& s, const bn_block_params* W, const void
     flush_wgrads(c, s, wg, true);
     return;
   }
-  add_wgrad(c, s, wg, wgrad(d, d, T, dx1, d, A.V, d, dW->A_o, d));
-  DT_CALL(s, rowscale, c, s, dq, d, A.rstd1, d, B.dqkv, 3 * d);
-  DT_CALL(s, rowscale, c, s, dk, d, A.rstd1, d, at(B.dqkv, d, s), 3 * d);
-  dx_gemm(c, s, dx1, d, W->A_o, d, d, at(B.dqkv, 2 * d, s), 3 * d, A.rstd1);
+  add_wgrad(c, s, wg, wgrad(d, d, T, dx1, d, s.attn ? A.O : A.V, d, dW->A_o, d));
+  if (s.attn) {
+    dx_gemm(c, s, dx1, d, W->A_o, d, d, B.dO, d);
+    track(c, attn_backward(c, attn_desc(s), A.Q, A.K, A.V, A.O, A.lse, B.dO, B.dQ, B.dK, B.dV,
+                           B.attn_rows, B.status));
+    DT_CALL(s, rowscale, c, s, B.dQ, d, A.rstd1, d, B.dqkv, 3 * d);
+    DT_CALL(s, rowscale, c, s, B.dK, d, A.rstd1, d, at(B.dqkv, d, s), 3 * d);
+    DT_CALL(s, rowscale, c, s, B.dV, d, A.rstd1, d, at(B.dqkv, 2 * d, s), 3 * d);
+  } else {
+    DT_CALL(s, rowscale, c, s, dq, d, A.rstd1, d, B.dqkv, 3 * d);
+    DT_CALL(s, rowscale, c, s, dk, d, A.rstd1, d, at(B.dqkv, d, s), 3 * d);
+    dx_gemm(c, s, dx1, d, W->A_o, d, d, at(B.dqkv, 2 * d, s), 3 * d, A.rstd1);
+  }
   add_wgrad(c, s, wg, wgrad(3 * d, d, T, B.dqkv, 3 * d, x, d, dW->A_qkv, d, W->w_norm1));
   dx_gemm(c, s, B.dqkv, 3 * d, W->A_qkv, d, d, B.dn, d);
   DT_CALL(s, normbwd, c, s, B, wg, B.dw_part1, B.dn, x, W->w_norm1, A.rstd1, dx1, dx,
@@ -902,7 +966,9 @@ bn_status bn_block_forward(const bn_block_desc* desc, const bn_block_params* W, 
   if (st != BN_OK) return st;
   if ((st = check_params(s, W)) != BN_OK) return st;
   if (!x || !y || !saved || !scratch) return BN_ERR_INVALID_ARG;
-  if (s.full() != (q_out != nullptr) || s.full() != (k_out != nullptr)) return BN_ERR_INVALID_ARG;
+  // q and k leave the block only when the attention core runs outside it
+  const bool qk_out = s.full() && !s.attn;
+  if (qk_out != (q_out != nullptr) || qk_out != (k_out != nullptr)) return BN_ERR_INVALID_ARG;
   for (const void* p : {x, static_cast<const void*>(y), static_cast<const void*>(q_out),
                         static_cast<const void*>(k_out), static_cast<const void*>(saved),
                         static_cast<const void*>(scratch)})
@@ -929,7 +995,7 @@ bn_status bn_block_backward(const bn_block_desc* desc, const bn_block_params* W,
   if ((st = check_params(s, W)) != BN_OK) return st;
   if ((st = check_params(s, dW)) != BN_OK) return st;
   if (!x || !saved || !dy || !dx || !scratch) return BN_ERR_INVALID_ARG;
-  if (!s.full() && (dq || dk)) return BN_ERR_INVALID_ARG;
+  if ((!s.full() || s.attn) && (dq || dk)) return BN_ERR_INVALID_ARG;
   for (const void* p : {x, saved, dy, dq, dk, static_cast<const void*>(dx),
                         static_cast<const void*>(scratch)})
     if (p && !aligned(p)) return BN_ERR_ALIGNMENT;
@@ -937,7 +1003,7 @@ bn_status bn_block_backward(const bn_block_desc* desc, const bn_block_params* W,
   Tmp B;
   plan(s, const_cast<void*>(saved), scratch, A, B, nullptr, nullptr);
   Ctx c = make_ctx(scratch, stream, B);
-  if (s.ckpt) recompute(c, s, W, x, A);
+  if (s.ckpt) recompute(c, s, W, x, A, B);
   if (s.dense)
     backward_dense(c, s, W, x, dy, dq, dk, dx, dW, A, B);
   else

@@ -20,7 +20,7 @@ def inputs(T, d, r, d_ff, *, kind="full", dense=False, dtype="bf16", seed=0):
 
 def oracle_cfg(cfg):
     return dict(kind=cfg.kind, dense=cfg.dense, sigma=cfg.sigma, eps=cfg.eps,
-                checkpoint=cfg.checkpoint)
+                checkpoint=cfg.checkpoint, attn=cfg.attn, seq_len=cfg.seq_len or None)
 
 
 def run_oracle(cfg, inp, rows=None):
@@ -29,8 +29,8 @@ def run_oracle(cfg, inp, rows=None):
     f = {k: v.astype(np.float64) for k, v in inp.items()}
     sel = (lambda a: a) if rows is None else (lambda a: a[rows])
     x, dy = sel(f["x"]), sel(f["dy"])
-    dq = sel(f["dq"]) if "dq" in f else None
-    dk = sel(f["dk"]) if "dk" in f else None
+    dq = sel(f["dq"]) if "dq" in f and not cfg.attn else None
+    dk = sel(f["dk"]) if "dk" in f and not cfg.attn else None
     p = {k: f[k] for k in cfg.param_shapes()}
     oc = oracle_cfg(cfg)
     out, saved = O.block_forward(p, x, oc)
@@ -71,8 +71,9 @@ def run_gpu(cfg, inp, device="cuda", drop_dq=False, drop_dk=False, ws=None):
     params, dev = to_device(cfg, inp, device)
     ws = B.Workspace(cfg, device) if ws is None else ws
     out = B.forward(cfg, params, dev["x"], ws)
-    dq = None if drop_dq else dev["dq"]
-    dk = None if drop_dk else dev["dk"]
+    # with the attention core inside the block, q and k never leave it
+    dq = None if (drop_dq or cfg.attn) else dev["dq"]
+    dk = None if (drop_dk or cfg.attn) else dev["dk"]
     dx, grads = B.backward(cfg, params, dev["x"], ws, dev["dy"], dq, dk)
     status = B.device_status(ws)
     assert status == 0, f"device status {status}"

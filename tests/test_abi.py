@@ -162,3 +162,29 @@ def test_attention_bad_pointers_rejected_before_launch(lib):
         assert bw(ctypes.byref(d), *args) == 1
         args[i] = ctypes.c_void_p(4096 * 20 + 4)
         assert bw(ctypes.byref(d), *args) == 2
+
+
+@pytest.mark.parametrize("bad, code", [
+    (dict(seq_len=0), 1), (dict(seq_len=100), 1),     # T % seq_len != 0
+    (dict(kind="mlp"), 1),                            # the attention core needs the full block
+    (dict(dtype="f32"), 3),                           # bf16 only
+    (dict(d=192, S=3), 3),                            # heads of 128
+])
+def test_block_attention_descriptor_checks(lib, bad, code):
+    from rank_bottleneck_gb300.block import BlockConfig
+    kw = dict(T=256, d=256, r=64, d_ff=333, S=4, attn=True, seq_len=128)
+    kw.update(bad)
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.bn_block_workspace_size(ctypes.byref(BlockConfig(**kw).desc()), ctypes.byref(a),
+                                       ctypes.byref(b)) == code
+
+
+def test_block_attention_workspace_holds_q_k_o_and_lse(lib):
+    from rank_bottleneck_gb300.block import BlockConfig, workspace_size
+    base = dict(T=16384, d=2048, r=512, d_ff=5461, S=4)
+    s0, c0 = workspace_size(BlockConfig(**base))
+    s1, c1 = workspace_size(BlockConfig(**base, attn=True, seq_len=4096))
+    T, d = 16384, 2048
+    lse = 4 * 16 * 4096 * 4
+    assert abs((s1 - s0) - (3 * T * d * 2 + lse)) <= 4 * 256
+    assert c1 - c0 >= 3 * T * d * 2 + 2 * lse

@@ -234,6 +234,11 @@ FD_CASES = [
     dict(kind="mlp", sigma="silu", checkpoint=True),
     dict(kind="full", dense=True),
     dict(kind="mlp", dense=True),
+    # the causal attention core inside the block: one sequence of the 3 tokens,
+    # 2 heads of 4
+    dict(kind="full", sigma="silu", attn=True, seq_len=3, heads=2),
+    dict(kind="full", sigma="silu", attn=True, seq_len=3, heads=2, checkpoint=True),
+    dict(kind="full", dense=True, attn=True, seq_len=3, heads=2),
 ]
 
 
@@ -367,3 +372,19 @@ def test_generator_is_deterministic_and_ordered():
     m = make_block_inputs(8, 16, 4, 24, kind="mlp", seed=5)
     assert np.array_equal(m["x"], a["x"])
     assert "dq" not in m and "A_qkv" not in m
+
+
+def test_attention_inside_block_two_sequences_do_not_mix():
+    """With the attention core inside, a token's output depends on its own
+    sequence only (causal within each of the T / seq_len sequences): changing
+    the second sequence leaves the first one's outputs as they were, and
+    changing a later token leaves earlier tokens of its sequence unchanged."""
+    T, d, r, d_ff = 8, 16, 4, 12
+    cfg = dict(kind="full", attn=True, seq_len=4, heads=2)
+    p, x, dy, dq, dk = split_inputs(T, d, r, d_ff, kind="full", seed=5)
+    y0 = O.block_forward(p, x, cfg)[0]["y"]
+    x2 = x.copy()
+    x2[6] += 1.0                      # the second sequence's third token
+    y1 = O.block_forward(p, x2, cfg)[0]["y"]
+    assert np.array_equal(y0[:6], y1[:6])
+    assert np.max(np.abs(y0[6:] - y1[6:])) > 1e-3
