@@ -13,23 +13,25 @@
 // 128-row tile (one row per TMEM lane and per epilogue thread) and a stream of
 // 64-row blocks of the other side, both d_head = 128 wide.
 //   FWD   stationary Q;        blocks K_j, V_j.   S = Q K_j^T (TMEM), online
-//         softmax in registers, P (bf16) to shared memory, PV = P V_j (TMEM),
-//         O = O alpha + PV in registers.
+//         softmax in registers, P (bf16) to shared memory, O += P V_j in TMEM;
+//         O is rescaled in place only when a row maximum grows by more than
+//         2^8 (lazy rescale), and divided by the row sum at the end.
 //   BKV   stationary K and V;  blocks Q_i, dO_i.  S^T = K Q_i^T, dP^T = V dO_i^T,
 //         P^T and dS^T (bf16) to shared memory, dV += P^T dO_i and
 //         dK += dS^T Q_i accumulated in TMEM.
 //   BQ    stationary Q and dO; blocks K_j, V_j.   S = Q K_j^T, dP = dO V_j^T,
 //         dS to shared memory, dQ += dS K_j in TMEM.
-// Per CTA (192 threads, persistent over the tiles, one CTA per SM):
-//   warp 0      TMA producer: the stationary tile(s), then a ring of NSTAGE
-//               stages of streamed blocks (plus, in BKV, the blocks' row terms);
+// Per CTA (320 threads, persistent over the tiles, one CTA per SM):
+//   warp 0      TMA producer: the stationary tile(s), then a ring of stages of
+//               streamed blocks (4, or 3 in BKV: what shared memory holds), in
+//               BKV with the blocks' row terms;
 //   warp 1      TMEM owner (512 columns) and, from one thread, the MMA issuer;
-//   warps 2..5  elementwise: warp w owns TMEM lanes 32 (w % 4) .. + 31, one
-//               tile row per thread.
-// TMEM columns: S (and the forward's rows of P V) double-buffered so that the
-// next block's S = Q K^T runs while the current block's softmax does:
+//   warps 2..9  elementwise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
+//               tile row per thread) and one 32-column half of every block.
+// TMEM columns: S double-buffered so that the next block's S = Q K^T runs
+// while the current block's softmax does:
 //   [0, 128)   S of block buffers 0 and 1 (64 columns each)
-//   FWD  [128, 384)  P V of block buffers 0 and 1 (128 columns each)
+//   FWD  [128, 384)  O of tile buffers 0 and 1 (128 columns each; P V accumulates)
 //   BKV, BQ  [128, 256)  dP of block buffers 0 and 1; [256, 384) dV; [384, 512) dK or dQ.
 // Every operand is bf16 in 128-byte-swizzled shared memory: K-major for the
 // S and dP products (rows of 64 elements per 128-byte line), and the streamed
@@ -54,7 +56,6 @@ using namespace tc;
 constexpr int DH = 128;      // head width
 constexpr int BR = 128;      // rows of the stationary tile
 constexpr int BC = 64;       // rows of a streamed block
-constexpr int NSTAGE = 3;    // streamed-block ring
 constexpr int NTHREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 elementwise
 constexpr int SUB_R = BR * 128;          // one 64-column half of a stationary tile: 16 KB
 constexpr int SUB_C = BC * 128;          // one 64-column half of a streamed block: 8 KB
@@ -71,14 +72,17 @@ template <int MODE>
 struct Lay {
   static constexpr int NX = (MODE == FWD) ? 1 : 2;   // stationary tiles
   static constexpr int NE = (MODE == BKV) ? 2 : 1;   // elementwise tiles (each double-buffered)
+  static constexpr int NST = (MODE == BKV) ? 3 : 4;  // streamed-block stages: what shared memory holds
   static constexpr int X_OFF = 0;
   static constexpr int Y_OFF = X_OFF + NX * XTILE;
-  static constexpr int E_OFF = Y_OFF + NSTAGE * STAGE;
+  static constexpr int E_OFF = Y_OFF + NST * STAGE;
   static constexpr int AUX_OFF = E_OFF + NE * 2 * EBUF;
-  static constexpr int XCH_OFF = AUX_OFF + ((MODE == BKV) ? NSTAGE * AUX : 0);
+  static constexpr int XCH_OFF = AUX_OFF + ((MODE == BKV) ? NST * AUX : 0);
   // FWD: row sums exchanged between the two warps of a row, [2 tile parity][2 half][128]
   static constexpr int BAR_OFF = XCH_OFF + ((MODE == FWD) ? 2 * 2 * BR * 4 : 0);
-  static constexpr int BYTES = BAR_OFF + 256;
+  // barriers (2 + 2 NST + 21 of 8 bytes), the TMEM address and the abort flag
+  static constexpr int BAR_BYTES = (2 + 2 * NST + 21) * 8 + 8 <= 256 ? 256 : 512;
+  static constexpr int BYTES = BAR_OFF + BAR_BYTES;
   static constexpr int SMEM = 1024 + BYTES;
   static_assert(E_OFF % 1024 == 0, "elementwise tiles must be 1024-byte aligned");
   static_assert(SMEM <= 232448, "shared memory over the per-CTA limit");
@@ -122,6 +126,12 @@ __device__ __forceinline__ float ex2f_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                      int* status, unsigned long long limit = kWaitLimitNs) {
@@ -189,9 +199,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
   uint64_t* x_full = bars;
   uint64_t* x_empty = bars + 1;
-  uint64_t* y_full = bars + 2;                // [NSTAGE]
-  uint64_t* y_empty = y_full + NSTAGE;        // [NSTAGE]
-  uint64_t* s_full = y_empty + NSTAGE;        // [2]
+  uint64_t* y_full = bars + 2;                // [NST]
+  uint64_t* y_empty = y_full + LY::NST;       // [NST]
+  uint64_t* s_full = y_empty + LY::NST;        // [2]
   uint64_t* s_empty = s_full + 2;             // [2]
   uint64_t* e_full = s_empty + 2;             // [2]
   uint64_t* e_empty = e_full + 2;             // [2]  backward: accumulating MMAs done with E
@@ -207,7 +217,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(x_full), 1);
     mbar_init(smem_u32(x_empty), 1);
-    for (int i = 0; i < NSTAGE; ++i) {
+    for (int i = 0; i < LY::NST; ++i) {
       mbar_init(smem_u32(&y_full[i]), 1);
       mbar_init(smem_u32(&y_empty[i]), 1);
     }
@@ -256,8 +266,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             tma_load_3d(smem_u32(sX + i * XTILE + c * SUB_R), &P.mx[i], col + 64 * c, t * BR, b, xb);
         ++x_loads;
         for (int j = first; j < last; ++j, ++jn) {
-          const int st = jn % NSTAGE;
-          if (!bwait(smem_u32(&y_empty[st]), ((jn / NSTAGE) & 1u) ^ 1u, abort_flag, P.status)) {
+          const int st = jn % LY::NST;
+          if (!bwait(smem_u32(&y_empty[st]), ((jn / LY::NST) & 1u) ^ 1u, abort_flag, P.status)) {
             ok = false;
             break;
           }
@@ -278,9 +288,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
       if (!ok) {
         // the copies in flight must land before the CTA exits
         const unsigned long long lim = 50ull * 1000 * 1000;
-        for (uint32_t i = 0; i < NSTAGE && i < jn; ++i) {
+        for (uint32_t i = 0; i < LY::NST && i < jn; ++i) {
           const uint32_t k = jn - 1 - i;
-          bwait(smem_u32(&y_full[k % NSTAGE]), (k / NSTAGE) & 1u, abort_flag, P.status, lim);
+          bwait(smem_u32(&y_full[k % LY::NST]), (k / LY::NST) & 1u, abort_flag, P.status, lim);
         }
         if (x_loads > 0) bwait(smem_u32(x_full), (x_loads - 1) & 1u, abort_flag, P.status, lim);
       }
@@ -294,8 +304,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
       uint32_t tn = 0, jn = 0;
       // S (and dP) of streamed block number n into TMEM buffer n & 1
       auto issue_sd = [&](uint32_t n) -> bool {
-        const int st = n % NSTAGE, bf = n & 1;
-        if (!bwait(smem_u32(&y_full[st]), (n / NSTAGE) & 1u, abort_flag, P.status)) return false;
+        const int st = n % LY::NST, bf = n & 1;
+        if (!bwait(smem_u32(&y_full[st]), (n / LY::NST) & 1u, abort_flag, P.status)) return false;
         if (!bwait(smem_u32(&s_empty[bf]), ((n >> 1) & 1u) ^ 1u, abort_flag, P.status)) return false;
         tc_fence_after();
         const uint32_t y = smem_u32(sY + st * STAGE);
@@ -338,7 +348,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             ok = false;
             break;
           }
-          const int st = jn % NSTAGE, bf = jn & 1;
+          const int st = jn % LY::NST, bf = jn & 1;
           if (!bwait(smem_u32(&e_full[bf]), (jn >> 1) & 1u, abort_flag, P.status)) {
             ok = false;
             break;
@@ -442,18 +452,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             break;
           }
           tc_fence_after();
+          // Raw scores of the row: both halves of the block (this warp's own half
+          // and the other warp's, for the row maximum). Scale > 0, so the maximum
+          // is taken on raw scores; masked scores are -inf.
           const int c0 = j * BC + 32 * hf, c1 = j * BC + 32 * (1 - hf);
-          float x[32], y[32];
-          tmem_ld32(tmem + lb + bf * BC + 32 * hf, x);
-          tmem_ld32(tmem + lb + bf * BC + 32 * (1 - hf), y);
-          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          const bool need_mask = (P.causal && j * BC + BC - 1 > t * BR) || j * BC + BC > P.L;
+          uint32_t xr[32], yr[32];
+          tmem_ld32_nowait(tmem + lb + bf * BC + 32 * hf, xr);
+          tmem_ld32_nowait(tmem + lb + bf * BC + 32 * (1 - hf), yr);
+          tmem_wait_ld2(xr, yr);
+          float x[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            x[i] = (c0 + i >= lo && c0 + i <= hi) ? x[i] * P.scale_log2 : -INFINITY;
-            const float yv = (c1 + i >= lo && c1 + i <= hi) ? y[i] * P.scale_log2 : -INFINITY;
-            mx[i & 3] = fmaxf(mx[i & 3], fmaxf(x[i], yv));
+          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(xr[i]);
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (need_mask) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              x[i] = (c0 + i >= lo && c0 + i <= hi) ? x[i] : -INFINITY;
+              const float yv = (c1 + i >= lo && c1 + i <= hi) ? __uint_as_float(yr[i]) : -INFINITY;
+              mx[i & 3] = max3(mx[i & 3], x[i], yv);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx[i & 3] = max3(mx[i & 3], x[i], __uint_as_float(yr[i]));
           }
-          const float bm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          const float bm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * P.scale_log2;
           const float m_new = fmaxf(m, bm);
           // (a warp-wide decision: the TMEM accesses below are warp-collective;
           // the row's other warp sees the same rows and decides the same)
@@ -486,7 +509,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float p0 = ex2f_approx(x[i] - m), p1 = ex2f_approx(x[i + 1] - m);
+            const float p0 = ex2f_approx(fmaf(x[i], P.scale_log2, -m));
+            const float p1 = ex2f_approx(fmaf(x[i + 1], P.scale_log2, -m));
             rs[(i >> 1) & 3] += p0 + p1;
             pk[i / 2] = pack2(p0, p1);
           }
@@ -535,7 +559,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           dr = P.dd[static_cast<int64_t>(bh) * P.Lp + row];
         }
         for (int j = first; j < last; ++j, ++jn) {
-          const int bf = jn & 1, st = jn % NSTAGE;
+          const int bf = jn & 1, st = jn % LY::NST;
           if (!wwait(&s_full[bf], (jn >> 1) & 1u) ||
               !wwait(&e_empty[bf], ((jn >> 1) & 1u) ^ 1u)) {
             ok = false;
@@ -543,17 +567,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           }
           if constexpr (MODE == BKV) {
             // the block's row terms arrived with its stage
-            if (!wwait(&y_full[st], (jn / NSTAGE) & 1u)) {
+            if (!wwait(&y_full[st], (jn / LY::NST) & 1u)) {
               ok = false;
               break;
             }
           }
           tc_fence_after();
           const int c0 = j * BC + 32 * hf;  // first column (query in BKV, key in BQ) of the half
+          // some (row, column) pair of the block is not visible: the diagonal
+          // blocks of the causal mask and the ragged ends of the sequence
+          const bool mask = (MODE == BKV)
+                                ? ((P.causal && j * BC < t * BR + BR - 1) || j * BC + BC > P.L ||
+                                   t * BR + BR > P.L)
+                                : ((P.causal && j * BC + BC - 1 > t * BR) || j * BC + BC > P.L ||
+                                   t * BR + BR > P.L);
           uint32_t sr[32], dr32[32];
           tmem_ld32_nowait(tmem + lb + bf * BC + 32 * hf, sr);
           tmem_ld32_nowait(tmem + lb + 128 + bf * BC + 32 * hf, dr32);
           tmem_wait_ld2(sr, dr32);
+          if (mask) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (!(c0 + i >= lo && c0 + i <= hi)) sr[i] = __float_as_uint(-INFINITY);
+          }
           uint32_t pp[16], pd[16];
           const float* al = sAux + st * (AUX / 4) + 32 * hf;
 #pragma unroll
@@ -571,11 +607,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             float p[4], ds[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const int c = c0 + i + k;
-              const float xs = (c >= lo && c <= hi)
-                                   ? fmaf(__uint_as_float(sr[i + k]), P.scale_log2, -lv[k])
-                                   : -INFINITY;
-              p[k] = ex2f_approx(xs);
+              p[k] = ex2f_approx(fmaf(__uint_as_float(sr[i + k]), P.scale_log2, -lv[k]));
               ds[k] = p[k] * (__uint_as_float(dr32[i + k]) - dv[k]);
             }
             pp[i / 2] = pack2(p[0], p[1]);
