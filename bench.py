@@ -384,7 +384,8 @@ def run_ours(args, rank, local_rank, world):
 
 def traffic_for(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    this workload with the current kernel source; None otherwise."""
+    this workload with the current kernel source (every file the entry names,
+    hashed in order); None otherwise."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -395,12 +396,15 @@ def traffic_for(kernel, workload):
     if not entry or entry.get("workload") != workload:
         return None
     import hashlib
-    src = os.path.join(ROOT, "rank_bottleneck_gb300", "csrc", entry["source"])
+    srcs = entry["source"] if isinstance(entry["source"], list) else [entry["source"]]
+    h = hashlib.sha256()
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for name in srcs:
+            with open(os.path.join(ROOT, "rank_bottleneck_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
     except OSError:
         return None
-    return entry["dram_bytes_per_launch"] if digest == entry["source_sha256_16"] else None
+    return entry["dram_bytes_per_launch"] if h.hexdigest()[:16] == entry["source_sha256_16"] else None
 
 
 def run_e2e(args, cfg, inp, params, ws, act_names, dev, stream, world):

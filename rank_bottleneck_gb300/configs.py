@@ -27,6 +27,9 @@ WORKLOADS = {
                                                     attn=True, seq_len=4096),
     "7b-attn-T16384-L4096-d4096-r1024-dff11008": dict(T=16384, d=4096, r=1024, d_ff=11008, S=8,
                                                       attn=True, seq_len=4096),
+    # one sequence of the 1B layer: small enough for multi-pass profiler captures
+    "1b-attn-T4096-L4096-d2048-r512-dff5461": dict(T=4096, d=2048, r=512, d_ff=5461, S=4,
+                                                   attn=True, seq_len=4096),
 }
 for _T in (4096, 16384, 32768):
     for _r in (256, 512, 1024, 2048):
