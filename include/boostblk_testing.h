@@ -57,6 +57,17 @@ bn_status bn_testing_gemm(int32_t dtype, int32_t epi, int32_t sigma, int32_t S, 
                           int32_t allow_split, int32_t nprob, const bn_gemm_problem* probs,
                           void* scratch, size_t scratch_bytes, bn_stream_t stream);
 
+/* Failure-detection check: one bf16 STORE problem (M <= 256), launched as a
+ * chained consumer of an upstream launch that never comes. Its operand
+ * producer waits for `counters` (two device ints, zero, that nothing
+ * increments) to count the upstream CTAs; after the engine's wait limit (1 s)
+ * it records a timeout in the status word at the start of `scratch`, every
+ * role of the kernel unwinds, TMEM is freed and the kernel returns. out0 is
+ * then not written. Returns BN_OK if the launch was made;
+ * bn_get_device_status(scratch) then reports BN_ERR_TIMEOUT. */
+bn_status bn_testing_gemm_unfed(const bn_gemm_problem* prob, int* counters, void* scratch,
+                                size_t scratch_bytes, bn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

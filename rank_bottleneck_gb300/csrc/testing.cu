@@ -65,3 +65,42 @@ extern "C" bn_status bn_testing_gemm(int32_t dtype, int32_t epi, int32_t sigma, 
   if (c.err != cudaSuccess) return BN_ERR_CUDA;
   return BN_OK;
 }
+
+extern "C" bn_status bn_testing_gemm_unfed(const bn_gemm_problem* prob, int* counters,
+                                           void* scratch, size_t scratch_bytes,
+                                           bn_stream_t stream) {
+  if (prob == nullptr || counters == nullptr || scratch == nullptr || scratch_bytes < 256 ||
+      prob->M < 1 || prob->M > 256 || prob->N < 1 || prob->K < 1)
+    return BN_ERR_INVALID_ARG;
+  GemmLaunch g;
+  g.epi = EPI_STORE;
+  g.nprob = 1;
+  GemmProblem& p = g.p[0];
+  p.M = prob->M;
+  p.N = prob->N;
+  p.K = prob->K;
+  p.a[0].ptr = prob->a;
+  p.a[0].ld = prob->lda;
+  p.a[0].mn_major = prob->a_mn_major != 0;
+  p.b[0].ptr = prob->b;
+  p.b[0].ld = prob->ldb;
+  p.b[0].mn_major = prob->b_mn_major != 0;
+  p.out[0] = prob->out0;
+  p.ldo[0] = prob->ldo;
+  Ctx c;
+  c.stream = reinterpret_cast<cudaStream_t>(stream);
+  c.status = static_cast<int*>(scratch);
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+    c.num_sms = n;
+  // an upstream launch that never enters: entered counter and the one row block's
+  c.chain_in.entered = counters;
+  c.chain_in.rows = counters + 1;
+  c.chain_in.entered_target = 1;
+  c.chain_in.rows_target = 1;
+  gemm_tc(c, g);
+  if (c.bad) return BN_ERR_UNSUPPORTED;
+  if (c.err != cudaSuccess) return BN_ERR_CUDA;
+  return BN_OK;
+}
