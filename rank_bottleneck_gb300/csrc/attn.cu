@@ -55,14 +55,12 @@ using namespace tc;
 
 constexpr int DH = 128;      // head width
 constexpr int BR = 128;      // rows of the stationary tile
-constexpr int BC = 64;       // rows of a streamed block
+constexpr int BC = 64;       // rows of a streamed block (backward)
+constexpr int BCF = 128;     // rows of a streamed block (forward)
 constexpr int NTHREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 elementwise
 constexpr int SUB_R = BR * 128;          // one 64-column half of a stationary tile: 16 KB
-constexpr int SUB_C = BC * 128;          // one 64-column half of a streamed block: 8 KB
 constexpr int XTILE = 2 * SUB_R;         // a stationary tile: 32 KB
-constexpr int STAGE = 2 * 2 * SUB_C;     // two streamed blocks: 32 KB
 constexpr int AUX = 512;                 // BKV: 64 l2 + 64 D floats per stage
-constexpr int EBUF = BR * 128;           // a 128 x 64 bf16 elementwise tile: 16 KB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -70,18 +68,28 @@ enum Mode : int { FWD = 0, BKV = 1, BQ = 2 };
 
 template <int MODE>
 struct Lay {
+  static constexpr int BCM = (MODE == FWD) ? BCF : BC;  // rows of a streamed block
+  static constexpr int SUBC = BCM * 128;              // a 64-column half of a streamed block
+  static constexpr int STG = 2 * 2 * SUBC;            // one stage: two streamed blocks
+  static constexpr int EB = BR * BCM * 2;             // one bf16 elementwise tile [128, BCM]
   static constexpr int NX = (MODE == FWD) ? 1 : 2;   // stationary tiles
-  static constexpr int NE = (MODE == BKV) ? 2 : 1;   // elementwise tiles (each double-buffered)
-  static constexpr int NST = (MODE == BKV) ? 3 : 4;  // streamed-block stages: what shared memory holds
+  static constexpr int NE = (MODE == BKV) ? 2 : 1;   // elementwise tiles
+  // buffers of each elementwise tile: the forward's P is single (shared memory);
+  // the softmax waits for the previous block's P V before it writes the next P
+  static constexpr int NPB = (MODE == FWD) ? 1 : 2;
+  static constexpr int NST = (MODE == FWD) ? 2 : (MODE == BKV) ? 3 : 4;  // stages: what fits
   static constexpr int X_OFF = 0;
   static constexpr int Y_OFF = X_OFF + NX * XTILE;
-  static constexpr int E_OFF = Y_OFF + NST * STAGE;
-  static constexpr int AUX_OFF = E_OFF + NE * 2 * EBUF;
+  static constexpr int E_OFF = Y_OFF + NST * STG;
+  static constexpr int AUX_OFF = E_OFF + NE * NPB * EB;
   static constexpr int XCH_OFF = AUX_OFF + ((MODE == BKV) ? NST * AUX : 0);
   // FWD: row sums exchanged between the two warps of a row, [2 tile parity][2 half][128]
   static constexpr int BAR_OFF = XCH_OFF + ((MODE == FWD) ? 2 * 2 * BR * 4 : 0);
-  // barriers (2 + 2 NST + 21 of 8 bytes), the TMEM address and the abort flag
-  static constexpr int BAR_BYTES = (2 + 2 * NST + 21) * 8 + 8 <= 256 ? 256 : 512;
+  // stage barriers: the forward's K and V halves of a stage are filled and freed
+  // apart (K after S, V after P V), the backward's stage as a whole
+  static constexpr int NYB = (MODE == FWD) ? 2 * NST : NST;
+  // barriers (2 + 2 NYB + 21 of 8 bytes), the TMEM address and the abort flag
+  static constexpr int BAR_BYTES = (2 + 2 * NYB + 21) * 8 + 8 <= 256 ? 256 : 512;
   static constexpr int BYTES = BAR_OFF + BAR_BYTES;
   static constexpr int SMEM = 1024 + BYTES;
   static_assert(E_OFF % 1024 == 0, "elementwise tiles must be 1024-byte aligned");
@@ -151,13 +159,14 @@ __device__ __forceinline__ void decode(const Params& P, int u, int& t, int& bh) 
 // streamed blocks [first, last) of tile t
 template <int MODE>
 __device__ __forceinline__ void blocks(const Params& P, int t, int& first, int& last) {
-  const int nb = (P.L + BC - 1) / BC;
+  constexpr int bcm = Lay<MODE>::BCM;
+  const int nb = (P.L + bcm - 1) / bcm;
   if (MODE == BKV) {
-    first = P.causal ? (t * BR) / BC : 0;
+    first = P.causal ? (t * BR) / bcm : 0;
     last = nb;
   } else {
     first = 0;
-    last = P.causal ? min(nb, (t * BR + BR) / BC) : nb;
+    last = P.causal ? min(nb, (t * BR + BR) / bcm) : nb;
   }
 }
 
@@ -189,6 +198,9 @@ __device__ __forceinline__ void store32(__nv_bfloat16* dst, const float* v, floa
 template <int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant__ Params P) {
   using LY = Lay<MODE>;
+  constexpr int BCM = LY::BCM, SUBC = LY::SUBC, STG = LY::STG, EB = LY::EB;
+  // forward: S buffers take TMEM columns [0, 2 BCM), O the two 128-column buffers after them
+  constexpr int OCOL = 2 * BCM;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -199,9 +211,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
   uint64_t* x_full = bars;
   uint64_t* x_empty = bars + 1;
-  uint64_t* y_full = bars + 2;                // [NST]
-  uint64_t* y_empty = y_full + LY::NST;       // [NST]
-  uint64_t* s_full = y_empty + LY::NST;        // [2]
+  uint64_t* y_full = bars + 2;                // [NYB] (FWD: K halves, then V halves)
+  uint64_t* y_empty = y_full + LY::NYB;       // [NYB]
+  uint64_t* s_full = y_empty + LY::NYB;       // [2]
   uint64_t* s_empty = s_full + 2;             // [2]
   uint64_t* e_full = s_empty + 2;             // [2]
   uint64_t* e_empty = e_full + 2;             // [2]  backward: accumulating MMAs done with E
@@ -217,7 +229,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(x_full), 1);
     mbar_init(smem_u32(x_empty), 1);
-    for (int i = 0; i < LY::NST; ++i) {
+    for (int i = 0; i < LY::NYB; ++i) {
       mbar_init(smem_u32(&y_full[i]), 1);
       mbar_init(smem_u32(&y_empty[i]), 1);
     }
@@ -244,7 +256,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // Lane 0 loads the stationary tiles and the streamed blocks; in the forward
+    // lane 1 loads the V blocks on their own barriers, so that a stage's K half
+    // is refilled as soon as S has read it, before P V has read the V half.
+    if (lane == 0 || (MODE == FWD && lane == 1)) {
+      const bool vlane = MODE == FWD && lane == 1;
       for (int i = 0; i < LY::NX; ++i) tma_prefetch_desc(&P.mx[i]);
       for (int i = 0; i < 2; ++i) tma_prefetch_desc(&P.my[i]);
       bool ok = true;
@@ -255,33 +271,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
         decode<MODE>(P, u, t, bh);
         blocks<MODE>(P, t, first, last);
         const int b = bh / P.H, col = (bh % P.H) * DH;
-        if (!bwait(smem_u32(x_empty), (tn & 1u) ^ 1u, abort_flag, P.status)) {
-          ok = false;
-          break;
-        }
-        const uint32_t xb = smem_u32(x_full);
-        mbar_expect_tx(xb, LY::NX * XTILE);
-        for (int i = 0; i < LY::NX; ++i)
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d(smem_u32(sX + i * XTILE + c * SUB_R), &P.mx[i], col + 64 * c, t * BR, b, xb);
-        ++x_loads;
-        for (int j = first; j < last; ++j, ++jn) {
-          const int st = jn % LY::NST;
-          if (!bwait(smem_u32(&y_empty[st]), ((jn / LY::NST) & 1u) ^ 1u, abort_flag, P.status)) {
+        if (!vlane) {
+          if (!bwait(smem_u32(x_empty), (tn & 1u) ^ 1u, abort_flag, P.status)) {
             ok = false;
             break;
           }
-          const uint32_t yb = smem_u32(&y_full[st]);
-          mbar_expect_tx(yb, STAGE + (MODE == BKV ? AUX : 0));
-          uint8_t* stg = sY + st * STAGE;
-          for (int i = 0; i < 2; ++i)
+          const uint32_t xb = smem_u32(x_full);
+          mbar_expect_tx(xb, LY::NX * XTILE);
+          for (int i = 0; i < LY::NX; ++i)
             for (int c = 0; c < 2; ++c)
-              tma_load_3d(smem_u32(stg + i * 2 * SUB_C + c * SUB_C), &P.my[i], col + 64 * c,
-                          j * BC, b, yb);
-          if constexpr (MODE == BKV) {
-            const int64_t off = static_cast<int64_t>(bh) * P.Lp + j * BC;
-            bulk_load(smem_u32(sAux + st * (AUX / 4)), P.l2 + off, BC * 4, yb);
-            bulk_load(smem_u32(sAux + st * (AUX / 4) + BC), P.dd + off, BC * 4, yb);
+              tma_load_3d(smem_u32(sX + i * XTILE + c * SUB_R), &P.mx[i], col + 64 * c, t * BR,
+                          b, xb);
+          ++x_loads;
+        }
+        for (int j = first; j < last; ++j, ++jn) {
+          const int st = jn % LY::NST;
+          const int bi = vlane ? LY::NST + st : st;  // this lane's barrier of the stage
+          if (!bwait(smem_u32(&y_empty[bi]), ((jn / LY::NST) & 1u) ^ 1u, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t yb = smem_u32(&y_full[bi]);
+          uint8_t* stg = sY + st * STG;
+          if constexpr (MODE == FWD) {
+            // one block of K (lane 0) or of V (lane 1)
+            const int i = vlane ? 1 : 0;
+            mbar_expect_tx(yb, 2 * SUBC);
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d(smem_u32(stg + i * 2 * SUBC + c * SUBC), &P.my[i], col + 64 * c,
+                          j * BCM, b, yb);
+          } else {
+            mbar_expect_tx(yb, STG + (MODE == BKV ? AUX : 0));
+            for (int i = 0; i < 2; ++i)
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d(smem_u32(stg + i * 2 * SUBC + c * SUBC), &P.my[i], col + 64 * c,
+                            j * BCM, b, yb);
+            if constexpr (MODE == BKV) {
+              const int64_t off = static_cast<int64_t>(bh) * P.Lp + j * BC;
+              bulk_load(smem_u32(sAux + st * (AUX / 4)), P.l2 + off, BC * 4, yb);
+              bulk_load(smem_u32(sAux + st * (AUX / 4) + BC), P.dd + off, BC * 4, yb);
+            }
           }
         }
       }
@@ -290,7 +319,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
         const unsigned long long lim = 50ull * 1000 * 1000;
         for (uint32_t i = 0; i < LY::NST && i < jn; ++i) {
           const uint32_t k = jn - 1 - i;
-          bwait(smem_u32(&y_full[k % LY::NST]), (k / LY::NST) & 1u, abort_flag, P.status, lim);
+          const int bi = (vlane ? LY::NST : 0) + static_cast<int>(k % LY::NST);
+          bwait(smem_u32(&y_full[bi]), (k / LY::NST) & 1u, abort_flag, P.status, lim);
         }
         if (x_loads > 0) bwait(smem_u32(x_full), (x_loads - 1) & 1u, abort_flag, P.status, lim);
       }
@@ -298,7 +328,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t ID_S = instr_desc(128, BC, false, false);   // S, dP: K-major B
+      constexpr uint32_t ID_S = instr_desc(128, BCM, false, false);  // S, dP: K-major B
       constexpr uint32_t ID_A = instr_desc(128, DH, false, true);    // sums: MN-major B
       bool ok = true;
       uint32_t tn = 0, jn = 0;
@@ -308,25 +338,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
         if (!bwait(smem_u32(&y_full[st]), (n / LY::NST) & 1u, abort_flag, P.status)) return false;
         if (!bwait(smem_u32(&s_empty[bf]), ((n >> 1) & 1u) ^ 1u, abort_flag, P.status)) return false;
         tc_fence_after();
-        const uint32_t y = smem_u32(sY + st * STAGE);
+        const uint32_t y = smem_u32(sY + st * STG);
         const uint32_t x = smem_u32(sX);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16<1>(tmem + bf * BC, smem_desc(x + c * SUB_R + kk * 32, false),
-                        smem_desc(y + c * SUB_C + kk * 32, false), ID_S, (c | kk) ? 1u : 0u);
+            mma_bf16<1>(tmem + bf * BCM, smem_desc(x + c * SUB_R + kk * 32, false),
+                        smem_desc(y + c * SUBC + kk * 32, false), ID_S, (c | kk) ? 1u : 0u);
         if constexpr (MODE != FWD) {
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16<1>(tmem + 128 + bf * BC,
+              mma_bf16<1>(tmem + 128 + bf * BCM,
                           smem_desc(x + XTILE + c * SUB_R + kk * 32, false),
-                          smem_desc(y + 2 * SUB_C + c * SUB_C + kk * 32, false), ID_S,
+                          smem_desc(y + 2 * SUBC + c * SUBC + kk * 32, false), ID_S,
                           (c | kk) ? 1u : 0u);
         }
         mma_commit<1>(smem_u32(&s_full[bf]));
+        if constexpr (MODE == FWD) mma_commit<1>(smem_u32(&y_empty[st]));  // K read
         return true;
       };
       for (int u = blockIdx.x; ok && u < P.ntiles; u += gridDim.x, ++tn) {
@@ -353,6 +384,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             ok = false;
             break;
           }
+          if constexpr (MODE == FWD) {
+            // the block's V half
+            if (!bwait(smem_u32(&y_full[LY::NST + st]), (jn / LY::NST) & 1u, abort_flag,
+                       P.status)) {
+              ok = false;
+              break;
+            }
+          }
           // the first accumulating product of a tile overwrites its TMEM sums: they
           // must have been read out (FWD: O alternates between two buffers by tile)
           const int ab = (MODE == FWD) ? static_cast<int>(tn & 1u) : 0;
@@ -362,35 +401,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             break;
           }
           tc_fence_after();
-          const uint32_t y = smem_u32(sY + st * STAGE);
-          const uint32_t e = smem_u32(sE + bf * EBUF);
+          const uint32_t y = smem_u32(sY + st * STG);
+          const uint32_t e = smem_u32(sE + (LY::NPB == 2 ? bf : 0) * EB);
           const uint32_t acc = (i > 0) ? 1u : 0u;
           if constexpr (MODE == FWD) {
-            // O += P V_j: A = P [128 x 64 keys], B = V_j read MN-major [d_head x 64 keys]
+            // O += P V_j: A = P [128 x BCM keys] (64-key sub-tiles of 16 KB), B = V_j
+            // read MN-major [d_head x BCM keys] (its two d_head halves SUBC apart)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16<1>(tmem + 128 + ab * DH, smem_desc(e + kk * 32, false),
-                          smem_desc(y + 2 * SUB_C + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
+            for (int kk = 0; kk < BCM / 16; ++kk)
+              mma_bf16<1>(tmem + OCOL + ab * DH,
+                          smem_desc(e + (kk >> 2) * (BR * 128) + (kk & 3) * 32, false),
+                          smem_desc_mn(y + 2 * SUBC + kk * 2048, SUBC), ID_A,
+                          (acc | kk) ? 1u : 0u);
           } else if constexpr (MODE == BKV) {
             // dV += P^T dO_i ; dK += dS^T Q_i
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_bf16<1>(tmem + 256, smem_desc(e + kk * 32, false),
-                          smem_desc(y + 2 * SUB_C + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
+                          smem_desc_mn(y + 2 * SUBC + kk * 2048, SUBC), ID_A, (acc | kk) ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16<1>(tmem + 384, smem_desc(e + 2 * EBUF + kk * 32, false),
-                          smem_desc(y + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
+              mma_bf16<1>(tmem + 384, smem_desc(e + LY::NPB * EB + kk * 32, false),
+                          smem_desc_mn(y + kk * 2048, SUBC), ID_A, (acc | kk) ? 1u : 0u);
           } else {
             // dQ += dS K_j
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_bf16<1>(tmem + 384, smem_desc(e + kk * 32, false),
-                          smem_desc(y + kk * 2048, true), ID_A, (acc | kk) ? 1u : 0u);
+                          smem_desc_mn(y + kk * 2048, SUBC), ID_A, (acc | kk) ? 1u : 0u);
           }
-          // the E tiles of this buffer are free, and (FWD) O holds block i
+          // the E tiles of this buffer are free, (FWD) O holds block i, the
+          // stage (FWD: its V half) is no longer read
           mma_commit<1>(smem_u32(&e_empty[bf]));
-          mma_commit<1>(smem_u32(&y_empty[st]));
+          mma_commit<1>(smem_u32(&y_empty[(MODE == FWD ? LY::NST : 0) + st]));
         }
         if (!ok) break;
         if constexpr (MODE != FWD) mma_commit<1>(smem_u32(&a_full[0]));
@@ -442,40 +485,63 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
       if constexpr (MODE == FWD) {
         float* xl = reinterpret_cast<float*>(smem + LY::XCH_OFF);  // [2 tile parity][2 half][128]
         const int ob = static_cast<int>(tn & 1u);                    // this tile's O buffer
-        const uint32_t ocol = 128 + ob * DH + 64 * hf;
+        const uint32_t ocol = OCOL + ob * DH + 64 * hf;
         float m = -INFINITY, l = 0.f;
         for (int j = first; j < last; ++j, ++jn) {
           const int bf = jn & 1;
-          if (!wwait(&s_full[bf], (jn >> 1) & 1u) ||
-              !wwait(&e_empty[bf], ((jn >> 1) & 1u) ^ 1u)) {
+          if (!wwait(&s_full[bf], (jn >> 1) & 1u)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // Raw scores of the row: both halves of the block (this warp's own half
-          // and the other warp's, for the row maximum). Scale > 0, so the maximum
-          // is taken on raw scores; masked scores are -inf.
-          const int c0 = j * BC + 32 * hf, c1 = j * BC + 32 * (1 - hf);
-          const bool need_mask = (P.causal && j * BC + BC - 1 > t * BR) || j * BC + BC > P.L;
-          uint32_t xr[32], yr[32];
-          tmem_ld32_nowait(tmem + lb + bf * BC + 32 * hf, xr);
-          tmem_ld32_nowait(tmem + lb + bf * BC + 32 * (1 - hf), yr);
-          tmem_wait_ld2(xr, yr);
-          float x[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(xr[i]);
+          // Raw scores of the row: this warp's own 64 columns of the block, and the
+          // other warp's 64 for the row maximum. Scale > 0, so the maximum is taken
+          // on raw scores; masked scores are -inf.
+          const int c0 = j * BCM + 64 * hf, c1 = j * BCM + 64 * (1 - hf);
+          const bool need_mask = (P.causal && j * BCM + BCM - 1 > t * BR) || j * BCM + BCM > P.L;
+          float x[64];
           float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          if (need_mask) {
+          {
+            uint32_t xa[32], xb[32];
+            tmem_ld32_nowait(tmem + lb + bf * BCM + 64 * hf, xa);
+            tmem_ld32_nowait(tmem + lb + bf * BCM + 64 * hf + 32, xb);
+            tmem_wait_ld2(xa, xb);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              x[i] = (c0 + i >= lo && c0 + i <= hi) ? x[i] : -INFINITY;
-              const float yv = (c1 + i >= lo && c1 + i <= hi) ? __uint_as_float(yr[i]) : -INFINITY;
-              mx[i & 3] = max3(mx[i & 3], x[i], yv);
+              x[i] = __uint_as_float(xa[i]);
+              x[32 + i] = __uint_as_float(xb[i]);
             }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mx[i & 3] = max3(mx[i & 3], x[i], __uint_as_float(yr[i]));
           }
+          if (need_mask) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) x[i] = (c0 + i >= lo && c0 + i <= hi) ? x[i] : -INFINITY;
+          }
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], x[i], x[i + 1]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t yr[32];
+            tmem_ld32_nowait(tmem + lb + bf * BCM + 64 * (1 - hf) + 32 * h, yr);
+            tmem_wait_ld2(yr, yr);
+            if (need_mask) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const int c = c1 + 32 * h + i;
+                const float y0 = (c >= lo && c <= hi) ? __uint_as_float(yr[i]) : -INFINITY;
+                const float y1 = (c + 1 >= lo && c + 1 <= hi) ? __uint_as_float(yr[i + 1]) : -INFINITY;
+                mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], y0, y1);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; i += 2)
+                mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], __uint_as_float(yr[i]),
+                                        __uint_as_float(yr[i + 1]));
+            }
+          }
+          // S is in registers: the MMA may compute the block after next into its buffer
+          tc_fence_before();
+          __syncwarp();
+          arrive(&s_empty[bf]);
           const float bm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * P.scale_log2;
           const float m_new = fmaxf(m, bm);
           // (a warp-wide decision: the TMEM accesses below are warp-collective;
@@ -505,22 +571,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             l *= a;
             m = m_new;
           }
+          // the single P tile: the previous block's P V must have read it
+          if (jn > 0) {
+            const uint32_t pj = jn - 1;
+            if (!wwait(&e_empty[pj & 1u], (pj >> 1) & 1u)) {
+              ok = false;
+              break;
+            }
+          }
+          uint8_t* pt = sE + hf * (BR * 128);  // this warp's 64-key sub-tile of P
           float rs[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float p0 = ex2f_approx(fmaf(x[i], P.scale_log2, -m));
-            const float p1 = ex2f_approx(fmaf(x[i + 1], P.scale_log2, -m));
-            rs[(i >> 1) & 3] += p0 + p1;
-            pk[i / 2] = pack2(p0, p1);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float p0 = ex2f_approx(fmaf(x[32 * h + i], P.scale_log2, -m));
+              const float p1 = ex2f_approx(fmaf(x[32 * h + i + 1], P.scale_log2, -m));
+              rs[(i >> 1) & 3] += p0 + p1;
+              pk[i / 2] = pack2(p0, p1);
+            }
+            put_row32(pt, r, h, pk);
           }
           l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-          put_row32(sE + bf * EBUF, r, hf, pk);
           fence_proxy_async();
           tc_fence_before();
           __syncwarp();
           arrive(&e_full[bf]);
-          arrive(&s_empty[bf]);
         }
         if (!ok) break;
         // O is complete once the tile's last product has committed
@@ -573,17 +650,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             }
           }
           tc_fence_after();
-          const int c0 = j * BC + 32 * hf;  // first column (query in BKV, key in BQ) of the half
+          const int c0 = j * BCM + 32 * hf;  // first column (query in BKV, key in BQ) of the half
           // some (row, column) pair of the block is not visible: the diagonal
           // blocks of the causal mask and the ragged ends of the sequence
           const bool mask = (MODE == BKV)
-                                ? ((P.causal && j * BC < t * BR + BR - 1) || j * BC + BC > P.L ||
+                                ? ((P.causal && j * BCM < t * BR + BR - 1) || j * BCM + BCM > P.L ||
                                    t * BR + BR > P.L)
-                                : ((P.causal && j * BC + BC - 1 > t * BR) || j * BC + BC > P.L ||
+                                : ((P.causal && j * BCM + BCM - 1 > t * BR) || j * BCM + BCM > P.L ||
                                    t * BR + BR > P.L);
           uint32_t sr[32], dr32[32];
-          tmem_ld32_nowait(tmem + lb + bf * BC + 32 * hf, sr);
-          tmem_ld32_nowait(tmem + lb + 128 + bf * BC + 32 * hf, dr32);
+          tmem_ld32_nowait(tmem + lb + bf * BCM + 32 * hf, sr);
+          tmem_ld32_nowait(tmem + lb + 128 + bf * BCM + 32 * hf, dr32);
           tmem_wait_ld2(sr, dr32);
           if (mask) {
 #pragma unroll
@@ -615,8 +692,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             pd[i / 2] = pack2(ds[0], ds[1]);
             pd[i / 2 + 1] = pack2(ds[2], ds[3]);
           }
-          if constexpr (MODE == BKV) put_row32(sE + bf * EBUF, r, hf, pp);
-          put_row32(sE + (LY::NE - 1) * 2 * EBUF + bf * EBUF, r, hf, pd);
+          if constexpr (MODE == BKV) put_row32(sE + bf * EB, r, hf, pp);
+          put_row32(sE + (LY::NE - 1) * LY::NPB * EB + bf * EB, r, hf, pd);
           fence_proxy_async();
           tc_fence_before();
           __syncwarp();
@@ -800,7 +877,8 @@ cudaError_t attn_forward(Ctx& c, const bn_attn_desc& d, const void* q, const voi
                          const void* v, void* o, float* lse, int* status) {
   using namespace attn;
   Params P = {};
-  if (!encode3(&P.mx[0], q, d, BR) || !encode3(&P.my[0], k, d, BC) || !encode3(&P.my[1], v, d, BC))
+  if (!encode3(&P.mx[0], q, d, BR) || !encode3(&P.my[0], k, d, BCF) ||
+      !encode3(&P.my[1], v, d, BCF))
     return cudaErrorInvalidValue;
   P.B = static_cast<int>(d.B);
   P.L = static_cast<int>(d.L);

@@ -362,6 +362,17 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, bool mn_major) {
   d |= 2ull << 61;                                                   // 128-byte swizzle
   return d;
 }
+// MN-major 128-byte-swizzled tile whose 64-element MN atoms are `lbo` bytes
+// apart (8192 for one TMA box of 64 x 64, 16384 for 64 x 128).
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(lbo >> 4) << 16;                // leading byte offset
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;              // stride byte offset
+  d |= 1ull << 46;                                           // descriptor version
+  d |= 2ull << 61;                                           // 128-byte swizzle
+  return d;
+}
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 D, dense.
 __host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
