@@ -11,7 +11,7 @@
 //
 // One kernel template, three modes, all built on one tile shape: a stationary
 // 128-row tile (one row per TMEM lane and per epilogue thread) and a stream of
-// 64-row blocks of the other side, both d_head = 128 wide.
+// blocks of the other side (128 rows in FWD and BQ, 64 in BKV), d_head = 128.
 //   FWD   stationary Q;        blocks K_j, V_j.   S = Q K_j^T (TMEM), online
 //         softmax in registers, P (bf16) to shared memory, O += P V_j in TMEM;
 //         O is rescaled in place only when a row maximum grows by more than
@@ -20,19 +20,23 @@
 //         P^T and dS^T (bf16) to shared memory, dV += P^T dO_i and
 //         dK += dS^T Q_i accumulated in TMEM.
 //   BQ    stationary Q and dO; blocks K_j, V_j.   S = Q K_j^T, dP = dO V_j^T,
-//         dS to shared memory, dQ += dS K_j in TMEM.
+//         dS to shared memory, dQ += dS K_j in TMEM. dP is read into registers
+//         first and its single TMEM buffer handed back, so the next block's dP
+//         runs during this block's softmax.
 // Per CTA (320 threads, persistent over the tiles, one CTA per SM):
 //   warp 0      TMA producer: the stationary tile(s), then a ring of stages of
-//               streamed blocks (4, or 3 in BKV: what shared memory holds), in
-//               BKV with the blocks' row terms;
+//               streamed blocks (2, or 3 in BKV: what shared memory holds), in
+//               BKV with the blocks' row terms; in FWD and BQ a second lane
+//               loads the V halves on their own barriers;
 //   warp 1      TMEM owner (512 columns) and, from one thread, the MMA issuer;
 //   warps 2..9  elementwise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
-//               tile row per thread) and one 32-column half of every block.
+//               tile row per thread) and one column half of every block.
 // TMEM columns: S double-buffered so that the next block's S = Q K^T runs
 // while the current block's softmax does:
-//   [0, 128)   S of block buffers 0 and 1 (64 columns each)
-//   FWD  [128, 384)  O of tile buffers 0 and 1 (128 columns each; P V accumulates)
-//   BKV, BQ  [128, 256)  dP of block buffers 0 and 1; [256, 384) dV; [384, 512) dK or dQ.
+//   FWD  [0, 256) S of block buffers 0 and 1; [256, 512) O of tile buffers 0 and 1
+//   BKV  [0, 128) S of block buffers 0 and 1; [128, 256) dP of the same;
+//        [256, 384) dV; [384, 512) dK
+//   BQ   [0, 256) S of block buffers 0 and 1; [256, 384) dP (single); [384, 512) dQ
 // Every operand is bf16 in 128-byte-swizzled shared memory: K-major for the
 // S and dP products (rows of 64 elements per 128-byte line), and the streamed
 // blocks' same bytes read MN-major for the accumulating products (the 64
@@ -68,16 +72,16 @@ enum Mode : int { FWD = 0, BKV = 1, BQ = 2 };
 
 template <int MODE>
 struct Lay {
-  static constexpr int BCM = (MODE == FWD) ? BCF : BC;  // rows of a streamed block
+  static constexpr int BCM = (MODE == BKV) ? BC : BCF;  // rows of a streamed block
   static constexpr int SUBC = BCM * 128;              // a 64-column half of a streamed block
   static constexpr int STG = 2 * 2 * SUBC;            // one stage: two streamed blocks
   static constexpr int EB = BR * BCM * 2;             // one bf16 elementwise tile [128, BCM]
   static constexpr int NX = (MODE == FWD) ? 1 : 2;   // stationary tiles
   static constexpr int NE = (MODE == BKV) ? 2 : 1;   // elementwise tiles
-  // buffers of each elementwise tile: the forward's P is single (shared memory);
-  // the softmax waits for the previous block's P V before it writes the next P
-  static constexpr int NPB = (MODE == FWD) ? 1 : 2;
-  static constexpr int NST = (MODE == FWD) ? 2 : (MODE == BKV) ? 3 : 4;  // stages: what fits
+  // buffers of each elementwise tile: the forward's P and dQ's dS are single
+  // (shared memory); the softmax waits for the previous block's product first
+  static constexpr int NPB = (MODE == BKV) ? 2 : 1;
+  static constexpr int NST = (MODE == BKV) ? 3 : 2;  // stages: what fits
   static constexpr int X_OFF = 0;
   static constexpr int Y_OFF = X_OFF + NX * XTILE;
   static constexpr int E_OFF = Y_OFF + NST * STG;
@@ -85,9 +89,10 @@ struct Lay {
   static constexpr int XCH_OFF = AUX_OFF + ((MODE == BKV) ? NST * AUX : 0);
   // FWD: row sums exchanged between the two warps of a row, [2 tile parity][2 half][128]
   static constexpr int BAR_OFF = XCH_OFF + ((MODE == FWD) ? 2 * 2 * BR * 4 : 0);
-  // stage barriers: the forward's K and V halves of a stage are filled and freed
-  // apart (K after S, V after P V), the backward's stage as a whole
-  static constexpr int NYB = (MODE == FWD) ? 2 * NST : NST;
+  // stage barriers: the two halves of a FWD or BQ stage are filled and freed
+  // apart (FWD: K after S, V after P V; BQ: V after dP, K after dQ), BKV's
+  // stage as a whole
+  static constexpr int NYB = (MODE == BKV) ? NST : 2 * NST;
   // barriers (2 + 2 NYB + 21 of 8 bytes), the TMEM address and the abort flag
   static constexpr int BAR_BYTES = (2 + 2 * NYB + 21) * 8 + 8 <= 256 ? 256 : 512;
   static constexpr int BYTES = BAR_OFF + BAR_BYTES;
@@ -256,11 +261,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    // Lane 0 loads the stationary tiles and the streamed blocks; in the forward
-    // lane 1 loads the V blocks on their own barriers, so that a stage's K half
-    // is refilled as soon as S has read it, before P V has read the V half.
-    if (lane == 0 || (MODE == FWD && lane == 1)) {
-      const bool vlane = MODE == FWD && lane == 1;
+    // Lane 0 loads the stationary tiles and the streamed blocks; in FWD and BQ
+    // lane 1 loads the V blocks on their own barriers, so that each half of a
+    // stage is refilled as soon as its last reader is done (FWD: K after S;
+    // BQ: V after dP).
+    if (lane == 0 || (MODE != BKV && lane == 1)) {
+      const bool vlane = MODE != BKV && lane == 1;
       for (int i = 0; i < LY::NX; ++i) tma_prefetch_desc(&P.mx[i]);
       for (int i = 0; i < 2; ++i) tma_prefetch_desc(&P.my[i]);
       bool ok = true;
@@ -293,7 +299,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           }
           const uint32_t yb = smem_u32(&y_full[bi]);
           uint8_t* stg = sY + st * STG;
-          if constexpr (MODE == FWD) {
+          if constexpr (MODE != BKV) {
             // one block of K (lane 0) or of V (lane 1)
             const int i = vlane ? 1 : 0;
             mbar_expect_tx(yb, 2 * SUBC);
@@ -346,7 +352,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16<1>(tmem + bf * BCM, smem_desc(x + c * SUB_R + kk * 32, false),
                         smem_desc(y + c * SUBC + kk * 32, false), ID_S, (c | kk) ? 1u : 0u);
-        if constexpr (MODE != FWD) {
+        if constexpr (MODE == BKV) {
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -360,6 +366,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
         if constexpr (MODE == FWD) mma_commit<1>(smem_u32(&y_empty[st]));  // K read
         return true;
       };
+      // BQ: dP = dO V_n^T of block n into its single TMEM buffer (columns 256..383),
+      // once the elementwise warps hold the previous block's dP in registers
+      // (a_full[1] / a_empty[1] serve as its full / empty barriers)
+      auto issue_dp = [&](uint32_t n) -> bool {
+        const int st = n % LY::NST;
+        if (!bwait(smem_u32(&y_full[LY::NST + st]), (n / LY::NST) & 1u, abort_flag, P.status))
+          return false;
+        if (!bwait(smem_u32(&a_empty[1]), (n & 1u) ^ 1u, abort_flag, P.status)) return false;
+        tc_fence_after();
+        const uint32_t y = smem_u32(sY + st * STG);
+        const uint32_t x = smem_u32(sX);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16<1>(tmem + 256, smem_desc(x + XTILE + c * SUB_R + kk * 32, false),
+                        smem_desc(y + 2 * SUBC + c * SUBC + kk * 32, false), ID_S,
+                        (c | kk) ? 1u : 0u);
+        mma_commit<1>(smem_u32(&a_full[1]));
+        mma_commit<1>(smem_u32(&y_empty[LY::NST + st]));  // V read
+        return true;
+      };
       for (int u = blockIdx.x; ok && u < P.ntiles; u += gridDim.x, ++tn) {
         int t, bh, first, last;
         decode<MODE>(P, u, t, bh);
@@ -370,12 +398,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
         }
         tc_fence_after();
         const int nblk = last - first;
-        if (!issue_sd(jn)) {
+        if (!issue_sd(jn) || (MODE == BQ && !issue_dp(jn))) {
           ok = false;
           break;
         }
         for (int i = 0; i < nblk; ++i, ++jn) {
-          if (i + 1 < nblk && !issue_sd(jn + 1)) {
+          if (i + 1 < nblk && (!issue_sd(jn + 1) || (MODE == BQ && !issue_dp(jn + 1)))) {
             ok = false;
             break;
           }
@@ -424,14 +452,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
               mma_bf16<1>(tmem + 384, smem_desc(e + LY::NPB * EB + kk * 32, false),
                           smem_desc_mn(y + kk * 2048, SUBC), ID_A, (acc | kk) ? 1u : 0u);
           } else {
-            // dQ += dS K_j
+            // dQ += dS K_j: A = dS [128 x BCM keys] (64-key sub-tiles), B = K_j read
+            // MN-major [d_head x BCM keys]
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16<1>(tmem + 384, smem_desc(e + kk * 32, false),
+            for (int kk = 0; kk < BCM / 16; ++kk)
+              mma_bf16<1>(tmem + 384,
+                          smem_desc(e + (kk >> 2) * (BR * 128) + (kk & 3) * 32, false),
                           smem_desc_mn(y + kk * 2048, SUBC), ID_A, (acc | kk) ? 1u : 0u);
           }
           // the E tiles of this buffer are free, (FWD) O holds block i, the
-          // stage (FWD: its V half) is no longer read
+          // stage (FWD: its V half; BQ: its K half) is no longer read
           mma_commit<1>(smem_u32(&e_empty[bf]));
           mma_commit<1>(smem_u32(&y_empty[(MODE == FWD ? LY::NST : 0) + st]));
         }
@@ -635,6 +665,73 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           lr = P.l2[static_cast<int64_t>(bh) * P.Lp + row];
           dr = P.dd[static_cast<int64_t>(bh) * P.Lp + row];
         }
+        if constexpr (MODE == BQ) {
+          for (int j = first; j < last; ++j, ++jn) {
+            const int bf = jn & 1;
+            // dP of the block into registers; its TMEM buffer goes back to the MMA
+            if (!wwait(&a_full[1], jn & 1u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            float dpv[64];
+            {
+              uint32_t da[32], db[32];
+              tmem_ld32_nowait(tmem + lb + 256 + 64 * hf, da);
+              tmem_ld32_nowait(tmem + lb + 256 + 64 * hf + 32, db);
+              tmem_wait_ld2(da, db);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                dpv[i] = __uint_as_float(da[i]) - dr;
+                dpv[32 + i] = __uint_as_float(db[i]) - dr;
+              }
+            }
+            tc_fence_before();
+            __syncwarp();
+            arrive(&a_empty[1]);
+            if (!wwait(&s_full[bf], (jn >> 1) & 1u)) {
+              ok = false;
+              break;
+            }
+            // the single dS tile: the previous block's dQ product must have read it
+            if (jn > 0) {
+              const uint32_t pj = jn - 1;
+              if (!wwait(&e_empty[pj & 1u], (pj >> 1) & 1u)) {
+                ok = false;
+                break;
+              }
+            }
+            tc_fence_after();
+            const bool mask = (P.causal && j * BCM + BCM - 1 > t * BR) || j * BCM + BCM > P.L ||
+                              t * BR + BR > P.L;
+            uint8_t* dt = sE + hf * (BR * 128);  // this warp's 64-key sub-tile of dS
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t sr[32];
+              tmem_ld32_nowait(tmem + lb + bf * BCM + 64 * hf + 32 * h, sr);
+              tmem_wait_ld2(sr, sr);
+              if (mask) {
+                const int c0 = j * BCM + 64 * hf + 32 * h;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (!(c0 + i >= lo && c0 + i <= hi)) sr[i] = __float_as_uint(-INFINITY);
+              }
+              uint32_t pd[16];
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const float p0 = ex2f_approx(fmaf(__uint_as_float(sr[i]), P.scale_log2, -lr));
+                const float p1 = ex2f_approx(fmaf(__uint_as_float(sr[i + 1]), P.scale_log2, -lr));
+                pd[i / 2] = pack2(p0 * dpv[32 * h + i], p1 * dpv[32 * h + i + 1]);
+              }
+              put_row32(dt, r, h, pd);
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncwarp();
+            arrive(&e_full[bf]);
+            arrive(&s_empty[bf]);
+          }
+        } else {
         for (int j = first; j < last; ++j, ++jn) {
           const int bf = jn & 1, st = jn % LY::NST;
           if (!wwait(&s_full[bf], (jn >> 1) & 1u) ||
@@ -699,6 +796,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           __syncwarp();
           arrive(&e_full[bf]);
           arrive(&s_empty[bf]);
+        }
         }
         if (!ok) break;
         if (!wwait(&a_full[0], tn & 1u)) {
@@ -936,7 +1034,7 @@ cudaError_t attn_backward(Ctx& c, const bn_attn_desc& d, const void* q, const vo
   if (e != cudaSuccess) return e;
   Params Q = P;
   if (!encode3(&Q.mx[0], q, d, BR) || !encode3(&Q.mx[1], dout, d, BR) ||
-      !encode3(&Q.my[0], k, d, BC) || !encode3(&Q.my[1], v, d, BC))
+      !encode3(&Q.my[0], k, d, BCF) || !encode3(&Q.my[1], v, d, BCF))
     return cudaErrorInvalidValue;
   Q.out1 = static_cast<__nv_bfloat16*>(dq);
   return launch<BQ>(c, Q, 6.0 * DH * pairs, 5.0 * elems * 2 + 2.0 * rows * 4);
