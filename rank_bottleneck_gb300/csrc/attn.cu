@@ -11,31 +11,32 @@
 //
 // One kernel template, three modes, all built on one tile shape: a stationary
 // 128-row tile (one row per TMEM lane and per epilogue thread) and a stream of
-// blocks of the other side (128 rows in FWD and BQ, 64 in BKV), d_head = 128.
+// 128-row blocks of the other side, d_head = 128.
 //   FWD   stationary Q;        blocks K_j, V_j.   S = Q K_j^T (TMEM), online
 //         softmax in registers, P (bf16) to shared memory, O += P V_j in TMEM;
 //         O is rescaled in place only when a row maximum grows by more than
 //         2^8 (lazy rescale), and divided by the row sum at the end.
-//   BKV   stationary K and V;  blocks Q_i, dO_i.  S^T = K Q_i^T, dP^T = V dO_i^T,
-//         P^T and dS^T (bf16) to shared memory, dV += P^T dO_i and
-//         dK += dS^T Q_i accumulated in TMEM.
+//   BKV   stationary K and V;  blocks Q_i, dO_i.  S^T = K Q_i^T, dP^T = V dO_i^T;
+//         dP^T is read into registers and its buffer handed back; P^T and dS^T
+//         (bf16 pairs) are written into TMEM over the S^T columns already read,
+//         and dV += P^T dO_i, dK += dS^T Q_i take them from there (A operand in
+//         TMEM), which leaves shared memory for a two-stage ring.
 //   BQ    stationary Q and dO; blocks K_j, V_j.   S = Q K_j^T, dP = dO V_j^T,
 //         dS to shared memory, dQ += dS K_j in TMEM. dP is read into registers
 //         first and its single TMEM buffer handed back, so the next block's dP
 //         runs during this block's softmax.
 // Per CTA (320 threads, persistent over the tiles, one CTA per SM):
 //   warp 0      TMA producer: the stationary tile(s), then a ring of stages of
-//               streamed blocks (2, or 3 in BKV: what shared memory holds), in
-//               BKV with the blocks' row terms; in FWD and BQ a second lane
-//               loads the V halves on their own barriers;
+//               streamed blocks (2: what shared memory holds), in BKV with the
+//               blocks' row terms; in FWD and BQ a second lane loads the V
+//               halves on their own barriers;
 //   warp 1      TMEM owner (512 columns) and, from one thread, the MMA issuer;
 //   warps 2..9  elementwise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
 //               tile row per thread) and one column half of every block.
 // TMEM columns: S double-buffered so that the next block's S = Q K^T runs
 // while the current block's softmax does:
 //   FWD  [0, 256) S of block buffers 0 and 1; [256, 512) O of tile buffers 0 and 1
-//   BKV  [0, 128) S of block buffers 0 and 1; [128, 256) dP of the same;
-//        [256, 384) dV; [384, 512) dK
+//   BKV  [0, 128) S^T (then P^T, dS^T); [128, 256) dP^T; [256, 384) dV; [384, 512) dK
 //   BQ   [0, 256) S of block buffers 0 and 1; [256, 384) dP (single); [384, 512) dQ
 // Every operand is bf16 in 128-byte-swizzled shared memory: K-major for the
 // S and dP products (rows of 64 elements per 128-byte line), and the streamed
@@ -59,12 +60,10 @@ using namespace tc;
 
 constexpr int DH = 128;      // head width
 constexpr int BR = 128;      // rows of the stationary tile
-constexpr int BC = 64;       // rows of a streamed block (backward)
-constexpr int BCF = 128;     // rows of a streamed block (forward)
+constexpr int BCF = 128;     // rows of a streamed block
 constexpr int NTHREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2..9 elementwise
 constexpr int SUB_R = BR * 128;          // one 64-column half of a stationary tile: 16 KB
 constexpr int XTILE = 2 * SUB_R;         // a stationary tile: 32 KB
-constexpr int AUX = 512;                 // BKV: 64 l2 + 64 D floats per stage
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -72,21 +71,23 @@ enum Mode : int { FWD = 0, BKV = 1, BQ = 2 };
 
 template <int MODE>
 struct Lay {
-  static constexpr int BCM = (MODE == BKV) ? BC : BCF;  // rows of a streamed block
+  static constexpr int BCM = BCF;                       // rows of a streamed block
   static constexpr int SUBC = BCM * 128;              // a 64-column half of a streamed block
   static constexpr int STG = 2 * 2 * SUBC;            // one stage: two streamed blocks
   static constexpr int EB = BR * BCM * 2;             // one bf16 elementwise tile [128, BCM]
   static constexpr int NX = (MODE == FWD) ? 1 : 2;   // stationary tiles
-  static constexpr int NE = (MODE == BKV) ? 2 : 1;   // elementwise tiles
+  // elementwise tiles in shared memory (BKV writes P^T and dS^T into TMEM)
+  static constexpr int NE = (MODE == BKV) ? 0 : 1;
   // buffers of each elementwise tile: the forward's P and dQ's dS are single
   // (shared memory); the softmax waits for the previous block's product first
   static constexpr int NPB = (MODE == BKV) ? 2 : 1;
-  static constexpr int NST = (MODE == BKV) ? 3 : 2;  // stages: what fits
+  static constexpr int NST = 2;  // stages: what shared memory holds
+  static constexpr int AUXB = (MODE == BKV) ? 2 * BCM * 4 : 0;  // BKV: a block's lse log2 e and D
   static constexpr int X_OFF = 0;
   static constexpr int Y_OFF = X_OFF + NX * XTILE;
   static constexpr int E_OFF = Y_OFF + NST * STG;
   static constexpr int AUX_OFF = E_OFF + NE * NPB * EB;
-  static constexpr int XCH_OFF = AUX_OFF + ((MODE == BKV) ? NST * AUX : 0);
+  static constexpr int XCH_OFF = AUX_OFF + NST * AUXB;
   // FWD: row sums exchanged between the two warps of a row, [2 tile parity][2 half][128]
   static constexpr int BAR_OFF = XCH_OFF + ((MODE == FWD) ? 2 * 2 * BR * 4 : 0);
   // stage barriers: the two halves of a FWD or BQ stage are filled and freed
@@ -307,15 +308,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
               tma_load_3d(smem_u32(stg + i * 2 * SUBC + c * SUBC), &P.my[i], col + 64 * c,
                           j * BCM, b, yb);
           } else {
-            mbar_expect_tx(yb, STG + (MODE == BKV ? AUX : 0));
+            mbar_expect_tx(yb, STG + LY::AUXB);
             for (int i = 0; i < 2; ++i)
               for (int c = 0; c < 2; ++c)
                 tma_load_3d(smem_u32(stg + i * 2 * SUBC + c * SUBC), &P.my[i], col + 64 * c,
                             j * BCM, b, yb);
             if constexpr (MODE == BKV) {
-              const int64_t off = static_cast<int64_t>(bh) * P.Lp + j * BC;
-              bulk_load(smem_u32(sAux + st * (AUX / 4)), P.l2 + off, BC * 4, yb);
-              bulk_load(smem_u32(sAux + st * (AUX / 4) + BC), P.dd + off, BC * 4, yb);
+              const int64_t off = static_cast<int64_t>(bh) * P.Lp + j * BCM;
+              bulk_load(smem_u32(sAux + st * (LY::AUXB / 4)), P.l2 + off, BCM * 4, yb);
+              bulk_load(smem_u32(sAux + st * (LY::AUXB / 4) + BCM), P.dd + off, BCM * 4, yb);
             }
           }
         }
@@ -388,6 +389,91 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
         mma_commit<1>(smem_u32(&y_empty[LY::NST + st]));  // V read
         return true;
       };
+      // BKV: S^T and dP^T of block n into their single TMEM buffers; S^T's buffer
+      // is free once block n - 1's dV, dK products (which read P^T, dS^T from it)
+      // have completed, dP^T's once the elementwise warps hold dP^T(n - 1)
+      auto kv_s = [&](uint32_t n) -> bool {
+        const int st = n % LY::NST;
+        if (!bwait(smem_u32(&y_full[st]), (n / LY::NST) & 1u, abort_flag, P.status)) return false;
+        if (n > 0 && !bwait(smem_u32(&e_empty[0]), (n - 1) & 1u, abort_flag, P.status))
+          return false;
+        tc_fence_after();
+        const uint32_t y = smem_u32(sY + st * STG);
+        const uint32_t x = smem_u32(sX);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16<1>(tmem, smem_desc(x + c * SUB_R + kk * 32, false),
+                        smem_desc(y + c * SUBC + kk * 32, false), ID_S, (c | kk) ? 1u : 0u);
+        mma_commit<1>(smem_u32(&s_full[0]));
+        return true;
+      };
+      auto kv_dp = [&](uint32_t n) -> bool {
+        const int st = n % LY::NST;
+        if (!bwait(smem_u32(&y_full[st]), (n / LY::NST) & 1u, abort_flag, P.status)) return false;
+        if (!bwait(smem_u32(&a_empty[1]), (n & 1u) ^ 1u, abort_flag, P.status)) return false;
+        tc_fence_after();
+        const uint32_t y = smem_u32(sY + st * STG);
+        const uint32_t x = smem_u32(sX);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16<1>(tmem + 128, smem_desc(x + XTILE + c * SUB_R + kk * 32, false),
+                        smem_desc(y + 2 * SUBC + c * SUBC + kk * 32, false), ID_S,
+                        (c | kk) ? 1u : 0u);
+        mma_commit<1>(smem_u32(&a_full[1]));
+        return true;
+      };
+      if constexpr (MODE == BKV) {
+        for (int u = blockIdx.x; ok && u < P.ntiles; u += gridDim.x, ++tn) {
+          int t, bh, first, last;
+          decode<MODE>(P, u, t, bh);
+          blocks<MODE>(P, t, first, last);
+          if (!bwait(smem_u32(x_full), tn & 1u, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nblk = last - first;
+          if (!kv_s(jn) || !kv_dp(jn)) {
+            ok = false;
+            break;
+          }
+          for (int i = 0; i < nblk; ++i, ++jn) {
+            const int st = jn % LY::NST;
+            if (!bwait(smem_u32(&e_full[0]), jn & 1u, abort_flag, P.status) ||
+                (i == 0 && !bwait(smem_u32(&a_empty[0]), (tn & 1u) ^ 1u, abort_flag, P.status))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // dV += P^T dO_i and dK += dS^T Q_i, P^T and dS^T read from TMEM: the
+            // 16 queries of k-step kk are warp half kk / 4's chunk (kk % 4) / 2,
+            // P^T in that chunk's first 16 columns, dS^T in the next 16
+            const uint32_t y = smem_u32(sY + st * STG);
+            const uint32_t acc = (i > 0) ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < BCM / 16; ++kk) {
+              const uint32_t pa = tmem + 64 * (kk >> 2) + 32 * ((kk >> 1) & 1) + 8 * (kk & 1);
+              mma_bf16_ta(tmem + 256, pa, smem_desc_mn(y + 2 * SUBC + kk * 2048, SUBC), ID_A,
+                          (acc | kk) ? 1u : 0u);
+              mma_bf16_ta(tmem + 384, pa + 16, smem_desc_mn(y + kk * 2048, SUBC), ID_A,
+                          (acc | kk) ? 1u : 0u);
+            }
+            mma_commit<1>(smem_u32(&e_empty[0]));
+            mma_commit<1>(smem_u32(&y_empty[st]));
+            if (i + 1 < nblk && (!kv_dp(jn + 1) || !kv_s(jn + 1))) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          mma_commit<1>(smem_u32(&a_full[0]));
+          mma_commit<1>(smem_u32(x_empty));
+        }
+      } else
       for (int u = blockIdx.x; ok && u < P.ntiles; u += gridDim.x, ++tn) {
         int t, bh, first, last;
         decode<MODE>(P, u, t, bh);
@@ -732,71 +818,81 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             arrive(&s_empty[bf]);
           }
         } else {
-        for (int j = first; j < last; ++j, ++jn) {
-          const int bf = jn & 1, st = jn % LY::NST;
-          if (!wwait(&s_full[bf], (jn >> 1) & 1u) ||
-              !wwait(&e_empty[bf], ((jn >> 1) & 1u) ^ 1u)) {
-            ok = false;
-            break;
-          }
-          if constexpr (MODE == BKV) {
-            // the block's row terms arrived with its stage
-            if (!wwait(&y_full[st], (jn / LY::NST) & 1u)) {
+          // BKV: rows are keys, columns the block's 128 queries
+          for (int j = first; j < last; ++j, ++jn) {
+            const int st = jn % LY::NST;
+            // the block's row terms (lse log2 e, D of its queries) came with its stage
+            if (!wwait(&y_full[st], (jn / LY::NST) & 1u) || !wwait(&a_full[1], jn & 1u)) {
               ok = false;
               break;
             }
-          }
-          tc_fence_after();
-          const int c0 = j * BCM + 32 * hf;  // first column (query in BKV, key in BQ) of the half
-          // some (row, column) pair of the block is not visible: the diagonal
-          // blocks of the causal mask and the ragged ends of the sequence
-          const bool mask = (MODE == BKV)
-                                ? ((P.causal && j * BCM < t * BR + BR - 1) || j * BCM + BCM > P.L ||
-                                   t * BR + BR > P.L)
-                                : ((P.causal && j * BCM + BCM - 1 > t * BR) || j * BCM + BCM > P.L ||
-                                   t * BR + BR > P.L);
-          uint32_t sr[32], dr32[32];
-          tmem_ld32_nowait(tmem + lb + bf * BCM + 32 * hf, sr);
-          tmem_ld32_nowait(tmem + lb + 128 + bf * BCM + 32 * hf, dr32);
-          tmem_wait_ld2(sr, dr32);
-          if (mask) {
+            tc_fence_after();
+            const float* al = sAux + st * (LY::AUXB / 4) + 64 * hf;  // this half's 64 queries
+            // dP^T into registers (minus D), then its TMEM buffer goes back to the MMA
+            float dpv[64];
+            {
+              uint32_t da[32], db[32];
+              tmem_ld32_nowait(tmem + lb + 128 + 64 * hf, da);
+              tmem_ld32_nowait(tmem + lb + 128 + 64 * hf + 32, db);
+              tmem_wait_ld2(da, db);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (!(c0 + i >= lo && c0 + i <= hi)) sr[i] = __float_as_uint(-INFINITY);
-          }
-          uint32_t pp[16], pd[16];
-          const float* al = sAux + st * (AUX / 4) + 32 * hf;
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float lv[4], dv[4];
-            if constexpr (MODE == BKV) {
-              const float4 a = *reinterpret_cast<const float4*>(al + i);
-              const float4 d4 = *reinterpret_cast<const float4*>(al + BC + i);
-              lv[0] = a.x; lv[1] = a.y; lv[2] = a.z; lv[3] = a.w;
-              dv[0] = d4.x; dv[1] = d4.y; dv[2] = d4.z; dv[3] = d4.w;
-            } else {
-              lv[0] = lv[1] = lv[2] = lv[3] = lr;
-              dv[0] = dv[1] = dv[2] = dv[3] = dr;
+              for (int i = 0; i < 32; i += 4) {
+                const float4 d0 = *reinterpret_cast<const float4*>(al + BCM + i);
+                const float4 d1 = *reinterpret_cast<const float4*>(al + BCM + 32 + i);
+                dpv[i] = __uint_as_float(da[i]) - d0.x;
+                dpv[i + 1] = __uint_as_float(da[i + 1]) - d0.y;
+                dpv[i + 2] = __uint_as_float(da[i + 2]) - d0.z;
+                dpv[i + 3] = __uint_as_float(da[i + 3]) - d0.w;
+                dpv[32 + i] = __uint_as_float(db[i]) - d1.x;
+                dpv[32 + i + 1] = __uint_as_float(db[i + 1]) - d1.y;
+                dpv[32 + i + 2] = __uint_as_float(db[i + 2]) - d1.z;
+                dpv[32 + i + 3] = __uint_as_float(db[i + 3]) - d1.w;
+              }
             }
-            float p[4], ds[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              p[k] = ex2f_approx(fmaf(__uint_as_float(sr[i + k]), P.scale_log2, -lv[k]));
-              ds[k] = p[k] * (__uint_as_float(dr32[i + k]) - dv[k]);
+            tc_fence_before();
+            __syncwarp();
+            arrive(&a_empty[1]);
+            if (!wwait(&s_full[0], jn & 1u)) {
+              ok = false;
+              break;
             }
-            pp[i / 2] = pack2(p[0], p[1]);
-            pp[i / 2 + 1] = pack2(p[2], p[3]);
-            pd[i / 2] = pack2(ds[0], ds[1]);
-            pd[i / 2 + 1] = pack2(ds[2], ds[3]);
+            tc_fence_after();
+            const bool mask = (P.causal && j * BCM < t * BR + BR - 1) || j * BCM + BCM > P.L ||
+                              t * BR + BR > P.L;
+            // Per 32-query chunk h: S^T in, then P^T (16 columns of bf16 pairs) and
+            // dS^T (the next 16) written over the chunk's own columns, already read.
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t sr[32];
+              tmem_ld32_nowait(tmem + lb + 64 * hf + 32 * h, sr);
+              tmem_wait_ld2(sr, sr);
+              if (mask) {
+                const int c0 = j * BCM + 64 * hf + 32 * h;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (!(c0 + i >= lo && c0 + i <= hi)) sr[i] = __float_as_uint(-INFINITY);
+              }
+              uint32_t o[32];
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                const float4 lv = *reinterpret_cast<const float4*>(al + 32 * h + i);
+                const float l4[4] = {lv.x, lv.y, lv.z, lv.w};
+                float pv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  pv[k] = ex2f_approx(fmaf(__uint_as_float(sr[i + k]), P.scale_log2, -l4[k]));
+                o[i / 2] = pack2(pv[0], pv[1]);
+                o[i / 2 + 1] = pack2(pv[2], pv[3]);
+                o[16 + i / 2] = pack2(pv[0] * dpv[32 * h + i], pv[1] * dpv[32 * h + i + 1]);
+                o[16 + i / 2 + 1] = pack2(pv[2] * dpv[32 * h + i + 2], pv[3] * dpv[32 * h + i + 3]);
+              }
+              tmem_st32u_nowait(tmem + lb + 64 * hf + 32 * h, o);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            arrive(&e_full[0]);
           }
-          if constexpr (MODE == BKV) put_row32(sE + bf * EB, r, hf, pp);
-          put_row32(sE + (LY::NE - 1) * LY::NPB * EB + bf * EB, r, hf, pd);
-          fence_proxy_async();
-          tc_fence_before();
-          __syncwarp();
-          arrive(&e_full[bf]);
-          arrive(&s_empty[bf]);
-        }
         }
         if (!ok) break;
         if (!wwait(&a_full[0], tn & 1u)) {
@@ -1026,7 +1122,7 @@ cudaError_t attn_backward(Ctx& c, const bn_attn_desc& d, const void* q, const vo
   if (e != cudaSuccess) return e;
   Params K = P;
   if (!encode3(&K.mx[0], k, d, BR) || !encode3(&K.mx[1], v, d, BR) ||
-      !encode3(&K.my[0], q, d, BC) || !encode3(&K.my[1], dout, d, BC))
+      !encode3(&K.my[0], q, d, BCF) || !encode3(&K.my[1], dout, d, BCF))
     return cudaErrorInvalidValue;
   K.out0 = static_cast<__nv_bfloat16*>(dv);
   K.out1 = static_cast<__nv_bfloat16*>(dk);
