@@ -28,7 +28,7 @@
 #ifndef BOOSTBLK_TESTING_H
 #define BOOSTBLK_TESTING_H
 
-#include "boostblk.h"
+#include "boostattn.h"
 
 #ifdef __cplusplus
 extern "C" {
@@ -67,6 +67,16 @@ bn_status bn_testing_gemm(int32_t dtype, int32_t epi, int32_t sigma, int32_t S, 
  * bn_get_device_status(scratch) then reports BN_ERR_TIMEOUT. */
 bn_status bn_testing_gemm_unfed(const bn_gemm_problem* prob, int* counters, void* scratch,
                                 size_t scratch_bytes, bn_stream_t stream);
+
+/* Failure-detection check of the attention core (boostattn.h): the forward,
+ * launched with its first stationary (query) tile never loaded. The MMA
+ * thread's wait for it gives up after the kernels' wait limit (1 s), every role
+ * unwinds, TMEM is freed and the kernel returns; the status word at the start
+ * of `scratch` then reads BN_ERR_TIMEOUT (bn_get_device_status). Argument rules
+ * as for bn_attn_forward. */
+bn_status bn_testing_attn_forward_unfed(const bn_attn_desc* desc, const void* q, const void* k,
+                                        const void* v, void* o, float* lse, void* scratch,
+                                        bn_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -116,6 +116,7 @@ struct Params {
   const float* l2;      // backward: lse * log2(e), [B H, Lp]
   const float* dd;      // backward: D = rowsum(dO * O), [B H, Lp]
   int* status;
+  int unfed;            // test hook: the first stationary tile is never loaded
 };
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
@@ -280,6 +281,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
         const int b = bh / P.H, col = (bh % P.H) * DH;
         if (!vlane) {
           if (!bwait(smem_u32(x_empty), (tn & 1u) ^ 1u, abort_flag, P.status)) {
+            ok = false;
+            break;
+          }
+          if (P.unfed) {  // (test hook) the MMA's wait for this tile must run out
             ok = false;
             break;
           }
@@ -1193,4 +1198,36 @@ extern "C" bn_status bn_attn_backward(const bn_attn_desc* d, const void* q, cons
     return BN_ERR_CUDA;
   }
   return BN_OK;
+}
+
+// Test hook (include/boostblk_testing.h): the forward with its first stationary
+// tile never loaded, so that the MMA thread's bounded wait for it runs out.
+extern "C" bn_status bn_testing_attn_forward_unfed(const bn_attn_desc* d, const void* q,
+                                                   const void* k, const void* v, void* o,
+                                                   float* lse, void* scratch, bn_stream_t stream) {
+  bn_status s = check(d);
+  if (s != BN_OK) return s;
+  for (const void* p : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(lse),
+                        static_cast<const void*>(scratch)})
+    if (!aligned(p)) return p == nullptr ? BN_ERR_INVALID_ARG : BN_ERR_ALIGNMENT;
+  Ctx c;
+  c.stream = reinterpret_cast<cudaStream_t>(stream);
+  c.num_sms = sms();
+  Params P = {};
+  if (!encode3(&P.mx[0], q, *d, BR) || !encode3(&P.my[0], k, *d, BCF) ||
+      !encode3(&P.my[1], v, *d, BCF))
+    return BN_ERR_CUDA;
+  P.B = static_cast<int>(d->B);
+  P.L = static_cast<int>(d->L);
+  P.H = static_cast<int>(d->H);
+  P.Lp = static_cast<int>(bn_attn_lse_stride(d->L));
+  P.causal = d->causal;
+  P.ntiles = static_cast<int>(d->B * d->H * (P.Lp / BR));
+  P.scale = 1.f / sqrtf(static_cast<float>(DH));
+  P.scale_log2 = P.scale * kLog2e;
+  P.out0 = static_cast<__nv_bfloat16*>(o);
+  P.lse = lse;
+  P.status = static_cast<int*>(scratch);
+  P.unfed = 1;
+  return launch<FWD>(c, P, 0.0, 0.0) == cudaSuccess ? BN_OK : BN_ERR_CUDA;
 }

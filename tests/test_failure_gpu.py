@@ -61,3 +61,39 @@ def test_unfed_consumer_times_out_and_context_survives(lib):
     ref = a.float() @ b.float().T
     err = (out2.float() - ref).abs().max() / ref.abs().max()
     assert err < 1e-2
+
+
+def test_attention_unfed_times_out_and_context_survives(lib):
+    """The attention forward with its first query tile never loaded: its MMA
+    thread's wait gives up after 1 s, every role unwinds, the status word reads
+    BN_ERR_TIMEOUT, and an ordinary forward right after it matches the oracle."""
+    import numpy as np
+    from oracle import attention as OA
+    from rank_bottleneck_gb300 import attention as A
+    from rank_bottleneck_gb300.synth import make_attention_inputs
+    B, L, H = 1, 256, 2
+    cfg = A.AttnConfig(B=B, L=L, H=H)
+    ws = A.AttnWorkspace(cfg)
+    inp = make_attention_inputs(B, L, H, 128, seed=5)
+    dev = {n: torch.from_numpy(a).to("cuda", torch.bfloat16) for n, a in inp.items()}
+    o = torch.zeros_like(dev["q"])
+    fn = lib.bn_testing_attn_forward_unfed
+    fn.argtypes = [ctypes.POINTER(A._AttnDesc)] + [ctypes.c_void_p] * 7
+    fn.restype = ctypes.c_int
+    stream = torch.cuda.current_stream()
+    t0 = time.perf_counter()
+    assert fn(ctypes.byref(cfg.desc()), dev["q"].data_ptr(), dev["k"].data_ptr(),
+              dev["v"].data_ptr(), o.data_ptr(), ws.lse.data_ptr(), ws.scratch.data_ptr(),
+              stream.cuda_stream) == 0
+    status = A.device_status(ws)
+    waited = time.perf_counter() - t0
+    assert status == 5, lib.bn_status_string(status)           # BN_ERR_TIMEOUT
+    assert 0.5 < waited < 30.0
+    assert torch.all(o == 0)                                    # nothing was stored
+    # the context is intact: the same forward, launched normally
+    o = A.forward(cfg, dev["q"], dev["k"], dev["v"], ws)
+    assert A.device_status(ws) == 0
+    f = {n: a.astype(np.float64) for n, a in inp.items()}
+    ref, _ = OA.attention_forward(f["q"], f["k"], f["v"], B, L, H, True)
+    err = np.max(np.abs(o.float().cpu().numpy() - ref)) / np.max(np.abs(ref))
+    assert err < 2e-2
