@@ -72,7 +72,7 @@ enum Mode : int { FWD = 0, BKV = 1, BQ = 2 };
 template <int MODE>
 struct Lay {
   static constexpr int BCM = BCF;                       // rows of a streamed block
-  static constexpr int SUBC = BCM * 128;              // a 64-column half of a streamed block
+  static constexpr int SUBC = BCM * 128;              // a 64-column (d_head) half of a streamed block
   static constexpr int STG = 2 * 2 * SUBC;            // one stage: two streamed blocks
   static constexpr int EB = BR * BCM * 2;             // one bf16 elementwise tile [128, BCM]
   static constexpr int NX = (MODE == FWD) ? 1 : 2;   // stationary tiles
@@ -218,14 +218,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
   uint64_t* x_full = bars;
   uint64_t* x_empty = bars + 1;
-  uint64_t* y_full = bars + 2;                // [NYB] (FWD: K halves, then V halves)
+  uint64_t* y_full = bars + 2;                // [NYB] (FWD, BQ: K halves, then V halves)
   uint64_t* y_empty = y_full + LY::NYB;       // [NYB]
   uint64_t* s_full = y_empty + LY::NYB;       // [2]
-  uint64_t* s_empty = s_full + 2;             // [2]
-  uint64_t* e_full = s_empty + 2;             // [2]
-  uint64_t* e_empty = e_full + 2;             // [2]  backward: accumulating MMAs done with E
-  uint64_t* a_full = e_empty + 2;             // FWD [2]: P V ready; backward [1]: tile's sums done
-  uint64_t* a_empty = a_full + 2;             // FWD [2]: P V read;  backward [1]: sums read out
+  uint64_t* s_empty = s_full + 2;             // [2]  FWD, BQ: S read (BKV: S^T's buffer frees
+                                              //      with e_empty[0])
+  uint64_t* e_full = s_empty + 2;             // [2]  P / dS (BKV: P^T, dS^T) written
+  uint64_t* e_empty = e_full + 2;             // [2]  the accumulating products that read them done
+  uint64_t* a_full = e_empty + 2;             // backward: [0] the tile's sums done, [1] dP ready
+  uint64_t* a_empty = a_full + 2;             // FWD: O buffer [tile parity] read out;
+                                              // backward: [0] sums read out, [1] dP read
   uint64_t* drain = a_empty + 2;
   uint64_t* lx = drain + 1;                   // FWD [4 row quarters][2 tile parity]: row sums exchanged
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lx + 8);
@@ -532,16 +534,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
                           smem_desc(e + (kk >> 2) * (BR * 128) + (kk & 3) * 32, false),
                           smem_desc_mn(y + 2 * SUBC + kk * 2048, SUBC), ID_A,
                           (acc | kk) ? 1u : 0u);
-          } else if constexpr (MODE == BKV) {
-            // dV += P^T dO_i ; dK += dS^T Q_i
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16<1>(tmem + 256, smem_desc(e + kk * 32, false),
-                          smem_desc_mn(y + 2 * SUBC + kk * 2048, SUBC), ID_A, (acc | kk) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16<1>(tmem + 384, smem_desc(e + LY::NPB * EB + kk * 32, false),
-                          smem_desc_mn(y + kk * 2048, SUBC), ID_A, (acc | kk) ? 1u : 0u);
           } else {
             // dQ += dS K_j: A = dS [128 x BCM keys] (64-key sub-tiles), B = K_j read
             // MN-major [d_head x BCM keys]
