@@ -511,13 +511,17 @@ def run_reference(args, rank, world):
         oracle_step(c, inp)
     dt = time.perf_counter() - t0
     value = rows * args.steps / dt
-    sample = (f"{rows} of the workload's {cfg.T} token rows per step, fp64 numpy forward+backward")
+    sample = (f"{rows} of the workload's {cfg.T} token rows per step, fp64 numpy forward+backward"
+              + (f"; attention over one sequence of {rows} tokens (the workload's are "
+                 f"{cfg.seq_len})" if cfg.attn else ""))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * dt / args.steps * cfg.T / rows, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "T": cfg.T, "d": cfg.d, "r": cfg.r,
-                       "d_ff": cfg.d_ff, "S": cfg.S, "sigma": cfg.sigma},
+                       "d_ff": cfg.d_ff, "S": cfg.S, "sigma": cfg.sigma, "kind": cfg.kind,
+                       "dense": cfg.dense, "checkpoint": cfg.checkpoint, "btp": cfg.btp,
+                       "attn": cfg.attn, "seq_len": cfg.seq_len if cfg.attn else None},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
