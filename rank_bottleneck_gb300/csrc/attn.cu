@@ -450,6 +450,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           }
           for (int i = 0; i < nblk; ++i, ++jn) {
             const int st = jn % LY::NST;
+            // the next block's dP^T first: it needs only its stage and the warps'
+            // copy of this block's dP^T, both early, and so runs during this
+            // block's softmax; its S^T must wait for this block's dV, dK products
+            if (i + 1 < nblk && !kv_dp(jn + 1)) {
+              ok = false;
+              break;
+            }
             if (!bwait(smem_u32(&e_full[0]), jn & 1u, abort_flag, P.status) ||
                 (i == 0 && !bwait(smem_u32(&a_empty[0]), (tn & 1u) ^ 1u, abort_flag, P.status))) {
               ok = false;
@@ -471,7 +478,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             }
             mma_commit<1>(smem_u32(&e_empty[0]));
             mma_commit<1>(smem_u32(&y_empty[st]));
-            if (i + 1 < nblk && (!kv_dp(jn + 1) || !kv_s(jn + 1))) {
+            if (i + 1 < nblk && !kv_s(jn + 1)) {
               ok = false;
               break;
             }
