@@ -188,3 +188,32 @@ def test_block_attention_workspace_holds_q_k_o_and_lse(lib):
     lse = 4 * 16 * 4096 * 4
     assert abs((s1 - s0) - (3 * T * d * 2 + lse)) <= 4 * 256
     assert c1 - c0 >= 3 * T * d * 2 + 2 * lse
+
+
+def test_attention_flop_model():
+    """Visible (query, key) pairs of the causal core: L (L + 1) / 2 per sequence
+    and head; the model counts 12 x 128 FLOPs per pair (forward q.k and p v,
+    backward dv, dp, dq, dk), the hardware 6 x 128 more (the backward's
+    recomputed q.k twice and do.v once)."""
+    from rank_bottleneck_gb300.block import BlockConfig
+    from rank_bottleneck_gb300.configs import WORKLOADS, attn_pairs, model_flops, recompute_flops
+    base = BlockConfig(**WORKLOADS["1b-T16384-d2048-r512-dff5461"])
+    layer = BlockConfig(**WORKLOADS["1b-attn-T16384-L4096-d2048-r512-dff5461"])
+    pairs = 4 * 16 * 4096 * 4097 / 2
+    assert attn_pairs(layer) == pairs and attn_pairs(base) == 0
+    assert model_flops(layer) - model_flops(base) == 12 * 128 * pairs
+    assert recompute_flops(layer) == 6 * 128 * pairs
+
+
+def test_attention_unfed_hook_rejects_bad_arguments(lib):
+    from rank_bottleneck_gb300 import attention as A
+    fn = lib.bn_testing_attn_forward_unfed
+    fn.argtypes = [ctypes.POINTER(A._AttnDesc)] + [ctypes.c_void_p] * 7
+    fn.restype = ctypes.c_int
+    d = A.AttnConfig(B=1, L=128, H=1, d_head=64).desc()
+    fake = [ctypes.c_void_p(4096 * (i + 1)) for i in range(7)]
+    assert fn(ctypes.byref(d), *fake) == 3                     # d_head 64: unsupported
+    d = A.AttnConfig(B=1, L=128, H=1).desc()
+    args = list(fake)
+    args[0] = None
+    assert fn(ctypes.byref(d), *args) == 1                     # q missing
