@@ -22,14 +22,15 @@
 //         and dV += P^T dO_i, dK += dS^T Q_i take them from there (A operand in
 //         TMEM), which leaves shared memory for a two-stage ring.
 //   BQ    stationary Q and dO; blocks K_j, V_j.   S = Q K_j^T, dP = dO V_j^T,
-//         dS to shared memory, dQ += dS K_j in TMEM. dP is read into registers
+//         dQ += dS K_j in TMEM with dS (bf16 pairs) written into S's buffer
+//         and read from there as the A operand. dP is read into registers
 //         first and its single TMEM buffer handed back, so the next block's dP
-//         runs during this block's softmax.
+//         runs during this block's softmax; the K ring is three deep.
 // Per CTA (320 threads, persistent over the tiles, one CTA per SM):
-//   warp 0      TMA producer: the stationary tile(s), then a ring of stages of
-//               streamed blocks (2: what shared memory holds), in BKV with the
-//               blocks' row terms; in FWD and BQ a second lane loads the V
-//               halves on their own barriers;
+//   warp 0      TMA producer: the stationary tile(s), then rings of streamed
+//               blocks (K and V, or BKV's Q and dO, two stages each, BQ's K
+//               three), in BKV with the blocks' row terms; in FWD and BQ a
+//               second lane loads the V ring on its own barriers;
 //   warp 1      TMEM owner (512 columns) and, from one thread, the MMA issuer;
 //   warps 2..9  elementwise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
 //               tile row per thread) and one column half of every block.
@@ -37,7 +38,7 @@
 // while the current block's softmax does:
 //   FWD  [0, 256) S of block buffers 0 and 1; [256, 512) O of tile buffers 0 and 1
 //   BKV  [0, 128) S^T (then P^T, dS^T); [128, 256) dP^T; [256, 384) dV; [384, 512) dK
-//   BQ   [0, 256) S of block buffers 0 and 1; [256, 384) dP (single); [384, 512) dQ
+//   BQ   [0, 256) S (then dS) of block buffers 0 and 1; [256, 384) dP (single); [384, 512) dQ
 // Every operand is bf16 in 128-byte-swizzled shared memory: K-major for the
 // S and dP products (rows of 64 elements per 128-byte line), and the streamed
 // blocks' same bytes read MN-major for the accumulating products (the 64
@@ -73,27 +74,32 @@ template <int MODE>
 struct Lay {
   static constexpr int BCM = BCF;                       // rows of a streamed block
   static constexpr int SUBC = BCM * 128;              // a 64-column (d_head) half of a streamed block
-  static constexpr int STG = 2 * 2 * SUBC;            // one stage: two streamed blocks
+  static constexpr int HALF = 2 * SUBC;               // one streamed block (both d_head halves)
   static constexpr int EB = BR * BCM * 2;             // one bf16 elementwise tile [128, BCM]
   static constexpr int NX = (MODE == FWD) ? 1 : 2;   // stationary tiles
-  // elementwise tiles in shared memory (BKV writes P^T and dS^T into TMEM)
-  static constexpr int NE = (MODE == BKV) ? 0 : 1;
+  // elementwise tiles in shared memory (the backward keeps P^T, dS^T and dS in TMEM)
+  static constexpr int NE = (MODE == FWD) ? 1 : 0;
   // buffers of each elementwise tile: the forward's P and dQ's dS are single
   // (shared memory); the softmax waits for the previous block's product first
   static constexpr int NPB = (MODE == BKV) ? 2 : 1;
-  static constexpr int NST = 2;  // stages: what shared memory holds
+  // Rings of streamed blocks, one for each operand half: FWD and BQ K (first)
+  // and V (second), BKV Q and dO (filled and freed together). BQ's K ring is
+  // three deep: K_j is read last by the dQ product, so a two-deep ring could
+  // refill it only after that product.
+  static constexpr int NSTK = (MODE == BQ) ? 3 : 2;
+  static constexpr int NSTV = 2;
   static constexpr int AUXB = (MODE == BKV) ? 2 * BCM * 4 : 0;  // BKV: a block's lse log2 e and D
   static constexpr int X_OFF = 0;
   static constexpr int Y_OFF = X_OFF + NX * XTILE;
-  static constexpr int E_OFF = Y_OFF + NST * STG;
+  static constexpr int E_OFF = Y_OFF + (NSTK + NSTV) * HALF;
   static constexpr int AUX_OFF = E_OFF + NE * NPB * EB;
-  static constexpr int XCH_OFF = AUX_OFF + NST * AUXB;
+  static constexpr int XCH_OFF = AUX_OFF + NSTK * AUXB;
   // FWD: row sums exchanged between the two warps of a row, [2 tile parity][2 half][128]
   static constexpr int BAR_OFF = XCH_OFF + ((MODE == FWD) ? 2 * 2 * BR * 4 : 0);
   // stage barriers: the two halves of a FWD or BQ stage are filled and freed
   // apart (FWD: K after S, V after P V; BQ: V after dP, K after dQ), BKV's
   // stage as a whole
-  static constexpr int NYB = (MODE == BKV) ? NST : 2 * NST;
+  static constexpr int NYB = (MODE == BKV) ? NSTK : NSTK + NSTV;
   // barriers (2 + 2 NYB + 21 of 8 bytes), the TMEM address and the abort flag
   static constexpr int BAR_BYTES = (2 + 2 * NYB + 21) * 8 + 8 <= 256 ? 256 : 512;
   static constexpr int BYTES = BAR_OFF + BAR_BYTES;
@@ -147,6 +153,16 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
+}
+// 16 32-bit columns into this thread's TMEM lane (completion: tcgen05.wait::st)
+__device__ __forceinline__ void tmem_st16u_nowait(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
 }
 __device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                      int* status, unsigned long long limit = kWaitLimitNs) {
@@ -205,20 +221,21 @@ __device__ __forceinline__ void store32(__nv_bfloat16* dst, const float* v, floa
 template <int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant__ Params P) {
   using LY = Lay<MODE>;
-  constexpr int BCM = LY::BCM, SUBC = LY::SUBC, STG = LY::STG, EB = LY::EB;
+  constexpr int BCM = LY::BCM, SUBC = LY::SUBC, HALF = LY::HALF;
   // forward: S buffers take TMEM columns [0, 2 BCM), O the two 128-column buffers after them
   constexpr int OCOL = 2 * BCM;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sX = smem + LY::X_OFF;
-  uint8_t* sY = smem + LY::Y_OFF;
+  uint8_t* sYK = smem + LY::Y_OFF;                  // first-half ring (K; BKV: Q)
+  uint8_t* sYV = sYK + LY::NSTK * HALF;              // second-half ring (V; BKV: dO)
   float* sAux = reinterpret_cast<float*>(smem + LY::AUX_OFF);
   uint8_t* sE = smem + LY::E_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
   uint64_t* x_full = bars;
   uint64_t* x_empty = bars + 1;
-  uint64_t* y_full = bars + 2;                // [NYB] (FWD, BQ: K halves, then V halves)
+  uint64_t* y_full = bars + 2;                // [NYB] (FWD, BQ: K ring, then V ring)
   uint64_t* y_empty = y_full + LY::NYB;       // [NYB]
   uint64_t* s_full = y_empty + LY::NYB;       // [2]
   uint64_t* s_empty = s_full + 2;             // [2]  FWD, BQ: S read (BKV: S^T's buffer frees
@@ -299,27 +316,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           ++x_loads;
         }
         for (int j = first; j < last; ++j, ++jn) {
-          const int st = jn % LY::NST;
-          const int bi = vlane ? LY::NST + st : st;  // this lane's barrier of the stage
-          if (!bwait(smem_u32(&y_empty[bi]), ((jn / LY::NST) & 1u) ^ 1u, abort_flag, P.status)) {
+          const int st = vlane ? static_cast<int>(jn % LY::NSTV) : static_cast<int>(jn % LY::NSTK);
+          const uint32_t par = vlane ? (jn / LY::NSTV) & 1u : (jn / LY::NSTK) & 1u;
+          const int bi = vlane ? LY::NSTK + st : st;  // this lane's barrier of the stage
+          if (!bwait(smem_u32(&y_empty[bi]), par ^ 1u, abort_flag, P.status)) {
             ok = false;
             break;
           }
           const uint32_t yb = smem_u32(&y_full[bi]);
-          uint8_t* stg = sY + st * STG;
           if constexpr (MODE != BKV) {
             // one block of K (lane 0) or of V (lane 1)
             const int i = vlane ? 1 : 0;
-            mbar_expect_tx(yb, 2 * SUBC);
+            uint8_t* dst = (vlane ? sYV : sYK) + st * HALF;
+            mbar_expect_tx(yb, HALF);
             for (int c = 0; c < 2; ++c)
-              tma_load_3d(smem_u32(stg + i * 2 * SUBC + c * SUBC), &P.my[i], col + 64 * c,
-                          j * BCM, b, yb);
+              tma_load_3d(smem_u32(dst + c * SUBC), &P.my[i], col + 64 * c, j * BCM, b, yb);
           } else {
-            mbar_expect_tx(yb, STG + LY::AUXB);
+            mbar_expect_tx(yb, 2 * HALF + LY::AUXB);
             for (int i = 0; i < 2; ++i)
               for (int c = 0; c < 2; ++c)
-                tma_load_3d(smem_u32(stg + i * 2 * SUBC + c * SUBC), &P.my[i], col + 64 * c,
-                            j * BCM, b, yb);
+                tma_load_3d(smem_u32((i ? sYV : sYK) + st * HALF + c * SUBC), &P.my[i],
+                            col + 64 * c, j * BCM, b, yb);
             if constexpr (MODE == BKV) {
               const int64_t off = static_cast<int64_t>(bh) * P.Lp + j * BCM;
               bulk_load(smem_u32(sAux + st * (LY::AUXB / 4)), P.l2 + off, BCM * 4, yb);
@@ -331,10 +348,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
       if (!ok) {
         // the copies in flight must land before the CTA exits
         const unsigned long long lim = 50ull * 1000 * 1000;
-        for (uint32_t i = 0; i < LY::NST && i < jn; ++i) {
+        const uint32_t depth = vlane ? LY::NSTV : LY::NSTK;
+        for (uint32_t i = 0; i < depth && i < jn; ++i) {
           const uint32_t k = jn - 1 - i;
-          const int bi = (vlane ? LY::NST : 0) + static_cast<int>(k % LY::NST);
-          bwait(smem_u32(&y_full[bi]), (k / LY::NST) & 1u, abort_flag, P.status, lim);
+          const int bi = (vlane ? LY::NSTK : 0) + static_cast<int>(k % depth);
+          bwait(smem_u32(&y_full[bi]), (k / depth) & 1u, abort_flag, P.status, lim);
         }
         if (x_loads > 0) bwait(smem_u32(x_full), (x_loads - 1) & 1u, abort_flag, P.status, lim);
       }
@@ -348,11 +366,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
       uint32_t tn = 0, jn = 0;
       // S (and dP) of streamed block number n into TMEM buffer n & 1
       auto issue_sd = [&](uint32_t n) -> bool {
-        const int st = n % LY::NST, bf = n & 1;
-        if (!bwait(smem_u32(&y_full[st]), (n / LY::NST) & 1u, abort_flag, P.status)) return false;
-        if (!bwait(smem_u32(&s_empty[bf]), ((n >> 1) & 1u) ^ 1u, abort_flag, P.status)) return false;
+        const int st = n % LY::NSTK, bf = n & 1;
+        if (!bwait(smem_u32(&y_full[st]), (n / LY::NSTK) & 1u, abort_flag, P.status)) return false;
+        // the buffer's previous block: S read (FWD), its dS read by dQ's product (BQ)
+        uint64_t* freed = (MODE == BQ) ? &e_empty[bf] : &s_empty[bf];
+        if (!bwait(smem_u32(freed), ((n >> 1) & 1u) ^ 1u, abort_flag, P.status)) return false;
         tc_fence_after();
-        const uint32_t y = smem_u32(sY + st * STG);
+        const uint32_t y = smem_u32(sYK + st * HALF);
         const uint32_t x = smem_u32(sX);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
@@ -360,16 +380,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16<1>(tmem + bf * BCM, smem_desc(x + c * SUB_R + kk * 32, false),
                         smem_desc(y + c * SUBC + kk * 32, false), ID_S, (c | kk) ? 1u : 0u);
-        if constexpr (MODE == BKV) {
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16<1>(tmem + 128 + bf * BCM,
-                          smem_desc(x + XTILE + c * SUB_R + kk * 32, false),
-                          smem_desc(y + 2 * SUBC + c * SUBC + kk * 32, false), ID_S,
-                          (c | kk) ? 1u : 0u);
-        }
         mma_commit<1>(smem_u32(&s_full[bf]));
         if constexpr (MODE == FWD) mma_commit<1>(smem_u32(&y_empty[st]));  // K read
         return true;
@@ -378,34 +388,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
       // once the elementwise warps hold the previous block's dP in registers
       // (a_full[1] / a_empty[1] serve as its full / empty barriers)
       auto issue_dp = [&](uint32_t n) -> bool {
-        const int st = n % LY::NST;
-        if (!bwait(smem_u32(&y_full[LY::NST + st]), (n / LY::NST) & 1u, abort_flag, P.status))
+        const int st = n % LY::NSTV;
+        if (!bwait(smem_u32(&y_full[LY::NSTK + st]), (n / LY::NSTV) & 1u, abort_flag, P.status))
           return false;
         if (!bwait(smem_u32(&a_empty[1]), (n & 1u) ^ 1u, abort_flag, P.status)) return false;
         tc_fence_after();
-        const uint32_t y = smem_u32(sY + st * STG);
+        const uint32_t y = smem_u32(sYV + st * HALF);
         const uint32_t x = smem_u32(sX);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16<1>(tmem + 256, smem_desc(x + XTILE + c * SUB_R + kk * 32, false),
-                        smem_desc(y + 2 * SUBC + c * SUBC + kk * 32, false), ID_S,
-                        (c | kk) ? 1u : 0u);
+                        smem_desc(y + c * SUBC + kk * 32, false), ID_S, (c | kk) ? 1u : 0u);
         mma_commit<1>(smem_u32(&a_full[1]));
-        mma_commit<1>(smem_u32(&y_empty[LY::NST + st]));  // V read
+        mma_commit<1>(smem_u32(&y_empty[LY::NSTK + st]));  // V read
         return true;
       };
       // BKV: S^T and dP^T of block n into their single TMEM buffers; S^T's buffer
       // is free once block n - 1's dV, dK products (which read P^T, dS^T from it)
       // have completed, dP^T's once the elementwise warps hold dP^T(n - 1)
       auto kv_s = [&](uint32_t n) -> bool {
-        const int st = n % LY::NST;
-        if (!bwait(smem_u32(&y_full[st]), (n / LY::NST) & 1u, abort_flag, P.status)) return false;
+        const int st = n % LY::NSTK;
+        if (!bwait(smem_u32(&y_full[st]), (n / LY::NSTK) & 1u, abort_flag, P.status)) return false;
         if (n > 0 && !bwait(smem_u32(&e_empty[0]), (n - 1) & 1u, abort_flag, P.status))
           return false;
         tc_fence_after();
-        const uint32_t y = smem_u32(sY + st * STG);
+        const uint32_t y = smem_u32(sYK + st * HALF);
         const uint32_t x = smem_u32(sX);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
@@ -417,19 +426,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
         return true;
       };
       auto kv_dp = [&](uint32_t n) -> bool {
-        const int st = n % LY::NST;
-        if (!bwait(smem_u32(&y_full[st]), (n / LY::NST) & 1u, abort_flag, P.status)) return false;
+        const int st = n % LY::NSTK;
+        if (!bwait(smem_u32(&y_full[st]), (n / LY::NSTK) & 1u, abort_flag, P.status)) return false;
         if (!bwait(smem_u32(&a_empty[1]), (n & 1u) ^ 1u, abort_flag, P.status)) return false;
         tc_fence_after();
-        const uint32_t y = smem_u32(sY + st * STG);
+        const uint32_t y = smem_u32(sYV + st * HALF);
         const uint32_t x = smem_u32(sX);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_bf16<1>(tmem + 128, smem_desc(x + XTILE + c * SUB_R + kk * 32, false),
-                        smem_desc(y + 2 * SUBC + c * SUBC + kk * 32, false), ID_S,
-                        (c | kk) ? 1u : 0u);
+                        smem_desc(y + c * SUBC + kk * 32, false), ID_S, (c | kk) ? 1u : 0u);
         mma_commit<1>(smem_u32(&a_full[1]));
         return true;
       };
@@ -449,7 +457,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             break;
           }
           for (int i = 0; i < nblk; ++i, ++jn) {
-            const int st = jn % LY::NST;
+            const int st = jn % LY::NSTK;
             // the next block's dP^T first: it needs only its stage and the warps'
             // copy of this block's dP^T, both early, and so runs during this
             // block's softmax; its S^T must wait for this block's dV, dK products
@@ -466,14 +474,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             // dV += P^T dO_i and dK += dS^T Q_i, P^T and dS^T read from TMEM: the
             // 16 queries of k-step kk are warp half kk / 4's chunk (kk % 4) / 2,
             // P^T in that chunk's first 16 columns, dS^T in the next 16
-            const uint32_t y = smem_u32(sY + st * STG);
+            const uint32_t yq = smem_u32(sYK + st * HALF), ydo = smem_u32(sYV + st * HALF);
             const uint32_t acc = (i > 0) ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < BCM / 16; ++kk) {
               const uint32_t pa = tmem + 64 * (kk >> 2) + 32 * ((kk >> 1) & 1) + 8 * (kk & 1);
-              mma_bf16_ta(tmem + 256, pa, smem_desc_mn(y + 2 * SUBC + kk * 2048, SUBC), ID_A,
+              mma_bf16_ta(tmem + 256, pa, smem_desc_mn(ydo + kk * 2048, SUBC), ID_A,
                           (acc | kk) ? 1u : 0u);
-              mma_bf16_ta(tmem + 384, pa + 16, smem_desc_mn(y + kk * 2048, SUBC), ID_A,
+              mma_bf16_ta(tmem + 384, pa + 16, smem_desc_mn(yq + kk * 2048, SUBC), ID_A,
                           (acc | kk) ? 1u : 0u);
             }
             mma_commit<1>(smem_u32(&e_empty[0]));
@@ -507,14 +515,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             ok = false;
             break;
           }
-          const int st = jn % LY::NST, bf = jn & 1;
+          const int stk = jn % LY::NSTK, stv = jn % LY::NSTV, bf = jn & 1;
           if (!bwait(smem_u32(&e_full[bf]), (jn >> 1) & 1u, abort_flag, P.status)) {
             ok = false;
             break;
           }
           if constexpr (MODE == FWD) {
             // the block's V half
-            if (!bwait(smem_u32(&y_full[LY::NST + st]), (jn / LY::NST) & 1u, abort_flag,
+            if (!bwait(smem_u32(&y_full[LY::NSTK + stv]), (jn / LY::NSTV) & 1u, abort_flag,
                        P.status)) {
               ok = false;
               break;
@@ -529,8 +537,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             break;
           }
           tc_fence_after();
-          const uint32_t y = smem_u32(sY + st * STG);
-          const uint32_t e = smem_u32(sE + (LY::NPB == 2 ? bf : 0) * EB);
+          const uint32_t e = smem_u32(sE);
           const uint32_t acc = (i > 0) ? 1u : 0u;
           if constexpr (MODE == FWD) {
             // O += P V_j: A = P [128 x BCM keys] (64-key sub-tiles of 16 KB), B = V_j
@@ -539,21 +546,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             for (int kk = 0; kk < BCM / 16; ++kk)
               mma_bf16<1>(tmem + OCOL + ab * DH,
                           smem_desc(e + (kk >> 2) * (BR * 128) + (kk & 3) * 32, false),
-                          smem_desc_mn(y + 2 * SUBC + kk * 2048, SUBC), ID_A,
+                          smem_desc_mn(smem_u32(sYV + stv * HALF) + kk * 2048, SUBC), ID_A,
                           (acc | kk) ? 1u : 0u);
           } else {
-            // dQ += dS K_j: A = dS [128 x BCM keys] (64-key sub-tiles), B = K_j read
-            // MN-major [d_head x BCM keys]
+            // dQ += dS K_j: A = dS in TMEM (bf16 pairs in S's buffer: the 16 keys of
+            // k-step kk are warp half kk / 4's, in that half's first 32 columns),
+            // B = K_j read MN-major [d_head x BCM keys]
 #pragma unroll
             for (int kk = 0; kk < BCM / 16; ++kk)
-              mma_bf16<1>(tmem + 384,
-                          smem_desc(e + (kk >> 2) * (BR * 128) + (kk & 3) * 32, false),
-                          smem_desc_mn(y + kk * 2048, SUBC), ID_A, (acc | kk) ? 1u : 0u);
+              mma_bf16_ta(tmem + 384, tmem + bf * BCM + 64 * (kk >> 2) + 8 * (kk & 3),
+                          smem_desc_mn(smem_u32(sYK + stk * HALF) + kk * 2048, SUBC), ID_A,
+                          (acc | kk) ? 1u : 0u);
+            (void)e;
           }
           // the E tiles of this buffer are free, (FWD) O holds block i, the
           // stage (FWD: its V half; BQ: its K half) is no longer read
           mma_commit<1>(smem_u32(&e_empty[bf]));
-          mma_commit<1>(smem_u32(&y_empty[(MODE == FWD ? LY::NST : 0) + st]));
+          mma_commit<1>(smem_u32(&y_empty[(MODE == FWD) ? LY::NSTK + stv : stk]));
         }
         if (!ok) break;
         if constexpr (MODE != FWD) mma_commit<1>(smem_u32(&a_full[0]));
@@ -783,18 +792,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
               ok = false;
               break;
             }
-            // the single dS tile: the previous block's dQ product must have read it
-            if (jn > 0) {
-              const uint32_t pj = jn - 1;
-              if (!wwait(&e_empty[pj & 1u], (pj >> 1) & 1u)) {
-                ok = false;
-                break;
-              }
-            }
             tc_fence_after();
             const bool mask = (P.causal && j * BCM + BCM - 1 > t * BR) || j * BCM + BCM > P.L ||
                               t * BR + BR > P.L;
-            uint8_t* dt = sE + hf * (BR * 128);  // this warp's 64-key sub-tile of dS
+            // Per 32-key chunk h: S in, then dS as 16 columns of bf16 pairs written
+            // over columns of this warp's half that are already read (the first
+            // chunk's): keys 32 h .. 32 h + 31 of the half go to columns 16 h ...
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               uint32_t sr[32];
@@ -813,20 +816,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
                 const float p1 = ex2f_approx(fmaf(__uint_as_float(sr[i + 1]), P.scale_log2, -lr));
                 pd[i / 2] = pack2(p0 * dpv[32 * h + i], p1 * dpv[32 * h + i + 1]);
               }
-              put_row32(dt, r, h, pd);
+              tmem_st16u_nowait(tmem + lb + bf * BCM + 64 * hf + 16 * h, pd);
             }
-            fence_proxy_async();
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             arrive(&e_full[bf]);
-            arrive(&s_empty[bf]);
           }
         } else {
           // BKV: rows are keys, columns the block's 128 queries
           for (int j = first; j < last; ++j, ++jn) {
-            const int st = jn % LY::NST;
+            const int st = jn % LY::NSTK;
             // the block's row terms (lse log2 e, D of its queries) came with its stage
-            if (!wwait(&y_full[st], (jn / LY::NST) & 1u) || !wwait(&a_full[1], jn & 1u)) {
+            if (!wwait(&y_full[st], (jn / LY::NSTK) & 1u) || !wwait(&a_full[1], jn & 1u)) {
               ok = false;
               break;
             }
