@@ -1066,6 +1066,36 @@ double visible_pairs(const bn_attn_desc& d) {
 }
 
 
+// The launch parameters every mode shares: shapes, tile count, scales, status word.
+Params shape_params(const bn_attn_desc& d, int* status) {
+  Params P = {};
+  P.B = static_cast<int>(d.B);
+  P.L = static_cast<int>(d.L);
+  P.H = static_cast<int>(d.H);
+  P.Lp = static_cast<int>(bn_attn_lse_stride(d.L));
+  P.causal = d.causal;
+  P.ntiles = static_cast<int>(d.B * d.H * (P.Lp / BR));
+  P.scale = 1.f / sqrtf(static_cast<float>(DH));
+  P.scale_log2 = P.scale * kLog2e;
+  P.status = status;
+  return P;
+}
+
+// The forward's launch; `unfed` (a test hook) withholds the first query tile.
+cudaError_t forward_launch(Ctx& c, const bn_attn_desc& d, const void* q, const void* k,
+                           const void* v, void* o, float* lse, int* status, bool unfed) {
+  Params P = shape_params(d, status);
+  if (!encode3(&P.mx[0], q, d, BR) || !encode3(&P.my[0], k, d, BCF) ||
+      !encode3(&P.my[1], v, d, BCF))
+    return cudaErrorInvalidValue;
+  P.out0 = static_cast<__nv_bfloat16*>(o);
+  P.lse = lse;
+  P.unfed = unfed ? 1 : 0;
+  const double elems = static_cast<double>(d.B * d.L * d.H * DH);
+  return launch<FWD>(c, P, unfed ? 0.0 : 4.0 * DH * visible_pairs(d),
+                     unfed ? 0.0 : 4.0 * elems * 2 + static_cast<double>(d.B * d.H * P.Lp) * 4);
+}
+
 }  // namespace attn
 
 bn_status attn_check(const bn_attn_desc& d) { return attn::check(&d); }
@@ -1075,25 +1105,7 @@ size_t attn_scratch_floats(const bn_attn_desc& d) {
 
 cudaError_t attn_forward(Ctx& c, const bn_attn_desc& d, const void* q, const void* k,
                          const void* v, void* o, float* lse, int* status) {
-  using namespace attn;
-  Params P = {};
-  if (!encode3(&P.mx[0], q, d, BR) || !encode3(&P.my[0], k, d, BCF) ||
-      !encode3(&P.my[1], v, d, BCF))
-    return cudaErrorInvalidValue;
-  P.B = static_cast<int>(d.B);
-  P.L = static_cast<int>(d.L);
-  P.H = static_cast<int>(d.H);
-  P.Lp = static_cast<int>(bn_attn_lse_stride(d.L));
-  P.causal = d.causal;
-  P.ntiles = static_cast<int>(d.B * d.H * (P.Lp / BR));
-  P.scale = 1.f / sqrtf(static_cast<float>(DH));
-  P.scale_log2 = P.scale * kLog2e;
-  P.out0 = static_cast<__nv_bfloat16*>(o);
-  P.lse = lse;
-  P.status = status;
-  const double elems = static_cast<double>(d.B * d.L * d.H * DH);
-  return launch<FWD>(c, P, 4.0 * DH * visible_pairs(d),
-                     4.0 * elems * 2 + static_cast<double>(d.B * d.H * P.Lp) * 4);
+  return attn::forward_launch(c, d, q, k, v, o, lse, status, false);
 }
 
 cudaError_t attn_backward(Ctx& c, const bn_attn_desc& d, const void* q, const void* k,
@@ -1104,18 +1116,9 @@ cudaError_t attn_backward(Ctx& c, const bn_attn_desc& d, const void* q, const vo
   const int64_t rows = d.B * d.H * Lp;
   float* dd = rows_scratch;
   float* l2 = dd + rows;
-  Params P = {};
-  P.B = static_cast<int>(d.B);
-  P.L = static_cast<int>(d.L);
-  P.H = static_cast<int>(d.H);
-  P.Lp = Lp;
-  P.causal = d.causal;
-  P.ntiles = static_cast<int>(d.B * d.H * (Lp / BR));
-  P.scale = 1.f / sqrtf(static_cast<float>(DH));
-  P.scale_log2 = P.scale * kLog2e;
+  Params P = shape_params(d, status);
   P.l2 = l2;
   P.dd = dd;
-  P.status = status;
   const double elems = static_cast<double>(d.B * d.L * d.H * DH);
   const double pairs = visible_pairs(d);
   const int64_t threads = rows * 32;
@@ -1214,21 +1217,7 @@ extern "C" bn_status bn_testing_attn_forward_unfed(const bn_attn_desc* d, const 
   Ctx c;
   c.stream = reinterpret_cast<cudaStream_t>(stream);
   c.num_sms = sms();
-  Params P = {};
-  if (!encode3(&P.mx[0], q, *d, BR) || !encode3(&P.my[0], k, *d, BCF) ||
-      !encode3(&P.my[1], v, *d, BCF))
-    return BN_ERR_CUDA;
-  P.B = static_cast<int>(d->B);
-  P.L = static_cast<int>(d->L);
-  P.H = static_cast<int>(d->H);
-  P.Lp = static_cast<int>(bn_attn_lse_stride(d->L));
-  P.causal = d->causal;
-  P.ntiles = static_cast<int>(d->B * d->H * (P.Lp / BR));
-  P.scale = 1.f / sqrtf(static_cast<float>(DH));
-  P.scale_log2 = P.scale * kLog2e;
-  P.out0 = static_cast<__nv_bfloat16*>(o);
-  P.lse = lse;
-  P.status = static_cast<int*>(scratch);
-  P.unfed = 1;
-  return launch<FWD>(c, P, 0.0, 0.0) == cudaSuccess ? BN_OK : BN_ERR_CUDA;
+  return forward_launch(c, *d, q, k, v, o, lse, static_cast<int*>(scratch), true) == cudaSuccess
+             ? BN_OK
+             : BN_ERR_CUDA;
 }
