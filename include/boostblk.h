@@ -109,9 +109,16 @@ typedef struct {
    * outside: the O projection reads V, Q and K leave through q_out and k_out. */
   int32_t attn;
   int32_t seq_len; /* tokens per sequence when attn = 1 (T % seq_len == 0); else ignored */
+  /* Bottlenecks of uneven size (BOOST page, Limitations -> "Untested extensions":
+   * the design also covers bottlenecks of different sizes): the rank of each
+   * factorised layer, in the order q, k, v, o, gate, up, down; 0 = r. Each is a
+   * multiple of 8. The grouped factors stack their layers' rows: A_qkv is
+   * [r_q + r_k + r_v, d], A_gu [r_g + r_u, d]. All zero for the dense block. */
+  int64_t r_layer[7];
 } bn_block_desc;
 
-/* Parameters (forward) or their gradients (backward). Shapes, low-rank block:
+/* Parameters (forward) or their gradients (backward). Shapes, low-rank block
+ * (every layer of rank r; with desc.r_layer, layer i's r_i in its place):
  *   w_norm1 [d], A_qkv [3r, d], B_q/B_k/B_v [d, r], A_o [r, d], B_o [d, r],
  *   w_norm2 [d], A_gu [2r, d], B_g/B_u [d_ff, r], A_d [r, ld_ff], B_d [d, r].
  * Dense block: A_qkv [3d, d], A_o [d, d], A_gu [2 d_ff, d], A_d [d, ld_ff], B_* NULL.
@@ -192,12 +199,22 @@ int bn_profile_stop(bn_launch_record* out, int max_records);
  * device current; make that first call before any stream capture. All calls
  * share the array, which keeps the last call's contents: calls whose kernels
  * overlap on the GPU (other streams, other threads) race and must be ordered
- * by the caller. Each call clears the array's status word first; a kernel
- * time-out is recorded there but not reported by this entry point.
- * Asynchronous on `stream`; argument errors return before any launch. */
+ * by the caller. Each call clears the array's status word first; a kernel whose
+ * internal wait runs out (dW is then incomplete) records a time-out there, which
+ * bn_weight_grad_noalloc_status() reports.
+ * Asynchronous on `stream`; argument errors return before any launch; a failed
+ * CUDA call returns BN_ERR_CUDA with its text in bn_last_cuda_error(). */
 bn_status bn_weight_grad_noalloc(int64_t M, int64_t N, int64_t T, const void* A, int64_t lda,
                                  const void* B, int64_t ldb, const void* colscale, void* dW,
                                  int64_t ldw, bn_stream_t stream);
+
+/* Status of the last bn_weight_grad_noalloc call on the current device, for the
+ * same callers (the paper has no counterpart either): synchronises `stream`,
+ * reads and clears the status word of the library's fixed array, and returns
+ * BN_OK, or BN_ERR_TIMEOUT if that call's kernel gave up on a wait (its dW is
+ * then incomplete), or BN_ERR_CUDA if the synchronisation failed. Allocates
+ * nothing. */
+bn_status bn_weight_grad_noalloc_status(bn_stream_t stream);
 
 /* Name of a status code (static storage). */
 const char* bn_status_string(bn_status s);

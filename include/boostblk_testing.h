@@ -78,6 +78,16 @@ bn_status bn_testing_attn_forward_unfed(const bn_attn_desc* desc, const void* q,
                                         const void* v, void* o, float* lse, void* scratch,
                                         bn_stream_t stream);
 
+/* Failure-detection check of bn_weight_grad_noalloc (boostblk.h): the same
+ * launch on the library's fixed array, for M <= 256 and with no K split, made a
+ * chained consumer of an upstream launch that never comes (`counters`: two
+ * device ints, zero, that nothing increments). Its wait gives up after 1 s,
+ * every role unwinds and the kernel returns with dW not written;
+ * bn_weight_grad_noalloc_status() then reports BN_ERR_TIMEOUT. */
+bn_status bn_testing_weight_grad_noalloc_unfed(int64_t M, int64_t N, int64_t T, const void* A,
+                                               int64_t lda, const void* B, int64_t ldb, void* dW,
+                                               int64_t ldw, int* counters, bn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -37,6 +37,11 @@ that name):
   pre-activations.
 * the pages give no backward pass; the gradients here are the plain
   derivatives of the forward definition above.
+* bottlenecks of uneven size: BOOST, Limitations -> "Untested extensions",
+  says the design also covers bottlenecks of different sizes. Each factorised
+  layer i then has its own rank r_i (A_i [r_i, d_in], B_i [d_out, r_i]); the
+  grouped tensors are the layers' slices side by side ([T, r_q + r_k + r_v],
+  [T, r_g + r_u]). The oracle reads every r_i off the parameter shapes.
 
 Readings where the pages are silent:
 eps = 1e-5 inside the square root of both the local and the global RMS;
@@ -197,10 +202,27 @@ def _split(a, parts):
     return np.split(a, parts, axis=1)
 
 
+def _cuts(widths):
+    """Column offsets at which a grouped [T, sum(widths)] tensor splits into its
+    layers' slices (np.split indices)."""
+    return list(np.cumsum(widths)[:-1])
+
+
+def qkv_ranks(p):
+    """Ranks of the grouped Q, K, V bottlenecks, read off their up-projections
+    B [d_out, r_i]: each factorised layer may have its own rank."""
+    return [p["B_q"].shape[1], p["B_k"].shape[1], p["B_v"].shape[1]]
+
+
+def gu_ranks(p):
+    """Ranks of the grouped gate and up bottlenecks."""
+    return [p["B_g"].shape[1], p["B_u"].shape[1]]
+
+
 def _qkv_up(p, z_qkv, c):
     """h = sigma(z) for the three grouped bottlenecks, then the Q, K, V up-projections."""
     h_qkv = act(z_qkv, c["sigma"])
-    h_q, h_k, h_v = _split(h_qkv, 3)
+    h_q, h_k, h_v = _split(h_qkv, _cuts(qkv_ranks(p)))
     return dict(h_qkv=h_qkv, q=h_q @ p["B_q"].T, k=h_k @ p["B_k"].T, v=h_v @ p["B_v"].T)
 
 
@@ -211,7 +233,7 @@ def _o_up(p, x, z_o, c):
 
 def _gu_up(p, z_gu, c):
     h_gu = act(z_gu, c["sigma"])
-    h_g, h_u = _split(h_gu, 2)
+    h_g, h_u = _split(h_gu, _cuts(gu_ranks(p)))
     G = h_g @ p["B_g"].T
     U = h_u @ p["B_u"].T
     return dict(h_gu=h_gu, G=G, U=U, m=swiglu(G, U))
@@ -340,9 +362,10 @@ def block_backward(p, x, saved, dy, dq=None, dk=None, cfg=None):
         dm, g["A_d"], g["B_d"] = lowrank_backward(dy, a["m"], a["z_d"], a["h_d"],
                                                   p["A_d"], p["B_d"], s)
         dG, dU = swiglu_backward(dm, a["G"], a["U"])
-        A_g, A_u = np.split(p["A_gu"], 2, axis=0)
-        z_g, z_u = _split(a["z_gu"], 2)
-        h_g, h_u = _split(a["h_gu"], 2)
+        cut = _cuts(gu_ranks(p))
+        A_g, A_u = np.split(p["A_gu"], cut, axis=0)
+        z_g, z_u = _split(a["z_gu"], cut)
+        h_g, h_u = _split(a["h_gu"], cut)
         dn2_g, dA_g, g["B_g"] = lowrank_backward(dG, a["n2"], z_g, h_g, A_g, p["B_g"], s)
         dn2_u, dA_u, g["B_u"] = lowrank_backward(dU, a["n2"], z_u, h_u, A_u, p["B_u"], s)
         g["A_gu"] = np.concatenate([dA_g, dA_u], axis=0)
@@ -376,9 +399,10 @@ def block_backward(p, x, saved, dy, dq=None, dk=None, cfg=None):
         dX, g["A_o"], g["B_o"] = lowrank_backward(dx1, X_o, a["z_o"], a["h_o"],
                                                   p["A_o"], p["B_o"], s)
         dq, dk, dv = core_backward(dX)
-        A_q, A_k, A_v = np.split(p["A_qkv"], 3, axis=0)
-        z_q, z_k, z_v = _split(a["z_qkv"], 3)
-        h_q, h_k, h_v = _split(a["h_qkv"], 3)
+        cut = _cuts(qkv_ranks(p))
+        A_q, A_k, A_v = np.split(p["A_qkv"], cut, axis=0)
+        z_q, z_k, z_v = _split(a["z_qkv"], cut)
+        h_q, h_k, h_v = _split(a["h_qkv"], cut)
         dn1_q, dA_q, g["B_q"] = lowrank_backward(dq, a["n1"], z_q, h_q, A_q, p["B_q"], s)
         dn1_k, dA_k, g["B_k"] = lowrank_backward(dk, a["n1"], z_k, h_k, A_k, p["B_k"], s)
         dn1_v, dA_v, g["B_v"] = lowrank_backward(dv, a["n1"], z_v, h_v, A_v, p["B_v"], s)

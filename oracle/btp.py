@@ -10,7 +10,8 @@ owns a slice of its d_out outputs) and ends at the next down-projection split
 by rows (each shard owns a slice of its d_in inputs and produces an r-wide
 partial product); one all-reduce of the r-wide partials closes the chunk. Per
 decoder block and pass the all-reduces carry 3r + r + 2r + r = 7r values per
-token (the page's volume table: BOOST 7bsr). The RMSNorms fall inside chunks
+token (the page's volume table: BOOST 7bsr; with bottlenecks of uneven size,
+the sum of the seven ranks). The RMSNorms fall inside chunks
 and use Online RMSNorm ("Three supporting changes" -> Online RMSNorm), whose
 shard statistics ride on the chunk's all-reduce; grouping makes the Q/K/V (and
 gate/up) all-reduces one each ("Linear layer grouping").
@@ -34,7 +35,12 @@ from __future__ import annotations
 
 import numpy as np
 
-from .block import EPS, act, act_grad, silu, silu_grad
+from .block import EPS, act, act_grad, gu_ranks, qkv_ranks, silu, silu_grad
+
+
+def _cuts(widths):
+    """np.split offsets of a grouped tensor made of slices of these widths."""
+    return list(np.cumsum(widths)[:-1])
 
 
 def even_bounds(n, S):
@@ -123,7 +129,7 @@ def block_forward_btp(p, x, S, cfg=None, bounds_d=None, bounds_ff=None):
         a["z_qkv"], a["n1_s"], a["rstd1"] = _online_norm_down(a["x_s"], p["w_norm1"], p["A_qkv"],
                                                               bd, c["eps"], comm)
         a["h_qkv"] = act(a["z_qkv"], c["sigma"])
-        h_q, h_k, h_v = np.split(a["h_qkv"], 3, axis=1)
+        h_q, h_k, h_v = np.split(a["h_qkv"], _cuts(qkv_ranks(p)), axis=1)
         a["q_s"] = _col_up(h_q, p["B_q"], bd)
         a["k_s"] = _col_up(h_k, p["B_k"], bd)
         a["v_s"] = _col_up(h_v, p["B_v"], bd)
@@ -136,7 +142,7 @@ def block_forward_btp(p, x, S, cfg=None, bounds_d=None, bounds_ff=None):
     a["z_gu"], a["n2_s"], a["rstd2"] = _online_norm_down(a["x1_s"], p["w_norm2"], p["A_gu"], bd,
                                                          c["eps"], comm)
     a["h_gu"] = act(a["z_gu"], c["sigma"])
-    h_g, h_u = np.split(a["h_gu"], 2, axis=1)
+    h_g, h_u = np.split(a["h_gu"], _cuts(gu_ranks(p)), axis=1)
     a["G_s"] = _col_up(h_g, p["B_g"], bf)
     a["U_s"] = _col_up(h_u, p["B_u"], bf)
     a["m_s"] = [silu(G) * U for G, U in zip(a["G_s"], a["U_s"])]      # SwiGLU, shard-local
@@ -197,7 +203,7 @@ def block_backward_btp(p, x, acts, dy, S, dq=None, dk=None, cfg=None, bounds_d=N
     dG_s = [dm * U * silu_grad(G) for dm, G, U in zip(dm_s, a["G_s"], a["U_s"])]
     dU_s = [dm * silu(G) for dm, G in zip(dm_s, a["G_s"])]
     # gate / up bottlenecks (grouped: one 2r-wide all-reduce)
-    h_g, h_u = np.split(a["h_gu"], 2, axis=1)
+    h_g, h_u = np.split(a["h_gu"], _cuts(gu_ranks(p)), axis=1)
     dh_g = [dG @ p["B_g"][lo:hi, :] for dG, (lo, hi) in zip(dG_s, bf)]
     dh_u = [dU @ p["B_u"][lo:hi, :] for dU, (lo, hi) in zip(dU_s, bf)]
     dh_gu = comm.allreduce([np.concatenate([gp, up], axis=1) for gp, up in zip(dh_g, dh_u)])
@@ -217,7 +223,7 @@ def block_backward_btp(p, x, acts, dy, S, dq=None, dk=None, cfg=None, bounds_d=N
     # Q / K / V bottlenecks (grouped: one 3r-wide all-reduce)
     dq_s = _slices(np.zeros((T, d)) if dq is None else dq, bd)
     dk_s = _slices(np.zeros((T, d)) if dk is None else dk, bd)
-    h_q, h_k, h_v = np.split(a["h_qkv"], 3, axis=1)
+    h_q, h_k, h_v = np.split(a["h_qkv"], _cuts(qkv_ranks(p)), axis=1)
     parts = [np.concatenate([dqs @ p["B_q"][lo:hi, :], dks @ p["B_k"][lo:hi, :],
                              dvs @ p["B_v"][lo:hi, :]], axis=1)
              for dqs, dks, dvs, (lo, hi) in zip(dq_s, dk_s, dv_s, bd)]

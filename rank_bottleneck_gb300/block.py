@@ -33,7 +33,8 @@ class _Desc(ctypes.Structure):
                 ("d_ff", ctypes.c_int64), ("ld_ff", ctypes.c_int64), ("S", ctypes.c_int32),
                 ("sigma", ctypes.c_int32), ("dtype", ctypes.c_int32), ("kind", ctypes.c_int32),
                 ("dense", ctypes.c_int32), ("checkpoint", ctypes.c_int32), ("eps", ctypes.c_float),
-                ("btp", ctypes.c_int32), ("attn", ctypes.c_int32), ("seq_len", ctypes.c_int32)]
+                ("btp", ctypes.c_int32), ("attn", ctypes.c_int32), ("seq_len", ctypes.c_int32),
+                ("r_layer", ctypes.c_int64 * 7)]
 
 
 class _Params(ctypes.Structure):
@@ -102,6 +103,9 @@ class BlockConfig:
     btp: bool = False  # bottleneck-aware tensor parallelism emulated over the S shards
     attn: bool = False  # the causal attention core inside the block (heads of 128)
     seq_len: int = 0    # tokens per sequence when attn
+    # per-layer ranks (q, k, v, o, gate, up, down) for bottlenecks of uneven size;
+    # None (or a 0 entry) = r
+    ranks: tuple | None = None
 
     def __post_init__(self):
         if self.ld_ff is None:
@@ -115,18 +119,24 @@ class BlockConfig:
         return _Desc(self.T, self.d, self.r, self.d_ff, self.ld_ff, self.S, SIGMAS[self.sigma],
                      BN_BF16 if self.dtype == "bf16" else BN_F32, KINDS[self.kind],
                      int(self.dense), int(self.checkpoint), self.eps, int(self.btp),
-                     int(self.attn), int(self.seq_len))
+                     int(self.attn), int(self.seq_len),
+                     (ctypes.c_int64 * 7)(*(self.ranks or (0,) * 7)))
+
+    def layer_ranks(self):
+        """(r_q, r_k, r_v, r_o, r_g, r_u, r_d)."""
+        return tuple(int(x) if x else self.r for x in (self.ranks or (0,) * 7))
 
     def param_shapes(self):
         """Logical shape of each parameter (A_d has ld_ff-strided rows)."""
-        d, r, dff = self.d, self.r, self.d_ff
+        d, dff = self.d, self.d_ff
         if self.dense:
             s = dict(w_norm1=(d,), A_qkv=(3 * d, d), A_o=(d, d), w_norm2=(d,),
                      A_gu=(2 * dff, d), A_d=(d, dff))
         else:
-            s = dict(w_norm1=(d,), A_qkv=(3 * r, d), B_q=(d, r), B_k=(d, r), B_v=(d, r),
-                     A_o=(r, d), B_o=(d, r), w_norm2=(d,), A_gu=(2 * r, d), B_g=(dff, r),
-                     B_u=(dff, r), A_d=(r, dff), B_d=(d, r))
+            rq, rk, rv, ro, rg, ru, rd = self.layer_ranks()
+            s = dict(w_norm1=(d,), A_qkv=(rq + rk + rv, d), B_q=(d, rq), B_k=(d, rk),
+                     B_v=(d, rv), A_o=(ro, d), B_o=(d, ro), w_norm2=(d,), A_gu=(rg + ru, d),
+                     B_g=(dff, rg), B_u=(dff, ru), A_d=(rd, dff), B_d=(d, rd))
         if self.kind == "mlp":
             for n in ATTN_NAMES:
                 s.pop(n, None)

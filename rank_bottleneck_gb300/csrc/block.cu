@@ -17,15 +17,28 @@
 #include "rowops.h"
 
 namespace bn {
+
+thread_local char g_cuda_err[256] = "no error";
+
+int record_cuda_error(cudaError_t e) {
+  std::snprintf(g_cuda_err, sizeof(g_cuda_err), "%s", cudaGetErrorString(e));
+  return BN_ERR_CUDA;
+}
+
 namespace {
 
 using bf16 = __nv_bfloat16;
 
 thread_local int g_last_launches = 0;
-thread_local char g_cuda_err[256] = "no error";
+
+// the factorised layers, in the order of bn_block_desc.r_layer
+enum Layer : int { LQ = 0, LK, LV, LO, LG, LU, LD };
 
 struct Shape {
   int64_t T, d, r, d_ff, ld_ff;
+  int64_t rl[7];        // each factorised layer's rank (bottlenecks of uneven size)
+  int64_t rqkv, rgu;    // widths of the grouped Q/K/V and gate/up bottlenecks
+  int64_t off[3];       // column offsets of the Q, K, V slices in the grouped tensors
   int64_t ld_act;  // row stride of the [T, d_ff] activations G, U, m, dG, dU: whole 128-byte lines
   int S, sigma, dtype, kind, dense, ckpt, btp;
   int attn;        // the attention core runs inside the block (H heads of 128, sequences of L)
@@ -115,10 +128,10 @@ void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
     A.ss1 = static_cast<float*>(rest.take(T * s.S * 4));
     A.rstd1 = static_cast<float*>(rest.take(T * 4));
     if (!s.dense) {
-      A.z_qkv = keep.take(T * 3 * s.r * E);
-      A.h_qkv = rest.take(T * 3 * s.r * E);
-      A.z_o = keep.take(T * s.r * E);
-      A.h_o = rest.take(T * s.r * E);
+      A.z_qkv = keep.take(T * s.rqkv * E);
+      A.h_qkv = rest.take(T * s.rqkv * E);
+      A.z_o = keep.take(T * s.rl[LO] * E);
+      A.h_o = rest.take(T * s.rl[LO] * E);
     }
     A.V = rest.take(T * s.d * E);
     A.x1 = rest.take(T * s.d * E);
@@ -133,21 +146,21 @@ void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
   A.ss2 = static_cast<float*>(rest.take(T * s.S * 4));
   A.rstd2 = static_cast<float*>(rest.take(T * 4));
   if (!s.dense) {
-    A.z_gu = keep.take(T * 2 * s.r * E);
-    A.h_gu = rest.take(T * 2 * s.r * E);
-    A.z_d = keep.take(T * s.r * E);
-    A.h_d = rest.take(T * s.r * E);
+    A.z_gu = keep.take(T * s.rgu * E);
+    A.h_gu = rest.take(T * s.rgu * E);
+    A.z_d = keep.take(T * s.rl[LD] * E);
+    A.h_d = rest.take(T * s.rl[LD] * E);
   }
   A.G = rest.take(T * s.ld_act * E);
   A.U = rest.take(T * s.ld_act * E);
   A.m = rest.take(T * s.ld_act * E);
 
-  const int64_t n1 = s.dense ? 3 * s.d : 3 * s.r, n2 = s.dense ? 2 * s.d_ff : 2 * s.r;
+  const int64_t n1 = s.dense ? 3 * s.d : s.rqkv, n2 = s.dense ? 2 * s.d_ff : s.rgu;
   if (s.full()) B.A1f = sc.take(n1 * s.d * E);
   B.A2f = sc.take(n2 * s.d * E);
   if (!s.dense) {
-    B.dz_d = sc.take(T * s.r * E);
-    B.dz_gu = sc.take(T * 2 * s.r * E);
+    B.dz_d = sc.take(T * s.rl[LD] * E);
+    B.dz_gu = sc.take(T * s.rgu * E);
   }
   B.dG = sc.take(T * s.ld_act * E);
   B.dU = sc.take(T * s.ld_act * E);
@@ -157,9 +170,9 @@ void plan(const Shape& s, void* saved_base, void* scratch_base, Acts& A, Tmp& B,
     if (s.dense) {
       B.dqkv = sc.take(T * 3 * s.d * E);
     } else {
-      B.dz_o = sc.take(T * s.r * E);
+      B.dz_o = sc.take(T * s.rl[LO] * E);
       B.dV = sc.take(T * s.d * E);
-      B.dz_qkv = sc.take(T * 3 * s.r * E);
+      B.dz_qkv = sc.take(T * s.rqkv * E);
     }
   }
   if (s.attn) {
@@ -216,13 +229,31 @@ bn_status check_desc(const bn_block_desc* D, Shape& s) {
   if (s.T < 1 || s.d < 1 || s.d_ff < 1 || s.ld_ff < s.d_ff || s.S < 1 || s.S > 16)
     return BN_ERR_INVALID_ARG;
   if (!(s.eps >= 0.f) || s.eps > 1.f) return BN_ERR_INVALID_ARG;
-  if (!s.dense && s.r < 1) return BN_ERR_INVALID_ARG;
+  // per-layer ranks: 0 = r; the dense block has no ranks
+  for (int i = 0; i < 7; ++i) {
+    const int64_t ri = D->r_layer[i];
+    if (ri < 0 || (s.dense && ri != 0)) return BN_ERR_INVALID_ARG;
+    s.rl[i] = ri > 0 ? ri : s.r;
+  }
+  if (!s.dense)
+    for (int i = 0; i < 7; ++i)
+      if (s.rl[i] < 1) return BN_ERR_INVALID_ARG;
   // the RMSNorm backward keeps at least one row of d fp32 column sums in shared memory
-  if (s.T > (int64_t(1) << 31) - 256 || s.d > 43688 || s.ld_ff > (int64_t(1) << 22) ||
-      s.r > (int64_t(1) << 20))
+  if (s.T > (int64_t(1) << 31) - 256 || s.d > 43688 || s.ld_ff > (int64_t(1) << 22))
     return BN_ERR_UNSUPPORTED;
+  if (!s.dense)
+    for (int i = 0; i < 7; ++i)
+      if (s.rl[i] > (int64_t(1) << 20)) return BN_ERR_UNSUPPORTED;
   if (s.d % s.S != 0 || (s.d / s.S) % 8 != 0) return BN_ERR_INVALID_ARG;
-  if (s.ld_ff % 8 != 0 || (!s.dense && s.r % 8 != 0)) return BN_ERR_ALIGNMENT;
+  if (s.ld_ff % 8 != 0) return BN_ERR_ALIGNMENT;
+  if (!s.dense)
+    for (int i = 0; i < 7; ++i)
+      if (s.rl[i] % 8 != 0) return BN_ERR_ALIGNMENT;
+  s.rqkv = s.rl[LQ] + s.rl[LK] + s.rl[LV];
+  s.rgu = s.rl[LG] + s.rl[LU];
+  s.off[0] = 0;
+  s.off[1] = s.rl[LQ];
+  s.off[2] = s.rl[LQ] + s.rl[LK];
   if (s.dense && s.ckpt) return BN_ERR_UNSUPPORTED;
   // tensor-parallel emulation of the factorised block; each shard of d_ff gets
   // at least one 64-column block
@@ -436,10 +467,7 @@ void zero2d(Ctx& c, void* p, int64_t ld_bytes, int64_t width_bytes, int64_t rows
 bn_status finish(Ctx& c) {
   g_last_launches = c.launches;
   if (c.bad) return BN_ERR_UNSUPPORTED;
-  if (c.err != cudaSuccess) {
-    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "%s", cudaGetErrorString(c.err));
-    return BN_ERR_CUDA;
-  }
+  if (c.err != cudaSuccess) return static_cast<bn_status>(record_cuda_error(c.err));
   return BN_OK;
 }
 
@@ -462,9 +490,9 @@ void qkv_up(Ctx& c, const Shape& s, const bn_block_params* W, const Acts& A, voi
     GemmProblem& p = g.p[g.nprob++];
     p.M = s.T;
     p.N = s.d;
-    p.K = s.r;
-    p.a[0] = op(at(A.h_qkv, i * s.r, s), 3 * s.r, KM);
-    p.b[0] = op(Bs[i], s.r, KM);
+    p.K = s.rl[LQ + i];
+    p.a[0] = op(at(A.h_qkv, s.off[i], s), s.rqkv, KM);
+    p.b[0] = op(Bs[i], s.rl[LQ + i], KM);
     p.out[0] = outs[i];
     p.ldo[0] = s.d;
   }
@@ -478,9 +506,9 @@ void o_up(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, const
   GemmProblem& p = g.p[0];
   p.M = s.T;
   p.N = s.d;
-  p.K = s.r;
-  p.a[0] = op(A.h_o, s.r, KM);
-  p.b[0] = op(W->B_o, s.r, KM);
+  p.K = s.rl[LO];
+  p.a[0] = op(A.h_o, s.rl[LO], KM);
+  p.b[0] = op(W->B_o, s.rl[LO], KM);
   p.in[0] = x;
   p.ldi[0] = s.d;
   p.out[0] = A.x1;
@@ -495,11 +523,12 @@ void gu_up(Ctx& c, const Shape& s, const bn_block_params* W, const Acts& A, bool
   GemmProblem& p = g.p[0];
   p.M = s.T;
   p.N = s.d_ff;
-  p.K = s.r;
-  p.a[0] = op(A.h_gu, 2 * s.r, KM);
-  p.b[0] = op(W->B_g, s.r, KM);
-  p.a[1] = op(at(A.h_gu, s.r, s), 2 * s.r, KM);
-  p.b[1] = op(W->B_u, s.r, KM);
+  p.K = s.rl[LG];
+  p.K2 = s.rl[LU];
+  p.a[0] = op(A.h_gu, s.rgu, KM);
+  p.b[0] = op(W->B_g, s.rl[LG], KM);
+  p.a[1] = op(at(A.h_gu, s.rl[LG], s), s.rgu, KM);
+  p.b[1] = op(W->B_u, s.rl[LU], KM);
   p.out[0] = keep_gu ? A.G : nullptr;
   p.out[1] = keep_gu ? A.U : nullptr;
   p.out[2] = A.m;
@@ -515,9 +544,9 @@ void down_up(Ctx& c, const Shape& s, const bn_block_params* W, const Acts& A, co
   GemmProblem& p = g.p[0];
   p.M = s.T;
   p.N = s.d;
-  p.K = s.r;
-  p.a[0] = op(A.h_d, s.r, KM);
-  p.b[0] = op(W->B_d, s.r, KM);
+  p.K = s.rl[LD];
+  p.a[0] = op(A.h_d, s.rl[LD], KM);
+  p.b[0] = op(W->B_d, s.rl[LD], KM);
   p.in[0] = x1;
   p.ldi[0] = s.d;
   p.out[0] = y;
@@ -548,19 +577,19 @@ void norm_down(Ctx& c, const Shape& s, const void* x, const float* ss, const voi
 // bottleneck-aware TP: a row-parallel down-projection, the S shards' partial
 // products summed in the epilogue (the chunk's all-reduce).
 void plain_down(Ctx& c, const Shape& s, const void* X, int64_t K, int64_t ldx, const void* Adown,
-                int64_t lda, void* z, void* h) {
+                int64_t lda, int64_t n, void* z, void* h) {
   GemmLaunch g = launch(s.btp ? EPI_NORM : EPI_SIGMA, s);  // EPI_NORM with no rowv: shard sum
   g.nprob = 1;
   GemmProblem& p = g.p[0];
   p.M = s.T;
-  p.N = s.r;
+  p.N = n;
   p.K = K;
   p.a[0] = op(X, ldx, KM);
   p.b[0] = op(Adown, lda, KM);
   p.out[0] = z;
-  p.ldo[0] = s.r;
+  p.ldo[0] = n;
   p.out[1] = h;
-  p.ldo[1] = s.r;
+  p.ldo[1] = n;
   gemm(c, s, g);
 }
 
@@ -570,18 +599,18 @@ void plain_down(Ctx& c, const Shape& s, const void* X, int64_t K, int64_t ldx, c
 void forward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, void* y,
                      void* q, void* k, const Acts& A, const Tmp& B) {
   const void* x1 = x;
-  const Fold f2{W->A_gu, W->w_norm2, 2 * s.r, s.d, B.A2f};
+  const Fold f2{W->A_gu, W->w_norm2, s.rgu, s.d, B.A2f};
   chain_reset(c, s, B, 0, 4);
   if (s.full()) {
-    const Fold f1{W->A_qkv, W->w_norm1, 3 * s.r, s.d, B.A1f};
+    const Fold f1{W->A_qkv, W->w_norm1, s.rqkv, s.d, B.A1f};
     DT_CALL(s, stats_fold, c, x, s, A.ss1, A.rstd1, f1, f2);
     produce(c, s, B, 0);
-    norm_down(c, s, x, A.ss1, B.A1f, 3 * s.r, A.z_qkv, A.h_qkv);
+    norm_down(c, s, x, A.ss1, B.A1f, s.rqkv, A.z_qkv, A.h_qkv);
     consume(c, s, B, 0);
     qkv_up(c, s, W, A, s.attn ? A.Q : q, s.attn ? A.K : k);
     if (s.attn) attention(c, s, A, B);
     produce(c, s, B, 1);
-    plain_down(c, s, s.attn ? A.O : A.V, s.d, s.d, W->A_o, s.d, A.z_o, A.h_o);
+    plain_down(c, s, s.attn ? A.O : A.V, s.d, s.d, W->A_o, s.d, s.rl[LO], A.z_o, A.h_o);
     consume(c, s, B, 1);
     o_up(c, s, W, x, A);
     x1 = A.x1;
@@ -590,11 +619,11 @@ void forward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const voi
     DT_CALL(s, stats_fold, c, x1, s, A.ss2, A.rstd2, f2, Fold{});
   }
   produce(c, s, B, 2);
-  norm_down(c, s, x1, A.ss2, B.A2f, 2 * s.r, A.z_gu, A.h_gu);
+  norm_down(c, s, x1, A.ss2, B.A2f, s.rgu, A.z_gu, A.h_gu);
   consume(c, s, B, 2);
   gu_up(c, s, W, A, !s.ckpt);
   produce(c, s, B, 3);
-  plain_down(c, s, A.m, s.d_ff, s.ld_act, W->A_d, s.ld_ff, A.z_d, A.h_d);
+  plain_down(c, s, A.m, s.d_ff, s.ld_act, W->A_d, s.ld_ff, s.rl[LD], A.z_d, A.h_d);
   consume(c, s, B, 3);
   down_up(c, s, W, A, x1, y);
 }
@@ -676,17 +705,17 @@ void recompute(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, 
   const void* x1 = x;
   if (s.full()) {
     DT_CALL(s, stats, c, x, s, A.ss1, A.rstd1);
-    DT_CALL(s, sigma_ew, c, s, A.z_qkv, 3 * s.r, 3 * s.r, A.h_qkv);
+    DT_CALL(s, sigma_ew, c, s, A.z_qkv, s.rqkv, s.rqkv, A.h_qkv);
     qkv_up(c, s, W, A, s.attn ? A.Q : nullptr, s.attn ? A.K : nullptr);
     if (s.attn) attention(c, s, A, B);  // O for the O bottleneck's backward
-    DT_CALL(s, sigma_ew, c, s, A.z_o, s.r, s.r, A.h_o);
+    DT_CALL(s, sigma_ew, c, s, A.z_o, s.rl[LO], s.rl[LO], A.h_o);
     o_up(c, s, W, x, A);
     x1 = A.x1;
   }
   DT_CALL(s, stats, c, x1, s, A.ss2, A.rstd2);
-  DT_CALL(s, sigma_ew, c, s, A.z_gu, 2 * s.r, 2 * s.r, A.h_gu);
+  DT_CALL(s, sigma_ew, c, s, A.z_gu, s.rgu, s.rgu, A.h_gu);
   gu_up(c, s, W, A, true);
-  DT_CALL(s, sigma_ew, c, s, A.z_d, s.r, s.r, A.h_d);
+  DT_CALL(s, sigma_ew, c, s, A.z_d, s.rl[LD], s.rl[LD], A.h_d);
 }
 
 // ---------------------------------------------------------------------------
@@ -699,14 +728,15 @@ void recompute(Ctx& c, const Shape& s, const bn_block_params* W, const void* x, 
 Epi dsigma_epi(const Shape& s) { return s.btp ? EPI_SHARD_DSIGMA : EPI_DSIGMA; }
 
 // dz = (dY Bup) * sigma'(z) * rowv: one problem of a grouped DSIGMA launch
+// (Bup [K, n]: the layer's up-projection, n its rank)
 GemmProblem dsigma(const Shape& s, const void* dY, int64_t ldy, int64_t K, const void* Bup,
-                   const void* z, int64_t ldz, void* dz, const float* rowv) {
+                   int64_t n, const void* z, int64_t ldz, void* dz, const float* rowv) {
   GemmProblem p;
   p.M = s.T;
-  p.N = s.r;
+  p.N = n;
   p.K = K;
   p.a[0] = op(dY, ldy, KM);
-  p.b[0] = op(Bup, s.r, MN);
+  p.b[0] = op(Bup, n, MN);
   p.in[0] = z;
   p.ldi[0] = ldz;
   p.out[0] = dz;
@@ -753,20 +783,22 @@ void flush_wgrads(Ctx& c, const Shape& s, Wgrads& w, bool final) {
 void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const void* x,
                       const void* dy, const void* dq, const void* dk, void* dx,
                       const bn_block_params* dW, const Acts& A, const Tmp& B) {
-  const int64_t T = s.T, d = s.d, r = s.r;
+  const int64_t T = s.T, d = s.d;
+  const int64_t ro = s.rl[LO], rg = s.rl[LG], ru = s.rl[LU], rd = s.rl[LD];
+  const int64_t rqkv = s.rqkv, rgu = s.rgu;
   Wgrads wg;
   const void* x1 = s.full() ? A.x1 : x;
   chain_reset(c, s, B, 4, 4);
   // ---- down bottleneck: y = x1 + B_d sigma(A_d m)
-  add_wgrad(c, s, wg, wgrad(d, r, T, dy, d, A.h_d, r, dW->B_d, r));
+  add_wgrad(c, s, wg, wgrad(d, rd, T, dy, d, A.h_d, rd, dW->B_d, rd));
   {
     GemmLaunch g = launch(dsigma_epi(s), s);
     g.nprob = 1;
-    g.p[0] = dsigma(s, dy, d, d, W->B_d, A.z_d, r, B.dz_d, nullptr);
+    g.p[0] = dsigma(s, dy, d, d, W->B_d, rd, A.z_d, rd, B.dz_d, nullptr);
     produce(c, s, B, 4);
     gemm(c, s, g);
   }
-  add_wgrad(c, s, wg, wgrad(r, s.d_ff, T, B.dz_d, r, A.m, s.ld_act, dW->A_d, s.ld_ff));
+  add_wgrad(c, s, wg, wgrad(rd, s.d_ff, T, B.dz_d, rd, A.m, s.ld_act, dW->A_d, s.ld_ff));
   consume(c, s, B, 4);
   {
     // dm = dz_d A_d, then the SwiGLU backward in the epilogue
@@ -775,8 +807,8 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
     GemmProblem& p = g.p[0];
     p.M = T;
     p.N = s.d_ff;
-    p.K = r;
-    p.a[0] = op(B.dz_d, r, KM);
+    p.K = rd;
+    p.a[0] = op(B.dz_d, rd, KM);
     p.b[0] = op(W->A_d, s.ld_ff, MN);
     p.in[0] = A.G;
     p.in[1] = A.U;
@@ -787,20 +819,20 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
     gemm(c, s, g);
   }
   // ---- gate / up bottlenecks
-  add_wgrad(c, s, wg, wgrad(s.d_ff, r, T, B.dG, s.ld_act, A.h_gu, 2 * r, dW->B_g, r));
-  add_wgrad(c, s, wg, wgrad(s.d_ff, r, T, B.dU, s.ld_act, at(A.h_gu, r, s), 2 * r, dW->B_u, r));
+  add_wgrad(c, s, wg, wgrad(s.d_ff, rg, T, B.dG, s.ld_act, A.h_gu, rgu, dW->B_g, rg));
+  add_wgrad(c, s, wg, wgrad(s.d_ff, ru, T, B.dU, s.ld_act, at(A.h_gu, rg, s), rgu, dW->B_u, ru));
   {
     GemmLaunch g = launch(dsigma_epi(s), s);
     g.nprob = 2;
-    g.p[0] = dsigma(s, B.dG, s.ld_act, s.d_ff, W->B_g, A.z_gu, 2 * r, B.dz_gu, A.rstd2);
-    g.p[1] = dsigma(s, B.dU, s.ld_act, s.d_ff, W->B_u, at(A.z_gu, r, s), 2 * r,
-                    at(B.dz_gu, r, s), A.rstd2);
+    g.p[0] = dsigma(s, B.dG, s.ld_act, s.d_ff, W->B_g, rg, A.z_gu, rgu, B.dz_gu, A.rstd2);
+    g.p[1] = dsigma(s, B.dU, s.ld_act, s.d_ff, W->B_u, ru, at(A.z_gu, rg, s), rgu,
+                    at(B.dz_gu, rg, s), A.rstd2);
     produce(c, s, B, 5);
     gemm(c, s, g);
   }
-  add_wgrad(c, s, wg, wgrad(2 * r, d, T, B.dz_gu, 2 * r, x1, d, dW->A_gu, d, W->w_norm2));
+  add_wgrad(c, s, wg, wgrad(rgu, d, T, B.dz_gu, rgu, x1, d, dW->A_gu, d, W->w_norm2));
   consume(c, s, B, 5);
-  dx_gemm(c, s, B.dz_gu, 2 * r, W->A_gu, d, d, B.dn, d);
+  dx_gemm(c, s, B.dz_gu, rgu, W->A_gu, d, d, B.dn, d);
   void* dx1 = s.full() ? B.dx1 : dx;
   DT_CALL(s, normbwd, c, s, B, wg, B.dw_part2, B.dn, x1, W->w_norm2, A.rstd2, dy, dx1,
           dW->w_norm2);
@@ -810,17 +842,17 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
   }
 
   // ---- O bottleneck: x1 = x + B_o sigma(A_o V)
-  add_wgrad(c, s, wg, wgrad(d, r, T, dx1, d, A.h_o, r, dW->B_o, r));
+  add_wgrad(c, s, wg, wgrad(d, ro, T, dx1, d, A.h_o, ro, dW->B_o, ro));
   {
     GemmLaunch g = launch(dsigma_epi(s), s);
     g.nprob = 1;
-    g.p[0] = dsigma(s, dx1, d, d, W->B_o, A.z_o, r, B.dz_o, nullptr);
+    g.p[0] = dsigma(s, dx1, d, d, W->B_o, ro, A.z_o, ro, B.dz_o, nullptr);
     produce(c, s, B, 6);
     gemm(c, s, g);
   }
-  add_wgrad(c, s, wg, wgrad(r, d, T, B.dz_o, r, s.attn ? A.O : A.V, d, dW->A_o, d));
+  add_wgrad(c, s, wg, wgrad(ro, d, T, B.dz_o, ro, s.attn ? A.O : A.V, d, dW->A_o, d));
   consume(c, s, B, 6);
-  dx_gemm(c, s, B.dz_o, r, W->A_o, d, d, s.attn ? B.dO : B.dV, d);
+  dx_gemm(c, s, B.dz_o, ro, W->A_o, d, d, s.attn ? B.dO : B.dV, d);
   if (s.attn)
     track(c, attn_backward(c, attn_desc(s), A.Q, A.K, A.V, A.O, A.lse, B.dO, B.dQ, B.dK, B.dV,
                            B.attn_rows, B.status));
@@ -830,28 +862,30 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
   const void* Bup[3] = {W->B_q, W->B_k, W->B_v};
   void* dB[3] = {dW->B_q, dW->B_k, dW->B_v};
   for (int i = 0; i < 3; ++i) {
+    const int64_t ri = s.rl[LQ + i];
     if (dQKV[i] == nullptr)
-      zero2d(c, dB[i], r * s.E, r * s.E, d);
+      zero2d(c, dB[i], ri * s.E, ri * s.E, d);
     else
-      add_wgrad(c, s, wg, wgrad(d, r, T, dQKV[i], d, at(A.h_qkv, i * r, s), 3 * r, dB[i], r));
+      add_wgrad(c, s, wg, wgrad(d, ri, T, dQKV[i], d, at(A.h_qkv, s.off[i], s), rqkv, dB[i], ri));
   }
   {
     GemmLaunch g = launch(dsigma_epi(s), s);
     for (int i = 0; i < 3; ++i) {
+      const int64_t ri = s.rl[LQ + i];
       if (dQKV[i] == nullptr) {
-        zero2d(c, at(B.dz_qkv, i * r, s), 3 * r * s.E, r * s.E, T);
+        zero2d(c, at(B.dz_qkv, s.off[i], s), rqkv * s.E, ri * s.E, T);
         continue;
       }
-      g.p[g.nprob++] = dsigma(s, dQKV[i], d, d, Bup[i], at(A.z_qkv, i * r, s), 3 * r,
-                              at(B.dz_qkv, i * r, s), A.rstd1);
+      g.p[g.nprob++] = dsigma(s, dQKV[i], d, d, Bup[i], ri, at(A.z_qkv, s.off[i], s), rqkv,
+                              at(B.dz_qkv, s.off[i], s), A.rstd1);
     }
     // with a zeroed slice (dq or dk absent) not every row block is counted
     if (g.nprob == 3) produce(c, s, B, 7);
     gemm(c, s, g);
   }
-  add_wgrad(c, s, wg, wgrad(3 * r, d, T, B.dz_qkv, 3 * r, x, d, dW->A_qkv, d, W->w_norm1));
+  add_wgrad(c, s, wg, wgrad(rqkv, d, T, B.dz_qkv, rqkv, x, d, dW->A_qkv, d, W->w_norm1));
   consume(c, s, B, 7);
-  dx_gemm(c, s, B.dz_qkv, 3 * r, W->A_qkv, d, d, B.dn, d);
+  dx_gemm(c, s, B.dz_qkv, rqkv, W->A_qkv, d, d, B.dn, d);
   DT_CALL(s, normbwd, c, s, B, wg, B.dw_part1, B.dn, x, W->w_norm1, A.rstd1, dx1, dx,
           dW->w_norm1);
   flush_wgrads(c, s, wg, true);
@@ -1018,10 +1052,7 @@ bn_status bn_get_device_status(void* scratch, bn_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(st);
   if (e == cudaSuccess) e = cudaMemcpy(&word, scratch, sizeof(int), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(scratch, 0, sizeof(int));
-  if (e != cudaSuccess) {
-    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "%s", cudaGetErrorString(e));
-    return BN_ERR_CUDA;
-  }
+  if (e != cudaSuccess) return static_cast<bn_status>(record_cuda_error(e));
   return (word & kStatusTimeout) ? BN_ERR_TIMEOUT : BN_OK;
 }
 

@@ -56,6 +56,7 @@ struct Operand {
 
 struct GemmProblem {
   int64_t M = 0, N = 0, K = 0;
+  int64_t K2 = 0;  // K of the second operand pair (SwiGLU, chain); 0 = the same K
   Operand a[2], b[2];
   void* out[3] = {nullptr, nullptr, nullptr};
   int64_t ldo[3] = {0, 0, 0};
@@ -127,10 +128,12 @@ inline void gemm_work(const GemmLaunch& g, int esize, double& flops, double& byt
   const int npair = (g.epi == EPI_SWIGLU || g.epi == EPI_STORE_CHAIN) ? 2 : 1;
   for (int i = 0; i < g.nprob; ++i) {
     const GemmProblem& p = g.p[i];
-    const double M = static_cast<double>(p.M), N = static_cast<double>(p.N),
-                 K = static_cast<double>(p.K);
-    flops += 2.0 * M * N * K * npair;
-    bytes += npair * (M + N) * K * esize;
+    const double M = static_cast<double>(p.M), N = static_cast<double>(p.N);
+    for (int j = 0; j < npair; ++j) {
+      const double K = static_cast<double>((j == 1 && p.K2 > 0) ? p.K2 : p.K);
+      flops += 2.0 * M * N * K;
+      bytes += (M + N) * K * esize;
+    }
     for (int j = 0; j < 3; ++j)
       if (p.out[j]) bytes += M * N * esize;
     for (int j = 0; j < 2; ++j)
@@ -139,6 +142,10 @@ inline void gemm_work(const GemmLaunch& g, int esize, double& flops, double& byt
     if (p.colv) bytes += N * esize;
   }
 }
+
+// Keep the text of a failed CUDA call for bn_last_cuda_error (this thread) and
+// return BN_ERR_CUDA (as an int: this header does not include the public ABI).
+int record_cuda_error(cudaError_t e);
 
 void gemm_tc(Ctx& c, const GemmLaunch& g);    // bf16 operands, tcgen05
 void gemm_simt(Ctx& c, const GemmLaunch& g);  // fp32 operands, FFMA

@@ -27,6 +27,7 @@ struct Op {
 struct Prob {
   Op a[2], b[2];
   int64_t M, N, K;
+  int64_t K2;  // K of the second operand pair (SwiGLU, chain)
   float* out[3];
   int64_t ldo[3];
   const float* in[2];
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(THREADS) simt_kernel(const __grid_constant__ P
   const int nseg = kFold ? P.S : (EK == EPI_SWIGLU || EK == EPI_STORE_CHAIN) ? 2 : 1;
   for (int s = 0; s < nseg; ++s) {
     const int pair = (EK == EPI_SWIGLU || EK == EPI_STORE_CHAIN) ? s : 0;
-    int k_lo = 0, k_hi = static_cast<int>(pr.K);
+    int k_lo = 0, k_hi = static_cast<int>(pair == 1 ? pr.K2 : pr.K);
     if (kFold) {  // emulated shard s of K
       k_lo = static_cast<int>(s * pr.K / P.S);
       k_hi = static_cast<int>((s + 1) * pr.K / P.S);
@@ -236,6 +237,7 @@ void gemm_simt(Ctx& c, const GemmLaunch& g) {
     p.M = q.M;
     p.N = q.N;
     p.K = q.K;
+    p.K2 = q.K2 > 0 ? q.K2 : q.K;
     for (int j = 0; j < 3; ++j) {
       p.out[j] = static_cast<float*>(q.out[j]);
       p.ldo[j] = q.ldo[j];

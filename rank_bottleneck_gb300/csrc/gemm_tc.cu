@@ -172,12 +172,13 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     const int npair = (ek == K_SWIGLU || ek == K_CHAIN) ? 2 : 1;
     for (int j = 0; j < npair; ++j) {
       // each CTA of a pair loads its own 128 rows of A and BN / CG rows of B
-      if (!encode_operand(&p.ma[j], q.a[j], q.M, q.K, BM) ||
-          !encode_operand(&p.mb[j], q.b[j], q.N, q.K, BN / CG)) {
+      const int64_t Kj = (j == 1 && q.K2 > 0) ? q.K2 : q.K;
+      if (!encode_operand(&p.ma[j], q.a[j], q.M, Kj, BM) ||
+          !encode_operand(&p.mb[j], q.b[j], q.N, Kj, BN / CG)) {
         c.bad = 2;
         return;
       }
-      p.nkb[j] = static_cast<int>(cdiv(q.K, BK));
+      p.nkb[j] = static_cast<int>(cdiv(Kj, BK));
     }
     // Online RMSNorm's shards are equal, whole k-blocks; a plain shard sum needs
     // at least one k-block per shard

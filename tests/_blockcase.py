@@ -14,8 +14,9 @@ from rank_bottleneck_gb300.synth import make_block_inputs
 TOL = {"f32": 1e-5, "bf16": 2e-2}
 
 
-def inputs(T, d, r, d_ff, *, kind="full", dense=False, dtype="bf16", seed=0):
-    return make_block_inputs(T, d, r, d_ff, kind=kind, dense=dense, dtype=dtype, seed=seed)
+def inputs(T, d, r, d_ff, *, kind="full", dense=False, dtype="bf16", seed=0, ranks=None):
+    return make_block_inputs(T, d, r, d_ff, kind=kind, dense=dense, dtype=dtype, seed=seed,
+                             ranks=ranks)
 
 
 def oracle_cfg(cfg):
@@ -64,7 +65,13 @@ def to_device(cfg, inp, device="cuda"):
     return params, dev
 
 
-def run_gpu(cfg, inp, device="cuda", drop_dq=False, drop_dk=False, ws=None):
+ROW_TENSORS = ("y", "q", "k", "dx")
+
+
+def run_gpu(cfg, inp, device="cuda", drop_dq=False, drop_dk=False, ws=None, rows=None):
+    """Block forward + backward through the C ABI; every result as an fp64 numpy
+    array. With `rows`, the token-row outputs (y, q, k, dx) come back on those
+    rows only (the weight gradients whole)."""
     import torch
     from rank_bottleneck_gb300 import block as B
 
@@ -81,6 +88,9 @@ def run_gpu(cfg, inp, device="cuda", drop_dq=False, drop_dk=False, ws=None):
     res["dx"] = dx
     res.update({"d" + k: v for k, v in grads.items()})
     torch.cuda.synchronize()
+    if rows is not None:
+        idx = torch.from_numpy(np.asarray(rows)).to(device)
+        res = {k: (v.index_select(0, idx) if k in ROW_TENSORS else v) for k, v in res.items()}
     return {k: v.float().cpu().numpy().astype(np.float64) for k, v in res.items()}
 
 
@@ -90,11 +100,12 @@ def rel_err(got, ref):
 
 
 def compare(got, ref, tol, rows=None, keys=None):
-    """Return {name: error} and assert every tensor is within tol."""
+    """Return {name: error} and assert every tensor is within tol. With `rows`,
+    the token-row outputs of `got` are whole and compared on those rows."""
     errs = {}
     for k in (keys or ref.keys()):
         g = got[k]
-        if rows is not None and k in ("y", "q", "k", "dx"):
+        if rows is not None and k in ROW_TENSORS:
             g = g[rows]
         assert g.shape == ref[k].shape, (k, g.shape, ref[k].shape)
         assert np.all(np.isfinite(g)), k

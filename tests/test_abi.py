@@ -8,7 +8,8 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADERS = [os.path.join(ROOT, "include", h) for h in ("boostblk.h", "boostattn.h")]
+HEADERS = [os.path.join(ROOT, "include", h)
+           for h in ("boostblk.h", "boostattn.h", "boostblk_testing.h")]
 
 
 @pytest.fixture(scope="module")
@@ -53,6 +54,16 @@ def test_workspace_sizes_and_checkpoint_saving():
     assert scratch_ck > scratch  # the recomputed activations live in scratch instead
 
 
+def test_workspace_with_uneven_ranks():
+    """Checkpoint mode saves the pre-activations of every layer: T x sum(r_i)."""
+    from rank_bottleneck_gb300.block import workspace_size
+    ranks = (384, 384, 768, 256, 640, 640, 512)
+    saved_ck, _ = workspace_size(cfg(checkpoint=True, ranks=ranks))
+    assert abs(saved_ck - 16384 * sum(ranks) * 2) <= 4 * 256
+    # all ranks given explicitly equal to r: the same sizes as the even block
+    assert workspace_size(cfg(ranks=(512,) * 7)) == workspace_size(cfg())
+
+
 @pytest.mark.parametrize("bad, code", [
     (dict(dtype="f32", S=3), 1),          # d % S != 0
     (dict(d_ff=100, ld_ff=50), 1),        # ld_ff < d_ff
@@ -64,6 +75,9 @@ def test_workspace_sizes_and_checkpoint_saving():
     (dict(d=512, S=16), 3),               # bf16 shards narrower than 64 columns
     (dict(dense=True, btp=True), 3),      # the TP emulation is of the factorised block
     (dict(d_ff=100, ld_ff=128, d=1024, S=4, btp=True), 3),  # fewer 64-column blocks than shards
+    (dict(ranks=(512, 512, 500, 512, 512, 512, 512)), 2),  # a layer's rank not a multiple of 8
+    (dict(ranks=(512, -8, 512, 512, 512, 512, 512)), 1),   # a negative rank
+    (dict(dense=True, ranks=(8, 0, 0, 0, 0, 0, 0)), 1),    # the dense block has no ranks
 ])
 def test_bad_descriptors_are_rejected(lib, bad, code):
     from rank_bottleneck_gb300.block import workspace_size

@@ -1,10 +1,12 @@
 """Parity of the block (forward + backward through the C ABI) with the fp64 oracle.
 
-Small cases compare every output and gradient element by element. Full-size
-cases (the benchmark shapes, same launch configuration) keep the upstream
-gradients dy / dq / dk only on a sample of token rows R and zero elsewhere: the
-block is row-independent, so y, q, k, dx on R and every weight gradient are
-then exactly what the oracle computes from the rows R alone.
+Small cases compare every output and gradient element by element. The 1B and
+7B benchmark shapes (same launch configuration as the bench) run with every
+row live and are compared whole with the oracle on all 16384 tokens. The 13B
+shape and the rank/size sweep keep the upstream gradients dy / dq / dk only on
+a sample of token rows R and zero elsewhere: the block is row-independent, so
+y, q, k, dx on R and every weight gradient are then exactly what the oracle
+computes from the rows R alone.
 Bars (max |gpu - ref| / max |ref| per tensor): 1e-5 fp32, 2e-2 bf16.
 """
 import numpy as np
@@ -32,7 +34,7 @@ def cfg_of(**kw):
 def case(kw, seed=0):
     cfg = cfg_of(**kw)
     inp = C.inputs(cfg.T, cfg.d, cfg.r, cfg.d_ff, kind=cfg.kind, dense=cfg.dense,
-                   dtype=cfg.dtype, seed=seed)
+                   dtype=cfg.dtype, seed=seed, ranks=cfg.ranks)
     return cfg, inp
 
 
@@ -51,6 +53,18 @@ SMALL = {
     "full-bf16-T1": dict(T=1, d=128, r=8, d_ff=24, S=2),
     "full-bf16-S16": dict(T=130, d=1024, r=64, d_ff=200, S=16),
     "full-bf16-r8": dict(T=129, d=192, r=8, d_ff=40, S=3),
+    # bottlenecks of uneven size: each factorised layer its own rank (q, k, v, o,
+    # gate, up, down), including ranks that are not multiples of the 64-wide
+    # k-block and grouped slices that start mid-tile
+    "full-bf16-uneven": dict(T=300, d=256, r=64, d_ff=333, S=4, ranks=(64, 32, 96, 40, 72, 24, 56)),
+    "mlp-bf16-uneven": dict(T=200, d=256, r=64, d_ff=400, S=2, kind="mlp",
+                            ranks=(0, 0, 0, 0, 128, 48, 16)),
+    "full-bf16-uneven-ckpt": dict(T=260, d=256, r=64, d_ff=300, S=4, checkpoint=True,
+                                  ranks=(16, 64, 40, 8, 96, 32, 64)),
+    "full-bf16-uneven-identity": dict(T=256, d=512, r=128, d_ff=1000, S=8, sigma="identity",
+                                      ranks=(128, 64, 256, 192, 96, 160, 320)),
+    "full-f32-uneven": dict(T=77, d=128, r=32, d_ff=200, S=2, dtype="f32",
+                            ranks=(8, 16, 24, 40, 32, 16, 48)),
 }
 
 
@@ -81,24 +95,31 @@ def test_absent_dq_dk_mean_zero():
 
 
 def test_fp32_online_norm_shards_match_single_shard():
-    """Online RMSNorm with S > 1 equals S = 1 (plain RMSNorm) in fp32: the block's
-    outputs to 1e-6 (the page's accuracy table reports 7e-7 for the norm and the
-    linear layer after it); gradients, which sum these rounding differences over
-    every row, to the fp32 parity bar."""
+    """Online RMSNorm with S > 1 equals S = 1 (plain RMSNorm) in fp32 within 1e-6
+    (the page's accuracy table reports 7e-7 for the norm and the linear layer
+    after it) on every output and gradient: y, q, k and dx, which depend on
+    their own row alone, and the weight gradients, which sum the rows' last-bit
+    differences (measured on GB300: at most 3.3e-7, S = 8). Every error is
+    printed."""
     base = dict(T=192, d=512, r=64, d_ff=400, dtype="f32")
     res = {}
     for S in (1, 2, 4, 8):
         cfg, inp = case(dict(base, S=S))
         res[S] = C.run_gpu(cfg, inp)
+    bad = []
     for S in (2, 4, 8):
-        for k in res[1]:
-            bar = 1e-6 if k in ("y", "q", "k") else C.TOL["f32"]
-            assert C.rel_err(res[S][k], res[1][k]) <= bar, (S, k)
+        errs = {k: C.rel_err(res[S][k], res[1][k]) for k in res[1]}
+        print(f"S={S} vs S=1:", " ".join(f"{k}={e:.2e}" for k, e in sorted(errs.items())))
+        for k, e in errs.items():
+            if not e <= 1e-6:
+                bad.append((S, k, e))
+    assert not bad, bad
 
 
+@pytest.mark.parametrize("ranks", [None, (64, 32, 96, 40, 72, 24, 56)])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_checkpoint_is_bit_identical(dtype):
-    kw = dict(T=300, d=256, r=64, d_ff=333, S=4, dtype=dtype)
+def test_checkpoint_is_bit_identical(dtype, ranks):
+    kw = dict(T=300, d=256, r=64, d_ff=333, S=4, dtype=dtype, ranks=ranks)
     cfg_a, inp = case(kw)
     cfg_b = cfg_of(**dict(kw, checkpoint=True))
     a = C.run_gpu(cfg_a, inp)
@@ -137,11 +158,17 @@ def masked_case(kw, seed=0):
     return cfg, inp, rows, keep
 
 
-def check_masked(cfg, inp, rows, keep, got=None):
-    got = C.run_gpu(cfg, inp) if got is None else got
+def check_masked(cfg, inp, rows, keep):
+    """Run the masked case; compare the sampled rows and every weight gradient
+    with the oracle on those rows, and check that rows with no upstream
+    gradient get dx = 0 exactly. Returns (results on the fetched rows, errors)."""
+    zero_rows = np.flatnonzero(~keep)[:64]
+    got = C.run_gpu(cfg, inp, rows=np.concatenate([rows, zero_rows]))
+    n = len(rows)
+    sampled = {k: (v[:n] if k in C.ROW_TENSORS else v) for k, v in got.items()}
     ref = C.run_oracle(cfg, inp, rows=rows)
-    errs = C.compare(got, ref, C.TOL[cfg.dtype], rows=rows)
-    assert np.all(got["dx"][~keep][:64] == 0.0)
+    errs = C.compare(sampled, ref, C.TOL[cfg.dtype])
+    assert np.all(got["dx"][n:] == 0.0)
     return got, errs
 
 
@@ -149,11 +176,25 @@ FULL = {
     "1B-T16384-d2048-r512-dff5461-S4": dict(T=16384, d=2048, r=512, d_ff=5461, S=4),
     "7B-T16384-d4096-r1024-dff11008-S8": dict(T=16384, d=4096, r=1024, d_ff=11008, S=8),
 }
+# the 1B shape with uneven ranks around r = 512 (sum 3584 = 7 x 512)
+UNEVEN_1B = dict(T=16384, d=2048, r=512, d_ff=5461, S=4, ranks=(384, 384, 768, 256, 640, 640, 512))
 
 
 @pytest.mark.parametrize("name", list(FULL))
-def test_full_size_block(name):
-    cfg, inp, rows, keep = masked_case(FULL[name])
+def test_full_size_block_all_rows_live(name):
+    """The benchmark shapes with every upstream-gradient row live: each weight
+    gradient (K = T = 16384, one launch over all 11 of them with the left-over
+    tiles split along K) and every output row is compared with the oracle run
+    on all the tokens."""
+    cfg, inp = case(FULL[name])
+    got = C.run_gpu(cfg, inp)
+    ref = C.run_oracle(cfg, inp)
+    errs = C.compare(got, ref, C.TOL[cfg.dtype])
+    print(name, " ".join(f"{k}={e:.2e}" for k, e in sorted(errs.items())))
+
+
+def test_uneven_ranks_1b_shape_sampled_rows():
+    cfg, inp, rows, keep = masked_case(UNEVEN_1B)
     check_masked(cfg, inp, rows, keep)
 
 
@@ -162,17 +203,20 @@ def test_13b_checkpoint_full_size():
     cfg, inp, rows, keep = masked_case(kw)
     got, _ = check_masked(cfg, inp, rows, keep)
     cfg_ck = cfg_of(**dict(kw, checkpoint=True))
-    got_ck = C.run_gpu(cfg_ck, inp)
+    got_ck = C.run_gpu(cfg_ck, inp, rows=np.concatenate([rows, np.flatnonzero(~keep)[:64]]))
     for k in got:
         assert np.array_equal(got[k], got_ck[k]), k
 
 
-SWEEP = {
-    "svd-r256-T4096": dict(T=4096, d=4096, r=256, d_ff=11008, S=8, sigma="identity"),
-    "cola-r2048-T4096": dict(T=4096, d=4096, r=2048, d_ff=11008, S=8),
-    "cola-r512-T32768": dict(T=32768, d=4096, r=512, d_ff=11008, S=8),
-    "dense-T4096": dict(T=4096, d=4096, r=1024, d_ff=11008, S=8, dense=True),
-}
+# the rank/size sweep: d = 4096, d_ff = 11008, S = 8; r in {256, 512, 1024, 2048}
+# x T in {4096, 16384, 32768} x sigma in {identity (SVD-style), SiLU (CoLA)},
+# and the dense full-rank block at each T
+SWEEP = {}
+for _T in (4096, 16384, 32768):
+    for _r in (256, 512, 1024, 2048):
+        for _s, _n in (("identity", "svd"), ("silu", "cola")):
+            SWEEP[f"{_n}-r{_r}-T{_T}"] = dict(T=_T, d=4096, r=_r, d_ff=11008, S=8, sigma=_s)
+    SWEEP[f"dense-T{_T}"] = dict(T=_T, d=4096, r=1024, d_ff=11008, S=8, dense=True)
 
 
 @pytest.mark.parametrize("name", list(SWEEP))

@@ -52,7 +52,8 @@ def run_oracle_btp(cfg, inp, rows=None):
     bf = ff_bounds(cfg.d_ff, cfg.S, cfg.dtype)
     out, acts, vol_f = OB.block_forward_btp(p, x, cfg.S, oc, bd, bf)
     dx, g, vol_b = OB.block_backward_btp(p, x, acts, dy, cfg.S, dq, dk, oc, bd, bf)
-    per_pass = 7 * cfg.r if cfg.kind == "full" else 3 * cfg.r
+    ranks = cfg.layer_ranks()
+    per_pass = sum(ranks) if cfg.kind == "full" else sum(ranks[4:])
     assert vol_f["r_wide"] == per_pass and vol_b["r_wide"] == per_pass
     res = dict(out)
     res["dx"] = dx
@@ -67,6 +68,11 @@ SMALL = {
     "full-bf16-S3-r8": dict(T=129, d=192, r=8, d_ff=200, S=3, btp=True),
     "full-f32-S4": dict(T=77, d=128, r=32, d_ff=200, S=4, dtype="f32", btp=True),
     "mlp-f32-S4": dict(T=256, d=256, r=64, d_ff=688, S=4, dtype="f32", kind="mlp", btp=True),
+    # bottlenecks of uneven size: the r-wide all-reduces carry sum(r_i) per token
+    "full-bf16-S4-uneven": dict(T=300, d=256, r=64, d_ff=333, S=4, btp=True,
+                                ranks=(64, 32, 96, 40, 72, 24, 56)),
+    "full-f32-S4-uneven": dict(T=77, d=128, r=32, d_ff=200, S=4, dtype="f32", btp=True,
+                               ranks=(8, 16, 24, 40, 32, 16, 48)),
 }
 
 
@@ -74,7 +80,7 @@ SMALL = {
 def test_btp_block_matches_oracle(name):
     kw = SMALL[name]
     cfg = cfg_of(**kw)
-    inp = C.inputs(cfg.T, cfg.d, cfg.r, cfg.d_ff, kind=cfg.kind, dtype=cfg.dtype)
+    inp = C.inputs(cfg.T, cfg.d, cfg.r, cfg.d_ff, kind=cfg.kind, dtype=cfg.dtype, ranks=cfg.ranks)
     got = C.run_gpu(cfg, inp)
     C.compare(got, run_oracle_btp(cfg, inp), C.TOL[cfg.dtype])
 
