@@ -1,8 +1,9 @@
 """The N > 1 path of bench.py on CPU: two ranks over gloo (127.0.0.1), through
-the same helpers the GPU run uses under torchrun. Each rank runs its own
-replica of the step on its own tokens (weak scaling, no collective on the data
-path); the timed region ends with a barrier and the slowest rank's time, taken
-with an all-reduce MAX, is what every rank reports."""
+the same helpers the GPU run uses under torchrun. Each rank runs the step on
+its own tokens (weak scaling; the weight-gradient all-reduce of data
+parallelism is tested in test_dp_cpu.py); the timed region ends with a barrier
+and the slowest rank's time, taken with an all-reduce MAX, is what every rank
+reports."""
 import json
 import os
 import socket
@@ -40,7 +41,7 @@ def test_two_ranks_gloo_max_over_ranks(tmp_path):
     mp.spawn(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
     res = [json.load(open(tmp_path / f"rank{r}.json")) for r in range(world)]
     assert [x["max_ms"] for x in res] == [15.0, 15.0]       # the slowest rank's time
-    assert len({x["seed"] for x in res}) == world           # each replica its own tokens
+    assert len({x["seed"] for x in res}) == world           # each rank its own tokens
     assert all(x["world"] == world for x in res)
 
 
@@ -63,3 +64,12 @@ def test_reference_arm_runs_on_rank0_only(capsys):
     bench.run_reference(args, rank=1, world=2)
     assert time.perf_counter() - t0 < 1.0
     assert capsys.readouterr().out == ""
+
+
+def test_gpus_flag_must_match_the_launch(monkeypatch):
+    """--gpus N without N launched processes is an error, not a silent 1-GPU run."""
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    import bench
+    with pytest.raises(SystemExit) as e:
+        bench.main(["--gpus", "2", "--steps", "1", "--warmup", "3"])
+    assert "--gpus 2" in str(e.value)
