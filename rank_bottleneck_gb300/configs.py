@@ -14,6 +14,10 @@ WORKLOADS = {
     "7b-T16384-d4096-r1024-dff11008": dict(T=16384, d=4096, r=1024, d_ff=11008, S=8),
     "13b-ckpt-T16384-d5120-r1280-dff13824": dict(T=16384, d=5120, r=1280, d_ff=13824, S=8,
                                                   checkpoint=True),
+    # the 1B block with checkpointing at a quarter of the tokens: profiler captures
+    # of the recompute kernels
+    "1b-ckpt-T4096-d2048-r512-dff5461": dict(T=4096, d=2048, r=512, d_ff=5461, S=4,
+                                             checkpoint=True),
     "13b-T16384-d5120-r1280-dff13824": dict(T=16384, d=5120, r=1280, d_ff=13824, S=8),
     # bottleneck-aware tensor parallelism emulated over the S shards: every
     # down-projection and up-projection input gradient sums S partials (the

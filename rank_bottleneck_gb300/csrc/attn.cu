@@ -48,6 +48,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <mutex>
 
@@ -936,38 +937,61 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
 
 // D[bh, i] = sum_e dO[i, h, e] O[i, h, e] (0 for L <= i < Lp) and
 // l2[bh, i] = lse[bh, i] log2(e): one warp per (token row, head).
-__global__ void attn_rows_kernel(const __nv_bfloat16* __restrict__ o,
+// One warp per token row (b, i), every head of it: the row's O and dO (H x 128
+// bf16 each) are read with 16-byte loads, eight heads at a time (4 x 16 bytes
+// of each tensor per lane in flight), and each head's D = sum(dO * O) is a
+// half-warp reduction (head 2u + (lane >= 16) of load u). Rows i in [L, Lp)
+// (the padding of the lse stride) get D = 0.
+__global__ void __launch_bounds__(256, 2) attn_rows_kernel(const __nv_bfloat16* __restrict__ o,
                                  const __nv_bfloat16* __restrict__ dout,
                                  const float* __restrict__ lse, float* __restrict__ dd,
                                  float* __restrict__ l2, int B, int L, int H, int Lp) {
   grid_dependency_sync();
-  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t total = static_cast<int64_t>(B) * H * Lp;
-  if (w >= total) return;
-  const int i = static_cast<int>(w % Lp);
-  const int64_t bh = w / Lp;
-  const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
-  float acc = 0.f;
-  if (i < L) {
-    const int64_t off = (static_cast<int64_t>(b) * L + i) * (static_cast<int64_t>(H) * DH) +
-                        h * DH + lane * 4;
-    const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-    const uint2 g = *reinterpret_cast<const uint2*>(dout + off);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t total = static_cast<int64_t>(B) * Lp;
+  const int64_t rowlen = static_cast<int64_t>(H) * DH;
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total;
+       w += nwarps) {
+    const int b = static_cast<int>(w / Lp), i = static_cast<int>(w % Lp);
+    // this lane's 8 columns of its first head (head lane >> 4, columns (lane & 15) * 8)
+    const int lo = (lane >> 4) * DH + (lane & 15) * 8;
+    const __nv_bfloat16* orow = o + (static_cast<int64_t>(b) * L + i) * rowlen + lo;
+    const __nv_bfloat16* grow = dout + (static_cast<int64_t>(b) * L + i) * rowlen + lo;
+    for (int h0 = 0; h0 < H; h0 += 8) {
+      uint4 a[4], g[4];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const float2 fa = __bfloat1622float2(a2[k]), fg = __bfloat1622float2(g2[k]);
-      acc = fmaf(fa.x, fg.x, acc);
-      acc = fmaf(fa.y, fg.y, acc);
+      for (int u = 0; u < 4; ++u) {
+        const int h = h0 + 2 * u + (lane >> 4);  // this lane's head for load u
+        const int off = (h0 + 2 * u) * DH;
+        if (i < L && h < H) {
+          a[u] = *reinterpret_cast<const uint4*>(orow + off);
+          g[u] = *reinterpret_cast<const uint4*>(grow + off);
+        } else {
+          a[u] = g[u] = make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[u]);
+        float acc = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 fa = __bfloat1622float2(a2[k]), fg = __bfloat1622float2(g2[k]);
+          acc = fmaf(fa.x, fg.x, acc);
+          acc = fmaf(fa.y, fg.y, acc);
+        }
+#pragma unroll
+        for (int sft = 8; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+        const int h = h0 + 2 * u + (lane >> 4);
+        if ((lane & 15) == 0 && h < H) {
+          const int64_t idx = (static_cast<int64_t>(b) * H + h) * Lp + i;
+          dd[idx] = acc;
+          l2[idx] = lse[idx] * kLog2e;
+        }
+      }
     }
-  }
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    dd[w] = acc;
-    l2[w] = lse[w] * kLog2e;
   }
 }
 
@@ -1121,9 +1145,12 @@ cudaError_t attn_backward(Ctx& c, const bn_attn_desc& d, const void* q, const vo
   P.dd = dd;
   const double elems = static_cast<double>(d.B * d.L * d.H * DH);
   const double pairs = visible_pairs(d);
-  const int64_t threads = rows * 32;
+  // one warp per token row (all heads); two blocks of eight warps per SM, each
+  // warp looping over rows
+  const int64_t row_warps = static_cast<int64_t>(d.B) * Lp;
+  const int64_t blocks = std::min<int64_t>((row_warps + 7) / 8, static_cast<int64_t>(c.num_sms) * 2);
   prof_start(c);
-  cudaError_t e = launch_pdl(attn_rows_kernel, dim3(static_cast<unsigned>((threads + 255) / 256)),
+  cudaError_t e = launch_pdl(attn_rows_kernel, dim3(static_cast<unsigned>(blocks)),
                              dim3(256), 0, c.stream, static_cast<const __nv_bfloat16*>(o),
                              static_cast<const __nv_bfloat16*>(dout), lse, dd, l2, P.B, P.L, P.H,
                              Lp);

@@ -77,14 +77,19 @@ struct EpiShape {
   static constexpr int NIN = (EK == K_RESID) ? 1 : (EK == K_DSWIGLU) ? 2 : 0;
   static constexpr int NOUT =
       (EK == K_SWIGLU) ? 3 : (EK == K_SIGMA || EK == K_NORM || EK == K_DSWIGLU) ? 2 : 1;
-  static constexpr int NT = NIN > NOUT ? NIN : NOUT;         // subtiles per ring entry
+  // subtiles per ring entry. SwiGLU's three outputs share two: G leaves its
+  // subtile (stored while the U MMAs run) before m, formed from G and U later,
+  // takes it over; the space saved goes to operand stages
+  static constexpr int NT = (EK == K_SWIGLU) ? 2 : (NIN > NOUT ? NIN : NOUT);
   static constexpr int ELEM = 2;                             // output element bytes (bf16)
   static constexpr int SUB_BYTES = BM * EPI_N * ELEM;        // one 128 x 32 subtile
   static constexpr int WARP_BYTES = 32 * EPI_N * ELEM;       // one warp's 32 rows of it
   // ring entries: kinds that read epilogue inputs keep several subtiles of them in
   // flight; the others only need each warp's previous store to have left shared
   // memory, and leave the rest to operand stages
-  static constexpr int NE = (NIN > 0) ? 8 : 4;
+  // (the sigma down-projection's tiles are long in K: its light epilogue keeps up
+  // with one entry per warp, and the space goes to a sixth operand stage)
+  static constexpr int NE = (NIN > 0) ? 8 : (EK == K_SIGMA ? 2 : 4);
   static constexpr int BYTES = NE * NT * SUB_BYTES;
 };
 
@@ -795,14 +800,14 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         signal_rows(w);
         continue;  // the tile is done
       } else if constexpr (EK == K_SWIGLU) {
-        // G first: keep this warp's columns of it as bf16 pairs and free its slot
-        // at once, so the MMAs of the next tile's G overlap this tile's epilogue
         sl0 = slot;
         const uint32_t p0 = sph;
         advance();
         sl1 = slot;
         const uint32_t p1 = sph;
         advance();
+        // G first: keep this warp's columns of it as bf16 pairs and free its slot
+        // at once, so the MMAs of the next tile's G overlap this tile's epilogue
         if (!acquire(sl0, p0)) {
           ok = false;
           break;
@@ -820,7 +825,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
         }
         release(sl0);
         // store G while the MMAs of U run: each chunk goes to subtile 0 of its ring
-        // entry, U and m follow in subtiles 1 and 2 once U has arrived
+        // entry; U (subtile 1) and m (subtile 0 again) follow once U has arrived
         if (pr.out_mask & 1) {
           const int rt = static_cast<int>(w.m0) + row_off + q * 32;
 #pragma unroll
@@ -887,8 +892,11 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
                                                            __fmul_rn(silu_fast(g1), u1));
             mpk[i] = *reinterpret_cast<const uint32_t*>(&h);
           }
+          // U in subtile 1, m in subtile 0: G's store from it was issued before
+          // every later bulk group of this warp, and each commit below waits for
+          // all but the newest group to have left shared memory
           smem_row_store_packed(ent + E::SUB_BYTES, lane, upk[k]);
-          smem_row_store_packed(ent + 2 * E::SUB_BYTES, lane, mpk);
+          smem_row_store_packed(ent, lane, mpk);
           if (row_ok && col0 + EPI_N > pr.N8 && col0 < N) {
             float f[32];
             if (pr.out_mask & 2) {
@@ -913,8 +921,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
               if (pr.out_mask & 2)
                 tma_store_2d(&pr.mo[1], smem_u32(ent + E::SUB_BYTES), static_cast<int>(col0), rt);
               if (pr.out_mask & 4)
-                tma_store_2d(&pr.mo[2], smem_u32(ent + 2 * E::SUB_BYTES), static_cast<int>(col0),
-                             rt);
+                tma_store_2d(&pr.mo[2], smem_u32(ent), static_cast<int>(col0), rt);
             }
             bulk_commit();
             bulk_wait_read<E::NE / EPI_GROUPS - 1>();

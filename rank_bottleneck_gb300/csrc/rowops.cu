@@ -521,23 +521,47 @@ void launch_finish(Ctx& c, const TileReduce& r) {
 // ---------------------------------------------------------------------------
 // elementwise passes
 // ---------------------------------------------------------------------------
-template <typename T, int OP>  // OP 0: h = sigma(z); 1: m = SiLU(G) U; 2: out = in * rowv
+template <typename T, int OP>
+__device__ __forceinline__ float ew_op(float a, float b, float rv, int sigma) {
+  if (OP == 0) return act_t<T>(a, sigma);
+  if (OP == 1) return __fmul_rn(silu_t<T>(a), b);
+  return a * rv;
+}
+
+// OP 0: h = sigma(z); 1: m = SiLU(G) U; 2: out = in * rowv (in == nullptr: zeros).
+// Rows are processed 8 columns (16 bytes of bf16) at a time when every row
+// stride is a multiple of 8 elements; the columns past the last whole group of
+// 8, and unaligned layouts, go element by element. Both forms evaluate the
+// same expression per element, so results do not depend on the form.
+template <typename T, int OP>
 __global__ void ew_kernel(const T* __restrict__ a, int64_t lda, const T* __restrict__ b,
                           int64_t rows, int64_t cols, const float* __restrict__ rowv, int sigma,
-                          T* __restrict__ out, int64_t ldo) {
+                          T* __restrict__ out, int64_t ldo, int vec) {
   grid_dependency_sync();
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows * cols;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / cols, col = i - r * cols;
-    float v;
-    if (OP == 0) {
-      v = act_t<T>(to_f<T>(a[r * lda + col]), sigma);
-    } else if (OP == 1) {
-      v = __fmul_rn(silu_t<T>(to_f<T>(a[r * lda + col])), to_f<T>(b[r * lda + col]));
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  const int64_t nvec = vec ? cols / 8 : 0;  // whole 8-column groups per row
+  for (int64_t i = t0; i < rows * nvec; i += stride) {
+    const int64_t r = i / nvec, col = (i - r * nvec) * 8;
+    float va[8], vb[8], vo[8];
+    const float rv = (OP == 2) ? rowv[r] : 0.f;
+    if (OP == 2 && a == nullptr) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) va[k] = 0.f;
     } else {
-      v = (a == nullptr) ? 0.f : to_f<T>(a[r * lda + col]) * rowv[r];
+      Vec8<T>::load(a + r * lda + col, va);
     }
-    out[r * ldo + col] = from_f<T>(v);
+    if (OP == 1) Vec8<T>::load(b + r * lda + col, vb);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) vo[k] = ew_op<T, OP>(va[k], OP == 1 ? vb[k] : 0.f, rv, sigma);
+    Vec8<T>::store(out + r * ldo + col, vo);
+  }
+  const int64_t tail = cols - nvec * 8;  // the remaining columns of every row
+  for (int64_t i = t0; i < rows * tail; i += stride) {
+    const int64_t r = i / tail, col = nvec * 8 + (i - r * tail);
+    const float va = (OP == 2 && a == nullptr) ? 0.f : to_f<T>(a[r * lda + col]);
+    const float vb = (OP == 1) ? to_f<T>(b[r * lda + col]) : 0.f;
+    out[r * ldo + col] = from_f<T>(ew_op<T, OP>(va, vb, OP == 2 ? rowv[r] : 0.f, sigma));
   }
 }
 
@@ -545,10 +569,16 @@ template <typename T, int OP>
 static void launch_ew(Ctx& c, const T* a, int64_t lda, const T* b, int64_t rows, int64_t cols,
                       const float* rowv, int sigma, T* out, int64_t ldo) {
   const int64_t n = rows * cols;
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 16));
+  // 16-byte vectors need 16-byte aligned rows in every tensor the kernel touches
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) |
+                        reinterpret_cast<uintptr_t>(out);
+  const bool vec = (mis & 15) == 0 && (lda * sizeof(T)) % 16 == 0 && (ldo * sizeof(T)) % 16 == 0;
+  const int64_t work = vec ? (n + 7) / 8 : n;
+  const unsigned grid = static_cast<unsigned>(
+      std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, c.num_sms * 8)));
   prof_start(c);
   track(c, launch_pdl(ew_kernel<T, OP>, grid, 256, 0, c.stream, a, lda, b, rows, cols, rowv, sigma,
-                      out, ldo));
+                      out, ldo, vec ? 1 : 0));
   note_launch(c, KK_ELEMENTWISE, OP, 4.0 * n, (OP == 1 ? 3.0 : 2.0) * n * sizeof(T));
 }
 
