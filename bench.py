@@ -255,11 +255,14 @@ def run_ours(args, rank, local_rank, world):
     stream = torch.cuda.current_stream()
     launches = [0, 0]
 
-    def step():
+    def compute():
         B.forward(cfg, params, acts["x"], ws, y, q, k)
         launches[0] = B.last_launch_count()
         B.backward(cfg, params, acts["x"], ws, acts["dy"], acts.get("dq"), acts.get("dk"), dx, grads)
         launches[1] = B.last_launch_count()
+
+    def step():
+        compute()
         if world > 1:
             allreduce_grads(gbuf)
 
@@ -269,6 +272,31 @@ def run_ours(args, rank, local_rank, world):
     torch.cuda.synchronize()
     if B.device_status(ws) != 0:
         raise RuntimeError("device status reports a timeout during warm-up")
+
+    # The step's library launches captured once into a CUDA graph and replayed:
+    # the same kernels with the same arguments, without the host issuing each
+    # launch through the C ABI every step (about 0.9 ms of host time a step at
+    # the 1B shape). The gradient all-reduce of N > 1 runs after each replay.
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            compute()
+        torch.cuda.synchronize()
+        for _ in range(2):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize()
+        if B.device_status(ws) != 0:
+            raise RuntimeError("device status reports a timeout in the captured step")
+
+    def timed_step():
+        if graph is None:
+            step()
+            return
+        graph.replay()
+        if world > 1:
+            allreduce_grads(gbuf)
 
     # ---- timed region: K steps, device time per step (L2 flushed between steps)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -281,7 +309,7 @@ def run_ours(args, rank, local_rank, world):
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
-        step()
+        timed_step()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -384,6 +412,8 @@ def run_ours(args, rank, local_rank, world):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": (launches[0] + launches[1]) * args.steps,
+            "execution": ("CUDA graph replay of the step's library launches (captured once "
+                          "through the C ABI)" if graph is not None else "eager launches"),
             "launches_per_step": {"forward": launches[0], "backward": launches[1]},
             "kernels": breakdown,
             "profiled_ms_per_step": statistics.median(prof_ms),
@@ -452,7 +482,9 @@ def run_e2e(args, cfg, inp, params, ws, act_names, dev, stream, world):
                 "q": torch.empty(cfg.T, cfg.d, dtype=dt, device=dev) if full else None,
                 "k": torch.empty(cfg.T, cfg.d, dtype=dt, device=dev) if full else None}
                for _ in range(NB)]
-    grads = [{n: B.empty_param(cfg, n, dev) for n in cfg.param_shapes()} for _ in range(NB)]
+    from rank_bottleneck_gb300.dp import GradBuffer, allreduce_grads
+    gbufs = [GradBuffer(cfg, dev) for _ in range(NB)]
+    grads = [gb.grads for gb in gbufs]
     host_out = [{"y": torch.empty(cfg.T, cfg.d, dtype=dt).pin_memory(),
                  "dx": torch.empty(cfg.T, cfg.d, dtype=dt).pin_memory()} for _ in range(NB)]
     host_grads = [{n: torch.empty(g.shape, dtype=dt).pin_memory() for n, g in grads[0].items()}
@@ -460,7 +492,9 @@ def run_e2e(args, cfg, inp, params, ws, act_names, dev, stream, world):
     h2d = sum(t.numel() * t.element_size() for t in host_in[0].values())
     d2h = sum(t.numel() * t.element_size() for t in host_out[0].values()) + \
         sum(t.numel() * t.element_size() for t in host_grads[0].values())
-    steps = max(3, min(args.steps, 20))
+    # enough steps that the pipeline's first input copy and last result copy,
+    # which nothing overlaps, are a small part of the timed region
+    steps = min(max(args.steps, 50), 200)
     h2d_stream = torch.cuda.Stream(device=dev)
     d2h_stream = torch.cuda.Stream(device=dev)
     done = [torch.cuda.Event() for _ in range(NB)]     # compute of the slot's last step
@@ -468,6 +502,14 @@ def run_e2e(args, cfg, inp, params, ws, act_names, dev, stream, world):
     read = [torch.cuda.Event() for _ in range(NB)]     # the slot's results are on the host
     for e in done + read:
         e.record(stream)
+
+    def compute(s):
+        o = dev_out[s]
+        B.forward(cfg, params, dev_in[s]["x"], ws, o["y"], o["q"], o["k"])
+        B.backward(cfg, params, dev_in[s]["x"], ws, dev_in[s]["dy"], dev_in[s].get("dq"),
+                   dev_in[s].get("dk"), o["dx"], grads[s])
+
+    run = [compute]  # eager; replaced by graph replays once they are captured
 
     def e2e_step(i):
         s = i % NB
@@ -478,13 +520,13 @@ def run_e2e(args, cfg, inp, params, ws, act_names, dev, stream, world):
             landed[s].record(h2d_stream)
         stream.wait_event(landed[s])
         stream.wait_event(read[s])          # its previous results have left the slot
-        o = dev_out[s]
-        B.forward(cfg, params, dev_in[s]["x"], ws, o["y"], o["q"], o["k"])
-        B.backward(cfg, params, dev_in[s]["x"], ws, dev_in[s]["dy"], dev_in[s].get("dq"),
-                   dev_in[s].get("dk"), o["dx"], grads[s])
+        run[0](s)
+        if world > 1:
+            allreduce_grads(gbufs[s])
         done[s].record(stream)
         with torch.cuda.stream(d2h_stream):
             d2h_stream.wait_event(done[s])
+            o = dev_out[s]
             host_out[s]["y"].copy_(o["y"], non_blocking=True)
             host_out[s]["dx"].copy_(o["dx"], non_blocking=True)
             for n in grads[s]:
@@ -494,6 +536,16 @@ def run_e2e(args, cfg, inp, params, ws, act_names, dev, stream, world):
     for i in range(NB):
         e2e_step(i)
     torch.cuda.synchronize()
+    if not args.no_graph:
+        # each buffer set's forward + backward captured once, replayed per step
+        graphs = []
+        for s_ in range(NB):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                compute(s_)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        run[0] = lambda s_: graphs[s_].replay()
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(h2d_stream)
@@ -505,6 +557,7 @@ def run_e2e(args, cfg, inp, params, ws, act_names, dev, stream, world):
     return {"value": world * steps * cfg.T / (ms / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": ms / steps,
+            "compute": "CUDA graph replay per buffer set" if not args.no_graph else "eager",
             "overlap": "double-buffered: step i's compute overlaps step i+1's input copies "
                        "and step i-1's result copies (two copy streams)"}
 
@@ -561,6 +614,9 @@ def main(argv=None):
     ap.add_argument("--workload", default=None)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="issue every launch through the C ABI each step instead of replaying "
+                         "a captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     from rank_bottleneck_gb300.configs import DEFAULT, WORKLOADS

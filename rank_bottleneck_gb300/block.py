@@ -9,6 +9,11 @@ and the current CUDA stream.
 
 `params` maps the names of ``PARAM_NAMES`` to tensors of the block's dtype;
 d_ff-wide tensors (A_d) may be views with a padded row stride (ld_ff).
+
+The library allocates no memory and does not synchronise inside a forward or
+backward call, so with every output buffer passed in, both calls can be
+captured into a CUDA graph (after one direct call on the device, which sets up
+per-device state) and replayed.
 """
 from __future__ import annotations
 

@@ -209,6 +209,51 @@ def test_full_rank_reduction_block():
     np.testing.assert_allclose(g_lr["B_u"], dWu @ A_u.T, rtol=1e-10, atol=1e-10)
 
 
+def _silu(v):
+    return v / (1 + math.exp(-v))
+
+
+@pytest.mark.parametrize("ranks", [None, (2, 1, 3, 2, 1, 3, 2)])
+def test_full_block_forward_brute_force(ranks):
+    """The whole factorised block (attention core outside: O reads V), every
+    token row and every output element of y, q, k written out as loops over the
+    definition: RMSNorm, the grouped Q/K/V bottlenecks, O, the residual, RMSNorm,
+    gate/up, SwiGLU, down, the residual -- with equal and with uneven ranks."""
+    T, d, r, d_ff = 3, 4, 2, 5
+    a = f64(make_block_inputs(T, d, r, d_ff, dtype="f32", seed=13, ranks=ranks))
+    p = {k: v for k, v in a.items() if k not in ("x", "dy", "dq", "dk")}
+    x = a["x"]
+    out, _ = O.block_forward(p, x, dict(kind="full"))
+    rq, rk, rv = p["B_q"].shape[1], p["B_k"].shape[1], p["B_v"].shape[1]
+    ro, rg, ru, rd = p["A_o"].shape[0], p["B_g"].shape[1], p["B_u"].shape[1], p["A_d"].shape[0]
+
+    def norm(row, w):
+        ms = sum(v * v for v in row) / len(row)
+        return [row[j] * w[j] / math.sqrt(ms + O.EPS) for j in range(len(row))]
+
+    def lin(W, v):  # W [out, in] times the vector v
+        return [sum(W[o][i] * v[i] for i in range(len(v))) for o in range(len(W))]
+
+    for t in range(T):
+        n1 = norm(list(x[t]), p["w_norm1"])
+        h = [_silu(z) for z in lin(p["A_qkv"], n1)]
+        q = lin(p["B_q"], h[:rq])
+        k = lin(p["B_k"], h[rq:rq + rk])
+        v = lin(p["B_v"], h[rq + rk:rq + rk + rv])
+        ho = [_silu(z) for z in lin(p["A_o"], v)]
+        x1 = [x[t][o] + sum(p["B_o"][o][c] * ho[c] for c in range(ro)) for o in range(d)]
+        n2 = norm(x1, p["w_norm2"])
+        hgu = [_silu(z) for z in lin(p["A_gu"], n2)]
+        G = lin(p["B_g"], hgu[:rg])
+        U = lin(p["B_u"], hgu[rg:rg + ru])
+        m = [_silu(G[i]) * U[i] for i in range(d_ff)]
+        hd = [_silu(z) for z in lin(p["A_d"], m)]
+        y = [x1[o] + sum(p["B_d"][o][c] * hd[c] for c in range(rd)) for o in range(d)]
+        np.testing.assert_allclose(out["q"][t], q, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(out["k"][t], k, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(out["y"][t], y, rtol=1e-12, atol=1e-14)
+
+
 def test_dense_layer_brute_force():
     # the dense path the reduction compares against: y = x1 + m W_d^T, one entry by loops
     T, d, d_ff = 2, 4, 6
