@@ -13,7 +13,9 @@
 // 128-row tile (one row per TMEM lane and per epilogue thread) and a stream of
 // 128-row blocks of the other side, d_head = 128.
 //   FWD   stationary Q;        blocks K_j, V_j.   S = Q K_j^T (TMEM), online
-//         softmax in registers, P (bf16) to shared memory, O += P V_j in TMEM;
+//         softmax in registers (the two warps of a row exchange their partial
+//         row maxima through shared memory), P (bf16 pairs) written over the
+//         warp's own S columns, O += P V_j in TMEM with P as the A operand;
 //         O is rescaled in place only when a row maximum grows by more than
 //         2^8 (lazy rescale), and divided by the row sum at the end.
 //   BKV   stationary K and V;  blocks Q_i, dO_i.  S^T = K Q_i^T, dP^T = V dO_i^T;
@@ -36,7 +38,7 @@
 //               tile row per thread) and one column half of every block.
 // TMEM columns: S double-buffered so that the next block's S = Q K^T runs
 // while the current block's softmax does:
-//   FWD  [0, 256) S of block buffers 0 and 1; [256, 512) O of tile buffers 0 and 1
+//   FWD  [0, 256) S (then P) of block buffers 0 and 1; [256, 512) O of tile buffers 0 and 1
 //   BKV  [0, 128) S^T (then P^T, dS^T); [128, 256) dP^T; [256, 384) dV; [384, 512) dK
 //   BQ   [0, 256) S (then dS) of block buffers 0 and 1; [256, 384) dP (single); [384, 512) dQ
 // Every operand is bf16 in 128-byte-swizzled shared memory: K-major for the
@@ -78,8 +80,9 @@ struct Lay {
   static constexpr int HALF = 2 * SUBC;               // one streamed block (both d_head halves)
   static constexpr int EB = BR * BCM * 2;             // one bf16 elementwise tile [128, BCM]
   static constexpr int NX = (MODE == FWD) ? 1 : 2;   // stationary tiles
-  // elementwise tiles in shared memory (the backward keeps P^T, dS^T and dS in TMEM)
-  static constexpr int NE = (MODE == FWD) ? 1 : 0;
+  // elementwise tiles in shared memory: none (the forward keeps P, the backward
+  // P^T, dS^T and dS in TMEM, over the score columns already read)
+  static constexpr int NE = 0;
   // buffers of each elementwise tile: the forward's P and dQ's dS are single
   // (shared memory); the softmax waits for the previous block's product first
   static constexpr int NPB = (MODE == BKV) ? 2 : 1;
@@ -95,14 +98,15 @@ struct Lay {
   static constexpr int E_OFF = Y_OFF + (NSTK + NSTV) * HALF;
   static constexpr int AUX_OFF = E_OFF + NE * NPB * EB;
   static constexpr int XCH_OFF = AUX_OFF + NSTK * AUXB;
-  // FWD: row sums exchanged between the two warps of a row, [2 tile parity][2 half][128]
-  static constexpr int BAR_OFF = XCH_OFF + ((MODE == FWD) ? 2 * 2 * BR * 4 : 0);
+  // FWD: row sums exchanged between the two warps of a row, [2 tile parity][2 half][128],
+  // then each block's row maxima, [2 block parity][2 half][128]
+  static constexpr int BAR_OFF = XCH_OFF + ((MODE == FWD) ? 2 * 2 * 2 * BR * 4 : 0);
   // stage barriers: the two halves of a FWD or BQ stage are filled and freed
   // apart (FWD: K after S, V after P V; BQ: V after dP, K after dQ), BKV's
   // stage as a whole
   static constexpr int NYB = (MODE == BKV) ? NSTK : NSTK + NSTV;
-  // barriers (2 + 2 NYB + 21 of 8 bytes), the TMEM address and the abort flag
-  static constexpr int BAR_BYTES = (2 + 2 * NYB + 21) * 8 + 8 <= 256 ? 256 : 512;
+  // barriers (2 + 2 NYB + 29 of 8 bytes), the TMEM address and the abort flag
+  static constexpr int BAR_BYTES = (2 + 2 * NYB + 29) * 8 + 8 <= 256 ? 256 : 512;
   static constexpr int BYTES = BAR_OFF + BAR_BYTES;
   static constexpr int SMEM = 1024 + BYTES;
   static_assert(E_OFF % 1024 == 0, "elementwise tiles must be 1024-byte aligned");
@@ -232,15 +236,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
   uint8_t* sYK = smem + LY::Y_OFF;                  // first-half ring (K; BKV: Q)
   uint8_t* sYV = sYK + LY::NSTK * HALF;              // second-half ring (V; BKV: dO)
   float* sAux = reinterpret_cast<float*>(smem + LY::AUX_OFF);
-  uint8_t* sE = smem + LY::E_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::BAR_OFF);
   uint64_t* x_full = bars;
   uint64_t* x_empty = bars + 1;
   uint64_t* y_full = bars + 2;                // [NYB] (FWD, BQ: K ring, then V ring)
   uint64_t* y_empty = y_full + LY::NYB;       // [NYB]
   uint64_t* s_full = y_empty + LY::NYB;       // [2]
-  uint64_t* s_empty = s_full + 2;             // [2]  FWD, BQ: S read (BKV: S^T's buffer frees
-                                              //      with e_empty[0])
+  uint64_t* s_empty = s_full + 2;             // [2]  unused: every S buffer is freed by the
+                                              //      product that reads what replaced it (e_empty)
   uint64_t* e_full = s_empty + 2;             // [2]  P / dS (BKV: P^T, dS^T) written
   uint64_t* e_empty = e_full + 2;             // [2]  the accumulating products that read them done
   uint64_t* a_full = e_empty + 2;             // backward: [0] the tile's sums done, [1] dP ready
@@ -248,7 +251,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
                                               // backward: [0] sums read out, [1] dP read
   uint64_t* drain = a_empty + 2;
   uint64_t* lx = drain + 1;                   // FWD [4 row quarters][2 tile parity]: row sums exchanged
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lx + 8);
+  uint64_t* mxb = lx + 8;                     // FWD [4 row quarters][2 block parity]: row maxima exchanged
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mxb + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -270,6 +274,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
     }
     mbar_init(smem_u32(drain), 1);
     for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&lx[i]), 64);
+    for (int i = 0; i < 8; ++i) mbar_init(smem_u32(&mxb[i]), 64);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -369,8 +374,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
       auto issue_sd = [&](uint32_t n) -> bool {
         const int st = n % LY::NSTK, bf = n & 1;
         if (!bwait(smem_u32(&y_full[st]), (n / LY::NSTK) & 1u, abort_flag, P.status)) return false;
-        // the buffer's previous block: S read (FWD), its dS read by dQ's product (BQ)
-        uint64_t* freed = (MODE == BQ) ? &e_empty[bf] : &s_empty[bf];
+        // the buffer's previous block: its P (FWD) or dS (BQ), written over its
+        // scores, read by that block's accumulating product
+        uint64_t* freed = &e_empty[bf];
         if (!bwait(smem_u32(freed), ((n >> 1) & 1u) ^ 1u, abort_flag, P.status)) return false;
         tc_fence_after();
         const uint32_t y = smem_u32(sYK + st * HALF);
@@ -538,15 +544,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             break;
           }
           tc_fence_after();
-          const uint32_t e = smem_u32(sE);
           const uint32_t acc = (i > 0) ? 1u : 0u;
           if constexpr (MODE == FWD) {
-            // O += P V_j: A = P [128 x BCM keys] (64-key sub-tiles of 16 KB), B = V_j
-            // read MN-major [d_head x BCM keys] (its two d_head halves SUBC apart)
+            // O += P V_j: A = P in TMEM (bf16 pairs in S's buffer: the 16 keys of
+            // k-step kk are warp half kk / 4's, in that half's first 32 columns),
+            // B = V_j read MN-major [d_head x BCM keys] (its two d_head halves SUBC apart)
 #pragma unroll
             for (int kk = 0; kk < BCM / 16; ++kk)
-              mma_bf16<1>(tmem + OCOL + ab * DH,
-                          smem_desc(e + (kk >> 2) * (BR * 128) + (kk & 3) * 32, false),
+              mma_bf16_ta(tmem + OCOL + ab * DH, tmem + bf * BCM + 64 * (kk >> 2) + 8 * (kk & 3),
                           smem_desc_mn(smem_u32(sYV + stv * HALF) + kk * 2048, SUBC), ID_A,
                           (acc | kk) ? 1u : 0u);
           } else {
@@ -558,10 +563,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
               mma_bf16_ta(tmem + 384, tmem + bf * BCM + 64 * (kk >> 2) + 8 * (kk & 3),
                           smem_desc_mn(smem_u32(sYK + stk * HALF) + kk * 2048, SUBC), ID_A,
                           (acc | kk) ? 1u : 0u);
-            (void)e;
           }
-          // the E tiles of this buffer are free, (FWD) O holds block i, the
-          // stage (FWD: its V half; BQ: its K half) is no longer read
+          // this S buffer is free again (its P / dS read), (FWD) O holds block i,
+          // the stage (FWD: its V half; BQ: its K half) is no longer read
           mma_commit<1>(smem_u32(&e_empty[bf]));
           mma_commit<1>(smem_u32(&y_empty[(MODE == FWD) ? LY::NSTK + stv : stk]));
         }
@@ -577,8 +581,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
     // ------------------------------------------------------------ elementwise
     // Eight warps: warp w owns TMEM lanes 32 (w % 4) .. + 31 (tile rows) and
     // column half hf of every block and of every TMEM sum. The forward's two
-    // warps of a row (w and w + 4) both read the whole block for its maximum and
-    // exchange their partial row sums once per tile (mbarrier lx).
+    // warps of a row (w and w + 4) exchange their partial row maxima once per
+    // block (mbarrier mxb) and their partial row sums once per tile (mbarrier lx).
     const int q = warp & 3;
     const int hf = (warp - 2) >> 2;
     const int r = 32 * q + lane;
@@ -624,10 +628,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             break;
           }
           tc_fence_after();
-          // Raw scores of the row: this warp's own 64 columns of the block, and the
-          // other warp's 64 for the row maximum. Scale > 0, so the maximum is taken
-          // on raw scores; masked scores are -inf.
-          const int c0 = j * BCM + 64 * hf, c1 = j * BCM + 64 * (1 - hf);
+          // Raw scores of the row: this warp's own 64 columns of the block. Scale > 0,
+          // so the maximum is taken on raw scores; masked scores are -inf. The row's
+          // other half comes from its other warp as a partial maximum through
+          // shared memory, so that each warp reads only its own columns and can
+          // write P over them.
+          const int c0 = j * BCM + 64 * hf;
           const bool need_mask = (P.causal && j * BCM + BCM - 1 > t * BR) || j * BCM + BCM > P.L;
           float x[64];
           float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -648,31 +654,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           }
 #pragma unroll
           for (int i = 0; i < 64; i += 2) mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], x[i], x[i + 1]);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t yr[32];
-            tmem_ld32_nowait(tmem + lb + bf * BCM + 64 * (1 - hf) + 32 * h, yr);
-            tmem_wait_ld2(yr, yr);
-            if (need_mask) {
-#pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                const int c = c1 + 32 * h + i;
-                const float y0 = (c >= lo && c <= hi) ? __uint_as_float(yr[i]) : -INFINITY;
-                const float y1 = (c + 1 >= lo && c + 1 <= hi) ? __uint_as_float(yr[i + 1]) : -INFINITY;
-                mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], y0, y1);
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; i += 2)
-                mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], __uint_as_float(yr[i]),
-                                        __uint_as_float(yr[i + 1]));
+          {
+            // exchange the partial maxima with the row's other warp (block parity bf)
+            float* xm = xl + 2 * 2 * BR + bf * 2 * BR;  // [2 half][128] of this block parity
+            xm[hf * BR + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            mbar_arrive(smem_u32(&mxb[2 * q + bf]));
+            if (!wwait(&mxb[2 * q + bf], (jn >> 1) & 1u)) {
+              ok = false;
+              break;
             }
+            mx[0] = fmaxf(xm[hf * BR + r], xm[(1 - hf) * BR + r]);
           }
-          // S is in registers: the MMA may compute the block after next into its buffer
-          tc_fence_before();
-          __syncwarp();
-          arrive(&s_empty[bf]);
-          const float bm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * P.scale_log2;
+          const float bm = mx[0] * P.scale_log2;
           const float m_new = fmaxf(m, bm);
           // (a warp-wide decision: the TMEM accesses below are warp-collective;
           // the row's other warp sees the same rows and decides the same)
@@ -701,15 +694,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             l *= a;
             m = m_new;
           }
-          // the single P tile: the previous block's P V must have read it
-          if (jn > 0) {
-            const uint32_t pj = jn - 1;
-            if (!wwait(&e_empty[pj & 1u], (pj >> 1) & 1u)) {
-              ok = false;
-              break;
-            }
-          }
-          uint8_t* pt = sE + hf * (BR * 128);  // this warp's 64-key sub-tile of P
+          // P as bf16 pairs over this warp's own score columns, already read: keys
+          // 32 h .. 32 h + 31 of the half go to columns 16 h .. 16 h + 15, where the
+          // P V product reads them as its A operand
           float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -721,10 +708,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
               rs[(i >> 1) & 3] += p0 + p1;
               pk[i / 2] = pack2(p0, p1);
             }
-            put_row32(pt, r, h, pk);
+            tmem_st16u_nowait(tmem + lb + bf * BCM + 64 * hf + 16 * h, pk);
           }
           l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-          fence_proxy_async();
+          tmem_wait_st();
           tc_fence_before();
           __syncwarp();
           arrive(&e_full[bf]);
