@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "rowops.h"
+#include "tc_ptx.cuh"
 
 namespace bn {
 
@@ -207,27 +208,19 @@ void launch_stats(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float eps,
 }
 
 // ---------------------------------------------------------------------------
-// B3: RMSNorm backward. One warp per row, 4 x 16 bytes of every tensor in
-// flight per lane; each warp keeps its own dw column sums in shared memory
-// (lane-exclusive columns, no atomics). Every block writes its column sums to
-// a row of `part`; colsum_kernel adds the rows in a fixed order, so dw is
-// bit-reproducible.
+// B3: RMSNorm backward. Every block writes the dw column sums of its rows to a
+// row of `part`; colsum_kernel (or the backward's final launch) adds the rows
+// in a fixed order, so dw is bit-reproducible.
 // ---------------------------------------------------------------------------
 constexpr int kNormBwdUnroll = 4;
 constexpr size_t kNormBwdSmemLimit = 200 * 1024;
 
-
-// NP > 0: rows of exactly NP * 256 bf16 elements, held in registers for the
-// whole row (dn, x and dres all loaded up front: one memory round trip per row;
-// one block per SM for the registers). NP = 0: any d, two passes over the row
-// (the second one mostly from L1/L2), two blocks per SM.
-// Register-resident rows run 12 warps in one block per SM (up to 168 registers a
-// thread); the two-pass form runs two blocks of 8 warps per SM.
-template <int NP>
-constexpr int norm_bwd_warps() { return NP > 0 ? 12 : 8; }
-
-template <typename T, int NP>
-__global__ void __launch_bounds__(norm_bwd_warps<NP>() * 32, NP > 0 ? 1 : 2)
+// Any T and d: one warp per row, two passes over the row (the second one mostly
+// from L1/L2), 4 x 16 bytes of every tensor in flight per lane, two blocks of
+// 8 warps per SM. Each warp keeps its own dw column sums in shared memory
+// (lane-exclusive columns, no atomics).
+template <typename T>
+__global__ void __launch_bounds__(256, 2)
     norm_bwd_kernel(const T* __restrict__ dn, const T* __restrict__ x, const T* __restrict__ w,
                     const float* __restrict__ rstd, const T* __restrict__ dres, int64_t rows,
                     int d, T* __restrict__ dx, float* __restrict__ part) {
@@ -238,9 +231,7 @@ __global__ void __launch_bounds__(norm_bwd_warps<NP>() * 32, NP > 0 ? 1 : 2)
   const int nw = blockDim.x >> 5;
   const int dp = d + d / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* wsm = acc + nw * dp;  // the norm weight as fp32, read by every row
   for (int i = threadIdx.x; i < nw * dp; i += blockDim.x) acc[i] = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) wsm[i] = to_f<T>(w[i]);
   __syncthreads();
   float* my = acc + warp * dp;
   const float inv_d = 1.0f / static_cast<float>(d);
@@ -249,47 +240,6 @@ __global__ void __launch_bounds__(norm_bwd_warps<NP>() * 32, NP > 0 ? 1 : 2)
        row += static_cast<int64_t>(gridDim.x) * nw) {
     const T* dnr = dn + row * d;
     const T* xr = x + row * d;
-    if constexpr (NP > 0) {
-      const T* dr = dres + row * d;
-      Pack8<T> a[NP], b[NP];
-#pragma unroll
-      for (int u = 0; u < NP; ++u) {
-        const int c = lane * 8 + u * 256;
-        a[u].load(dnr + c);
-        b[u].load(xr + c);
-      }
-      float s = 0.f;
-#pragma unroll
-      for (int u = 0; u < NP; ++u) {
-        const int c = lane * 8 + u * 256;
-        const float4 w0 = *reinterpret_cast<const float4*>(wsm + c);
-        const float4 w1 = *reinterpret_cast<const float4*>(wsm + c + 4);
-        const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) s = fmaf(a[u][i] * ww[i], b[u][i], s);
-      }
-      s = warp_sum(s);
-      const float r = rstd[row];
-      const float coef = r * r * s * inv_d;
-      T* o = dx + row * d;
-#pragma unroll
-      for (int u = 0; u < NP; ++u) {
-        const int c = lane * 8 + u * 256;
-        const float4 w0 = *reinterpret_cast<const float4*>(wsm + c);
-        const float4 w1 = *reinterpret_cast<const float4*>(wsm + c + 4);
-        const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        Pack8<T> g;  // the residual gradient, read only here: fewer registers live
-        g.load(dr + c);
-        float out[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          out[i] = g[i] + (a[u][i] * ww[i] - b[u][i] * coef);
-          my[c + c / 8 + i] = fmaf(a[u][i], b[u][i], my[c + c / 8 + i]);
-        }
-        Vec8<T>::store(o + c, out);
-      }
-      continue;
-    }
     float s = 0.f;
     for (int base = lane * 8; base < d; base += 256 * U) {
       Pack8<T> a[U], b[U], ww[U];
@@ -351,6 +301,178 @@ __global__ void __launch_bounds__(norm_bwd_warps<NP>() * 32, NP > 0 ? 1 : 2)
   }
 }
 
+// bf16 rows of at most 256 NP columns, streamed through shared memory. Every
+// warp owns a ring of two stages; a stage holds one row of dn', x and dres,
+// brought in by three bulk copies that complete on the stage's mbarrier. While
+// a warp works on one row, the copies of its next row are in flight, so an SM
+// keeps up to 2 x warps rows of reads outstanding without holding them in
+// registers. A lane owns the columns 256 u + 8 lane + (0..7), u < NP: their
+// norm weight and their dw sums stay in registers for the whole launch. Block
+// b takes the contiguous rows [b rows / grid, (b + 1) rows / grid); its warps
+// take them round robin. One block per SM. Arithmetic per element, and the
+// order of the row sum, as in norm_bwd_kernel.
+constexpr size_t kNormBwdStreamSmem = 227 * 1024;
+
+// Untiled bulk copy from global memory into this CTA's shared memory,
+// completing on `bar`. Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+template <int NP>
+constexpr int norm_bwd_stream_warps() { return NP > 4 ? 9 : 16; }
+
+template <int NP>
+__global__ void __launch_bounds__(norm_bwd_stream_warps<NP>() * 32, 1)
+    norm_bwd_stream_kernel(const bf16* __restrict__ dn, const bf16* __restrict__ x,
+                           const bf16* __restrict__ w, const float* __restrict__ rstd,
+                           const bf16* __restrict__ dres, int64_t rows, int d,
+                           bf16* __restrict__ dx, float* __restrict__ part, int* status) {
+  extern __shared__ __align__(128) unsigned char nbs[];
+  const int nw = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t row_bytes = static_cast<uint32_t>(d) * 2u;
+  const uint32_t stage_bytes = 3u * row_bytes;  // dn' | x | dres
+  unsigned char* ring = nbs + static_cast<size_t>(warp) * 2 * stage_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(nbs + static_cast<size_t>(nw) * 2 * stage_bytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * nw);
+  const uint32_t bar0 = tc::smem_u32(bars + 2 * warp);
+  const uint32_t ring0 = tc::smem_u32(ring);
+  if (lane == 0) {
+    tc::mbar_init(bar0, 1);
+    tc::mbar_init(bar0 + 8, 1);
+  }
+  if (threadIdx.x == 0) *abort_flag = 0;
+  // the norm weight is a parameter: no kernel of the stream writes it
+  Pack8<bf16> wv[NP];
+  float acc[NP][8];
+#pragma unroll
+  for (int u = 0; u < NP; ++u) {
+    const int c = u * 256 + lane * 8;
+    if (c < d)
+      wv[u].load(w + c);
+    else
+      wv[u].zero();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncthreads();
+  grid_dependency_sync();
+
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows / gridDim.x;
+  const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * rows / gridDim.x;
+  const int64_t first = r0 + warp;
+  const int64_t n = first < r1 ? (r1 - first + nw - 1) / nw : 0;  // this warp's rows
+  // copies of the warp's row j into stage j & 1 (lane 0)
+  auto issue = [&](int64_t j) {
+    const int64_t off = (first + j * nw) * d;
+    const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(j & 1);
+    const uint32_t dst = ring0 + static_cast<uint32_t>(j & 1) * stage_bytes;
+    tc::mbar_expect_tx(bar, stage_bytes);
+    bulk_load(dst, dn + off, row_bytes, bar);
+    bulk_load(dst + row_bytes, x + off, row_bytes, bar);
+    bulk_load(dst + 2 * row_bytes, dres + off, row_bytes, bar);
+  };
+  if (lane == 0) {
+    if (n > 0) issue(0);
+    if (n > 1) issue(1);
+  }
+  const float inv_d = 1.0f / static_cast<float>(d);
+  float r_next = n > 0 ? rstd[first] : 0.f;
+  int64_t j = 0;
+  for (; j < n; ++j) {
+    const int64_t row = first + j * nw;
+    const float r = r_next;
+    if (j + 1 < n) r_next = rstd[row + nw];  // in flight while this row is worked on
+    const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(j & 1);
+    // every lane waits (the wait makes the copies visible to it); the warp
+    // leaves together if any lane gave up
+    const bool landed =
+        tc::wait_bar_inline(bar, static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status);
+    if (!__all_sync(0xffffffffu, landed)) break;
+    const bf16* sdn = reinterpret_cast<const bf16*>(ring + (j & 1) * stage_bytes);
+    const bf16* sx = sdn + d;
+    const bf16* sg = sdn + 2 * d;
+    // dn' and x are read from the stage twice (for the row sum, then for the
+    // outputs) rather than held in registers across the warp reduction
+    float s = 0.f;
+#pragma unroll
+    for (int u = 0; u < NP; ++u) {
+      const int c = u * 256 + lane * 8;
+      Pack8<bf16> a, b;
+      if (c < d) {
+        a.load(sdn + c);
+        b.load(sx + c);
+      } else {
+        a.zero();
+        b.zero();
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s = fmaf(a[i] * wv[u][i], b[i], s);
+    }
+    s = warp_sum(s);
+    const float coef = r * r * s * inv_d;
+    bf16* o = dx + row * d;
+#pragma unroll
+    for (int u = 0; u < NP; ++u) {
+      const int c = u * 256 + lane * 8;
+      if (c < d) {
+        Pack8<bf16> a, b, g;
+        a.load(sdn + c);
+        b.load(sx + c);
+        g.load(sg + c);
+        float out[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          out[i] = g[i] + (a[i] * wv[u][i] - b[i] * coef);
+          acc[u][i] = fmaf(a[i], b[i], acc[u][i]);
+        }
+        Vec8<bf16>::store(o + c, out);
+      }
+    }
+    __syncwarp();  // every lane has read the stage
+    if (lane == 0 && j + 2 < n) {
+      tc::fence_proxy_async();
+      issue(j + 2);
+    }
+  }
+  if (j < n) {
+    // a wait gave up: let this warp's copies still in flight (rows j and j + 1)
+    // land before the block's shared memory is reused or released
+    for (int64_t k = j; k < n && k < j + 2; ++k) {
+      const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(k & 1);
+      const unsigned long long t0 = globaltimer_ns();
+      while (!tc::mbar_try_wait(bar, static_cast<uint32_t>(k >> 1) & 1u) &&
+             globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  }
+  // block sum of the warps' dw columns, in warp order, through shared memory
+  __syncthreads();
+  float* red = reinterpret_cast<float*>(nbs);  // [nw][d], inside the stages
+#pragma unroll
+  for (int u = 0; u < NP; ++u) {
+    const int c = u * 256 + lane * 8;
+    if (c < d) {
+      float* p = red + static_cast<size_t>(warp) * d + c;
+      *reinterpret_cast<float4*>(p) = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+      *reinterpret_cast<float4*>(p + 4) = make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
+    }
+  }
+  __syncthreads();
+  for (int col = threadIdx.x; col < d; col += blockDim.x) {
+    float v = red[col];
+    for (int k = 1; k < nw; ++k) v += red[static_cast<size_t>(k) * d + col];
+    part[static_cast<int64_t>(blockIdx.x) * d + col] = v;
+  }
+}
+
 // dw[col] = sum over blocks b of part[b][col] for the 32 columns of block `cb`:
 // each of the 8 warps sums a fixed contiguous range of b, the 8 sums are added
 // in warp order.
@@ -385,35 +507,62 @@ __global__ void __launch_bounds__(256) colsum_kernel(const float* __restrict__ p
 
 int norm_bwd_blocks(int num_sms) { return 2 * num_sms; }
 
+using NormBwdStream = void (*)(const bf16*, const bf16*, const bf16*, const float*, const bf16*,
+                               int64_t, int, bf16*, float*, int*);
+static NormBwdStream norm_bwd_stream(int np) {
+  static const NormBwdStream k[8] = {
+      norm_bwd_stream_kernel<1>, norm_bwd_stream_kernel<2>, norm_bwd_stream_kernel<3>,
+      norm_bwd_stream_kernel<4>, norm_bwd_stream_kernel<5>, norm_bwd_stream_kernel<6>,
+      norm_bwd_stream_kernel<7>, norm_bwd_stream_kernel<8>};
+  static const bool attr = [] {
+    for (auto f : k)
+      cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kNormBwdStreamSmem));
+    return true;
+  }();
+  (void)attr;
+  return k[np - 1];
+}
+static int norm_bwd_stream_max_warps(int np) {
+  return np > 4 ? norm_bwd_stream_warps<8>() : norm_bwd_stream_warps<1>();
+}
+
 template <typename T>
 int launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rstd,
                     const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw,
                     bool colsum) {
-  // bf16 rows of 1024 or 2048 elements stay in registers
-  constexpr bool kResident = sizeof(T) == 2;  // register-resident rows for bf16 only
-  constexpr int kNP4 = kResident ? 4 : 0, kNP8 = kResident ? 8 : 0;
-  const bool resident = kResident && (d == 2048 || d == 1024);
-  if (resident) nblk = std::min(nblk, c.num_sms);  // one block per SM
-  // as many warps as their column sums fit in shared memory, beside the weight
-  const size_t row_bytes = sizeof(float) * static_cast<size_t>(d + d / 8);
-  const size_t w_bytes = sizeof(float) * static_cast<size_t>(d);
-  const int max_warps = resident ? norm_bwd_warps<4>() : norm_bwd_warps<0>();
-  const int nw = static_cast<int>(std::max<size_t>(
-      1, std::min<size_t>(max_warps, (kNormBwdSmemLimit - w_bytes) / row_bytes)));
-  const size_t smem = row_bytes * nw + w_bytes;
-  auto kern = norm_bwd_kernel<T, 0>;
-  if (kResident && d == 2048) kern = norm_bwd_kernel<T, kNP8>;
-  if (kResident && d == 1024) kern = norm_bwd_kernel<T, kNP4>;
-  static const bool attr = [] {
-    for (auto k : {norm_bwd_kernel<T, 0>, norm_bwd_kernel<T, kNP4>, norm_bwd_kernel<T, kNP8>})
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kNormBwdSmemLimit));
-    return true;
-  }();
-  (void)attr;
+  // bf16 rows of up to 2048 columns are streamed through shared memory (one
+  // block per SM); anything else takes the two-pass kernel
+  constexpr bool kBf16 = sizeof(T) == 2;
+  const bool stream = kBf16 && d <= 2048 && d % 8 == 0;
   prof_start(c);
-  track(c, launch_pdl(kern, nblk, nw * 32, smem, c.stream, dn, x, w, rstd, dres, rows,
-                      static_cast<int>(d), dx, part));
+  if (stream) {
+    nblk = std::min(nblk, c.num_sms);
+    const int np = static_cast<int>((d + 255) / 256);
+    // two stages of three rows per warp, then 16 bytes of barriers per warp and the abort flag
+    const size_t warp_bytes = 12 * static_cast<size_t>(d) + 16;
+    const int nw = static_cast<int>(std::max<size_t>(
+        1, std::min<size_t>(norm_bwd_stream_max_warps(np), (kNormBwdStreamSmem - 16) / warp_bytes)));
+    const size_t smem = warp_bytes * nw + 16;
+    track(c, launch_pdl(norm_bwd_stream(np), nblk, nw * 32, smem, c.stream,
+                        reinterpret_cast<const bf16*>(dn), reinterpret_cast<const bf16*>(x),
+                        reinterpret_cast<const bf16*>(w), rstd, reinterpret_cast<const bf16*>(dres),
+                        rows, static_cast<int>(d), reinterpret_cast<bf16*>(dx), part, c.status));
+  } else {
+    // as many warps as their column sums fit in shared memory
+    const size_t row_bytes = sizeof(float) * static_cast<size_t>(d + d / 8);
+    const int nw = static_cast<int>(
+        std::max<size_t>(1, std::min<size_t>(8, kNormBwdSmemLimit / row_bytes)));
+    const size_t smem = row_bytes * nw;
+    static const bool attr = [] {
+      cudaFuncSetAttribute(norm_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kNormBwdSmemLimit));
+      return true;
+    }();
+    (void)attr;
+    track(c, launch_pdl(norm_bwd_kernel<T>, nblk, nw * 32, smem, c.stream, dn, x, w, rstd, dres,
+                        rows, static_cast<int>(d), dx, part));
+  }
   note_launch(c, KK_NORM_BWD, -1, 8.0 * rows * d,
               4.0 * rows * d * sizeof(T) + d * sizeof(T) + 4.0 * rows + 4.0 * nblk * d);
   if (!colsum) return nblk;  // the caller sums `part` later (launch_finish)
