@@ -36,9 +36,9 @@
 //   warp 1      TMEM owner (512 columns) and, from one thread, the MMA issuer;
 //   warps 2..9  elementwise: warp w owns TMEM lanes 32 (w % 4) .. + 31 (one
 //               tile row per thread) and one column half of every block.
-// TMEM columns: S double-buffered so that the next block's S = Q K^T runs
-// while the current block's softmax does:
-//   FWD  [0, 256) S (then P) of block buffers 0 and 1; [256, 512) O of tile buffers 0 and 1
+// TMEM columns: S in two or three buffers so that the next blocks' S = Q K^T
+// run while the current block's softmax does:
+//   FWD  [0, 384) S (then P) of block buffers 0, 1 and 2; [384, 512) O
 //   BKV  [0, 128) S^T (then P^T, dS^T); [128, 256) dP^T; [256, 384) dV; [384, 512) dK
 //   BQ   [0, 256) S (then dS) of block buffers 0 and 1; [256, 384) dP (single); [384, 512) dQ
 // Every operand is bf16 in 128-byte-swizzled shared memory: K-major for the
@@ -105,8 +105,11 @@ struct Lay {
   // apart (FWD: K after S, V after P V; BQ: V after dP, K after dQ), BKV's
   // stage as a whole
   static constexpr int NYB = (MODE == BKV) ? NSTK : NSTK + NSTV;
-  // barriers (2 + 2 NYB + 29 of 8 bytes), the TMEM address and the abort flag
-  static constexpr int BAR_BYTES = (2 + 2 * NYB + 29) * 8 + 8 <= 256 ? 256 : 512;
+  // TMEM buffers of the scores (then P or dS): the forward's three let the MMA
+  // thread issue the score products two blocks ahead of the softmax
+  static constexpr int NSB = (MODE == FWD) ? 3 : 2;
+  // barriers (2 + 2 NYB + 3 NSB + 21 of 8 bytes), the TMEM address and the abort flag
+  static constexpr int BAR_BYTES = (2 + 2 * NYB + 3 * NSB + 21) * 8 + 8 <= 256 ? 256 : 512;
   static constexpr int BYTES = BAR_OFF + BAR_BYTES;
   static constexpr int SMEM = 1024 + BYTES;
   static_assert(E_OFF % 1024 == 0, "elementwise tiles must be 1024-byte aligned");
@@ -227,8 +230,9 @@ template <int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant__ Params P) {
   using LY = Lay<MODE>;
   constexpr int BCM = LY::BCM, SUBC = LY::SUBC, HALF = LY::HALF;
-  // forward: S buffers take TMEM columns [0, 2 BCM), O the two 128-column buffers after them
-  constexpr int OCOL = 2 * BCM;
+  // forward: S buffers take TMEM columns [0, 3 BCM), O the 128 columns after them
+  constexpr int NSB = LY::NSB;
+  constexpr int OCOL = NSB * BCM;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -241,13 +245,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
   uint64_t* x_empty = bars + 1;
   uint64_t* y_full = bars + 2;                // [NYB] (FWD, BQ: K ring, then V ring)
   uint64_t* y_empty = y_full + LY::NYB;       // [NYB]
-  uint64_t* s_full = y_empty + LY::NYB;       // [2]
-  uint64_t* s_empty = s_full + 2;             // [2]  unused: every S buffer is freed by the
-                                              //      product that reads what replaced it (e_empty)
-  uint64_t* e_full = s_empty + 2;             // [2]  P / dS (BKV: P^T, dS^T) written
-  uint64_t* e_empty = e_full + 2;             // [2]  the accumulating products that read them done
-  uint64_t* a_full = e_empty + 2;             // backward: [0] the tile's sums done, [1] dP ready
-  uint64_t* a_empty = a_full + 2;             // FWD: O buffer [tile parity] read out;
+  uint64_t* s_full = y_empty + LY::NYB;       // [NSB] scores of the buffer's block ready
+  uint64_t* e_full = s_full + NSB;            // [NSB] P / dS (BKV: P^T, dS^T) written
+  uint64_t* e_empty = e_full + NSB;           // [NSB] the accumulating products that read them
+                                              //       done (the buffer is free again)
+  uint64_t* a_full = e_empty + NSB;           // backward: [0] the tile's sums done, [1] dP ready
+  uint64_t* a_empty = a_full + 2;             // FWD: [0] O read out;
                                               // backward: [0] sums read out, [1] dP read
   uint64_t* drain = a_empty + 2;
   uint64_t* lx = drain + 1;                   // FWD [4 row quarters][2 tile parity]: row sums exchanged
@@ -264,11 +267,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
       mbar_init(smem_u32(&y_full[i]), 1);
       mbar_init(smem_u32(&y_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NSB; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_empty[i]), 8);
       mbar_init(smem_u32(&e_full[i]), 8);
       mbar_init(smem_u32(&e_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&a_full[i]), 1);
       mbar_init(smem_u32(&a_empty[i]), 8);
     }
@@ -370,14 +374,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
       constexpr uint32_t ID_A = instr_desc(128, DH, false, true);    // sums: MN-major B
       bool ok = true;
       uint32_t tn = 0, jn = 0;
-      // S (and dP) of streamed block number n into TMEM buffer n & 1
+      // S (and dP) of streamed block number n into TMEM buffer n % NSB
       auto issue_sd = [&](uint32_t n) -> bool {
-        const int st = n % LY::NSTK, bf = n & 1;
+        const int st = n % LY::NSTK, bf = n % NSB;
         if (!bwait(smem_u32(&y_full[st]), (n / LY::NSTK) & 1u, abort_flag, P.status)) return false;
         // the buffer's previous block: its P (FWD) or dS (BQ), written over its
         // scores, read by that block's accumulating product
         uint64_t* freed = &e_empty[bf];
-        if (!bwait(smem_u32(freed), ((n >> 1) & 1u) ^ 1u, abort_flag, P.status)) return false;
+        if (!bwait(smem_u32(freed), ((n / NSB) & 1u) ^ 1u, abort_flag, P.status)) return false;
         tc_fence_after();
         const uint32_t y = smem_u32(sYK + st * HALF);
         const uint32_t x = smem_u32(sX);
@@ -513,17 +517,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
         }
         tc_fence_after();
         const int nblk = last - first;
-        if (!issue_sd(jn) || (MODE == BQ && !issue_dp(jn))) {
+        // scores issued LA blocks ahead of the accumulating product (FWD: two, into
+        // the third S buffer, so that a block's scores never wait behind the
+        // product of the block before; BQ: one)
+        constexpr int LA = NSB - 1;
+        bool pre = true;
+        for (int i = 0; pre && i < LA && i < nblk; ++i)
+          pre = issue_sd(jn + i) && (MODE != BQ || issue_dp(jn + i));
+        if (!pre) {
           ok = false;
           break;
         }
         for (int i = 0; i < nblk; ++i, ++jn) {
-          if (i + 1 < nblk && (!issue_sd(jn + 1) || (MODE == BQ && !issue_dp(jn + 1)))) {
+          if (i + LA < nblk && (!issue_sd(jn + LA) || (MODE == BQ && !issue_dp(jn + LA)))) {
             ok = false;
             break;
           }
-          const int stk = jn % LY::NSTK, stv = jn % LY::NSTV, bf = jn & 1;
-          if (!bwait(smem_u32(&e_full[bf]), (jn >> 1) & 1u, abort_flag, P.status)) {
+          const int stk = jn % LY::NSTK, stv = jn % LY::NSTV, bf = jn % NSB;
+          if (!bwait(smem_u32(&e_full[bf]), (jn / NSB) & 1u, abort_flag, P.status)) {
             ok = false;
             break;
           }
@@ -536,10 +547,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             }
           }
           // the first accumulating product of a tile overwrites its TMEM sums: they
-          // must have been read out (FWD: O alternates between two buffers by tile)
-          const int ab = (MODE == FWD) ? static_cast<int>(tn & 1u) : 0;
-          const uint32_t apar = ((MODE == FWD) ? ((tn >> 1) & 1u) : (tn & 1u)) ^ 1u;
-          if (i == 0 && !bwait(smem_u32(&a_empty[ab]), apar, abort_flag, P.status)) {
+          // must have been read out
+          if (i == 0 && !bwait(smem_u32(&a_empty[0]), (tn & 1u) ^ 1u, abort_flag, P.status)) {
             ok = false;
             break;
           }
@@ -551,7 +560,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             // B = V_j read MN-major [d_head x BCM keys] (its two d_head halves SUBC apart)
 #pragma unroll
             for (int kk = 0; kk < BCM / 16; ++kk)
-              mma_bf16_ta(tmem + OCOL + ab * DH, tmem + bf * BCM + 64 * (kk >> 2) + 8 * (kk & 3),
+              mma_bf16_ta(tmem + OCOL, tmem + bf * BCM + 64 * (kk >> 2) + 8 * (kk & 3),
                           smem_desc_mn(smem_u32(sYV + stv * HALF) + kk * 2048, SUBC), ID_A,
                           (acc | kk) ? 1u : 0u);
           } else {
@@ -618,12 +627,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
       }
       if constexpr (MODE == FWD) {
         float* xl = reinterpret_cast<float*>(smem + LY::XCH_OFF);  // [2 tile parity][2 half][128]
-        const int ob = static_cast<int>(tn & 1u);                    // this tile's O buffer
-        const uint32_t ocol = OCOL + ob * DH + 64 * hf;
+        const int tp = static_cast<int>(tn & 1u);                    // tile parity: exchange slots
+        const uint32_t ocol = OCOL + 64 * hf;                        // this warp's half of O
         float m = -INFINITY, l = 0.f;
         for (int j = first; j < last; ++j, ++jn) {
-          const int bf = jn & 1;
-          if (!wwait(&s_full[bf], (jn >> 1) & 1u)) {
+          const int bf = jn % NSB;                 // the block's S (then P) buffer
+          const int bp = static_cast<int>(jn & 1u);  // block parity: max exchange slot
+          if (!wwait(&s_full[bf], (jn / NSB) & 1u)) {
             ok = false;
             break;
           }
@@ -655,11 +665,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
 #pragma unroll
           for (int i = 0; i < 64; i += 2) mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], x[i], x[i + 1]);
           {
-            // exchange the partial maxima with the row's other warp (block parity bf)
-            float* xm = xl + 2 * 2 * BR + bf * 2 * BR;  // [2 half][128] of this block parity
+            // exchange the partial maxima with the row's other warp (block parity bp)
+            float* xm = xl + 2 * 2 * BR + bp * 2 * BR;  // [2 half][128] of this block parity
             xm[hf * BR + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            mbar_arrive(smem_u32(&mxb[2 * q + bf]));
-            if (!wwait(&mxb[2 * q + bf], (jn >> 1) & 1u)) {
+            mbar_arrive(smem_u32(&mxb[2 * q + bp]));
+            if (!wwait(&mxb[2 * q + bp], (jn >> 1) & 1u)) {
               ok = false;
               break;
             }
@@ -677,7 +687,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             // m lags the true one by at most 8; past that, O (in TMEM, complete
             // through the previous block) and l move to the new maximum.
             const uint32_t pj = jn - 1;
-            if (!wwait(&e_empty[pj & 1u], (pj >> 1) & 1u)) {
+            if (!wwait(&e_empty[pj % NSB], (pj / NSB) & 1u)) {
               ok = false;
               break;
             }
@@ -719,15 +729,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
         if (!ok) break;
         // O is complete once the tile's last product has committed
         const uint32_t pj = jn - 1;
-        if (!wwait(&e_empty[pj & 1u], (pj >> 1) & 1u)) {
+        if (!wwait(&e_empty[pj % NSB], (pj / NSB) & 1u)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float* ls = xl + ob * 2 * BR;
+        float* ls = xl + tp * 2 * BR;
         ls[hf * BR + r] = l;
-        mbar_arrive(smem_u32(&lx[2 * q + ob]));
-        if (!wwait(&lx[2 * q + ob], (tn >> 1) & 1u)) {
+        mbar_arrive(smem_u32(&lx[2 * q + tp]));
+        if (!wwait(&lx[2 * q + tp], (tn >> 1) & 1u)) {
           ok = false;
           break;
         }
@@ -744,7 +754,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
               lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
         tc_fence_before();
         __syncwarp();
-        arrive(&a_empty[ob]);
+        arrive(&a_empty[0]);
       } else {
         // backward: per-row terms of the stationary rows (BQ) come from global memory
         float lr = 0.f, dr = 0.f;
