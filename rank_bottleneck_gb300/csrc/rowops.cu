@@ -137,65 +137,82 @@ __device__ __forceinline__ void stats_rows(const T* __restrict__ x, int64_t rows
   }
 }
 
-// out = A diag(w) on block b of the nb blocks given to the job
+// Norm-weight folds (out = A diag(w)) in chunks of up to 1024 columns of one
+// row of A, one warp per chunk: kFoldChunks returns the chunks of a job, and
+// fold_chunk does chunk k of them (row k / per-row, columns from (k % per-row) 1024).
+constexpr int kFoldCols = 1024;
 template <typename T>
-__device__ __forceinline__ void fold_blocks(const FoldJob<T>& f, int b, int nb) {
-  const int64_t nvec = f.cols / 8;
-  for (int64_t i = b * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < f.rows * nvec;
-       i += static_cast<int64_t>(nb) * blockDim.x) {
-    const int64_t r = i / nvec, c = (i - r * nvec) * 8;
-    float a[8], ww[8];
-    Vec8<T>::load(f.A + r * f.cols + c, a);
-    Vec8<T>::load(f.w + c, ww);
+__device__ __forceinline__ int64_t fold_chunks(const FoldJob<T>& f) {
+  return f.A == nullptr ? 0 : f.rows * ((f.cols + kFoldCols - 1) / kFoldCols);
+}
+template <typename T>
+__device__ __forceinline__ void fold_chunk(const FoldJob<T>& f, int64_t k, int lane) {
+  const int64_t per_row = (f.cols + kFoldCols - 1) / kFoldCols;
+  const int64_t r = k / per_row;
+  const int64_t c0 = (k - r * per_row) * kFoldCols;
+  const int64_t c1 = c0 + kFoldCols < f.cols ? c0 + kFoldCols : f.cols;
+  constexpr int U = kFoldCols / 256;
+  Pack8<T> a[U];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) a[k] *= ww[k];
-    Vec8<T>::store(f.out + r * f.cols + c, a);
+  for (int u = 0; u < U; ++u) {  // every load of the chunk before any store
+    const int64_t c = c0 + 256 * u + 8 * lane;
+    if (c < c1) a[u].load(f.A + r * f.cols + c);
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int64_t c = c0 + 256 * u + 8 * lane;
+    if (c < c1) {
+      float ww[8], o[8];
+      Vec8<T>::load(f.w + c, ww);
+#pragma unroll
+      for (int k2 = 0; k2 < 8; ++k2) o[k2] = a[u][k2] * ww[k2];
+      Vec8<T>::store(f.out + r * f.cols + c, o);
+    }
   }
 }
 
-// Blocks [0, stat_blocks): the row statistics, each of their warps taking rows
-// warp, warp + 8 stat_blocks, ... The blocks after them fold norm weights into
-// down-projections: job 0 on the next fold_blocks0 blocks, job 1 on the rest.
+// The row statistics, then the norm-weight folds, over one index space of work
+// items dealt round robin to the W = 8 gridDim.x warps: items [0, rows) are the
+// rows of x, then come the fold chunks of job 0 and of job 1. A chunk moves
+// 2 x 1024 elements, a row of x reads d; dealing them together keeps every
+// warp's share within one item of the others.
 template <typename T>
-__global__ void __launch_bounds__(256) stats_kernel(const T* __restrict__ x, int64_t rows, int d,
+__global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 1)
+    stats_kernel(const T* __restrict__ x, int64_t rows, int d,
                                                     int S, float eps, float* __restrict__ ss,
-                                                    float* __restrict__ rstd, int stat_blocks,
-                                                    const FoldJob<T> f0, int fold_blocks0,
+                                                    float* __restrict__ rstd, const FoldJob<T> f0,
                                                     const FoldJob<T> f1) {
   grid_dependency_sync();
-  const int b = static_cast<int>(blockIdx.x);
-  if (b >= stat_blocks) {
-    const int fb = b - stat_blocks;
-    if (fb < fold_blocks0)
-      fold_blocks(f0, fb, fold_blocks0);
-    else
-      fold_blocks(f1, fb - fold_blocks0, static_cast<int>(gridDim.x) - stat_blocks - fold_blocks0);
-    return;
-  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  stats_rows(x, rows, d, S, eps, ss, rstd, static_cast<int64_t>(b) * 8 + warp,
-             static_cast<int64_t>(stat_blocks) * 8, lane);
-}
-
-template <typename T>
-static unsigned fold_grid(const Ctx& c, const FoldJob<T>& f) {
-  if (f.A == nullptr || f.rows * f.cols == 0) return 0;
-  const int64_t n = f.rows * (f.cols / 8);
-  return static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, c.num_sms * 4));
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  const int64_t W = static_cast<int64_t>(gridDim.x) * 8;
+  stats_rows(x, rows, d, S, eps, ss, rstd, gw, W, lane);
+  const int64_t n0 = fold_chunks(f0), n1 = fold_chunks(f1);
+  // this warp's first chunk: the item index rows + k is dealt to warp (rows + k) mod W
+  for (int64_t k = ((gw - rows) % W + W) % W; k < n0 + n1; k += W) {
+    if (k < n0)
+      fold_chunk(f0, k, lane);
+    else
+      fold_chunk(f1, k - n0, lane);
+  }
 }
 
 template <typename T>
 void launch_stats_fold(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float eps, float* ss,
                        float* rstd, const FoldJob<T>& f0, const FoldJob<T>& f1) {
   // three blocks of 8 warps per SM (80 registers a thread for bf16), each warp
-  // looping over rows
-  const unsigned sb = static_cast<unsigned>(std::min<int64_t>((rows + 7) / 8, c.num_sms * 3));
-  const unsigned g0 = fold_grid(c, f0), g1 = fold_grid(c, f1);
-  const double fold_elems = static_cast<double>(g0 ? f0.rows * f0.cols : 0) +
-                            static_cast<double>(g1 ? f1.rows * f1.cols : 0);
+  // looping over its rows and then its fold chunks
+  const auto chunks = [](const FoldJob<T>& f) -> int64_t {
+    return f.A == nullptr ? 0 : f.rows * ((f.cols + kFoldCols - 1) / kFoldCols);
+  };
+  const int64_t items = rows + chunks(f0) + chunks(f1);
+  const unsigned blocks =
+      static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>((items + 7) / 8, c.num_sms * 3)));
+  const double fold_elems = static_cast<double>(f0.A ? f0.rows * f0.cols : 0) +
+                            static_cast<double>(f1.A ? f1.rows * f1.cols : 0);
   prof_start(c);
-  track(c, launch_pdl(stats_kernel<T>, sb + g0 + g1, 256, 0, c.stream, x, rows, static_cast<int>(d),
-                      S, eps, ss, rstd, static_cast<int>(sb), f0, static_cast<int>(g0), f1));
+  track(c, launch_pdl(stats_kernel<T>, blocks, 256, 0, c.stream, x, rows, static_cast<int>(d), S,
+                      eps, ss, rstd, f0, f1));
   note_launch(c, KK_STATS, -1, 2.0 * rows * d + fold_elems,
               static_cast<double>(rows) * (d * sizeof(T) + 4 * S + 4) +
                   2.0 * fold_elems * sizeof(T));
