@@ -88,6 +88,23 @@ bn_status bn_testing_weight_grad_noalloc_unfed(int64_t M, int64_t N, int64_t T, 
                                                int64_t lda, const void* B, int64_t ldb, void* dW,
                                                int64_t ldw, int* counters, bn_stream_t stream);
 
+/* One launch of the block's RMSNorm backward (bf16; the kernel the block's
+ * backward runs for these rows), then its dw column sums:
+ *   dx[t, j] = dres[t, j] + dn[t, j] w[j] - x[t, j] rstd[t]^2 sum_k(dn w x)[t, k] / d
+ *   dw[j]    = sum_t dn[t, j] x[t, j]
+ * where dn is the gradient of the normalised input already multiplied by the
+ * row's rstd. All tensors [rows, d] row-major (d a multiple of 8), w [d];
+ * `part` is fp32 scratch of part_elems >= 2 x SMs x d. With `unfed` != 0 (d at
+ * most 2048) the first row of the kernel's first warp is never loaded: that
+ * warp's bounded wait gives up after 1 s, the kernel records a timeout in the
+ * status word at the start of `scratch` (bn_get_device_status reports
+ * BN_ERR_TIMEOUT), waits (bounded) for its other copies in flight and returns;
+ * dx and dw are then not meaningful. Returns BN_OK if the launches were made. */
+bn_status bn_testing_norm_bwd(int64_t rows, int64_t d, const void* dn, const void* x,
+                              const void* w, const float* rstd, const void* dres, void* dx,
+                              void* dw, float* part, int64_t part_elems, int32_t unfed,
+                              void* scratch, bn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,11 +33,13 @@ void launch_stats_fold(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float
 //   dw[j]    = sum_t dn'[t, j] x[t, j]
 // dw is reduced deterministically through `part` (nblk x d fp32): in a second
 // launch when `colsum`, else by the caller (launch_finish). Returns the rows of
-// `part` written (at most nblk).
+// `part` written (at most nblk). `unfed` (a test hook, bf16 rows of at most
+// 2048 columns) never loads the first row of the first warp, so that its
+// bounded wait runs out and the kernel records a timeout.
 template <typename T>
 int launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rstd,
                     const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw,
-                    bool colsum);
+                    bool colsum, bool unfed = false);
 int norm_bwd_blocks(int num_sms);
 
 // End of a bf16 backward, one launch: the reduction of the GEMM's split tiles

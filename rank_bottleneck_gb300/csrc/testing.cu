@@ -4,6 +4,7 @@
 
 #include "../../include/boostblk_testing.h"
 #include "gemm.h"
+#include "rowops.h"
 
 using namespace bn;
 
@@ -101,6 +102,31 @@ extern "C" bn_status bn_testing_gemm_unfed(const bn_gemm_problem* prob, int* cou
   c.chain_in.rows_target = 1;
   gemm_tc(c, g);
   if (c.bad) return BN_ERR_UNSUPPORTED;
+  if (c.err != cudaSuccess) return BN_ERR_CUDA;
+  return BN_OK;
+}
+
+extern "C" bn_status bn_testing_norm_bwd(int64_t rows, int64_t d, const void* dn, const void* x,
+                                         const void* w, const float* rstd, const void* dres,
+                                         void* dx, void* dw, float* part, int64_t part_elems,
+                                         int32_t unfed, void* scratch, bn_stream_t stream) {
+  if (rows < 1 || d < 8 || d % 8 != 0 || (unfed && d > 2048) || dn == nullptr || x == nullptr ||
+      w == nullptr || rstd == nullptr || dres == nullptr || dx == nullptr || dw == nullptr ||
+      part == nullptr || scratch == nullptr)
+    return BN_ERR_INVALID_ARG;
+  Ctx c;
+  c.stream = reinterpret_cast<cudaStream_t>(stream);
+  c.status = static_cast<int*>(scratch);
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+    c.num_sms = n;
+  const int nblk = norm_bwd_blocks(c.num_sms);
+  if (part_elems < static_cast<int64_t>(nblk) * d) return BN_ERR_INVALID_ARG;
+  using bf = __nv_bfloat16;
+  launch_norm_bwd<bf>(c, static_cast<const bf*>(dn), static_cast<const bf*>(x),
+                      static_cast<const bf*>(w), rstd, static_cast<const bf*>(dres), rows, d,
+                      static_cast<bf*>(dx), part, nblk, static_cast<bf*>(dw), true, unfed != 0);
   if (c.err != cudaSuccess) return BN_ERR_CUDA;
   return BN_OK;
 }
