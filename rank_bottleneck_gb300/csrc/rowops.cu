@@ -138,8 +138,8 @@ __device__ __forceinline__ void stats_rows(const T* __restrict__ x, int64_t rows
 }
 
 // Norm-weight folds (out = A diag(w)) in chunks of up to 1024 columns of one
-// row of A, one warp per chunk: kFoldChunks returns the chunks of a job, and
-// fold_chunk does chunk k of them (row k / per-row, columns from (k % per-row) 1024).
+// row of A, one warp per chunk: fold_chunks counts a job's chunks, fold_chunk
+// does chunk k (row k / p, columns from 1024 (k % p), p = chunks per row).
 constexpr int kFoldCols = 1024;
 template <typename T>
 __device__ __forceinline__ int64_t fold_chunks(const FoldJob<T>& f) {
@@ -178,10 +178,9 @@ __device__ __forceinline__ void fold_chunk(const FoldJob<T>& f, int64_t k, int l
 // warp's share within one item of the others.
 template <typename T>
 __global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 1)
-    stats_kernel(const T* __restrict__ x, int64_t rows, int d,
-                                                    int S, float eps, float* __restrict__ ss,
-                                                    float* __restrict__ rstd, const FoldJob<T> f0,
-                                                    const FoldJob<T> f1) {
+    stats_kernel(const T* __restrict__ x, int64_t rows, int d, int S, float eps,
+                 float* __restrict__ ss, float* __restrict__ rstd, const FoldJob<T> f0,
+                 const FoldJob<T> f1) {
   grid_dependency_sync();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * 8 + warp;
