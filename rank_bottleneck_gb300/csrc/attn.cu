@@ -933,60 +933,113 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
 }
 
 // D[bh, i] = sum_e dO[i, h, e] O[i, h, e] (0 for L <= i < Lp) and
-// l2[bh, i] = lse[bh, i] log2(e): one warp per (token row, head).
-// One warp per token row (b, i), every head of it: the row's O and dO (H x 128
-// bf16 each) are read with 16-byte loads, eight heads at a time (4 x 16 bytes
-// of each tensor per lane in flight), and each head's D = sum(dO * O) is a
-// half-warp reduction (head 2u + (lane >= 16) of load u). Rows i in [L, Lp)
-// (the padding of the lse stride) get D = 0.
-__global__ void __launch_bounds__(256, 2) attn_rows_kernel(const __nv_bfloat16* __restrict__ o,
-                                 const __nv_bfloat16* __restrict__ dout,
-                                 const float* __restrict__ lse, float* __restrict__ dd,
-                                 float* __restrict__ l2, int B, int L, int H, int Lp) {
+// l2[bh, i] = lse[bh, i] log2(e).
+// One warp per token row (b, i < L), every head of it, the row's O and dO
+// (H x 128 bf16 each) streamed through shared memory: each warp owns a ring of
+// two stages, a stage holds one row of O and of dO, brought in by two bulk
+// copies that complete on the stage's mbarrier, and the copies of the warp's
+// next row are in flight while it works on this one. Each head's D is a
+// half-warp reduction (head 2u + (lane >= 16) at step u, 16-byte shared-memory
+// reads). Block k takes the contiguous real rows [k n / grid, (k + 1) n / grid),
+// its warps take them round robin. l2, and D = 0 on the padding rows i in
+// [L, Lp) of the lse stride, are one coalesced grid-stride pass.
+// Every wait is bounded; a warp that gives up waits (bounded) for its copies in
+// flight before the block leaves.
+constexpr size_t kRowsSmem = 227 * 1024;
+constexpr int kRowsMaxWarps = 12;
+__global__ void __launch_bounds__(kRowsMaxWarps * 32, 1)
+    attn_rows_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                     const float* __restrict__ lse, float* __restrict__ dd,
+                     float* __restrict__ l2, int B, int L, int H, int Lp, int* status) {
+  extern __shared__ __align__(128) unsigned char ars[];
+  const int nw = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t row_bytes = static_cast<uint32_t>(H) * DH * 2u;
+  const uint32_t stage_bytes = 2u * row_bytes;  // O | dO
+  unsigned char* ring = ars + static_cast<size_t>(warp) * 2 * stage_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ars + static_cast<size_t>(nw) * 2 * stage_bytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * nw);
+  const uint32_t bar0 = smem_u32(bars + 2 * warp);
+  const uint32_t ring0 = smem_u32(ring);
+  if (lane == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8, 1);
+  }
+  if (threadIdx.x == 0) *abort_flag = 0;
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncthreads();
   grid_dependency_sync();
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int64_t total = static_cast<int64_t>(B) * Lp;
+
+  // l2 = lse log2(e) for every entry, and D = 0 on the padding rows of the lse
+  // stride: one coalesced grid-stride pass
+  const int64_t nrow_terms = static_cast<int64_t>(B) * H * Lp;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < nrow_terms;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    l2[t] = lse[t] * kLog2e;
+    if (static_cast<int>(t % Lp) >= L) dd[t] = 0.f;
+  }
+  const int64_t rows = static_cast<int64_t>(B) * L;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows / gridDim.x;
+  const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * rows / gridDim.x;
+  const int64_t first = r0 + warp;
+  const int64_t n = first < r1 ? (r1 - first + nw - 1) / nw : 0;  // this warp's rows
   const int64_t rowlen = static_cast<int64_t>(H) * DH;
-  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total;
-       w += nwarps) {
-    const int b = static_cast<int>(w / Lp), i = static_cast<int>(w % Lp);
-    // this lane's 8 columns of its first head (head lane >> 4, columns (lane & 15) * 8)
-    const int lo = (lane >> 4) * DH + (lane & 15) * 8;
-    const __nv_bfloat16* orow = o + (static_cast<int64_t>(b) * L + i) * rowlen + lo;
-    const __nv_bfloat16* grow = dout + (static_cast<int64_t>(b) * L + i) * rowlen + lo;
-    for (int h0 = 0; h0 < H; h0 += 8) {
-      uint4 a[4], g[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int h = h0 + 2 * u + (lane >> 4);  // this lane's head for load u
-        const int off = (h0 + 2 * u) * DH;
-        if (i < L && h < H) {
-          a[u] = *reinterpret_cast<const uint4*>(orow + off);
-          g[u] = *reinterpret_cast<const uint4*>(grow + off);
-        } else {
-          a[u] = g[u] = make_uint4(0, 0, 0, 0);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
-        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g[u]);
-        float acc = 0.f;
+  auto issue = [&](int64_t j) {  // copies of the warp's row j into stage j & 1 (lane 0)
+    const int64_t off = (first + j * nw) * rowlen;  // token row b L + i
+    const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(j & 1);
+    const uint32_t dst = ring0 + static_cast<uint32_t>(j & 1) * stage_bytes;
+    mbar_expect_tx(bar, stage_bytes);
+    bulk_load(dst, o + off, row_bytes, bar);
+    bulk_load(dst + row_bytes, dout + off, row_bytes, bar);
+  };
+  if (lane == 0) {
+    if (n > 0) issue(0);
+    if (n > 1) issue(1);
+  }
+  const int lo = (lane >> 4) * DH + (lane & 15) * 8;  // this lane's columns of head pair u
+  int64_t j = 0;
+  for (; j < n; ++j) {
+    const int64_t row = first + j * nw;
+    const int b = static_cast<int>(row / L), i = static_cast<int>(row % L);
+    const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(j & 1);
+    const bool landed =
+        bwait(bar, static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status);
+    if (!__all_sync(0xffffffffu, landed)) break;
+    const __nv_bfloat16* so = reinterpret_cast<const __nv_bfloat16*>(ring + (j & 1) * stage_bytes);
+    const __nv_bfloat16* sg = so + rowlen;
+    for (int u = 0; 2 * u < H; ++u) {
+      const int h = 2 * u + (lane >> 4);
+      float acc = 0.f;
+      if (h < H) {
+        const uint4 a = *reinterpret_cast<const uint4*>(so + 2 * u * DH + lo);
+        const uint4 g = *reinterpret_cast<const uint4*>(sg + 2 * u * DH + lo);
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 fa = __bfloat1622float2(a2[k]), fg = __bfloat1622float2(g2[k]);
           acc = fmaf(fa.x, fg.x, acc);
           acc = fmaf(fa.y, fg.y, acc);
         }
+      }
 #pragma unroll
-        for (int sft = 8; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
-        const int h = h0 + 2 * u + (lane >> 4);
-        if ((lane & 15) == 0 && h < H) {
-          const int64_t idx = (static_cast<int64_t>(b) * H + h) * Lp + i;
-          dd[idx] = acc;
-          l2[idx] = lse[idx] * kLog2e;
-        }
+      for (int sft = 8; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+      if ((lane & 15) == 0 && h < H) dd[(static_cast<int64_t>(b) * H + h) * Lp + i] = acc;
+    }
+    __syncwarp();  // every lane has read the stage
+    if (lane == 0 && j + 2 < n) {
+      fence_proxy_async();
+      issue(j + 2);
+    }
+  }
+  if (j < n) {
+    // a wait gave up: this warp's copies still in flight (rows j and j + 1) land
+    // before the block's shared memory is released
+    for (int64_t k = j; k < n && k < j + 2; ++k) {
+      const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(k & 1);
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar, static_cast<uint32_t>(k >> 1) & 1u) &&
+             globaltimer_ns() - t0 < kWaitLimitNs) {
       }
     }
   }
@@ -1142,15 +1195,26 @@ cudaError_t attn_backward(Ctx& c, const bn_attn_desc& d, const void* q, const vo
   P.dd = dd;
   const double elems = static_cast<double>(d.B * d.L * d.H * DH);
   const double pairs = visible_pairs(d);
-  // one warp per token row (all heads); two blocks of eight warps per SM, each
-  // warp looping over rows
-  const int64_t row_warps = static_cast<int64_t>(d.B) * Lp;
-  const int64_t blocks = std::min<int64_t>((row_warps + 7) / 8, static_cast<int64_t>(c.num_sms) * 2);
+  // one block per SM, as many warps as two stages of a row of O and dO fit (at
+  // most twelve), each warp streaming its rows
+  const size_t warp_bytes = 4 * static_cast<size_t>(d.H) * DH * 2 + 16;
+  const int nw = static_cast<int>(std::max<size_t>(
+      1, std::min<size_t>(kRowsMaxWarps, (kRowsSmem - 16) / warp_bytes)));
+  const size_t rows_smem = warp_bytes * nw + 16;
+  static const bool rows_attr = [] {
+    cudaFuncSetAttribute(attn_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(kRowsSmem));
+    return true;
+  }();
+  (void)rows_attr;
+  const int64_t blocks = std::max<int64_t>(
+      1, std::min<int64_t>((static_cast<int64_t>(d.B) * d.L + nw - 1) / nw, c.num_sms));
   prof_start(c);
   cudaError_t e = launch_pdl(attn_rows_kernel, dim3(static_cast<unsigned>(blocks)),
-                             dim3(256), 0, c.stream, static_cast<const __nv_bfloat16*>(o),
+                             dim3(nw * 32), rows_smem, c.stream,
+                             static_cast<const __nv_bfloat16*>(o),
                              static_cast<const __nv_bfloat16*>(dout), lse, dd, l2, P.B, P.L, P.H,
-                             Lp);
+                             Lp, status);
   note_launch(c, KK_ATTN, 3, 2.0 * elems, 2.0 * elems * 2 + 3.0 * rows * 4);
   if (e != cudaSuccess) return e;
   Params K = P;
