@@ -934,15 +934,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
 
 // D[bh, i] = sum_e dO[i, h, e] O[i, h, e] (0 for L <= i < Lp) and
 // l2[bh, i] = lse[bh, i] log2(e).
-// One warp per token row (b, i < L), every head of it, the row's O and dO
-// (H x 128 bf16 each) streamed through shared memory: each warp owns a ring of
-// two stages, a stage holds one row of O and of dO, brought in by two bulk
-// copies that complete on the stage's mbarrier, and the copies of the warp's
-// next row are in flight while it works on this one. Each head's D is a
-// half-warp reduction (head 2u + (lane >= 16) at step u, 16-byte shared-memory
-// reads). Block k takes the contiguous real rows [k n / grid, (k + 1) n / grid),
-// its warps take them round robin. l2, and D = 0 on the padding rows i in
-// [L, Lp) of the lse stride, are one coalesced grid-stride pass.
+// Work items are (token row (b, i < L), group of up to 16 heads); a warp takes
+// an item's O and dO (up to 16 x 128 bf16 each) through shared memory: each
+// warp owns a ring of two stages, a stage holds one item of O and of dO,
+// brought in by two bulk copies that complete on the stage's mbarrier, and the
+// copies of the warp's next item are in flight while it works on this one.
+// Each head's D is a half-warp reduction (head 2u + (lane >= 16) of the group
+// at step u, 16-byte shared-memory reads). Block k takes the contiguous items
+// [k n / grid, (k + 1) n / grid), its warps take them round robin. l2, and
+// D = 0 on the padding rows i in [L, Lp) of the lse stride, are one coalesced
+// grid-stride pass.
 // Every wait is bounded; a warp that gives up waits (bounded) for its copies in
 // flight before the block leaves.
 constexpr size_t kRowsSmem = 227 * 1024;
@@ -954,7 +955,9 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1)
   extern __shared__ __align__(128) unsigned char ars[];
   const int nw = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t row_bytes = static_cast<uint32_t>(H) * DH * 2u;
+  const int HG = H < 16 ? H : 16;                        // heads of a full group
+  const int ngroups = (H + 15) / 16;
+  const uint32_t row_bytes = static_cast<uint32_t>(HG) * DH * 2u;  // one item of one tensor
   const uint32_t stage_bytes = 2u * row_bytes;  // O | dO
   unsigned char* ring = ars + static_cast<size_t>(warp) * 2 * stage_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(ars + static_cast<size_t>(nw) * 2 * stage_bytes);
@@ -978,19 +981,27 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1)
     l2[t] = lse[t] * kLog2e;
     if (static_cast<int>(t % Lp) >= L) dd[t] = 0.f;
   }
-  const int64_t rows = static_cast<int64_t>(B) * L;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows / gridDim.x;
-  const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * rows / gridDim.x;
+  const int64_t items = static_cast<int64_t>(B) * L * ngroups;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * items / gridDim.x;
+  const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * items / gridDim.x;
   const int64_t first = r0 + warp;
-  const int64_t n = first < r1 ? (r1 - first + nw - 1) / nw : 0;  // this warp's rows
+  const int64_t n = first < r1 ? (r1 - first + nw - 1) / nw : 0;  // this warp's items
   const int64_t rowlen = static_cast<int64_t>(H) * DH;
-  auto issue = [&](int64_t j) {  // copies of the warp's row j into stage j & 1 (lane 0)
-    const int64_t off = (first + j * nw) * rowlen;  // token row b L + i
+  // item t: token row t / ngroups (b L + i), heads from 16 (t % ngroups)
+  // (one group when H <= 16: no division)
+  auto group_of = [&](int64_t t) { return ngroups == 1 ? 0 : static_cast<int>(t % ngroups); };
+  auto row_of = [&](int64_t t) { return ngroups == 1 ? t : t / ngroups; };
+  auto heads_of = [&](int g) { return H - 16 * g < 16 ? H - 16 * g : 16; };
+  auto issue = [&](int64_t j) {  // copies of the warp's item j into stage j & 1 (lane 0)
+    const int64_t t = first + j * nw;
+    const int g = group_of(t);
+    const int64_t off = row_of(t) * rowlen + static_cast<int64_t>(g) * 16 * DH;
+    const uint32_t bytes = static_cast<uint32_t>(heads_of(g)) * DH * 2u;
     const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(j & 1);
     const uint32_t dst = ring0 + static_cast<uint32_t>(j & 1) * stage_bytes;
-    mbar_expect_tx(bar, stage_bytes);
-    bulk_load(dst, o + off, row_bytes, bar);
-    bulk_load(dst + row_bytes, dout + off, row_bytes, bar);
+    mbar_expect_tx(bar, 2u * bytes);
+    bulk_load(dst, o + off, bytes, bar);
+    bulk_load(dst + row_bytes, dout + off, bytes, bar);
   };
   if (lane == 0) {
     if (n > 0) issue(0);
@@ -999,18 +1010,22 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1)
   const int lo = (lane >> 4) * DH + (lane & 15) * 8;  // this lane's columns of head pair u
   int64_t j = 0;
   for (; j < n; ++j) {
-    const int64_t row = first + j * nw;
+    const int64_t t = first + j * nw;
+    const int64_t row = row_of(t);
+    const int g = group_of(t);
+    const int g0 = 16 * g;  // the group's first head
+    const int nh = heads_of(g);
     const int b = static_cast<int>(row / L), i = static_cast<int>(row % L);
     const uint32_t bar = bar0 + 8u * static_cast<uint32_t>(j & 1);
     const bool landed =
         bwait(bar, static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status);
     if (!__all_sync(0xffffffffu, landed)) break;
     const __nv_bfloat16* so = reinterpret_cast<const __nv_bfloat16*>(ring + (j & 1) * stage_bytes);
-    const __nv_bfloat16* sg = so + rowlen;
-    for (int u = 0; 2 * u < H; ++u) {
-      const int h = 2 * u + (lane >> 4);
+    const __nv_bfloat16* sg = so + HG * DH;
+    for (int u = 0; 2 * u < nh; ++u) {
+      const int h = 2 * u + (lane >> 4);  // head within the group
       float acc = 0.f;
-      if (h < H) {
+      if (h < nh) {
         const uint4 a = *reinterpret_cast<const uint4*>(so + 2 * u * DH + lo);
         const uint4 g = *reinterpret_cast<const uint4*>(sg + 2 * u * DH + lo);
         const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -1024,7 +1039,7 @@ __global__ void __launch_bounds__(kRowsMaxWarps * 32, 1)
       }
 #pragma unroll
       for (int sft = 8; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
-      if ((lane & 15) == 0 && h < H) dd[(static_cast<int64_t>(b) * H + h) * Lp + i] = acc;
+      if ((lane & 15) == 0 && h < nh) dd[(static_cast<int64_t>(b) * H + g0 + h) * Lp + i] = acc;
     }
     __syncwarp();  // every lane has read the stage
     if (lane == 0 && j + 2 < n) {
@@ -1195,9 +1210,9 @@ cudaError_t attn_backward(Ctx& c, const bn_attn_desc& d, const void* q, const vo
   P.dd = dd;
   const double elems = static_cast<double>(d.B * d.L * d.H * DH);
   const double pairs = visible_pairs(d);
-  // one block per SM, as many warps as two stages of a row of O and dO fit (at
-  // most twelve), each warp streaming its rows
-  const size_t warp_bytes = 4 * static_cast<size_t>(d.H) * DH * 2 + 16;
+  // one block per SM, as many warps as two stages of an item (a row's O and dO
+  // for up to 16 heads) fit (at most twelve), each warp streaming its items
+  const size_t warp_bytes = 4 * static_cast<size_t>(std::min<int64_t>(d.H, 16)) * DH * 2 + 16;
   const int nw = static_cast<int>(std::max<size_t>(
       1, std::min<size_t>(kRowsMaxWarps, (kRowsSmem - 16) / warp_bytes)));
   const size_t rows_smem = warp_bytes * nw + 16;
@@ -1207,8 +1222,8 @@ cudaError_t attn_backward(Ctx& c, const bn_attn_desc& d, const void* q, const vo
     return true;
   }();
   (void)rows_attr;
-  const int64_t blocks = std::max<int64_t>(
-      1, std::min<int64_t>((static_cast<int64_t>(d.B) * d.L + nw - 1) / nw, c.num_sms));
+  const int64_t items = static_cast<int64_t>(d.B) * d.L * ((d.H + 15) / 16);
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((items + nw - 1) / nw, c.num_sms));
   prof_start(c);
   cudaError_t e = launch_pdl(attn_rows_kernel, dim3(static_cast<unsigned>(blocks)),
                              dim3(nw * 32), rows_smem, c.stream,
