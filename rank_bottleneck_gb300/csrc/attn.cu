@@ -529,7 +529,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
           break;
         }
         for (int i = 0; i < nblk; ++i, ++jn) {
-          if (i + LA < nblk && (!issue_sd(jn + LA) || (MODE == BQ && !issue_dp(jn + LA)))) {
+          // FWD: the scores LA blocks ahead are issued k-step by k-step between
+          // this block's P V steps (two independent accumulators in the pipe);
+          // BQ: issued whole, before this block's product
+          static_assert(MODE != FWD || BCM == DH, "the interleave pairs the k-steps one to one");
+          const bool s2 = MODE == FWD && i + LA < nblk;
+          const uint32_t n2 = jn + LA;
+          const int st2 = n2 % LY::NSTK, bf2 = n2 % NSB;
+          if constexpr (MODE == FWD) {
+            if (s2 && (!bwait(smem_u32(&y_full[st2]), (n2 / LY::NSTK) & 1u, abort_flag, P.status) ||
+                       !bwait(smem_u32(&e_empty[bf2]), ((n2 / NSB) & 1u) ^ 1u, abort_flag,
+                              P.status))) {
+              ok = false;
+              break;
+            }
+          } else if (i + LA < nblk && (!issue_sd(jn + LA) || (MODE == BQ && !issue_dp(jn + LA)))) {
             ok = false;
             break;
           }
@@ -558,11 +572,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_kernel(const __grid_constant
             // O += P V_j: A = P in TMEM (bf16 pairs in S's buffer: the 16 keys of
             // k-step kk are warp half kk / 4's, in that half's first 32 columns),
             // B = V_j read MN-major [d_head x BCM keys] (its two d_head halves SUBC apart)
+            const uint32_t y2 = smem_u32(sYK + st2 * HALF);
+            const uint32_t x = smem_u32(sX);
 #pragma unroll
-            for (int kk = 0; kk < BCM / 16; ++kk)
+            for (int kk = 0; kk < BCM / 16; ++kk) {
               mma_bf16_ta(tmem + OCOL, tmem + bf * BCM + 64 * (kk >> 2) + 8 * (kk & 3),
                           smem_desc_mn(smem_u32(sYV + stv * HALF) + kk * 2048, SUBC), ID_A,
                           (acc | kk) ? 1u : 0u);
+              if (s2)  // k-step kk of S = Q K^T of block n2 (d_head half kk / 4)
+                mma_bf16<1>(tmem + bf2 * BCM,
+                            smem_desc(x + (kk >> 2) * SUB_R + (kk & 3) * 32, false),
+                            smem_desc(y2 + (kk >> 2) * SUBC + (kk & 3) * 32, false), ID_S,
+                            kk ? 1u : 0u);
+            }
+            if (s2) {
+              mma_commit<1>(smem_u32(&s_full[bf2]));
+              mma_commit<1>(smem_u32(&y_empty[st2]));  // K read
+            }
           } else {
             // dQ += dS K_j: A = dS in TMEM (bf16 pairs in S's buffer: the 16 keys of
             // k-step kk are warp half kk / 4's, in that half's first 32 columns),
