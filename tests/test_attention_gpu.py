@@ -73,6 +73,8 @@ CASES = [
     (3, 65, 1, False),     # ragged non-causal, one row past a block
     (1, 1, 2, True),       # a single token: o = v
     (2, 129, 1, True),     # one row into the second tile
+    (1, 136, 20, True),    # 20 heads: the backward's row terms take each row as a
+                           # group of 16 heads and one of 4
 ]
 
 
