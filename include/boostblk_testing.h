@@ -95,7 +95,7 @@ bn_status bn_testing_weight_grad_noalloc_unfed(int64_t M, int64_t N, int64_t T, 
  * where dn is the gradient of the normalised input already multiplied by the
  * row's rstd. All tensors [rows, d] row-major (d a multiple of 8), w [d];
  * `part` is fp32 scratch of part_elems >= 2 x SMs x d. With `unfed` != 0 (d at
- * most 2048) the first row of the kernel's first warp is never loaded: that
+ * most 5120) the first row of the kernel's first warp is never loaded: that
  * warp's bounded wait gives up after 1 s, the kernel records a timeout in the
  * status word at the start of `scratch` (bn_get_device_status reports
  * BN_ERR_TIMEOUT), waits (bounded) for its other copies in flight and returns;

@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(256, 2)
   }
 }
 
-// bf16 rows of at most 256 NP columns, streamed through shared memory. Every
+// bf16 rows of at most 256 NP columns (NP <= 20), streamed through shared memory. Every
 // warp owns a ring of two stages; a stage holds one row of dn', x and dres,
 // brought in by three bulk copies that complete on the stage's mbarrier. While
 // a warp works on one row, the copies of its next row are in flight, so an SM
@@ -326,7 +326,8 @@ __global__ void __launch_bounds__(256, 2)
 // norm weight and their dw sums stay in registers for the whole launch. Block
 // b takes the contiguous rows [b rows / grid, (b + 1) rows / grid); its warps
 // take them round robin. One block per SM. Arithmetic per element, and the
-// order of the row sum, as in norm_bwd_kernel.
+// order of the row sum, as in norm_bwd_kernel. Past 8 chunks a lane the weights
+// sit once in shared memory, after the barriers, instead of in registers.
 constexpr size_t kNormBwdStreamSmem = 227 * 1024;
 
 // Untiled bulk copy from global memory into this CTA's shared memory,
@@ -340,8 +341,13 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Warps per block: registers bound them up to 8 chunks a lane (8 NP float sums
+// and 4 NP registers of weights a lane), shared memory beyond (two stages of 3
+// rows, 6 x 2 x 256 NP bytes a warp, and the weights).
 template <int NP>
-constexpr int norm_bwd_stream_warps() { return NP > 4 ? 9 : 16; }
+constexpr int norm_bwd_stream_warps() {
+  return NP > 16 ? 3 : NP > 12 ? 4 : NP > 8 ? 6 : NP > 4 ? 9 : 16;
+}
 
 template <int NP>
 __global__ void __launch_bounds__(norm_bwd_stream_warps<NP>() * 32, 1)
@@ -366,18 +372,40 @@ __global__ void __launch_bounds__(norm_bwd_stream_warps<NP>() * 32, 1)
   }
   if (threadIdx.x == 0) *abort_flag = 0;
   // the norm weight is a parameter: no kernel of the stream writes it
-  Pack8<bf16> wv[NP];
+  constexpr bool kSharedW = NP > 8;
+  bf16* sw = reinterpret_cast<bf16*>(bars + 2 * nw + 2);
+  Pack8<bf16> wv[kSharedW ? 1 : NP];
   float acc[NP][8];
+  if constexpr (kSharedW) {
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x)
+      *reinterpret_cast<uint4*>(sw + 8 * i) = *reinterpret_cast<const uint4*>(w + 8 * i);
+  }
 #pragma unroll
   for (int u = 0; u < NP; ++u) {
-    const int c = u * 256 + lane * 8;
-    if (c < d)
-      wv[u].load(w + c);
-    else
-      wv[u].zero();
+    if constexpr (!kSharedW) {
+      const int c = u * 256 + lane * 8;
+      if (c < d)
+        wv[u].load(w + c);
+      else
+        wv[u].zero();
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
   }
+  // the weights of chunk u (zero past d)
+  auto weights = [&](int u) {
+    if constexpr (kSharedW) {
+      Pack8<bf16> t;
+      const int c = u * 256 + lane * 8;
+      if (c < d)
+        t.load(sw + c);
+      else
+        t.zero();
+      return t;
+    } else {
+      return wv[u];
+    }
+  };
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
   grid_dependency_sync();
@@ -431,8 +459,9 @@ __global__ void __launch_bounds__(norm_bwd_stream_warps<NP>() * 32, 1)
         a.zero();
         b.zero();
       }
+      const Pack8<bf16> wu = weights(u);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s = fmaf(a[i] * wv[u][i], b[i], s);
+      for (int i = 0; i < 8; ++i) s = fmaf(a[i] * wu[i], b[i], s);
     }
     s = warp_sum(s);
     const float coef = r * r * s * inv_d;
@@ -445,10 +474,11 @@ __global__ void __launch_bounds__(norm_bwd_stream_warps<NP>() * 32, 1)
         a.load(sdn + c);
         b.load(sx + c);
         g.load(sg + c);
+        const Pack8<bf16> wu = weights(u);
         float out[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          out[i] = g[i] + (a[i] * wv[u][i] - b[i] * coef);
+          out[i] = g[i] + (a[i] * wu[i] - b[i] * coef);
           acc[u][i] = fmaf(a[i], b[i], acc[u][i]);
         }
         Vec8<bf16>::store(o + c, out);
@@ -527,11 +557,15 @@ int norm_bwd_blocks(int num_sms) { return 2 * num_sms; }
 
 using NormBwdStream = void (*)(const bf16*, const bf16*, const bf16*, const float*, const bf16*,
                                int64_t, int, bf16*, float*, int*, int);
+// the instance for rows of np chunks: exact up to 8, then 12, 16 or 20 (the
+// chunks past d are skipped)
+static int norm_bwd_stream_np(int np) { return np <= 8 ? np : np <= 12 ? 12 : np <= 16 ? 16 : 20; }
 static NormBwdStream norm_bwd_stream(int np) {
-  static const NormBwdStream k[8] = {
-      norm_bwd_stream_kernel<1>, norm_bwd_stream_kernel<2>, norm_bwd_stream_kernel<3>,
-      norm_bwd_stream_kernel<4>, norm_bwd_stream_kernel<5>, norm_bwd_stream_kernel<6>,
-      norm_bwd_stream_kernel<7>, norm_bwd_stream_kernel<8>};
+  static const NormBwdStream k[11] = {
+      norm_bwd_stream_kernel<1>, norm_bwd_stream_kernel<2>,  norm_bwd_stream_kernel<3>,
+      norm_bwd_stream_kernel<4>, norm_bwd_stream_kernel<5>,  norm_bwd_stream_kernel<6>,
+      norm_bwd_stream_kernel<7>, norm_bwd_stream_kernel<8>,  norm_bwd_stream_kernel<12>,
+      norm_bwd_stream_kernel<16>, norm_bwd_stream_kernel<20>};
   static const bool attr = [] {
     for (auto f : k)
       cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -539,29 +573,37 @@ static NormBwdStream norm_bwd_stream(int np) {
     return true;
   }();
   (void)attr;
-  return k[np - 1];
+  const int q = norm_bwd_stream_np(np);
+  return k[q <= 8 ? q - 1 : q == 12 ? 8 : q == 16 ? 9 : 10];
 }
 static int norm_bwd_stream_max_warps(int np) {
-  return np > 4 ? norm_bwd_stream_warps<8>() : norm_bwd_stream_warps<1>();
+  const int q = norm_bwd_stream_np(np);
+  return q > 16   ? norm_bwd_stream_warps<20>()
+         : q > 12 ? norm_bwd_stream_warps<16>()
+         : q > 8  ? norm_bwd_stream_warps<12>()
+         : q > 4  ? norm_bwd_stream_warps<8>()
+                  : norm_bwd_stream_warps<1>();
 }
 
 template <typename T>
 int launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rstd,
                     const T* dres, int64_t rows, int64_t d, T* dx, float* part, int nblk, T* dw,
                     bool colsum, bool unfed) {
-  // bf16 rows of up to 2048 columns are streamed through shared memory (one
+  // bf16 rows of up to 5120 columns are streamed through shared memory (one
   // block per SM); anything else takes the two-pass kernel
   constexpr bool kBf16 = sizeof(T) == 2;
-  const bool stream = kBf16 && d <= 2048 && d % 8 == 0;
+  const bool stream = kBf16 && d <= 5120 && d % 8 == 0;
   prof_start(c);
   if (stream) {
     nblk = std::min(nblk, c.num_sms);
     const int np = static_cast<int>((d + 255) / 256);
-    // two stages of three rows per warp, then 16 bytes of barriers per warp and the abort flag
+    // two stages of three rows per warp, then 16 bytes of barriers per warp, the
+    // abort flag (16 bytes) and, past 8 chunks a lane, the weights
     const size_t warp_bytes = 12 * static_cast<size_t>(d) + 16;
+    const size_t fixed = 16 + (norm_bwd_stream_np(np) > 8 ? 2 * static_cast<size_t>(d) : 0);
     const int nw = static_cast<int>(std::max<size_t>(
-        1, std::min<size_t>(norm_bwd_stream_max_warps(np), (kNormBwdStreamSmem - 16) / warp_bytes)));
-    const size_t smem = warp_bytes * nw + 16;
+        1, std::min<size_t>(norm_bwd_stream_max_warps(np), (kNormBwdStreamSmem - fixed) / warp_bytes)));
+    const size_t smem = warp_bytes * nw + fixed;
     track(c, launch_pdl(norm_bwd_stream(np), nblk, nw * 32, smem, c.stream,
                         reinterpret_cast<const bf16*>(dn), reinterpret_cast<const bf16*>(x),
                         reinterpret_cast<const bf16*>(w), rstd, reinterpret_cast<const bf16*>(dres),

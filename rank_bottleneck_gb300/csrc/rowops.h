@@ -34,7 +34,7 @@ void launch_stats_fold(Ctx& c, const T* x, int64_t rows, int64_t d, int S, float
 // dw is reduced deterministically through `part` (nblk x d fp32): in a second
 // launch when `colsum`, else by the caller (launch_finish). Returns the rows of
 // `part` written (at most nblk). `unfed` (a test hook, bf16 rows of at most
-// 2048 columns) never loads the first row of the first warp, so that its
+// 5120 columns) never loads the first row of the first warp, so that its
 // bounded wait runs out and the kernel records a timeout.
 template <typename T>
 int launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rstd,

@@ -110,7 +110,7 @@ extern "C" bn_status bn_testing_norm_bwd(int64_t rows, int64_t d, const void* dn
                                          const void* w, const float* rstd, const void* dres,
                                          void* dx, void* dw, float* part, int64_t part_elems,
                                          int32_t unfed, void* scratch, bn_stream_t stream) {
-  if (rows < 1 || d < 8 || d % 8 != 0 || (unfed && d > 2048) || dn == nullptr || x == nullptr ||
+  if (rows < 1 || d < 8 || d % 8 != 0 || (unfed && d > 5120) || dn == nullptr || x == nullptr ||
       w == nullptr || rstd == nullptr || dres == nullptr || dx == nullptr || dw == nullptr ||
       part == nullptr || scratch == nullptr)
     return BN_ERR_INVALID_ARG;

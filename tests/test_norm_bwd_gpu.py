@@ -6,9 +6,12 @@ The kernel takes dn' = rstd * dn (the block's dX GEMM epilogue folds the row's
     dx = dres + rstd dn w - x rstd^3 mean(dn w x),   dw = sum_t rstd dn x,
 which is the oracle's (dx, dw) for dn = dn' / rstd, plus dres. Widths: 2048
 (rows streamed through shared memory, one 256-column chunk per lane and
-step), 320 (a ragged last chunk: lanes past the row hold nothing), 1024, and
-4096 (the two-pass kernel for wider rows); 1000 rows over the GPU's blocks
-leave every block a different row count.
+step, the weights in registers), 320 (a ragged last chunk: lanes past the row
+hold nothing), 1024, 2056 (9 chunks on the 12-chunk instance, the weights in
+shared memory), 3072, 4096 (16 chunks, four warps a block), 4104 (17 chunks
+on the 20-chunk instance, three warps), 5120 (the 13B width), and 5128 (the
+two-pass kernel for wider rows); 1000 rows over the GPU's blocks leave every
+block a different row count.
 
 Failure detection: with `unfed` the first row of the kernel's first warp is
 never loaded; its bounded wait gives up after 1 s, the status word reads
@@ -78,7 +81,7 @@ def launch(lib, x, w, dres, rstd, dnp, unfed=0, scratch=None):
     return dx, dw, scratch
 
 
-@pytest.mark.parametrize("d", [2048, 320, 1024, 4096])
+@pytest.mark.parametrize("d", [2048, 320, 1024, 2056, 3072, 4096, 4104, 5120, 5128])
 def test_norm_backward_matches_oracle(lib, d):
     x, w, dres, rstd, dnp, dx_ref, dw_ref = case(1000, d, seed=d)
     dx, dw, scratch = launch(lib, x, w, dres, rstd, dnp)
@@ -92,8 +95,9 @@ def test_norm_backward_matches_oracle(lib, d):
     assert e_dx < tol and e_dw < tol
 
 
-def test_unfed_norm_backward_times_out_and_context_survives(lib):
-    x, w, dres, rstd, dnp, dx_ref, dw_ref = case(1000, 2048, seed=7)
+@pytest.mark.parametrize("d", [2048, 4096, 5120])
+def test_unfed_norm_backward_times_out_and_context_survives(lib, d):
+    x, w, dres, rstd, dnp, dx_ref, dw_ref = case(1000, d, seed=7)
     stream = torch.cuda.current_stream()
     t0 = time.perf_counter()
     _, _, scratch = launch(lib, x, w, dres, rstd, dnp, unfed=1)
