@@ -90,6 +90,10 @@ struct Ctx {
   int launches = 0;
   // targets a consumer of the last tcgen05 launch waits for (ChainLink)
   int chain_entered_target = 0, chain_rows_target = 0;
+  // that producer's units, CTA groups and estimated cost of one unit (lead
+  // rounds of its consumer)
+  int chain_prod_units = 0, chain_prod_groups = 0;
+  double chain_prod_cost = 0;
   // links for the next tcgen05 launch (taken and cleared by it)
   ChainLink chain_out, chain_in;
   cudaError_t err = cudaSuccess;

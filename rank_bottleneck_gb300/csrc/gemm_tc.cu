@@ -3,6 +3,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -99,14 +100,36 @@ int cta_group_for(const GemmLaunch& g) {
 }
 }  // namespace
 
+// Estimated time of one tile of an epilogue kind, in units of k-elements of a
+// plain 256 x 256 tile: the k extent (both operand pairs of SwiGLU) times a
+// per-kind factor from the kinds' measured rates at the 1B and 7B shapes (the
+// epilogues that read inputs or write two outputs are the slower ones).
+static double unit_cost(int ek, const GemmProblem& q) {
+  double k = static_cast<double>(q.K);
+  if (ek == tc::K_SWIGLU || ek == tc::K_CHAIN) k += static_cast<double>(q.K2 > 0 ? q.K2 : q.K);
+  switch (ek) {
+    case tc::K_NORM: return 1.15 * k;
+    case tc::K_SIGMA: return 0.9 * k;
+    case tc::K_STORE: return 0.95 * k;
+    case tc::K_SWIGLU: return 1.15 * k;
+    case tc::K_RESID: return 1.5 * k;
+    case tc::K_DSWIGLU: return 1.9 * k;
+    default: return k;
+  }
+}
+
 void gemm_tc(Ctx& c, const GemmLaunch& g) {
   using namespace tc;
   // this launch's chain links, if any (none carry over to a later launch)
   const ChainLink chain_out = c.chain_out, chain_in = c.chain_in;
+  const int prod_units = c.chain_prod_units, prod_groups = c.chain_prod_groups;
+  const double prod_cost = c.chain_prod_cost;
   c.chain_out = ChainLink{};
   c.chain_in = ChainLink{};
   c.chain_entered_target = 0;
   c.chain_rows_target = 0;
+  c.chain_prod_units = c.chain_prod_groups = 0;
+  c.chain_prod_cost = 0;
   int ek = epi_kind(g.epi);
   if (ek < 0 || g.nprob < 1 || g.nprob > kMaxProblems) {
     c.bad = 1;
@@ -247,6 +270,22 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
     }
     tiles_per_row_block += P.p[i].tiles_n;
   }
+  // A chained consumer after a producer whose last round was partial: the
+  // producer's last (units mod groups) groups hold their SMs about one producer
+  // unit longer, and the consumer CTAs that land there (its last groups, as
+  // CTAs are placed in index order) start that much later. The other groups
+  // take the first lead_rounds rounds alone: about as many of this launch's
+  // units as fit in one producer unit (rounded down).
+  const double cost = unit_cost(ek, g.p[0]);
+  static const bool lead_off = [] {
+    const char* v = std::getenv("BN_GEMM_LEAD");
+    return v != nullptr && v[0] == '0';
+  }();
+  if (P.in.rows != nullptr && !lead_off && prod_groups > 0 && prod_units > prod_groups &&
+      prod_units % prod_groups > 0 && cost > 0) {
+    P.lead_late = prod_units % prod_groups;
+    P.lead_rounds = static_cast<int>(std::min(16.0, std::floor(prod_cost / cost)));
+  }
   prof_start(c);
   int ctas;
   if (CG == 2)
@@ -263,6 +302,11 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
   // wait, and per row block one count from each epilogue warp of each tile
   c.chain_entered_target = P.out.rows ? ctas : 0;
   c.chain_rows_target = P.out.rows ? tiles_per_row_block * NUM_EPI_WARPS * CG : 0;
+  if (P.out.rows != nullptr) {
+    c.chain_prod_units = P.total_units;
+    c.chain_prod_groups = ctas / CG;
+    c.chain_prod_cost = cost;
+  }
   note_launch(c, KK_GEMM_TC, static_cast<int>(g.epi), flops, bytes);
   TileReduce local;
   TileReduce& r = g.finish ? *g.finish : local;

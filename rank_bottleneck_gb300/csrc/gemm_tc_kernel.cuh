@@ -184,6 +184,31 @@ struct Params {
   float* part;  // per split unit j: [CG x 128][BN] fp32 at j * CG * 128 * BN
   ChainLink out;  // this launch produces rows for the next launch (counts them)
   ChainLink in;   // this launch consumes the previous launch's rows (waits on them)
+  // Lead rounds of a chained consumer: its last lead_late groups start on the
+  // SMs its producer's partial last round holds, about one producer tile late,
+  // so the first lead_rounds rounds go to the other groups only (see
+  // first_unit / next_unit). 0: plain round robin.
+  int lead_late, lead_rounds;
+};
+
+// The units of group `pair` of `npairs`, in increasing order. With E = npairs -
+// lead_late early groups and base = lead_rounds x E, units [0, base) are dealt
+// round robin to the early groups, then units from base round robin to all
+// groups; without a lead (base = 0) that is plain round robin.
+struct UnitSeq {
+  int pair, npairs, early, base;
+  __device__ __forceinline__ UnitSeq(const Params& P, int pair_, int npairs_)
+      : pair(pair_), npairs(npairs_), early(npairs_ - P.lead_late), base(0) {
+    if (P.lead_late > 0 && P.lead_rounds > 0 && early > 0) base = P.lead_rounds * early;
+  }
+  __device__ __forceinline__ int first() const { return pair < early ? pair : base + pair; }
+  __device__ __forceinline__ int next(int u) const {
+    if (u < base) {
+      u += early;
+      return u < base ? u : base + pair;
+    }
+    return u + npairs;
+  }
 };
 
 // ---------------------------------------------------------------------------
@@ -403,6 +428,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
     if (P.out.entered != nullptr && threadIdx.x == 0) red_release_add(P.out.entered, 1);
   const uint32_t tmem = *tmem_slot;
   const int nseg = num_segments<EK>(P);
+  const UnitSeq seq(P, pair, npairs);
 
   // Online RMSNorm's register split is made per warpgroup, in one place for
   // each: a point where the register count differs between the branches
@@ -422,7 +448,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
       int issued = 0;
       bool ok = !can_consume<EK>() || P.in.entered == nullptr ||
                 wait_count(P.in.entered, P.in.entered_target, abort_flag, P.status);
-      for (int u = pair; ok && u < P.total_units; u += npairs) {
+      for (int u = seq.first(); ok && u < P.total_units; u = seq.next(u)) {
         const Work w = decode<CG>(P, u);
         const Prob& pr = P.p[w.pi];
         if (can_consume<EK>() && P.in.rows != nullptr) {
@@ -500,7 +526,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
       int slot = 0;
       uint32_t sph = 0;
       bool ok = true;
-      for (int u = pair; ok && u < P.total_units; u += npairs) {
+      for (int u = seq.first(); ok && u < P.total_units; u = seq.next(u)) {
         const Work w = decode<CG>(P, u);
         const Prob& pr = P.p[w.pi];
         for (int s = 0; ok && s < nseg; ++s) {
@@ -560,7 +586,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
       bool ok = !can_consume<EK>() || P.in.entered == nullptr ||
                 wait_count(P.in.entered, P.in.entered_target, abort_flag, P.status);
       if (can_consume<EK>() && ok && P.in.entered != nullptr) fence_proxy_async_global();
-      for (int u = pair; ok && u < P.total_units; u += npairs) {
+      for (int u = seq.first(); ok && u < P.total_units; u = seq.next(u)) {
         const Work w = decode<CG>(P, u);
         const Prob& pr = P.p[w.pi];
         const int m0 = static_cast<int>(w.m0) + row_off;
@@ -653,7 +679,7 @@ __global__ void __launch_bounds__(kernel_threads<EK>(), 1) gemm_kernel(const __g
     // (a chained consumer's epilogue needs no wait of its own: it touches global
     // memory only after its accumulators are complete, i.e. after the operand
     // producer's waits)
-    for (int u = pair; ok && u < P.total_units; u += npairs, ++tile_no) {
+    for (int u = seq.first(); ok && u < P.total_units; u = seq.next(u), ++tile_no) {
       const Work w = decode<CG>(P, u);
       const Prob& pr = P.p[w.pi];
       const int64_t row = w.m0 + row_off + q * 32 + lane;
