@@ -169,7 +169,9 @@ int bn_last_launch_count(void);
  * algorithmic FLOPs and bytes (each input read once, each output written once).
  * bn_profile_stop() ends recording, waits for the recorded events, copies up to
  * max_records records (device time in ms) into `out` (host memory) and returns
- * how many launches were recorded. */
+ * how many launches were recorded. The events keep each launch from overlapping
+ * the one before it, so while recording the GEMM engine's consumers deal their
+ * units in plain round robin (no lead rounds: no group of theirs starts late). */
 typedef struct {
   int32_t kernel;
   int32_t epi;

@@ -116,6 +116,8 @@ enum KernelKind : int {
 // Call right before a kernel launch: starts its timing record when the
 // launch-timing facility is on for this thread.
 void prof_start(Ctx& c);
+// Whether this thread's launches are being timed one by one (bn_profile_start).
+bool prof_active();
 // Call right after a kernel launch: counts it, records a launch error, and
 // closes its timing record with the launch's algorithmic FLOPs and bytes.
 void note_launch(Ctx& c, int kind, int epi, double flops, double bytes);

@@ -275,13 +275,15 @@ void gemm_tc(Ctx& c, const GemmLaunch& g) {
   // unit longer, and the consumer CTAs that land there (its last groups, as
   // CTAs are placed in index order) start that much later. The other groups
   // take the first lead_rounds rounds alone: about as many of this launch's
-  // units as fit in one producer unit (rounded down).
+  // units as fit in one producer unit (rounded down). While launches are timed
+  // one by one, the events between them keep a launch from overlapping the one
+  // before it: no consumer group starts late, and there is no lead.
   const double cost = unit_cost(ek, g.p[0]);
   static const bool lead_off = [] {
     const char* v = std::getenv("BN_GEMM_LEAD");
     return v != nullptr && v[0] == '0';
   }();
-  if (P.in.rows != nullptr && !lead_off && prod_groups > 0 && prod_units > prod_groups &&
+  if (P.in.rows != nullptr && !lead_off && !prof_active() && prod_groups > 0 && prod_units > prod_groups &&
       prod_units % prod_groups > 0 && cost > 0) {
     P.lead_late = prod_units % prod_groups;
     P.lead_rounds = static_cast<int>(std::min(16.0, std::floor(prod_cost / cost)));

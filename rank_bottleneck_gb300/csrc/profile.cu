@@ -36,6 +36,8 @@ thread_local Prof g_prof;
 
 }  // namespace
 
+bool prof_active() { return g_prof.on; }
+
 void prof_start(Ctx& c) {
   if (!g_prof.on) return;
   g_prof.pending = g_prof.next_event();
