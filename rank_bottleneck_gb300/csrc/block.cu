@@ -330,11 +330,15 @@ ChainLink chain_link(const Shape& s, const Tmp& B, int i) {
   l.rows = l.entered + 32;
   return l;
 }
-// zero links [first, first + n) before the launches that use them
-void chain_reset(Ctx& c, const Shape& s, const Tmp& B, int first, int n) {
+// zero links [first, first + n) before the launches that use them; the last
+// n_late of them after the kernel ahead has completed (it may be the consumer
+// of one of them, still reading its counters: the previous forward's last
+// launch is link 3's consumer), the others at once
+void chain_reset(Ctx& c, const Shape& s, const Tmp& B, int first, int n, int n_late) {
   if (!chains_on(s, B)) return;
-  track(c, cudaMemsetAsync(B.chain + first * chain_stride(s), 0,
-                           static_cast<size_t>(n * chain_stride(s)) * 4, c.stream));
+  const int64_t st = chain_stride(s);
+  launch_zero_counters(c, B.chain + first * st, (n - n_late) * st, B.chain + (first + n - n_late) * st,
+                       n_late * st);
 }
 // the next GEMM launch produces rows for link i
 void produce(Ctx& c, const Shape& s, const Tmp& B, int i) {
@@ -600,7 +604,7 @@ void forward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const voi
                      void* q, void* k, const Acts& A, const Tmp& B) {
   const void* x1 = x;
   const Fold f2{W->A_gu, W->w_norm2, s.rgu, s.d, B.A2f};
-  chain_reset(c, s, B, 0, 4);
+  chain_reset(c, s, B, 0, 4, 1);
   if (s.full()) {
     const Fold f1{W->A_qkv, W->w_norm1, s.rqkv, s.d, B.A1f};
     DT_CALL(s, stats_fold, c, x, s, A.ss1, A.rstd1, f1, f2);
@@ -788,7 +792,7 @@ void backward_lowrank(Ctx& c, const Shape& s, const bn_block_params* W, const vo
   const int64_t rqkv = s.rqkv, rgu = s.rgu;
   Wgrads wg;
   const void* x1 = s.full() ? A.x1 : x;
-  chain_reset(c, s, B, 4, 4);
+  chain_reset(c, s, B, 4, 4, 0);
   // ---- down bottleneck: y = x1 + B_d sigma(A_d m)
   add_wgrad(c, s, wg, wgrad(d, rd, T, dy, d, A.h_d, rd, dW->B_d, rd));
   {

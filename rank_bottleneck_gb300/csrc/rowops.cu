@@ -709,6 +709,23 @@ __global__ void __launch_bounds__(256) finish_kernel(const TileReduce r) {
   }
 }
 
+// One CTA: lets the next launch start at once, clears `early`, waits for the
+// kernel ahead, clears `late`.
+__global__ void __launch_bounds__(256) zero_counters_kernel(int* __restrict__ early, int n_early,
+                                                            int* __restrict__ late, int n_late) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = threadIdx.x; i < n_early; i += blockDim.x) early[i] = 0;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int i = threadIdx.x; i < n_late; i += blockDim.x) late[i] = 0;
+}
+
+void launch_zero_counters(Ctx& c, int* early, int64_t n_early, int* late, int64_t n_late) {
+  prof_start(c);
+  track(c, launch_pdl(zero_counters_kernel, 1, 256, 0, c.stream, early, static_cast<int>(n_early),
+                      late, static_cast<int>(n_late)));
+  note_launch(c, KK_ELEMENTWISE, -1, 0.0, 4.0 * static_cast<double>(n_early + n_late));
+}
+
 void launch_finish(Ctx& c, const TileReduce& r) {
   int blocks = r.rem_tiles > 0 ? r.rem_tiles * reduce_slabs(r) : 0;
   double flops = 0, bytes = 0;

@@ -73,6 +73,13 @@ struct TileReduce {
 };
 void launch_finish(Ctx& c, const TileReduce& r);
 
+// Zero the counters of a pass's chained launches (one small launch). `early`
+// must belong to launches that completed before the kernel ahead of this one
+// started its dependency wait: it is cleared at once, overlapping that kernel's
+// tail. `late` may still be read by the kernel ahead and is cleared after the
+// dependency wait. The launch completes only after the kernel ahead.
+void launch_zero_counters(Ctx& c, int* early, int64_t n_early, int* late, int64_t n_late);
+
 // h = sigma(z) elementwise, rounded exactly like the GEMM epilogues round it.
 template <typename T>
 void launch_sigma(Ctx& c, const T* z, int64_t rows, int64_t cols, int64_t ldz, T* h, int64_t ldh,
