@@ -521,6 +521,189 @@ __global__ void __launch_bounds__(norm_bwd_stream_warps<NP>() * 32, 1)
   }
 }
 
+// bf16 rows of 4097 to 256 x 2 NPH columns: each row is split between the two
+// warps of a pair (warp h of the pair owns chunks h NPH .. h NPH + NPH - 1 of
+// 256 columns), so that a row is worked on twice as fast and a pair can keep
+// three stages (dn' | x | dres of one row each): two rows of reads in flight
+// while it works on a third. The two halves' row sums meet through shared
+// memory behind an mbarrier and are added in a fixed order (warp 0's first).
+// Stage refills wait on an "empty" mbarrier that both warps arrive on. Every
+// wait is bounded; a pair leaves a row together (each warp posts whether its
+// stage landed next to its partial sum), drains its copies in flight and joins
+// the block's dw reduction.
+constexpr int kPairs = 2, kPairStages = 3;
+template <int NPH>
+__global__ void __launch_bounds__(kPairs * 64, 1)
+    norm_bwd_pair_kernel(const bf16* __restrict__ dn, const bf16* __restrict__ x,
+                         const bf16* __restrict__ w, const float* __restrict__ rstd,
+                         const bf16* __restrict__ dres, int64_t rows, int d,
+                         bf16* __restrict__ dx, float* __restrict__ part, int* status, int unfed) {
+  extern __shared__ __align__(128) unsigned char nbs[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = warp >> 1, h = warp & 1;
+  const uint32_t row_bytes = static_cast<uint32_t>(d) * 2u;
+  const uint32_t stage_bytes = 3u * row_bytes;  // dn' | x | dres
+  const size_t off_b = static_cast<size_t>(kPairs) * kPairStages * stage_bytes;
+  unsigned char* ring = nbs + static_cast<size_t>(pair) * kPairStages * stage_bytes;
+  uint64_t* pb = reinterpret_cast<uint64_t*>(nbs + off_b) + pair * 8;  // full[3] empty[3] xch[2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(nbs + off_b + kPairs * 64);
+  volatile float* xsum = reinterpret_cast<volatile float*>(nbs + off_b + kPairs * 64 + 16) + pair * 4;
+  volatile int* xok = reinterpret_cast<volatile int*>(nbs + off_b + kPairs * 64 + 16 + kPairs * 16) +
+                      pair * 4;
+  bf16* sw = reinterpret_cast<bf16*>(nbs + off_b + kPairs * 64 + 16 + kPairs * 32);
+  const uint32_t full0 = tc::smem_u32(pb), empty0 = full0 + 24, xch0 = full0 + 48;
+  const uint32_t ring0 = tc::smem_u32(ring);
+  if (h == 0 && lane == 0) {
+    for (int i = 0; i < kPairStages; ++i) {
+      tc::mbar_init(full0 + 8u * i, 1);
+      tc::mbar_init(empty0 + 8u * i, 2);
+    }
+    tc::mbar_init(xch0, 2);
+    tc::mbar_init(xch0 + 8, 2);
+  }
+  if (threadIdx.x == 0) *abort_flag = 0;
+  // the norm weight is a parameter: no kernel of the stream writes it
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x)
+    *reinterpret_cast<uint4*>(sw + 8 * i) = *reinterpret_cast<const uint4*>(w + 8 * i);
+  float acc[NPH][8];
+#pragma unroll
+  for (int k = 0; k < NPH; ++k)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[k][i] = 0.f;
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncthreads();
+  grid_dependency_sync();
+
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows / gridDim.x;
+  const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * rows / gridDim.x;
+  const int64_t first = r0 + pair;
+  const int64_t n = first < r1 ? (r1 - first + kPairs - 1) / kPairs : 0;  // this pair's rows
+  const bool issuer = h == 0 && lane == 0;
+  int64_t issued = 0;
+  // copies of the pair's row j into stage j % 3 (the issuer)
+  auto issue = [&](int64_t j) {
+    const int64_t off = (first + j * kPairs) * d;
+    const uint32_t st = static_cast<uint32_t>(j % kPairStages);
+    const uint32_t bar = full0 + 8u * st;
+    const uint32_t dst = ring0 + st * stage_bytes;
+    tc::mbar_expect_tx(bar, stage_bytes);
+    bulk_load(dst, dn + off, row_bytes, bar);
+    bulk_load(dst + row_bytes, x + off, row_bytes, bar);
+    bulk_load(dst + 2 * row_bytes, dres + off, row_bytes, bar);
+  };
+  if (issuer) {
+    for (int64_t j = 0; j < n && j < kPairStages; ++j) {
+      // (test hook) the first pair's first row is never loaded: its waits must run out
+      if (!(j == 0 && unfed && blockIdx.x == 0 && pair == 0)) issue(j);
+      issued = j + 1;
+    }
+  }
+  const float inv_d = 1.0f / static_cast<float>(d);
+  float r_next = n > 0 ? rstd[first] : 0.f;
+  int64_t j = 0;
+  for (; j < n; ++j) {
+    const int64_t row = first + j * kPairs;
+    const float r = r_next;
+    if (j + 1 < n) r_next = rstd[row + kPairs];
+    const uint32_t st = static_cast<uint32_t>(j % kPairStages);
+    const uint32_t uph = static_cast<uint32_t>(j / kPairStages) & 1u;
+    const bool landed = __all_sync(
+        0xffffffffu, tc::wait_bar_inline(full0 + 8u * st, uph, abort_flag, status));
+    const bf16* sdn = reinterpret_cast<const bf16*>(ring + st * stage_bytes);
+    const bf16* sx = sdn + d;
+    const bf16* sg = sdn + 2 * d;
+    float s = 0.f;
+    if (landed) {
+#pragma unroll
+      for (int k = 0; k < NPH; ++k) {
+        const int c = (h * NPH + k) * 256 + lane * 8;
+        if (c < d) {
+          Pack8<bf16> a, b, wu;
+          a.load(sdn + c);
+          b.load(sx + c);
+          wu.load(sw + c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) s = fmaf(a[i] * wu[i], b[i], s);
+        }
+      }
+      s = warp_sum(s);
+    }
+    // post this half's sum and whether its stage landed; meet the other half
+    const uint32_t xb = xch0 + 8u * static_cast<uint32_t>(j & 1);
+    const int slot = static_cast<int>(j & 1) * 2;
+    if (lane == 0) {
+      xsum[slot + h] = s;
+      xok[slot + h] = landed ? 1 : 0;
+      tc::mbar_arrive(xb);
+    }
+    const bool met = __all_sync(0xffffffffu, tc::wait_bar_inline(
+                                                  xb, static_cast<uint32_t>(j >> 1) & 1u,
+                                                  abort_flag, status));
+    if (!met || !xok[slot] || !xok[slot + 1]) break;
+    const float total = xsum[slot] + xsum[slot + 1];
+    const float coef = r * r * total * inv_d;
+    bf16* o = dx + row * d;
+#pragma unroll
+    for (int k = 0; k < NPH; ++k) {
+      const int c = (h * NPH + k) * 256 + lane * 8;
+      if (c < d) {
+        Pack8<bf16> a, b, g, wu;
+        a.load(sdn + c);
+        b.load(sx + c);
+        g.load(sg + c);
+        wu.load(sw + c);
+        float out[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          out[i] = g[i] + (a[i] * wu[i] - b[i] * coef);
+          acc[k][i] = fmaf(a[i], b[i], acc[k][i]);
+        }
+        Vec8<bf16>::store(o + c, out);
+      }
+    }
+    __syncwarp();  // every lane of this half has read the stage
+    if (lane == 0) tc::mbar_arrive(empty0 + 8u * st);
+    if (issuer && j + kPairStages < n) {
+      // both halves are done with the stage before it is refilled
+      if (!tc::wait_bar_inline(empty0 + 8u * st, uph, abort_flag, status)) break;
+      tc::fence_proxy_async();
+      issue(j + kPairStages);
+      issued = j + kPairStages + 1;
+    }
+    __syncwarp();
+  }
+  if (issuer && j < n) {
+    // the pair left early: let its copies still in flight land before the
+    // block's shared memory is reused or released
+    for (int64_t k = j; k < issued; ++k) {
+      if (k == 0 && unfed && blockIdx.x == 0 && pair == 0) continue;  // never issued
+      const uint32_t bar = full0 + 8u * static_cast<uint32_t>(k % kPairStages);
+      const uint32_t ph = static_cast<uint32_t>(k / kPairStages) & 1u;
+      const unsigned long long t0 = globaltimer_ns();
+      while (!tc::mbar_try_wait(bar, ph) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  }
+  // block sum of the pairs' dw columns, in pair order, through shared memory
+  __syncthreads();
+  float* red = reinterpret_cast<float*>(nbs);  // [kPairs][d], inside the stages
+#pragma unroll
+  for (int k = 0; k < NPH; ++k) {
+    const int c = (h * NPH + k) * 256 + lane * 8;
+    if (c < d) {
+      float* q = red + static_cast<size_t>(pair) * d + c;
+      *reinterpret_cast<float4*>(q) = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+      *reinterpret_cast<float4*>(q + 4) = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
+    }
+  }
+  __syncthreads();
+  for (int col = threadIdx.x; col < d; col += blockDim.x) {
+    float v = red[col];
+    for (int k = 1; k < kPairs; ++k) v += red[static_cast<size_t>(k) * d + col];
+    part[static_cast<int64_t>(blockIdx.x) * d + col] = v;
+  }
+}
+
 // dw[col] = sum over blocks b of part[b][col] for the 32 columns of block `cb`:
 // each of the 8 warps sums a fixed contiguous range of b, the 8 sums are added
 // in warp order.
@@ -597,6 +780,32 @@ int launch_norm_bwd(Ctx& c, const T* dn, const T* x, const T* w, const float* rs
   if (stream) {
     nblk = std::min(nblk, c.num_sms);
     const int np = static_cast<int>((d + 255) / 256);
+    if (np > 16) {
+      // rows split between the warps of a pair: three stages of three rows per
+      // pair, 64 bytes of barriers per pair, the abort flag, the halves' sums and
+      // flags (32 bytes per pair) and the weights
+      const size_t smem = static_cast<size_t>(kPairs) * kPairStages * 6 * static_cast<size_t>(d) +
+                          kPairs * 64 + 16 + kPairs * 32 + 2 * static_cast<size_t>(d);
+      static const bool attr = [] {
+        cudaFuncSetAttribute(norm_bwd_pair_kernel<10>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kNormBwdStreamSmem));
+        return true;
+      }();
+      (void)attr;
+      track(c, launch_pdl(norm_bwd_pair_kernel<10>, nblk, kPairs * 64, smem, c.stream,
+                          reinterpret_cast<const bf16*>(dn), reinterpret_cast<const bf16*>(x),
+                          reinterpret_cast<const bf16*>(w), rstd,
+                          reinterpret_cast<const bf16*>(dres), rows, static_cast<int>(d),
+                          reinterpret_cast<bf16*>(dx), part, c.status, unfed ? 1 : 0));
+      note_launch(c, KK_NORM_BWD, -1, 8.0 * rows * d,
+                  4.0 * rows * d * sizeof(T) + d * sizeof(T) + 4.0 * rows + 4.0 * nblk * d);
+      if (!colsum) return nblk;
+      prof_start(c);
+      track(c, launch_pdl(colsum_kernel<T>, static_cast<unsigned>((d + 31) / 32), 256, 0, c.stream,
+                          part, nblk, static_cast<int>(d), dw));
+      note_launch(c, KK_COLSUM, -1, 1.0 * nblk * d, 4.0 * nblk * d + d * sizeof(T));
+      return nblk;
+    }
     // two stages of three rows per warp, then 16 bytes of barriers per warp, the
     // abort flag (16 bytes) and, past 8 chunks a lane, the weights
     const size_t warp_bytes = 12 * static_cast<size_t>(d) + 16;

@@ -8,10 +8,11 @@ which is the oracle's (dx, dw) for dn = dn' / rstd, plus dres. Widths: 2048
 (rows streamed through shared memory, one 256-column chunk per lane and
 step, the weights in registers), 320 (a ragged last chunk: lanes past the row
 hold nothing), 1024, 2056 (9 chunks on the 12-chunk instance, the weights in
-shared memory), 3072, 4096 (16 chunks, four warps a block), 4104 (17 chunks
-on the 20-chunk instance, three warps), 5120 (the 13B width), and 5128 (the
-two-pass kernel for wider rows); 1000 rows over the GPU's blocks leave every
-block a different row count.
+shared memory), 3072, 4096 (16 chunks, four warps a block), 4104 and 5120
+(the 13B width: each row split between the two warps of a pair, the second
+warp's last chunks past the row at 4104), and 5128 (the two-pass kernel for
+wider rows); 1000 rows over the GPU's blocks leave every block a different row
+count.
 
 Failure detection: with `unfed` the first row of the kernel's first warp is
 never loaded; its bounded wait gives up after 1 s, the status word reads
