@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(256, 2)
   }
 }
 
-// bf16 rows of at most 256 NP columns (NP <= 20), streamed through shared memory. Every
+// bf16 rows of at most 256 NP columns (NP <= 16), streamed through shared memory. Every
 // warp owns a ring of two stages; a stage holds one row of dn', x and dres,
 // brought in by three bulk copies that complete on the stage's mbarrier. While
 // a warp works on one row, the copies of its next row are in flight, so an SM
@@ -346,7 +346,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // rows, 6 x 2 x 256 NP bytes a warp, and the weights).
 template <int NP>
 constexpr int norm_bwd_stream_warps() {
-  return NP > 16 ? 3 : NP > 12 ? 4 : NP > 8 ? 6 : NP > 4 ? 9 : 16;
+  return NP > 12 ? 4 : NP > 8 ? 6 : NP > 4 ? 9 : 16;
 }
 
 template <int NP>
@@ -740,15 +740,15 @@ int norm_bwd_blocks(int num_sms) { return 2 * num_sms; }
 
 using NormBwdStream = void (*)(const bf16*, const bf16*, const bf16*, const float*, const bf16*,
                                int64_t, int, bf16*, float*, int*, int);
-// the instance for rows of np chunks: exact up to 8, then 12, 16 or 20 (the
-// chunks past d are skipped)
-static int norm_bwd_stream_np(int np) { return np <= 8 ? np : np <= 12 ? 12 : np <= 16 ? 16 : 20; }
+// the instance for rows of np <= 16 chunks: exact up to 8, then 12 or 16 (the
+// chunks past d are skipped); longer rows take norm_bwd_pair_kernel
+static int norm_bwd_stream_np(int np) { return np <= 8 ? np : np <= 12 ? 12 : 16; }
 static NormBwdStream norm_bwd_stream(int np) {
-  static const NormBwdStream k[11] = {
+  static const NormBwdStream k[10] = {
       norm_bwd_stream_kernel<1>, norm_bwd_stream_kernel<2>,  norm_bwd_stream_kernel<3>,
       norm_bwd_stream_kernel<4>, norm_bwd_stream_kernel<5>,  norm_bwd_stream_kernel<6>,
       norm_bwd_stream_kernel<7>, norm_bwd_stream_kernel<8>,  norm_bwd_stream_kernel<12>,
-      norm_bwd_stream_kernel<16>, norm_bwd_stream_kernel<20>};
+      norm_bwd_stream_kernel<16>};
   static const bool attr = [] {
     for (auto f : k)
       cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -757,12 +757,11 @@ static NormBwdStream norm_bwd_stream(int np) {
   }();
   (void)attr;
   const int q = norm_bwd_stream_np(np);
-  return k[q <= 8 ? q - 1 : q == 12 ? 8 : q == 16 ? 9 : 10];
+  return k[q <= 8 ? q - 1 : q == 12 ? 8 : 9];
 }
 static int norm_bwd_stream_max_warps(int np) {
   const int q = norm_bwd_stream_np(np);
-  return q > 16   ? norm_bwd_stream_warps<20>()
-         : q > 12 ? norm_bwd_stream_warps<16>()
+  return q > 12   ? norm_bwd_stream_warps<16>()
          : q > 8  ? norm_bwd_stream_warps<12>()
          : q > 4  ? norm_bwd_stream_warps<8>()
                   : norm_bwd_stream_warps<1>();
